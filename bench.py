@@ -1,0 +1,447 @@
+"""Benchmark of the masked flash-attention forward on GB300.
+
+One step = one fa_fwd call over one batch of the workload (all of the hot
+path: top-k preparation or mask summary when the workload has one, tile
+classification, the attention kernel and the split combine).
+
+Default workload: causal prefill over past KV with grouped-query heads
+(B=4, Hq=32, Hkv=8, d=128, 512 new queries over 4096 keys), metric "useful
+TFLOP/s": 4*d FLOP per (query, key) pair that the mask keeps, per query head.
+``--workload paged_varlen_decode`` reports KV-cache GB/s (K/V bytes inside
+each sequence's window) instead.
+
+Rules kept here: W >= 3 untimed warm-up steps; each timed step is bracketed by
+CUDA events on the launching stream; between timed steps L2 is flushed by
+writing a 256 MB buffer (outside the events); inputs are resident in HBM when
+a step starts.  ``e2e`` repeats the measurement through the same public call
+with the inputs copied from pinned host memory and the outputs copied back
+inside the timed region.  Under torchrun every rank runs its own batch
+(independent problems, no collective on the data path): weak scaling.
+
+``--impl reference`` times the fp64 CPU oracle (the method's plain
+definition) on the host cores instead, on a bounded sample of the same
+workload, and prints the same JSON line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "masked attn fwd useful TFLOP/s (prefill) and KV-cache GB/s (decode), 1×GB300"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p["bf16_tflops_sustained"],
+                    src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work (counted from the definition, not from the kernels)
+# ---------------------------------------------------------------------------
+
+def useful_pairs(case):
+    """Number of (query row, key, q-head) triples the mask keeps, counted with
+    closed forms for the causal/window rules and exactly for top-k."""
+    p = case["params"]
+    q, k = case["q"], case["k"]
+    if p["cu_seqlens_q"] is not None:
+        cu_q = p["cu_seqlens_q"].tolist()
+        cu_k = p["cu_seqlens_k"].tolist()
+        lens = [(cu_q[i + 1] - cu_q[i], cu_k[i + 1] - cu_k[i]) for i in range(len(cu_q) - 1)]
+        Hq = q.shape[1]
+    else:
+        lens = [(q.shape[1], k.shape[1])] * q.shape[0]
+        Hq = q.shape[2]
+    total = 0
+    for Sq, Sk in lens:
+        off = Sk - Sq
+        i = np.arange(Sq, dtype=np.int64)
+        hi = np.full(Sq, Sk - 1, dtype=np.int64)
+        lo = np.zeros(Sq, dtype=np.int64)
+        if p["causal"]:
+            hi = np.minimum(hi, i + off)
+        if p["window_left"] >= 0:
+            lo = np.maximum(lo, i + off - p["window_left"])
+        if p["window_right"] >= 0:
+            hi = np.minimum(hi, i + off + p["window_right"])
+        cnt = np.maximum(hi - lo + 1, 0)
+        if p["zero_hold_states"] is not None:
+            cnt = np.minimum(cnt, p["keep_window"])
+        total += int(cnt.sum()) * Hq
+    if p["mask"] is not None:  # dense mask: count finite entries over allowed pairs
+        m = p["mask"]
+        total = int(torch.isfinite(m).sum().item()) * (q.shape[0] if m.dim() == 2 else 1) * \
+            (Hq if m.dim() == 2 else 1)
+    return total
+
+
+def kv_window_bytes(case):
+    """K and V bytes inside each sequence's window (decode workloads)."""
+    p = case["params"]
+    cu_k = p["cu_seqlens_k"].tolist()
+    cu_q = p["cu_seqlens_q"].tolist()
+    Hkv, d = case["k"].shape[-2], case["k"].shape[-1]
+    tot = 0
+    for s in range(len(cu_k) - 1):
+        Sk, Sq = cu_k[s + 1] - cu_k[s], cu_q[s + 1] - cu_q[s]
+        lo = max(0, (Sk - Sq) - p["window_left"]) if p["window_left"] >= 0 else 0
+        tot += (Sk - lo) * Hkv * d * 2 * 2
+    return tot
+
+
+def workload_units(case, name):
+    d = case["q"].shape[-1]
+    if name == "paged_varlen_decode":
+        b = kv_window_bytes(case)
+        return dict(metric_units=b / 1e9, unit="GB/s", bound="hbm",
+                    flops=4.0 * d * useful_pairs(case), bytes=b)
+    f = 4.0 * d * useful_pairs(case)
+    return dict(metric_units=f / 1e12, unit="TFLOP/s", bound="tensor", flops=f, bytes=None)
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def _dist():
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
+        return dist
+    return None
+
+
+def run_gpu(args):
+    import masked_flash_attention_gb300 as fa
+
+    dist = _dist()
+    rank = dist.get_rank() if dist else 0
+    world = dist.get_world_size() if dist else 1
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    case = W.WORKLOADS[args.workload](seed=args.seed + rank)
+    units = workload_units(case, args.workload)
+    p = dict(case["params"])
+    gp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    q, k, v = case["q"].to(dev), case["k"].to(dev), case["v"].to(dev)
+    stream = torch.cuda.current_stream()
+    rc, plan = fa.fa_fwd_plan(q, k, v, stream=stream.cuda_stream, **gp)
+    assert rc == 0, rc
+    ws = fa.alloc_workspace(plan["workspace_bytes"], dev)
+    out = torch.empty_like(q)
+    lse_shape = (q.shape[1], q.shape[0]) if p["cu_seqlens_q"] is not None else (q.shape[0], q.shape[2], q.shape[1])
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ev_kb = torch.cuda.Event(enable_timing=True)
+    ev_ke = torch.cuda.Event(enable_timing=True)
+    ev_kb.record(); ev_ke.record()
+
+    def step(timing=False, kb=None, ke=None):
+        fa.fa_fwd(q, k, v, out=out, lse=lse, workspace=ws, stream=stream.cuda_stream,
+                  event_begin=kb, event_end=ke, **gp)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    rc_, info = fa.fa_check_device_error(ws)
+    assert rc_ == 0, (rc_, info)
+
+    # ---- device-resident timing ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            kev[i][0].record(); kev[i][1].record()  # materialise the handles
+            ev[i][0].record()
+            step(kb=kev[i][0], ke=kev[i][1])
+            ev[i][1].record()
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    ms_per_step = total_ms / args.steps
+    value = units["metric_units"] * world / (ms_per_step / 1e3)
+
+    # ---- end to end: pinned host inputs in, outputs back, same public call ----
+    hq, hk, hv = (case["q"].pin_memory(), case["k"].pin_memory(), case["v"].pin_memory())
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+        fa.fa_fwd(dq, dk, dv, out=out, lse=lse, workspace=ws, stream=stream.cuda_stream, **gp)
+        hout.copy_(out, non_blocking=True); hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(); e2e_step(); b.record()
+        torch.cuda.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_total = sum(e2e_ms)
+    if dist:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = units["metric_units"] * world / (e2e_total / args.steps / 1e3)
+    rc_, info = fa.fa_check_device_error(ws)
+    assert rc_ == 0, (rc_, info)
+
+    if rank != 0:
+        return None
+    pk = peaks()
+    kern_avg = sum(kern_ms) / len(kern_ms)
+    if units["bound"] == "tensor":
+        achieved = units["flops"] / (kern_avg / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16"], 4)}
+    else:
+        achieved = units["bytes"] / (kern_avg / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4)}
+    roof["peak_source"] = pk["src"]
+    roof["kernel"] = "decode_kernel" if plan["path"] == fa._lib.FA_PATH_DECODE else "prefill_kernel"
+    roof["kernel_ms"] = round(kern_avg, 5)
+    roof["traffic"] = args.traffic
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": units["unit"],
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": case["name"], "seed": args.seed,
+                   "l2": "flushed between timed steps (256 MB write outside the events)",
+                   "parallelism": f"replica per GPU x{world}", "path": plan["path"],
+                   "n_items": plan["n_items"], "n_splits": plan["n_splits"]},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_value, 3), "unit": units["unit"], "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_total / args.steps, 5)},
+        "gpu_launches": int(plan["n_kernels"]) * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, units, args)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(case, n_heads):
+    """Oracle on the first ``n_heads`` (sequence, head) pairs of the workload;
+    returns (seconds, fraction of the workload's units covered)."""
+    from oracle import attention as O
+    p = case["params"]
+    q, k, v = case["q"], case["k"], case["v"]
+    packed = p["cu_seqlens_q"] is not None
+    Hq = q.shape[-2]
+    Hkv = k.shape[-2]
+    G = Hq // Hkv
+    pairs = [(b, h) for b in range(len(p["cu_seqlens_q"]) - 1 if packed else q.shape[0])
+             for h in range(Hq)]
+    sel = pairs[:n_heads]
+    qn = q.float().numpy(); kn = k.float().numpy(); vn = v.float().numpy()
+    t0 = time.perf_counter()
+    for b, h in sel:
+        if packed:
+            cu_q = p["cu_seqlens_q"].tolist(); cu_k = p["cu_seqlens_k"].tolist()
+            Sk = cu_k[b + 1] - cu_k[b]
+            qb = qn[cu_q[b]:cu_q[b + 1], h]
+            if p["block_table"] is not None:
+                kb = O.gather_paged(kn, p["block_table"][b].numpy(), Sk)[:, h // G]
+                vb = O.gather_paged(vn, p["block_table"][b].numpy(), Sk)[:, h // G]
+            else:
+                kb = kn[cu_k[b]:cu_k[b + 1], h // G]; vb = vn[cu_k[b]:cu_k[b + 1], h // G]
+        else:
+            qb = qn[b, :, h]; kb = kn[b, :, h // G]; vb = vn[b, :, h // G]
+            Sk = kb.shape[0]
+        z = None if p["zero_hold_states"] is None else p["zero_hold_states"][b, h].numpy()
+        m = None if p["mask"] is None else p["mask"].numpy()
+        O.attention_rows(qb, kb, vb, np.arange(qb.shape[0]), qb.shape[0], Sk,
+                         scale=p["scale"], causal=p["causal"], window_left=p["window_left"],
+                         window_right=p["window_right"], softcap=p["softcap"], mask_rows=m, z=z,
+                         keep_window=p["keep_window"])
+    dt = time.perf_counter() - t0
+    return dt, len(sel) / len(pairs)
+
+
+def _pick_heads(case, budget_s):
+    """Number of (sequence, head) pairs whose oracle run takes about budget_s."""
+    dt1, _ = _oracle_sample(case, 1)
+    return max(1, int(budget_s / max(dt1, 1e-3))), dt1
+
+
+def cpu_baseline(case, units, args, budget_s=None):
+    budget_s = args.cpu_budget if budget_s is None else budget_s
+    n, _ = _pick_heads(case, budget_s)
+    dt, frac = _oracle_sample(case, n)
+    val = units["metric_units"] * frac / dt
+    return {"value": round(val, 6), "unit": units["unit"], "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle on {n} of the workload's (sequence, q-head) pairs "
+                      f"({frac * 100:.2f}% of the units) in {dt:.2f} s; numpy BLAS on all cores, "
+                      "elementwise work single-threaded"}
+
+
+def run_reference(args):
+    dist_rank = int(os.environ.get("RANK", "0"))
+    if dist_rank != 0:
+        return None
+    case = W.WORKLOADS[args.workload](seed=args.seed)
+    units = workload_units(case, args.workload)
+    per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    n, _ = _pick_heads(case, per_step_budget)
+    for _ in range(args.warmup):
+        _oracle_sample(case, n)
+    times, frac = [], 0.0
+    for _ in range(args.steps):
+        dt, frac = _oracle_sample(case, n)
+        times.append(dt)
+    ms = sum(times) / len(times) * 1e3
+    val = units["metric_units"] * frac / (ms / 1e3)
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"each step: fp64 numpy oracle on {n} (sequence, q-head) pairs = {frac * 100:.2f}% of "
+              f"the workload; value scaled to the workload's units")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": units["unit"],
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": case["name"], "seed": args.seed},
+        "cpu_baseline": {"value": round(val, 6), "unit": units["unit"], "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 6), "unit": units["unit"], "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="causal_prefill_past_kv", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,227 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) masked flash-attention forward library
+ * (libmfa_gb300.so).
+ *
+ * One call, fa_fwd(), computes masked softmax attention
+ *
+ *     O[i] = sum_j softmax_j(x_ij) V[j],   LSE[i] = log sum_j exp(x_ij)
+ *
+ * with the logit x_ij built, in this order, from
+ *   - the scaled dot product  scale * <Q[i], K[j]>;
+ *   - the logit soft-cap  softcap * tanh(x / softcap)  when softcap > 0
+ *     (the `softcap` argument of vLLM pull request 11277's
+ *     flash_attn_varlen_func call);
+ *   - pair rules that set x_ij = -inf: causal aligned bottom-right, i.e. the
+ *     last query row sits on the last key, j <= i + (kv_len - q_len)
+ *     (FastChat pull request 2315, "Optimize for proper flash attn causal
+ *     handling": q_len != kv_len over past key-values without padding q);
+ *     a sliding window j >= i + off - window_left, j <= i + off + window_right
+ *     (`window_size` of the vLLM call; the ExecuTorch pull request 10466
+ *     "Summary" builds the same window from an additive mask); j < kv_len;
+ *   - an additive term added after the soft-cap: a dense fp32 mask M[i, j]
+ *     whose -inf entries drop keys (ExecuTorch pull request 10466,
+ *     "Summary"), or the dynamic top-k mask of flash-sparse-attention issue
+ *     11 ("[Integration Progress Report] Dynamic Mask Attention Integration
+ *     into FlashAttention", "Overview"): for each query row, among the keys
+ *     the pair rules allow, only the keep_window keys with the largest
+ *     zero_hold_states value are kept (ties: lower key index wins) and that
+ *     value is added to their logit.
+ * A query row with no kept key gets O = 0 and LSE = -inf, never NaN
+ * (ExecuTorch pull request 10466, "Summary": a fully -inf chunk must not
+ * poison the running softmax).
+ *
+ * Grouped-query heads: Hq must be a multiple of Hkv; q-head h reads K/V head
+ * h / (Hq / Hkv); K/V are never expanded (InfiniTrain pull request 193, "feat:
+ * Flash Attention", sections "Framework 与 autograd" and "Transformer 接入").
+ *
+ * Layouts (element strides; the head-dim stride must be 1, every other stride
+ * a multiple of 8 elements, every base pointer 16-byte aligned):
+ *   q    bf16 [B, Sq, Hq, d]                      fixed-length batch
+ *        bf16 [total_q, Hq, d]                    with cu_seqlens_q
+ *   k, v bf16 [B, Sk, Hkv, d]                     fixed-length batch
+ *        bf16 [total_k, Hkv, d]                   with cu_seqlens_k
+ *        bf16 [num_pages, page_size, Hkv, d]      with block_table (paged)
+ *   out  bf16, same shape as q (own strides)
+ *   lse  fp32 [B, Hq, Sq], or [Hq, total_q] with cu_seqlens_q
+ *   cu_seqlens_q / cu_seqlens_k  int32 [n_seq + 1] prefix sums of lengths
+ *        (the flash_attn_varlen_func arguments of the same name); with a
+ *        block_table, cu_seqlens_k gives each sequence's key count.
+ *   block_table  int32 [n_seq, max_pages]: key j of sequence s is row
+ *        j % page_size of page block_table[s][j / page_size].
+ *   head dim d is 64 or 128.
+ *
+ * Ownership and synchronisation: every buffer belongs to the caller and lives
+ * in device memory (except fa_tensor/fa_mask/fa_opts structs themselves, and
+ * the host outputs of the query functions).  The library allocates no memory;
+ * the caller passes a workspace of at least fa_fwd_workspace_size() bytes.
+ * fa_fwd() only enqueues kernels on opts->stream and returns; it never
+ * synchronises.  There is no CPU fallback and no alternative backend: on a
+ * device that is not sm_103 the call fails with FA_ERR_NO_DEVICE.
+ *
+ * Errors: every entry point returns an fa_status.  Argument errors are found
+ * on the host before anything is enqueued.  Faults found by kernels (a page
+ * index outside the cache, a bounded wait that gave up) are recorded in an
+ * error word in the first bytes of the workspace; fa_check_device_error()
+ * reads and clears it.  The caller zero-fills the workspace's first 256 bytes
+ * once, before its first use; fa_fwd never clears the word itself, so a fault
+ * stays visible until it is checked.
+ */
+#ifndef MFA_GB300_FA_H
+#define MFA_GB300_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_ABI_VERSION 1
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,    /* bad dtype, shape, stride, alignment, Hq % Hkv, d, window, ... */
+  FA_ERR_UNSUPPORTED = 2,    /* a valid combination this build does not implement */
+  FA_ERR_WORKSPACE = 3,      /* workspace missing, too small or not 256-byte aligned */
+  FA_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, tensor-map encode) */
+  FA_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait gave up (reported by fa_check_device_error) */
+  FA_ERR_DEVICE_BOUNDS = 6,  /* a kernel met an out-of-range index, e.g. a page (ditto) */
+  FA_ERR_NO_DEVICE = 7       /* no usable sm_103 device is current */
+} fa_status;
+
+typedef enum { FA_DTYPE_BF16 = 1, FA_DTYPE_F32 = 2, FA_DTYPE_I32 = 3 } fa_dtype;
+
+/* A strided view of device memory; shape/stride are in elements, outermost
+ * first; only the first ndim entries are read. */
+typedef struct {
+  void* data;
+  int32_t dtype; /* fa_dtype */
+  int32_t ndim;
+  int64_t shape[4];
+  int64_t stride[4];
+} fa_tensor;
+
+typedef enum { FA_MASK_NONE = 0, FA_MASK_DENSE = 1, FA_MASK_TOPK = 2 } fa_mask_kind;
+
+/* Additive mask.
+ *  DENSE: t is fp32 [Sq, Sk] or [B|1, Hq|1, Sq, Sk]; a stride of 0 broadcasts.
+ *         Entries must be finite or -inf.  Not combinable with cu_seqlens or
+ *         block_table (FA_ERR_UNSUPPORTED).
+ *  TOPK:  t is fp32 zero_hold_states [B, Hq, Sk]; keep_window >= 1.  Needs a
+ *         fixed-length batch, Sk <= 16384, and no sliding window
+ *         (FA_ERR_UNSUPPORTED otherwise). */
+typedef struct {
+  int32_t kind; /* fa_mask_kind */
+  int32_t keep_window;
+  fa_tensor t;
+} fa_mask;
+
+/* Debug flags (opts->debug_flags). */
+#define FA_DEBUG_NO_SKIP 0x1u /* schedule EMPTY tiles too (as PARTIAL): exercises the -inf guard */
+
+typedef struct {
+  void* stream;            /* cudaStream_t to enqueue on; NULL = legacy default stream */
+  void* workspace;         /* device buffer, 256-byte aligned */
+  size_t workspace_bytes;
+  int32_t max_seqlen_q;    /* required with cu_seqlens_q: the longest query sequence */
+  int32_t max_seqlen_k;    /* required with cu_seqlens_k: the longest key sequence */
+  uint32_t debug_flags;
+  int32_t reserved;
+  /* Optional cudaEvent_t handles (NULL = none), recorded on `stream` right
+   * before the main attention kernel is enqueued and right after its last
+   * pass (split combine included): lets a caller time that kernel alone. */
+  void* event_begin;
+  void* event_end;
+} fa_opts;
+
+/* Kernel path chosen by the planner. */
+typedef enum { FA_PATH_DECODE = 1, FA_PATH_PREFILL = 2 } fa_path;
+
+/* Tile classes produced by the scheduler. */
+typedef enum { FA_TILE_EMPTY = 0, FA_TILE_FULL = 1, FA_TILE_PARTIAL = 2 } fa_tile_class;
+
+/* The plan fa_fwd() would execute for given arguments (host-only query).
+ *
+ * Work is cut into items: item = (seq * n_heads_sched + head) * n_row_tiles
+ * + row_tile.  For the PREFILL path head is a q-head and a row tile is
+ * rows_per_tile query rows.  For the DECODE path head is a K/V head and a row
+ * tile is 16 consecutive packed rows p = i * (Hq/Hkv) + (h % (Hq/Hkv)) of that
+ * K/V head's query heads.  Keys are cut into tiles of keys_per_tile.
+ *
+ * Work list in the workspace after fa_fwd (device memory, int32):
+ *   counts[n_items]                   at workspace + off_counts
+ *   tiles[n_items][n_k_tiles]         at workspace + off_tiles;
+ *     entry = (k_tile << 1) | (class == FA_TILE_PARTIAL); only the first
+ *     counts[item] entries are valid; EMPTY tiles never appear.
+ *   stats: int64 [3] = tiles scheduled FULL, PARTIAL, and key tiles left out
+ *     as EMPTY, at workspace + off_stats.
+ *   top-k masks only: int32 e[n_seq][Hq][Sk] at workspace + off_topk_e, the
+ *     first query row at which key j is no longer kept (key j is kept on rows
+ *     i with j <= i + Sk - Sq and i < e; INT32_MAX = never dropped,
+ *     INT32_MIN = never kept). */
+typedef struct {
+  int32_t path;            /* fa_path */
+  int32_t n_seq;
+  int32_t n_heads_sched;
+  int32_t n_row_tiles;
+  int32_t rows_per_tile;   /* query rows (PREFILL) or packed rows (DECODE) per item */
+  int32_t keys_per_tile;
+  int32_t n_k_tiles;       /* key tiles of the longest key sequence */
+  int32_t n_splits;        /* DECODE: key splits per item (1 = no combine pass) */
+  int32_t tiles_per_split; /* DECODE: key tiles per split */
+  int32_t reserved;
+  int64_t n_items;
+  size_t off_counts;
+  size_t off_tiles;
+  size_t off_stats;
+  size_t off_topk_e;       /* 0 unless the mask is FA_MASK_TOPK */
+  int64_t n_kernels;       /* kernel launches one fa_fwd call enqueues */
+  size_t workspace_bytes;  /* minimum workspace size */
+} fa_plan;
+
+/* Masked attention forward; see the file comment for the semantics.
+ *   scale <= 0 selects 1/sqrt(d); softcap == 0 disables the soft-cap;
+ *   window_left / window_right == -1 leave that side unbounded; causal != 0
+ *   applies the bottom-right causal rule. */
+int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+           const fa_tensor* out, const fa_tensor* lse,
+           const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+           const fa_tensor* block_table, const fa_mask* mask,
+           int32_t window_left, int32_t window_right, float softcap, float scale,
+           int32_t causal, const fa_opts* opts);
+
+/* Host-only: validate the arguments of fa_fwd and describe its plan
+ * (pointers are checked for alignment but never dereferenced; opts->workspace
+ * may be NULL).  Same status codes as fa_fwd, except FA_ERR_WORKSPACE. */
+int fa_fwd_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+                const fa_tensor* out, const fa_tensor* lse,
+                const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+                const fa_tensor* block_table, const fa_mask* mask,
+                int32_t window_left, int32_t window_right, float softcap, float scale,
+                int32_t causal, const fa_opts* opts, fa_plan* plan_out);
+
+/* Host-only: minimum workspace size for these arguments (fa_fwd_plan's
+ * workspace_bytes). */
+int fa_fwd_workspace_size(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+                          const fa_tensor* out, const fa_tensor* lse,
+                          const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+                          const fa_tensor* block_table, const fa_mask* mask,
+                          int32_t window_left, int32_t window_right, float softcap,
+                          float scale, int32_t causal, const fa_opts* opts, size_t* bytes);
+
+/* Synchronises `stream`, then reads and clears the device error word at the
+ * start of `workspace`: FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BOUNDS.
+ * `info` (nullable) receives the first recorded detail (e.g. the bad page). */
+int fa_check_device_error(void* stream, void* workspace, uint32_t* info);
+
+/* Static text for a status code. */
+const char* fa_status_string(int status);
+
+/* FA_ABI_VERSION of the loaded library. */
+int fa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MFA_GB300_FA_H */

@@ -1,0 +1,237 @@
+"""ctypes binding of libmfa_gb300.so (argument marshalling only).
+
+Every function here mirrors an entry point of ``include/fa.h`` by name.  Torch
+is used for device memory and streams: tensors are described to the library
+as (pointer, dtype, shape, strides) and every step of the attention runs in the
+library's CUDA kernels.  There is no fallback: if the shared library is
+missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_WORKSPACE = 3
+FA_ERR_CUDA = 4
+FA_ERR_DEVICE_TIMEOUT = 5
+FA_ERR_DEVICE_BOUNDS = 6
+FA_ERR_NO_DEVICE = 7
+
+FA_DTYPE_BF16, FA_DTYPE_F32, FA_DTYPE_I32 = 1, 2, 3
+FA_MASK_NONE, FA_MASK_DENSE, FA_MASK_TOPK = 0, 1, 2
+FA_DEBUG_NO_SKIP = 0x1
+FA_PATH_DECODE, FA_PATH_PREFILL = 1, 2
+FA_TILE_EMPTY, FA_TILE_FULL, FA_TILE_PARTIAL = 0, 1, 2
+
+_DTYPES = {torch.bfloat16: FA_DTYPE_BF16, torch.float32: FA_DTYPE_F32, torch.int32: FA_DTYPE_I32}
+
+
+class fa_tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class fa_mask(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("keep_window", ctypes.c_int32), ("t", fa_tensor)]
+
+
+class fa_opts(ctypes.Structure):
+    _fields_ = [("stream", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("max_seqlen_q", ctypes.c_int32),
+                ("max_seqlen_k", ctypes.c_int32), ("debug_flags", ctypes.c_uint32),
+                ("reserved", ctypes.c_int32), ("event_begin", ctypes.c_void_p),
+                ("event_end", ctypes.c_void_p)]
+
+
+class fa_plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("n_seq", ctypes.c_int32),
+                ("n_heads_sched", ctypes.c_int32), ("n_row_tiles", ctypes.c_int32),
+                ("rows_per_tile", ctypes.c_int32), ("keys_per_tile", ctypes.c_int32),
+                ("n_k_tiles", ctypes.c_int32), ("n_splits", ctypes.c_int32),
+                ("tiles_per_split", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("n_items", ctypes.c_int64), ("off_counts", ctypes.c_size_t),
+                ("off_tiles", ctypes.c_size_t), ("off_stats", ctypes.c_size_t),
+                ("off_topk_e", ctypes.c_size_t), ("n_kernels", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_P = ctypes.POINTER
+_ARGS = [_P(fa_tensor), _P(fa_tensor), _P(fa_tensor), _P(fa_tensor), _P(fa_tensor),
+         _P(fa_tensor), _P(fa_tensor), _P(fa_tensor), _P(fa_mask), ctypes.c_int32,
+         ctypes.c_int32, ctypes.c_float, ctypes.c_float, ctypes.c_int32, _P(fa_opts)]
+
+EXPORTS = ("fa_fwd", "fa_fwd_plan", "fa_fwd_workspace_size", "fa_check_device_error",
+           "fa_status_string", "fa_abi_version")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.fa_fwd.argtypes = _ARGS
+    lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_fwd_plan.argtypes = _ARGS + [_P(fa_plan)]
+    lib.fa_fwd_plan.restype = ctypes.c_int
+    lib.fa_fwd_workspace_size.argtypes = _ARGS + [_P(ctypes.c_size_t)]
+    lib.fa_fwd_workspace_size.restype = ctypes.c_int
+    lib.fa_check_device_error.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _P(ctypes.c_uint32)]
+    lib.fa_check_device_error.restype = ctypes.c_int
+    lib.fa_status_string.argtypes = [ctypes.c_int]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_abi_version.argtypes = []
+    lib.fa_abi_version.restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+class FaError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {lib.fa_status_string(status).decode()} (status {status})")
+
+
+def fa_status_string(status: int) -> str:
+    return lib.fa_status_string(int(status)).decode()
+
+
+def fa_abi_version() -> int:
+    return lib.fa_abi_version()
+
+
+def describe(t: torch.Tensor | None):
+    """fa_tensor for a torch tensor (None -> None)."""
+    if t is None:
+        return None
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    d = fa_tensor()
+    d.data = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or 16)
+    d.dtype = _DTYPES.get(t.dtype, 0)
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(x):
+    return ctypes.byref(x) if x is not None else None
+
+
+def _args(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask, zero_hold_states,
+          keep_window, window_left, window_right, softcap, scale, causal, opts):
+    m = None
+    if mask is not None:
+        m = fa_mask(FA_MASK_DENSE, 0, describe(mask))
+    elif zero_hold_states is not None:
+        m = fa_mask(FA_MASK_TOPK, int(keep_window), describe(zero_hold_states))
+    descs = [describe(x) for x in (q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table)]
+    keep = (descs, m, opts)  # keep the structs alive for the call
+    args = [_ref(x) for x in descs] + [_ref(m), int(window_left), int(window_right),
+                                       float(softcap), float(scale), int(bool(causal)),
+                                       ctypes.byref(opts)]
+    return args, keep
+
+
+def _out_shapes(q, cu_seqlens_q, max_seqlen_q):
+    if cu_seqlens_q is not None:
+        return q.shape, (q.shape[1], q.shape[0])
+    return q.shape, (q.shape[0], q.shape[2], q.shape[1])
+
+
+def make_opts(stream=None, workspace=None, max_seqlen_q=0, max_seqlen_k=0, debug_flags=0,
+              event_begin=None, event_end=None):
+    o = fa_opts()
+    o.event_begin = event_begin.cuda_event if event_begin is not None else None
+    o.event_end = event_end.cuda_event if event_end is not None else None
+    o.stream = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    o.workspace = workspace.data_ptr() if workspace is not None else None
+    o.workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    o.max_seqlen_q = int(max_seqlen_q or 0)
+    o.max_seqlen_k = int(max_seqlen_k or 0)
+    o.debug_flags = int(debug_flags)
+    return o
+
+
+def fa_fwd_plan(q, k, v, *, out=None, lse=None, cu_seqlens_q=None, cu_seqlens_k=None,
+                block_table=None, mask=None, zero_hold_states=None, keep_window=0,
+                window_left=-1, window_right=-1, softcap=0.0, scale=None, causal=False,
+                max_seqlen_q=None, max_seqlen_k=None, debug_flags=0, stream=0, **_):
+    """Host-only plan query; returns (status, plan dict).  ``out``/``lse`` may
+    be omitted (a same-shaped stand-in descriptor is used)."""
+    if out is None:
+        out = q
+    if lse is None:
+        lse = torch.empty(_out_shapes(q, cu_seqlens_q, max_seqlen_q)[1], dtype=torch.float32,
+                          device=q.device)
+    opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                     debug_flags=debug_flags)
+    args, keep = _args(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask,
+                       zero_hold_states, keep_window, window_left, window_right, softcap,
+                       scale or 0.0, causal, opts)
+    plan = fa_plan()
+    rc = lib.fa_fwd_plan(*args, ctypes.byref(plan))
+    return rc, plan.as_dict()
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """Zero-filled, 256-byte aligned device workspace (torch allocates it)."""
+    return torch.zeros(max(256, int(nbytes)), dtype=torch.uint8, device=device)
+
+
+def fa_fwd(q, k, v, *, out=None, lse=None, cu_seqlens_q=None, cu_seqlens_k=None,
+           block_table=None, mask=None, zero_hold_states=None, keep_window=0, window_left=-1,
+           window_right=-1, softcap=0.0, scale=None, causal=False, max_seqlen_q=None,
+           max_seqlen_k=None, workspace=None, stream=None, debug_flags=0, event_begin=None,
+           event_end=None, **_):
+    """Masked attention forward on the GPU through the C ABI.  Returns
+    ``(out, lse, workspace)``; ``out``/``lse``/``workspace`` are allocated with
+    torch when not given.  Raises FaError on a non-zero status."""
+    if not q.is_cuda:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_fwd (tensors must be CUDA tensors)")
+    oshape, lshape = _out_shapes(q, cu_seqlens_q, max_seqlen_q)
+    if out is None:
+        out = torch.empty(oshape, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(lshape, dtype=torch.float32, device=q.device)
+    opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                     debug_flags=debug_flags, event_begin=event_begin, event_end=event_end)
+    args, keep = _args(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask,
+                       zero_hold_states, keep_window, window_left, window_right, softcap,
+                       scale or 0.0, causal, opts)
+    if workspace is None:
+        nbytes = ctypes.c_size_t(0)
+        rc = lib.fa_fwd_workspace_size(*args, ctypes.byref(nbytes))
+        if rc != FA_OK:
+            raise FaError(rc, "fa_fwd_workspace_size")
+        workspace = alloc_workspace(nbytes.value, q.device)
+    opts.workspace = workspace.data_ptr()
+    opts.workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib.fa_fwd(*args)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return out, lse, workspace
+
+
+def fa_check_device_error(workspace, stream=None):
+    """Synchronise and read/clear the device error word; returns (status, info)."""
+    info = ctypes.c_uint32(0)
+    st = stream if stream is not None else torch.cuda.current_stream().cuda_stream
+    rc = lib.fa_check_device_error(st, workspace.data_ptr(), ctypes.byref(info))
+    return rc, info.value

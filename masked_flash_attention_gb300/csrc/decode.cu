@@ -1,0 +1,444 @@
+// decode.cu -- split-KV attention for few query rows per K/V head (decode,
+// speculative decode, short chunks), plus the split combine pass.
+//
+// One CTA = one item (sequence, K/V head, 16 packed rows) x one split of its
+// scheduled key tiles.  The packed rows are the query heads of the K/V head's
+// group times the query positions, so a group shares every K/V byte it reads
+// (grouped-query heads without K/V expansion, InfiniTrain pull request 193
+// "Transformer 接入").  K/V rows are streamed into shared memory with 16-byte
+// cp.async copies (coalesced: a warp copies whole 128/256-byte rows), through a
+// paged block_table when there is one (vLLM pull request 11277's
+// flash_attn_varlen_func `block_table`), three 64-key stages in flight.  Each
+// of the 4 warps owns 16 keys of a stage: S = Q K^T and O += P V run on
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate); 16 rows are too few for a
+// 128-row tcgen05 tile.  The running softmax is guarded so that a fully
+// masked stage never produces NaN (ExecuTorch pull request 10466 "Summary").
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_device.cuh"
+
+namespace mfa {
+
+namespace {
+
+constexpr int kStageKeys = 64;
+constexpr int kStages = 3;
+constexpr int kThreads = 128;
+
+template <int D>
+struct DecodeSmem {
+  static constexpr int kChunks = D / 8;                      // 16-byte chunks per row
+  static constexpr int kKvBytes = kStageKeys * D * 2;        // K or V of one stage
+  static constexpr int kStageBytes = 2 * kKvBytes;
+  static constexpr int kQBytes = kDecodeRows * D * 2;
+  static constexpr int kTotal = kStages * kStageBytes + kQBytes;
+  static_assert(4 * kDecodeRows * D * 4 <= kStages * kStageBytes, "merge buffer must fit");
+};
+
+// swizzled 16-byte chunk offset (bytes) of (row, chunk) in a [rows][D] bf16 tile
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)((row * (D / 8) + (chunk ^ (row & 7))) * 16);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Address of key/value row j (head g) of sequence b.
+__device__ __forceinline__ const uint16_t* kv_row(const Params& p, const uint16_t* base, int64_t sb,
+                                                  int64_t ss, int64_t sh, int b, int g, int j) {
+  if (p.block_table) {
+    int pg = __ldg(p.block_table + (int64_t)b * p.bt_stride + j / p.page_size);
+    if ((unsigned)pg >= (unsigned)p.num_pages) {
+      record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)pg);
+      pg = 0;
+    }
+    return base + (int64_t)pg * sb + (int64_t)(j % p.page_size) * ss + (int64_t)g * sh;
+  }
+  if (p.cu_k) return base + (int64_t)(p.cu_k[b] + j) * ss + (int64_t)g * sh;
+  return base + (int64_t)b * sb + (int64_t)j * ss + (int64_t)g * sh;
+}
+
+struct ItemGeo {
+  int b, g, rt, q_len, kv_len, off, i0, i1, jlo, jhi;
+};
+
+__device__ __forceinline__ ItemGeo item_geo(const Params& p, int64_t item) {
+  ItemGeo t;
+  t.rt = (int)(item % p.n_row_tiles);
+  int64_t r = item / p.n_row_tiles;
+  t.g = (int)(r % p.n_heads_sched);
+  t.b = (int)(r / p.n_heads_sched);
+  t.q_len = seq_qlen(p, t.b);
+  t.kv_len = seq_klen(p, t.b);
+  t.off = t.kv_len - t.q_len;
+  tile_rows(p, t.rt, t.i0, t.i1);
+  t.i1 = min(t.i1, t.q_len - 1);
+  key_range(p, t.i0, t.i1, t.off, t.kv_len, t.jlo, t.jhi);
+  if (p.debug_flags & FA_DEBUG_NO_SKIP) { t.jlo = 0; t.jhi = t.kv_len - 1; }
+  return t;
+}
+
+// Output row pointers / LSE index for packed row P of an item.
+__device__ __forceinline__ void out_ptrs(const Params& p, const ItemGeo& t, int P, uint16_t*& optr,
+                                         float*& lptr, bool& valid) {
+  int qi = P / p.G, h = t.g * p.G + P % p.G;
+  valid = qi < t.q_len;
+  int64_t qrow = p.cu_q ? (int64_t)p.cu_q[t.b] + qi : (int64_t)qi;
+  int64_t bo = p.cu_q ? 0 : (int64_t)t.b;
+  optr = p.o + bo * p.o_sb + qrow * p.o_ss + (int64_t)h * p.o_sh;
+  lptr = p.lse + bo * p.lse_sb + (int64_t)h * p.lse_sh + qrow * p.lse_ss;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
+  using S = DecodeSmem<D>;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t cta = blockIdx.x;
+  const int64_t item = cta / p.n_splits;
+  const int split = (int)(cta % p.n_splits);
+  const int count = p.item_count[item];
+  if (count < 0) return;  // sequence rejected by the scheduler's length checks
+  const int t_begin = split * p.tiles_per_split;
+  // an item with nothing scheduled still owes its rows O = 0, LSE = -inf
+  if (t_begin >= count && !(split == 0 && count == 0)) return;
+  const int t_end = min(count, t_begin + p.tiles_per_split);
+  const bool single = count <= p.tiles_per_split;
+  const ItemGeo geo = item_geo(p, item);
+  const int32_t* tiles = p.item_tiles + item * p.n_kt;
+
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t sQ = sbase + kStages * S::kStageBytes;
+
+  // ---- Q: 16 packed rows -> smem (zero for padding rows) ----
+  for (int idx = tid; idx < kDecodeRows * S::kChunks; idx += kThreads) {
+    int r = idx / S::kChunks, c = idx % S::kChunks;
+    int P = geo.rt * kDecodeRows + r;
+    int qi = P / p.G, h = geo.g * p.G + P % p.G;
+    uint32_t dst = sQ + swz<D>(r, c);
+    if (qi < geo.q_len) {
+      int64_t qrow = p.cu_q ? (int64_t)p.cu_q[geo.b] + qi : (int64_t)qi;
+      int64_t bo = p.cu_q ? 0 : (int64_t)geo.b;
+      cp_async16(dst, p.q + bo * p.q_sb + qrow * p.q_ss + (int64_t)h * p.q_sh + c * 8);
+    } else {
+      asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0));
+    }
+  }
+  cp_async_commit();
+
+  // ---- stage schedule: stage s = half (s & 1) of list entry t_begin + s/2 ----
+  const int n_stages = 2 * (t_end - t_begin);
+  auto stage_key0 = [&](int s, bool& partial, bool& live) -> int {
+    int e = tiles[t_begin + (s >> 1)];
+    partial = (e & 1) != 0;
+    int kj0 = (e >> 1) * kKeysPerTile + (s & 1) * kStageKeys;
+    live = (kj0 <= geo.jhi) && (kj0 + kStageKeys - 1 >= geo.jlo) && (kj0 < geo.kv_len);
+    return kj0;
+  };
+  auto load_stage = [&](int s) {
+    bool partial, live;
+    int kj0 = stage_key0(s, partial, live);
+    if (live) {
+      uint32_t sK = sbase + (s % kStages) * S::kStageBytes;
+      uint32_t sV = sK + S::kKvBytes;
+#pragma unroll
+      for (int it = 0; it < kStageKeys * S::kChunks / kThreads; ++it) {
+        int idx = it * kThreads + tid;
+        int r = idx / S::kChunks, c = idx % S::kChunks;
+        int j = min(kj0 + r, geo.kv_len - 1);
+        cp_async16(sK + swz<D>(r, c), kv_row(p, p.k, p.k_sb, p.k_ss, p.k_sh, geo.b, geo.g, j) + c * 8);
+        cp_async16(sV + swz<D>(r, c), kv_row(p, p.v, p.v_sb, p.v_ss, p.v_sh, geo.b, geo.g, j) + c * 8);
+      }
+    }
+  };
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < n_stages) load_stage(s);
+    cp_async_commit();
+  }
+
+  // per-thread rows of the mma fragments: r0 = lane/4, r1 = r0 + 8
+  const int r0 = lane >> 2;
+  int qi_r[2], h_r[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    int P = geo.rt * kDecodeRows + r0 + 8 * e;
+    qi_r[e] = P / p.G;
+    h_r[e] = geo.g * p.G + P % p.G;
+  }
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  float o_acc[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
+  uint32_t qa[D / 16][4];
+  bool q_loaded = false;
+
+  for (int s = 0; s < n_stages; ++s) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    if (s + kStages - 1 < n_stages) load_stage(s + kStages - 1);
+    cp_async_commit();
+    if (!q_loaded) {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        int row = (lane & 7) + 8 * ((lane >> 3) & 1);
+        int chunk = 2 * ks + (lane >> 4);
+        ldsm_x4(sQ + swz<D>(row, chunk), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+      }
+      q_loaded = true;
+    }
+    bool partial, live;
+    const int kj0 = stage_key0(s, partial, live);
+    const int wk0 = kj0 + 16 * warp;  // this warp's first key
+    if (!live || wk0 > geo.jhi || wk0 + 15 < geo.jlo || wk0 >= geo.kv_len) continue;
+    const uint32_t sK = sbase + (s % kStages) * S::kStageBytes;
+    const uint32_t sV = sK + S::kKvBytes;
+
+    // ---- S = Q K^T : 16 rows x 16 keys ----
+    float sc[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      int key = 16 * warp + (lane & 7) + 8 * (lane >> 4);
+      int chunk = 2 * ks + ((lane >> 3) & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(sK + swz<D>(key, chunk), b0, b1, b2, b3);
+      mma_bf16(sc[0], qa[ks], b0, b1);
+      mma_bf16(sc[1], qa[ks], b2, b3);
+    }
+    // ---- logit transform (log2 units) ----
+    const bool plain = !partial && p.softcap == 0.f && p.mask_kind == FA_MASK_NONE;
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int j = wk0 + 8 * n + 2 * (lane & 3) + (e & 1);
+        int rr = e >> 1;
+        if (plain) {
+          sc[n][e] *= p.scale_log2;
+        } else if (qi_r[rr] >= geo.q_len) {
+          sc[n][e] = -INFINITY;  // padding row: never read the mask out of range
+        } else {
+          sc[n][e] = logit_log2(p, sc[n][e], geo.b, h_r[rr], qi_r[rr], j, geo.off, geo.kv_len);
+        }
+      }
+    }
+    // ---- online softmax, -inf guarded ----
+    float alpha[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      float mx = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]), fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      float m_new = fmaxf(m_run[rr], mx);
+      float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+      alpha[rr] = fast_exp2(m_run[rr] - m_ref);
+      m_run[rr] = m_new;
+      float rs = 0.f;
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        sc[n][2 * rr] = fast_exp2(sc[n][2 * rr] - m_ref);
+        sc[n][2 * rr + 1] = fast_exp2(sc[n][2 * rr + 1] - m_ref);
+        rs += sc[n][2 * rr] + sc[n][2 * rr + 1];
+      }
+      l_run[rr] = l_run[rr] * alpha[rr] + rs;
+    }
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      o_acc[n][0] *= alpha[0]; o_acc[n][1] *= alpha[0];
+      o_acc[n][2] *= alpha[1]; o_acc[n][3] *= alpha[1];
+    }
+    // ---- O += P V ----
+    uint32_t pa[4];
+    pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+    pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+    pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+    pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+#pragma unroll
+    for (int dn = 0; dn < D / 16; ++dn) {
+      int key = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1);
+      int chunk = 2 * dn + (lane >> 4);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(sV + swz<D>(key, chunk), b0, b1, b2, b3);
+      mma_bf16(o_acc[2 * dn], pa, b0, b1);
+      mma_bf16(o_acc[2 * dn + 1], pa, b2, b3);
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- merge the 4 warps' (m, l, O) ----
+  float* red_m = reinterpret_cast<float*>(smem + kStages * S::kStageBytes);  // over Q: [4][16]
+  float* red_l = red_m + 4 * kDecodeRows;
+  float* obuf = reinterpret_cast<float*>(smem);  // [4][16][D]
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
+    l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
+  }
+  __syncthreads();  // Q area no longer read
+  if ((lane & 3) == 0) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      red_m[warp * kDecodeRows + r0 + 8 * rr] = m_run[rr];
+      red_l[warp * kDecodeRows + r0 + 8 * rr] = l_run[rr];
+    }
+  }
+  __syncthreads();
+  float f_own[2];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    int row = r0 + 8 * rr;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w * kDecodeRows + row]);
+    float Mref = (M == -INFINITY) ? 0.f : M;
+    f_own[rr] = fast_exp2(m_run[rr] - Mref);
+  }
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    int col = 8 * n + 2 * (lane & 3);
+    float* o0 = obuf + (warp * kDecodeRows + r0) * D + col;
+    float* o1 = obuf + (warp * kDecodeRows + r0 + 8) * D + col;
+    o0[0] = o_acc[n][0] * f_own[0]; o0[1] = o_acc[n][1] * f_own[0];
+    o1[0] = o_acc[n][2] * f_own[1]; o1[1] = o_acc[n][3] * f_own[1];
+  }
+  __syncthreads();
+  // each thread: one row, D/8 consecutive columns
+  {
+    const int row = tid >> 3;            // 16 rows x 8 threads
+    const int c0 = (tid & 7) * (D / 8);
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w * kDecodeRows + row]);
+    float Mref = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) L += red_l[w * kDecodeRows + row] * fast_exp2(red_m[w * kDecodeRows + row] - Mref);
+    const bool empty = !(L > 0.f);
+    const float inv = empty ? 0.f : 1.f / L;
+    const float lse_val = empty ? -INFINITY : (Mref + __log2f(L)) * kLn2;
+    float vals[D / 8];
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) acc += obuf[(w * kDecodeRows + row) * D + c0 + c];
+      vals[c] = acc * inv;
+    }
+    const int P = geo.rt * kDecodeRows + row;
+    if (single) {
+      uint16_t* optr; float* lptr; bool valid;
+      out_ptrs(p, geo, P, optr, lptr, valid);
+      if (valid) {
+#pragma unroll
+        for (int c = 0; c < D / 8; c += 8) {
+          uint4 pk;
+          pk.x = pack_bf16(vals[c + 0], vals[c + 1]);
+          pk.y = pack_bf16(vals[c + 2], vals[c + 3]);
+          pk.z = pack_bf16(vals[c + 4], vals[c + 5]);
+          pk.w = pack_bf16(vals[c + 6], vals[c + 7]);
+          *reinterpret_cast<uint4*>(optr + c0 + c) = pk;
+        }
+        if ((tid & 7) == 0) *lptr = lse_val;
+      }
+    } else {
+      int64_t slot = (item * p.n_splits + split) * kDecodeRows + row;
+      float* po = p.part_o + slot * D + c0;
+#pragma unroll
+      for (int c = 0; c < D / 8; c += 4)
+        *reinterpret_cast<float4*>(po + c) = make_float4(vals[c], vals[c + 1], vals[c + 2], vals[c + 3]);
+      if ((tid & 7) == 0) p.part_lse[slot] = lse_val;
+    }
+  }
+}
+
+// Merge the splits of items that had more than one: LSE = logsumexp of the
+// split LSEs (all -inf -> -inf), O = sum_s exp(LSE_s - LSE) O_s (0 if empty).
+template <int D>
+__global__ void __launch_bounds__(512) combine_kernel(const Params p) {
+  const int64_t item = blockIdx.x;
+  const int count = p.item_count[item];
+  if (count <= p.tiles_per_split) return;
+  const int n_eff = (count + p.tiles_per_split - 1) / p.tiles_per_split;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ItemGeo geo = item_geo(p, item);
+  const int row = warp;  // 16 warps = 16 packed rows
+  uint16_t* optr; float* lptr; bool valid;
+  out_ptrs(p, geo, geo.rt * kDecodeRows + row, optr, lptr, valid);
+  if (!valid) return;
+  const int64_t base = item * p.n_splits * kDecodeRows + row;
+  float M = -INFINITY;
+  for (int s = 0; s < n_eff; ++s) M = fmaxf(M, p.part_lse[base + (int64_t)s * kDecodeRows]);
+  constexpr int kPer = D / 32;
+  float acc[kPer];
+#pragma unroll
+  for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < n_eff; ++s) {
+      float ls = p.part_lse[base + (int64_t)s * kDecodeRows];
+      float w = __expf(ls - M);
+      L += w;
+      const float* po = p.part_o + (base + (int64_t)s * kDecodeRows) * D + lane * kPer;
+#pragma unroll
+      for (int c = 0; c < kPer; ++c) acc[c] += w * po[c];
+    }
+  }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+  for (int c = 0; c < kPer; c += 2)
+    *reinterpret_cast<uint32_t*>(optr + lane * kPer + c) = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
+  if (lane == 0) *lptr = (L > 0.f) ? (M + __logf(L)) : -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_decode_d(const Params& p, cudaStream_t st) {
+  using S = DecodeSmem<D>;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
+  if (e != cudaSuccess) return e;
+  int64_t grid = p.n_items * p.n_splits;
+  decode_kernel<D><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_splits <= 1) return e;
+  combine_kernel<D><<<(unsigned)p.n_items, 512, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const Params& p, cudaStream_t st) {
+  if (p.n_items <= 0) return cudaSuccess;
+  if (p.d == 64) return launch_decode_d<64>(p, st);
+  return launch_decode_d<128>(p, st);
+}
+
+}  // namespace mfa

@@ -1,0 +1,99 @@
+// fa_device.cuh -- device helpers shared by the scheduler and attention kernels:
+// sequence geometry, the pair rules, the logit transform and the error word.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+
+namespace mfa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kRowInf = 0x7fffffff;        // top-k: key never dropped
+constexpr int kRowNever = (int)0x80000000; // top-k: key never kept
+
+__device__ __forceinline__ int seq_qlen(const Params& p, int b) {
+  return p.cu_q ? (p.cu_q[b + 1] - p.cu_q[b]) : p.Sq;
+}
+__device__ __forceinline__ int seq_klen(const Params& p, int b) {
+  return p.cu_k ? (p.cu_k[b + 1] - p.cu_k[b]) : p.Sk;
+}
+
+// Record the first device fault; later ones are dropped.
+__device__ __forceinline__ void record_error(const Params& p, uint32_t code, uint32_t info) {
+  if (atomicCAS(&p.ws->error, 0u, code) == 0u) atomicExch(&p.ws->error_info, info);
+}
+
+// Query-row span [i0, i1] (inclusive, unclipped) of row tile `rt`.  For the
+// decode path rows are packed (query, head-in-group) with `pack` = Hq/Hkv.
+__device__ __forceinline__ void tile_rows(const Params& p, int rt, int& i0, int& i1) {
+  if (p.path == FA_PATH_DECODE) {
+    int P0 = rt * kDecodeRows;
+    i0 = P0 / p.G;
+    i1 = (P0 + kDecodeRows - 1) / p.G;
+  } else {
+    i0 = rt * p.rows_per_tile;
+    i1 = i0 + p.rows_per_tile - 1;
+  }
+}
+
+// The pair rules (bottom-right causal, sliding window, key bound) for one pair.
+__device__ __forceinline__ bool pair_allowed(const Params& p, int i, int j, int off, int kv_len) {
+  bool ok = (j >= 0) & (j < kv_len);
+  if (p.causal) ok &= (j <= i + off);
+  if (p.wl >= 0) ok &= (j >= i + off - p.wl);
+  if (p.wr >= 0) ok &= (j <= i + off + p.wr);
+  return ok;
+}
+
+// Inclusive key range any row of [i0, i1] may see under the pair rules.
+__device__ __forceinline__ void key_range(const Params& p, int i0, int i1, int off, int kv_len,
+                                          int& jlo, int& jhi) {
+  jlo = 0;
+  jhi = kv_len - 1;
+  if (p.causal) jhi = min(jhi, i1 + off);
+  if (p.wl >= 0) jlo = max(jlo, i0 + off - p.wl);
+  if (p.wr >= 0) jhi = min(jhi, i1 + off + p.wr);
+}
+
+// True when every pair of rows [i0, i1] x keys [kj0, kj1] passes the pair rules.
+__device__ __forceinline__ bool tile_all_allowed(const Params& p, int i0, int i1, int kj0, int kj1,
+                                                 int off, int kv_len) {
+  bool ok = (kj1 < kv_len);
+  if (p.causal) ok &= (kj1 <= i0 + off);
+  if (p.wl >= 0) ok &= (kj0 >= i1 + off - p.wl);
+  if (p.wr >= 0) ok &= (kj1 <= i0 + off + p.wr);
+  return ok;
+}
+
+// Full logit transform of one raw dot product `s` for (sequence b, q-head h,
+// query row i, key j), returned in log2 units (x * log2 e), -inf if dropped:
+// scale, soft-cap, pair rules, dense mask or top-k (keep test + bias).
+__device__ __forceinline__ float logit_log2(const Params& p, float s, int b, int h, int i, int j,
+                                            int off, int kv_len) {
+  float x = s * p.scale;
+  if (p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap);
+  if (!pair_allowed(p, i, j, off, kv_len)) return -INFINITY;
+  if (p.mask_kind == FA_MASK_DENSE) {
+    const float* m = p.mask + (int64_t)(p.m_nb > 1 ? b : 0) * p.m_sb +
+                     (int64_t)(p.m_nh > 1 ? h : 0) * p.m_sh + (int64_t)i * p.m_sq +
+                     (int64_t)j * p.m_sk;
+    x += __ldg(m);
+  } else if (p.mask_kind == FA_MASK_TOPK) {
+    int64_t bh = (int64_t)b * p.Hq + h;
+    int e = __ldg(p.topk_e + bh * p.Sk + j);
+    if (!(i < e)) return -INFINITY;
+    x += __ldg(p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh + (int64_t)j * p.z_sk);
+  }
+  return x * kLog2e;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace mfa

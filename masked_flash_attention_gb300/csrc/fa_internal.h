@@ -1,0 +1,83 @@
+// fa_internal.h -- parameters shared by the host planner and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+
+namespace mfa {
+
+constexpr int kKeysPerTile = 128;     // scheduler key tile
+constexpr int kPrefillRows = 128;     // query rows per prefill item (tcgen05 M)
+constexpr int kDecodeRows = 16;       // packed rows per decode item (mma M)
+constexpr int kMaxTopkKeys = 16384;   // top-k preparation keeps all keys of a row in smem
+
+// Workspace header (first 256 bytes of the workspace).
+struct WsHeader {
+  uint32_t error;       // fa_status of the first device fault, 0 = none
+  uint32_t error_info;  // detail of that fault
+  uint32_t pad[2];
+};
+
+// mask summary byte values
+enum : uint8_t { kMaskEmpty = 0, kMaskZero = 1, kMaskMixed = 2 };
+
+// Everything the kernels need; passed by value (fits the 32 KB param space).
+struct Params {
+  // tensors (element strides; head-dim stride is 1)
+  const uint16_t* q; const uint16_t* k; const uint16_t* v;
+  uint16_t* o; float* lse;
+  int64_t q_sb, q_ss, q_sh;
+  int64_t k_sb, k_ss, k_sh;  // paged: k_sb = page stride, k_ss = row-in-page stride
+  int64_t v_sb, v_ss, v_sh;
+  int64_t o_sb, o_ss, o_sh;
+  int64_t lse_sb, lse_sh, lse_ss;
+  const int32_t* cu_q;   // nullable
+  const int32_t* cu_k;   // nullable
+  const int32_t* block_table;  // nullable
+  int64_t bt_stride;
+  int32_t page_size, num_pages;
+
+  int32_t n_seq, Sq, Sk;  // Sq/Sk: fixed lengths, or max lengths for varlen
+  int64_t tot_q, tot_k;   // rows of packed Q / K (varlen), for device-side checks
+  int32_t Hq, Hkv, G, d;
+  float scale;        // natural-log units
+  float scale_log2;   // scale * log2(e)
+  float softcap;      // 0 = off
+  int32_t causal, wl, wr;
+
+  // additive mask
+  int32_t mask_kind;
+  const float* mask; int64_t m_sb, m_sh, m_sq, m_sk; int32_t m_nb, m_nh;
+  const float* z; int64_t z_sb, z_sh, z_sk; int32_t keep_window;
+
+  // scheduler
+  int32_t path;
+  int32_t rows_per_tile, n_row_tiles, n_heads_sched, n_kt;
+  int64_t n_items;
+  int32_t* item_count;   // [n_items]
+  int32_t* item_tiles;   // [n_items][n_kt]
+  unsigned long long* stats;  // [3]
+  uint8_t* mask_summary; // [m_nb][m_nh][n_row_tiles][n_kt]
+  int32_t* topk_e;       // [n_seq][Hq][Sk]: first query row at which key j is dropped
+  int32_t* topk_tile_maxe;  // [n_seq][Hq][n_kt]
+
+  // decode split-KV
+  int32_t n_splits, tiles_per_split;
+  float* part_o;    // [n_items][n_splits][16][d]
+  float* part_lse;  // [n_items][n_splits][16]
+
+  WsHeader* ws;
+  uint32_t debug_flags;
+};
+
+// ---- launchers (defined in the .cu files; all enqueue on `st`) ----
+cudaError_t launch_mask_summary(const Params& p, cudaStream_t st);
+cudaError_t launch_topk_prep(const Params& p, cudaStream_t st);
+cudaError_t launch_classify(const Params& p, cudaStream_t st);
+cudaError_t launch_decode(const Params& p, cudaStream_t st);
+
+}  // namespace mfa

@@ -1,0 +1,290 @@
+// sched.cu -- the tile scheduler: dense-mask summary, dynamic top-k preparation
+// and (query-tile, key-tile) classification into FULL / PARTIAL / EMPTY.
+//
+// EMPTY tiles (every pair masked) are left out of the work list, so no kernel
+// ever computes them: the ExecuTorch pull request 10466 "Summary" notes that
+// a chunk whose mask is entirely -inf could have been skipped outright.
+#include <cuda_runtime.h>
+
+#include "fa_device.cuh"
+
+namespace mfa {
+
+// ---------------------------------------------------------------------------
+// Dense mask summary: one block per (mask batch, mask head, row tile, key tile)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) mask_summary_kernel(const Params p) {
+  const int64_t blk = blockIdx.x;
+  const int kt = (int)(blk % p.n_kt);
+  int64_t t = blk / p.n_kt;
+  const int rt = (int)(t % p.n_row_tiles);
+  t /= p.n_row_tiles;
+  const int mh = (int)(t % p.m_nh);
+  const int mb = (int)(t / p.m_nh);
+  int i0, i1;
+  tile_rows(p, rt, i0, i1);
+  i1 = min(i1, p.Sq - 1);
+  const int kj0 = kt * kKeysPerTile;
+  const int kj1 = min(kj0 + kKeysPerTile, p.Sk) - 1;
+  const int nr = i1 - i0 + 1, nk = kj1 - kj0 + 1;
+  bool any_nonneg = false, any_nonzero = false;
+  if (nr > 0 && nk > 0) {
+    const float* base = p.mask + (int64_t)mb * p.m_sb + (int64_t)mh * p.m_sh;
+    for (int e = threadIdx.x; e < nr * nk; e += blockDim.x) {
+      int r = i0 + e / nk, j = kj0 + e % nk;
+      float m = __ldg(base + (int64_t)r * p.m_sq + (int64_t)j * p.m_sk);
+      any_nonneg |= (m != -INFINITY);
+      any_nonzero |= (m != 0.f);
+    }
+  }
+  int nonneg = __syncthreads_or(any_nonneg);
+  int nonzero = __syncthreads_or(any_nonzero);
+  if (threadIdx.x == 0) {
+    uint8_t cls = !nonneg ? kMaskEmpty : (!nonzero ? kMaskZero : kMaskMixed);
+    p.mask_summary[blk] = cls;
+  }
+}
+
+cudaError_t launch_mask_summary(const Params& p, cudaStream_t st) {
+  int64_t n = (int64_t)p.m_nb * p.m_nh * p.n_row_tiles * p.n_kt;
+  if (n <= 0) return cudaSuccess;
+  mask_summary_kernel<<<(unsigned)n, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Dynamic top-k preparation, one block per (sequence, q-head).
+//
+// For a causal row i the candidates are keys 0..i+off; key j is kept while
+// fewer than keep_window candidates beat it (larger z, or equal z and lower
+// index).  Because the candidate set only grows with i, key j is kept exactly
+// on rows [j - off, e_j), where e_j + off is the keep_window-th smallest index
+// among the keys that beat j (never dropped if fewer than keep_window keys
+// beat it).  Without the causal rule every row sees all keys, so the kept set
+// is the global top keep_window.  This block computes e_j for every key:
+//   1. sort (z descending, index ascending) -> rank of every key;
+//   2. per bucket of 128 consecutive indices, the ascending list of ranks;
+//   3. per key of rank r >= keep_window, walk the buckets counting members of
+//      rank < r (binary search) until keep_window is reached, then find the
+//      exact index inside that bucket.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ordered_desc(float f) {
+  if (f == 0.f) f = 0.f;  // -0 and +0 tie
+  uint32_t u = __float_as_uint(f);
+  u ^= (u & 0x80000000u) ? 0xffffffffu : 0x80000000u;  // ascending order of floats
+  return ~u;                                             // descending
+}
+
+__global__ void __launch_bounds__(1024) topk_prep_kernel(const Params p, int npow2) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint64_t* keys = reinterpret_cast<uint64_t*>(smem);            // [npow2], later int32 R[n]
+  int32_t* rank = reinterpret_cast<int32_t*>(smem + (size_t)npow2 * 8);  // [n]
+  int32_t* R = reinterpret_cast<int32_t*>(smem);
+  const int bh = blockIdx.x;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int n = p.Sk;
+  const int W = p.keep_window;
+  const float* z = p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh;
+  const int tid = threadIdx.x, nt = blockDim.x;
+
+  for (int i = tid; i < npow2; i += nt)
+    keys[i] = (i < n) ? (((uint64_t)ordered_desc(__ldg(z + (int64_t)i * p.z_sk)) << 32) | (uint32_t)i)
+                      : ~0ull;
+  __syncthreads();
+  // bitonic sort, ascending
+  for (int size = 2; size <= npow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = tid; t < (npow2 >> 1); t += nt) {
+        int lo = 2 * t - (t & (stride - 1));
+        int hi = lo + stride;
+        bool up = ((lo & size) == 0);
+        uint64_t a = keys[lo], c = keys[hi];
+        if ((a > c) == up) { keys[lo] = c; keys[hi] = a; }
+      }
+      __syncthreads();
+    }
+  }
+  for (int r = tid; r < n; r += nt) rank[(int)(keys[r] & 0xffffffffu)] = r;
+  __syncthreads();
+  // per-bucket ascending rank lists (R aliases the sort buffer, now free)
+  for (int j = tid; j < n; j += nt) {
+    int c0 = (j / kKeysPerTile) * kKeysPerTile;
+    int c1 = min(c0 + kKeysPerTile, n);
+    int rj = rank[j], pos = 0;
+    for (int jj = c0; jj < c1; ++jj) pos += (rank[jj] < rj);
+    R[c0 + pos] = rj;
+  }
+  __syncthreads();
+  const int off = p.Sk - p.Sq;  // top-k needs a fixed-length batch
+  int32_t* e_out = p.topk_e + (int64_t)bh * n;
+  const int nb = (n + kKeysPerTile - 1) / kKeysPerTile;
+  for (int j = tid; j < n; j += nt) {
+    int r = rank[j];
+    int e;
+    if (r < W) {
+      e = kRowInf;
+    } else if (!p.causal) {
+      e = kRowNever;
+    } else {
+      int need = W, bw = n;
+      for (int c = 0; c < nb; ++c) {
+        int c0 = c * kKeysPerTile, bs = min(kKeysPerTile, n - c0);
+        int lo = 0, hi = bs;  // lower_bound of r in R[c0 .. c0+bs)
+        while (lo < hi) {
+          int mid = (lo + hi) >> 1;
+          if (R[c0 + mid] < r) lo = mid + 1; else hi = mid;
+        }
+        if (lo >= need) {
+          for (int jj = c0; jj < c0 + bs; ++jj) {
+            if (rank[jj] < r && --need == 0) { bw = jj; break; }
+          }
+          break;
+        }
+        need -= lo;
+      }
+      e = bw - off;
+    }
+    e_out[j] = e;
+  }
+  __syncthreads();
+  // per key tile: the largest e (a tile is dead for rows >= max e)
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int kt = warp; kt < p.n_kt; kt += nt / 32) {
+    int mx = kRowNever;
+    for (int j = kt * kKeysPerTile + lane; j < min(n, (kt + 1) * kKeysPerTile); j += 32)
+      mx = max(mx, e_out[j]);
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) p.topk_tile_maxe[(int64_t)bh * p.n_kt + kt] = mx;
+  }
+}
+
+static int next_pow2(int n) {
+  int v = 2;
+  while (v < n) v <<= 1;
+  return v;
+}
+
+size_t topk_prep_smem(int Sk) { return (size_t)next_pow2(Sk) * 8 + (size_t)Sk * 4; }
+
+cudaError_t launch_topk_prep(const Params& p, cudaStream_t st) {
+  int npow2 = next_pow2(p.Sk);
+  size_t smem = topk_prep_smem(p.Sk);
+  cudaError_t e = cudaFuncSetAttribute(topk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  topk_prep_kernel<<<p.n_seq * p.Hq, 1024, smem, st>>>(p, npow2);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Classification: one warp per item (sequence, head, row tile).  Emits the
+// ordered list of non-EMPTY key tiles, each flagged FULL or PARTIAL.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) classify_kernel(const Params p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (item >= p.n_items) return;
+  const int rt = (int)(item % p.n_row_tiles);
+  const int64_t t = item / p.n_row_tiles;
+  const int hs = (int)(t % p.n_heads_sched);
+  const int b = (int)(t / p.n_heads_sched);
+  const int q_len = seq_qlen(p, b), kv_len = seq_klen(p, b);
+  // the lengths come from device memory: check them against the sizes the
+  // host planned for before anything indexes with them
+  bool bad = q_len < 0 || kv_len < 0 || q_len > p.Sq || kv_len > p.Sk;
+  if (p.cu_q) bad |= p.cu_q[b] < 0 || (int64_t)p.cu_q[b + 1] > p.tot_q;
+  if (p.cu_k && !p.block_table) bad |= p.cu_k[b] < 0 || (int64_t)p.cu_k[b + 1] > p.tot_k;
+  if (bad) {
+    if (lane == 0) {
+      p.item_count[item] = -1;  // the attention kernels leave this item alone
+      record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)b);
+    }
+    return;
+  }
+  const int off = kv_len - q_len;
+  int i0, i1;
+  tile_rows(p, rt, i0, i1);
+  int32_t* out = p.item_tiles + item * p.n_kt;
+  const int n_kt_b = (kv_len + kKeysPerTile - 1) / kKeysPerTile;
+  if (i0 >= q_len || kv_len <= 0) {
+    if (lane == 0) {
+      p.item_count[item] = 0;
+      if (i0 < q_len) atomicAdd(&p.stats[2], (unsigned long long)n_kt_b);
+    }
+    return;
+  }
+  i1 = min(i1, q_len - 1);
+  // q-heads covered by this item (decode items pack a group's heads)
+  int h_lo, h_hi;
+  if (p.path == FA_PATH_DECODE) {
+    h_lo = hs * p.G;
+    h_hi = h_lo + p.G - 1;
+  } else {
+    h_lo = h_hi = hs;
+  }
+  const bool no_skip = (p.debug_flags & FA_DEBUG_NO_SKIP) != 0;
+  int kt_lo = 0, kt_hi = n_kt_b - 1;
+  if (!no_skip) {
+    int jlo, jhi;
+    key_range(p, i0, i1, off, kv_len, jlo, jhi);
+    if (jlo > jhi) { kt_lo = 0; kt_hi = -1; }
+    else { kt_lo = jlo / kKeysPerTile; kt_hi = jhi / kKeysPerTile; }
+  }
+  int count = 0;
+  unsigned long long n_full = 0, n_part = 0;
+  for (int base = kt_lo; base <= kt_hi; base += 32) {
+    int kt = base + lane;
+    bool live = kt <= kt_hi;
+    bool partial = true;
+    if (live && !no_skip) {
+      int kj0 = kt * kKeysPerTile, kj1 = kj0 + kKeysPerTile - 1;
+      partial = !tile_all_allowed(p, i0, i1, kj0, kj1, off, kv_len);
+      if (p.mask_kind == FA_MASK_DENSE) {
+        bool any_live = false, any_mixed = false;
+        for (int h = h_lo; h <= h_hi; ++h) {
+          int mb = p.m_nb > 1 ? b : 0, mh = p.m_nh > 1 ? h : 0;
+          uint8_t c = p.mask_summary[(((int64_t)mb * p.m_nh + mh) * p.n_row_tiles + rt) * p.n_kt + kt];
+          any_live |= (c != kMaskEmpty);
+          any_mixed |= (c == kMaskMixed);
+          if (p.m_nh == 1) break;
+        }
+        if (!any_live) live = false;
+        partial |= any_mixed;
+      } else if (p.mask_kind == FA_MASK_TOPK) {
+        bool any_live = false;
+        for (int h = h_lo; h <= h_hi; ++h) {
+          int mx = p.topk_tile_maxe[((int64_t)b * p.Hq + h) * p.n_kt + kt];
+          any_live |= (mx > i0);
+        }
+        if (!any_live) live = false;
+        partial = true;  // the bias is added on every kept pair
+      }
+    }
+    unsigned bal = __ballot_sync(0xffffffffu, live);
+    if (live) {
+      int pos = count + __popc(bal & ((1u << lane) - 1u));
+      out[pos] = (kt << 1) | (partial ? 1 : 0);
+      if (partial) ++n_part; else ++n_full;
+    }
+    count += __popc(bal);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    n_full += __shfl_xor_sync(0xffffffffu, n_full, o);
+    n_part += __shfl_xor_sync(0xffffffffu, n_part, o);
+  }
+  if (lane == 0) {
+    p.item_count[item] = count;
+    atomicAdd(&p.stats[0], n_full);
+    atomicAdd(&p.stats[1], n_part);
+    atomicAdd(&p.stats[2], (unsigned long long)(n_kt_b - count));
+  }
+}
+
+cudaError_t launch_classify(const Params& p, cudaStream_t st) {
+  if (p.n_items <= 0) return cudaSuccess;
+  int64_t blocks = (p.n_items + 7) / 8;
+  classify_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mfa

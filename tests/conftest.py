@@ -8,7 +8,19 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def _ensure_library():
+    # compile libmfa_gb300.so if it is missing or stale (nvcc cross-compiles
+    # without a GPU); loaded by path so the package import is not triggered
+    import importlib.util
+    path = os.path.join(ROOT, "masked_flash_attention_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_mfa_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+
+
 def pytest_configure(config):
+    _ensure_library()
     config.addinivalue_line("markers", "gpu: needs a CUDA device (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long CPU oracle work")
 

@@ -1,0 +1,126 @@
+"""Host-side tests of the C ABI (no GPU work): the library loads, exports every
+function include/fa.h declares, and the planner validates arguments with the
+documented status codes (InfiniTrain pull request 193: an unsupported or
+ill-formed call must report an error, never fall back)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import masked_flash_attention_gb300 as fa
+from masked_flash_attention_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BF = torch.bfloat16
+
+
+def header_functions():
+    txt = open(os.path.join(ROOT, "include", "fa.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*|size_t)\s+(fa_\w+)\s*\(", txt, flags=re.M)))
+
+
+def test_library_exports_every_declared_function():
+    names = header_functions()
+    assert "fa_fwd" in names and len(names) >= 6
+    for n in names:
+        assert hasattr(fa.lib, n), n
+        assert ctypes.cast(getattr(fa.lib, n), ctypes.c_void_p).value
+    assert fa.fa_abi_version() == 1
+    assert fa.fa_status_string(0) == "ok"
+
+
+def T(*shape, dtype=BF):
+    return torch.zeros(*shape, dtype=dtype)
+
+
+def plan(q, k, v, **kw):
+    return fa.fa_fwd_plan(q, k, v, **kw)
+
+
+def test_plan_ok_and_geometry():
+    rc, p = plan(T(4, 1, 32, 128), T(4, 700, 8, 128), T(4, 700, 8, 128), causal=True)
+    assert rc == 0
+    assert p["path"] == _lib.FA_PATH_DECODE
+    assert p["n_heads_sched"] == 8 and p["rows_per_tile"] == 16 and p["n_row_tiles"] == 1
+    assert p["n_k_tiles"] == 6 and p["n_items"] == 32
+    assert p["workspace_bytes"] >= p["off_tiles"] + 32 * 6 * 4
+
+
+@pytest.mark.parametrize("hq,hkv,ok", [(12, 12, True), (32, 8, True), (16, 1, True),
+                                       (12, 5, False), (8, 16, False)])
+def test_head_rule(hq, hkv, ok):
+    rc, _ = plan(T(1, 4, hq, 64), T(1, 8, hkv, 64), T(1, 8, hkv, 64))
+    assert (rc == 0) == ok
+    if not ok:
+        assert rc == _lib.FA_ERR_INVALID_ARG
+
+
+def test_invalid_arguments():
+    q, k = T(1, 4, 2, 64), T(1, 8, 2, 64)
+    E = _lib.FA_ERR_INVALID_ARG
+    assert plan(q.float(), k, k)[0] == E                       # dtype
+    assert plan(T(1, 4, 2, 96), T(1, 8, 2, 96), T(1, 8, 2, 96))[0] == E  # head dim
+    assert plan(q, k, T(1, 9, 2, 64))[0] == E                  # K/V mismatch
+    assert plan(q, k, k, window_left=-2)[0] == E
+    assert plan(q, k, k, softcap=-1.0)[0] == E
+    assert plan(q, k, k, softcap=float("inf"))[0] == E
+    assert plan(q, k, k, scale=float("nan"))[0] == E
+    assert plan(q, T(2, 8, 2, 64), T(2, 8, 2, 64))[0] == E     # batch mismatch
+    qt = T(1, 2, 4, 64).transpose(1, 2)                         # transposed view is fine
+    assert plan(qt, k, k)[0] == 0
+    qs = T(1, 4, 2, 128)[..., :64]                              # head dim must be contiguous
+    assert plan(qs, k, k)[0] == 0 or plan(qs, k, k)[0] == E
+    assert plan(T(1, 4, 2, 64)[..., ::2], k, k)[0] == E         # non-unit head-dim stride
+    assert plan(q, k, k, out=T(1, 4, 2, 64).float())[0] == E    # out dtype
+    assert plan(q, k, k, lse=T(1, 2, 5, dtype=torch.float32))[0] == E  # lse shape
+
+
+def test_mask_rules():
+    q, k = T(2, 4, 2, 64), T(2, 8, 2, 64)
+    m = T(4, 8, dtype=torch.float32)
+    assert plan(q, k, k, mask=m)[0] == 0
+    assert plan(q, k, k, mask=T(1, 2, 4, 8, dtype=torch.float32))[0] == 0
+    assert plan(q, k, k, mask=T(4, 9, dtype=torch.float32))[0] == _lib.FA_ERR_INVALID_ARG
+    assert plan(q, k, k, mask=m.to(BF))[0] == _lib.FA_ERR_INVALID_ARG
+    z = T(2, 2, 8, dtype=torch.float32)
+    assert plan(q, k, k, zero_hold_states=z, keep_window=2, causal=True)[0] == 0
+    assert plan(q, k, k, zero_hold_states=z, keep_window=0)[0] == _lib.FA_ERR_INVALID_ARG
+    assert plan(q, k, k, zero_hold_states=z, keep_window=2,
+                window_left=3)[0] == _lib.FA_ERR_UNSUPPORTED
+    # dense mask with a packed variable-length batch is not implemented
+    qv, kv = T(5, 2, 64), T(9, 2, 64)
+    cu = torch.tensor([0, 5], dtype=torch.int32)
+    cuk = torch.tensor([0, 9], dtype=torch.int32)
+    assert plan(qv, kv, kv, cu_seqlens_q=cu, cu_seqlens_k=cuk, max_seqlen_q=5, max_seqlen_k=9,
+                mask=T(5, 9, dtype=torch.float32))[0] == _lib.FA_ERR_UNSUPPORTED
+
+
+def test_varlen_and_paged_rules():
+    qv, kv = T(7, 4, 128), T(20, 2, 128)
+    cu = torch.tensor([0, 3, 7], dtype=torch.int32)
+    cuk = torch.tensor([0, 12, 20], dtype=torch.int32)
+    ok = dict(cu_seqlens_q=cu, cu_seqlens_k=cuk, max_seqlen_q=4, max_seqlen_k=12)
+    assert plan(qv, kv, kv, **ok)[0] == 0
+    bad = dict(ok, max_seqlen_q=0)
+    assert plan(qv, kv, kv, **bad)[0] == _lib.FA_ERR_INVALID_ARG
+    assert plan(qv, kv, kv, cu_seqlens_q=cu, cu_seqlens_k=torch.tensor([0, 1], dtype=torch.int32),
+                max_seqlen_q=4, max_seqlen_k=12)[0] == _lib.FA_ERR_INVALID_ARG
+    kc = T(6, 16, 2, 128)
+    bt = torch.zeros(2, 3, dtype=torch.int32)
+    assert plan(qv, kc, kc, block_table=bt, **ok)[0] == 0
+    assert plan(qv, kc, kc, block_table=bt, **dict(ok, max_seqlen_k=49))[0] == _lib.FA_ERR_INVALID_ARG
+    # a page table without key counts is an error
+    assert plan(qv, kc, kc, block_table=bt, cu_seqlens_q=cu, max_seqlen_q=4)[0] == _lib.FA_ERR_INVALID_ARG
+
+
+def test_fwd_rejects_cpu_tensors():
+    with pytest.raises(fa.FaError):
+        fa.fa_fwd(T(1, 1, 1, 64), T(1, 2, 1, 64), T(1, 2, 1, 64))
+
+
+def test_empty_problem_plans_no_items():
+    rc, p = plan(T(2, 0, 4, 64), T(2, 5, 4, 64), T(2, 5, 4, 64))
+    assert rc == 0 and p["n_items"] == 0

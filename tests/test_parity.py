@@ -1,0 +1,241 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle on
+the same seeded inputs (small cases element by element; full-size workloads
+on sampled rows)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as O
+from parity_util import DEV, compare, run_gpu, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def check(case, **over):
+    out, lse, _ = run_gpu(case, **over)
+    ref_o, ref_l = run_oracle(case, **over)
+    return compare(out, lse, ref_o, ref_l, case["name"])
+
+
+# ---------------------------------------------------------------------------
+# ExecuTorch worked example: 700-key cache, keys 515..575, -inf first chunk
+# ---------------------------------------------------------------------------
+
+def test_worked_example():
+    check(W.sliding_window_decode(seed=0))
+
+
+def test_worked_example_all_masked_row():
+    case = W.sliding_window_decode(seed=0, all_masked=True)
+    out, lse, _ = run_gpu(case)
+    assert (out == 0).all() and (lse == -np.inf).all()
+
+
+@pytest.mark.parametrize("all_masked", [False, True])
+def test_worked_example_without_skipping(all_masked):
+    """Every key tile computed, including the all -inf ones: the -inf guard of
+    the running softmax alone must keep the result NaN-free and exact."""
+    from masked_flash_attention_gb300 import FA_DEBUG_NO_SKIP
+    case = W.sliding_window_decode(seed=3, all_masked=all_masked)
+    res_out, res_lse, _ = run_gpu(case, debug_flags=FA_DEBUG_NO_SKIP)
+    ref_o, ref_l = run_oracle(case)
+    compare(res_out, res_lse, ref_o, ref_l, "no-skip")
+
+
+# ---------------------------------------------------------------------------
+# Shape / feature sweep (several tiles, ragged tails)
+# ---------------------------------------------------------------------------
+
+SWEEP = [
+    # B, Sq, Sk, Hq, Hkv, d, extra params
+    (1, 1, 1, 1, 1, 64, dict()),
+    (2, 1, 17, 4, 1, 128, dict(causal=True)),
+    (1, 1, 700, 8, 8, 64, dict(causal=True, window_left=60)),
+    (3, 1, 1030, 32, 8, 128, dict(causal=True, softcap=30.0)),
+    (2, 3, 300, 12, 4, 64, dict(causal=True)),
+    (1, 5, 129, 6, 2, 128, dict(causal=True, window_left=7, window_right=2)),
+    (2, 4, 260, 16, 2, 128, dict()),                       # group of 8, not causal
+    (1, 17, 200, 3, 1, 64, dict(causal=True)),             # 17*3 packed rows: 4 row tiles
+    (2, 130, 300, 4, 2, 128, dict(causal=True)),
+    (1, 257, 257, 2, 2, 64, dict(causal=True)),
+    (1, 200, 100, 2, 1, 128, dict(causal=True)),           # q_len > kv_len: empty rows
+    (1, 64, 500, 4, 4, 128, dict(causal=False, window_left=100, window_right=100)),
+    (1, 33, 33, 32, 1, 64, dict(causal=True, softcap=5.0)),  # MQA
+    (2, 2, 4096, 32, 8, 128, dict(causal=True, window_left=1000)),
+]
+
+
+@pytest.mark.parametrize("i", range(len(SWEEP)))
+def test_sweep(i):
+    B, Sq, Sk, Hq, Hkv, d, extra = SWEEP[i]
+    check(W.random_case(100 + i, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, d=d, **extra))
+
+
+def test_custom_scale():
+    check(W.random_case(7, B=1, Sq=9, Sk=300, Hq=4, Hkv=2, d=64, causal=True, scale=0.3))
+
+
+def test_transposed_kv_layout():
+    """Past K/V stored as [B, H, S, d] and passed as a transposed view (a
+    zero-copy metadata change, FastChat pull request 2315)."""
+    c = W.random_case(8, B=2, Sq=3, Sk=333, Hq=8, Hkv=2, d=128, causal=True)
+    kt = c["k"].transpose(1, 2).contiguous().transpose(1, 2)
+    vt = c["v"].transpose(1, 2).contiguous().transpose(1, 2)
+    assert not kt.is_contiguous()
+    c2 = dict(c, k=kt, v=vt)
+    check(c2)
+
+
+def test_deterministic():
+    c = W.random_case(9, B=2, Sq=2, Sk=900, Hq=8, Hkv=2, d=128, causal=True)
+    a = run_gpu(c)
+    b = run_gpu(c)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------------------
+# Dense additive masks
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed,B,Sq,Sk,Hq,Hkv,d,causal", [
+    (0, 1, 1, 700, 1, 1, 64, False),
+    (1, 2, 5, 300, 4, 2, 128, False),
+    (2, 1, 3, 520, 8, 8, 64, True),
+])
+def test_dense_mask(seed, B, Sq, Sk, Hq, Hkv, d, causal):
+    c = W.random_case(seed, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, d=d, causal=causal)
+    m = W.random_dense_mask(seed, Sq, Sk)
+    m[:, :128] = float("-inf")          # an all -inf key tile
+    m[0, :] = float("-inf")             # a fully masked row
+    m[:, 256:384] = 0.0                 # an all-zero tile
+    check(c, mask=m)
+
+
+def test_dense_mask_per_head():
+    c = W.random_case(4, B=2, Sq=2, Sk=260, Hq=4, Hkv=2, d=64)
+    m = torch.stack([torch.stack([W.random_dense_mask(10 * b + h, 2, 260) for h in range(4)])
+                     for b in range(2)])
+    m[1, 2] = float("-inf")
+    check(c, mask=m)
+
+
+# ---------------------------------------------------------------------------
+# Dynamic top-k mask
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed,B,Sq,Sk,H,d,keep,causal,ties", [
+    (0, 1, 4, 4, 1, 64, 2, True, False),        # flash-sparse-attention minimal example
+    (1, 2, 3, 300, 4, 128, 50, True, True),
+    (2, 1, 9, 1000, 2, 64, 300, True, False),
+    (3, 1, 2, 700, 2, 128, 100, False, True),
+    (4, 1, 1, 129, 1, 64, 200, True, False),    # keep_window larger than the row
+])
+def test_topk(seed, B, Sq, Sk, H, d, keep, causal, ties):
+    c = W.random_case(seed, B=B, Sq=Sq, Sk=Sk, Hq=H, Hkv=H, d=d, causal=causal)
+    z = W.random_zero_hold_states(seed, B, H, Sk, ties=ties)
+    check(c, zero_hold_states=z, keep_window=keep)
+
+
+# ---------------------------------------------------------------------------
+# Varlen and paged
+# ---------------------------------------------------------------------------
+
+def _varlen_case(seed, n_seq, max_q, max_k, Hq, Hkv, d, **p):
+    q, k, v, cu_q, cu_k = W.random_varlen(seed, n_seq, max_q, max_k, Hq, Hkv, d)
+    lq = (cu_q[1:] - cu_q[:-1]).max().item()
+    lk = (cu_k[1:] - cu_k[:-1]).max().item()
+    params = W.base_params(scale=d ** -0.5, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+                           max_seqlen_q=max(1, lq), max_seqlen_k=max(1, lk))
+    params.update(p)
+    return dict(name=f"varlen{seed}", q=q, k=k, v=v, params=params), cu_k
+
+
+@pytest.mark.parametrize("seed,n_seq,max_q,max_k,Hq,Hkv,d,extra", [
+    (0, 5, 3, 600, 8, 2, 128, dict(causal=True)),
+    (1, 4, 1, 300, 4, 4, 64, dict(causal=True, window_left=50, softcap=10.0)),
+    (2, 3, 20, 200, 2, 1, 128, dict(causal=False)),
+    (3, 6, 2, 64, 4, 2, 64, dict(causal=True)),         # some sequences may be empty
+])
+def test_varlen(seed, n_seq, max_q, max_k, Hq, Hkv, d, extra):
+    case, _ = _varlen_case(seed, n_seq, max_q, max_k, Hq, Hkv, d, **extra)
+    check(case)
+
+
+@pytest.mark.parametrize("page", [16, 1, 64])
+def test_paged(page):
+    case, cu_k = _varlen_case(11, 4, 2, 500, 8, 2, 128, causal=True, softcap=30.0)
+    kc, vc, bt = W.paginate(case["k"], case["v"], cu_k, page, seed=page)
+    paged = dict(case, k=kc, v=vc)
+    paged["params"] = dict(case["params"], block_table=bt)
+    out, lse, _ = run_gpu(paged)
+    ref_o, ref_l = run_oracle(case)   # same sequences, contiguous
+    compare(out, lse, ref_o, ref_l, "paged")
+
+
+def test_paged_decode_workload_small():
+    c = W.paged_varlen_decode(seed=1, n_seq=8, max_len=2000)
+    check(c)
+
+
+def test_bad_page_index_is_reported():
+    """An out-of-range page index is found on the device, recorded in the
+    error word and skipped (no fault): the caller sees FA_ERR_DEVICE_BOUNDS."""
+    import masked_flash_attention_gb300 as fa
+    case, cu_k = _varlen_case(12, 2, 1, 100, 4, 2, 64, causal=True)
+    kc, vc, bt = W.paginate(case["k"], case["v"], cu_k, 16, seed=1)
+    bt[0, 0] = kc.shape[0] + 5
+    p = dict(case["params"], block_table=bt)
+    out, lse, ws = fa.fa_fwd(case["q"].to(DEV), kc.to(DEV), vc.to(DEV), **to_dev(p))
+    rc, info = fa.fa_check_device_error(ws)
+    assert rc == fa._lib.FA_ERR_DEVICE_BOUNDS and info == kc.shape[0] + 5
+    assert fa.fa_check_device_error(ws)[0] == 0  # cleared
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, sampled rows
+# ---------------------------------------------------------------------------
+
+def _sampled(case, n_rows=48, seed=0):
+    """Run the GPU on the whole workload; compare sampled (b, h, i) rows with
+    the oracle evaluated row by row."""
+    out, lse, _ = run_gpu(case)
+    p = dict(case["params"])
+    q, k, v = case["q"], case["k"], case["v"]
+    B, Sq, Hq, d = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    rng = np.random.default_rng(seed)
+    rows = [(int(rng.integers(B)), int(rng.integers(Hq)), int(rng.integers(Sq))) for _ in range(n_rows)]
+    rows += [(0, 0, 0), (B - 1, Hq - 1, Sq - 1)]
+    ro, rl, go, gl = [], [], [], []
+    kw = {kk: p[kk] for kk in ("causal", "window_left", "window_right", "softcap", "keep_window")}
+    for b, h, i in rows:
+        Sk = k.shape[1]
+        z = None if p["zero_hold_states"] is None else p["zero_hold_states"][b, h].numpy()
+        o_, l_ = O.attention_rows(q[b, i:i + 1, h].double().numpy(), k[b, :, h // G].double().numpy(),
+                                  v[b, :, h // G].double().numpy(), [i], Sq, Sk, scale=p["scale"],
+                                  z=z, **kw)
+        ro.append(o_[0]); rl.append(l_[0]); go.append(out[b, i, h]); gl.append(lse[b, h, i])
+    return compare(np.array(go)[None, :, None, :], np.array(gl)[None, None, :],
+                   np.array(ro)[None, :, None, :], np.array(rl)[None, None, :], case["name"])
+
+
+def test_causal_prefill_past_kv_full():
+    _sampled(W.causal_prefill_past_kv(seed=0))
+
+
+def test_gpt2_small_layer_full():
+    _sampled(W.gpt2_small_layer(seed=0))
+
+
+def test_llama3_8b_layer_full():
+    _sampled(W.llama3_8b_layer(seed=0), n_rows=32)
+
+
+def test_dynamic_topk_full():
+    _sampled(W.dynamic_topk(seed=0), n_rows=24)
+
+
+def test_paged_varlen_decode_full():
+    check(W.paged_varlen_decode(seed=0))

@@ -1,0 +1,173 @@
+"""GPU tests of the tile scheduler: the work list it leaves in the workspace
+against a classification recomputed on the CPU from the oracle's logits;
+EMPTY tiles never appear (ExecuTorch pull request 10466 "Summary": a fully
+-inf chunk need not be computed); top-k kept sets match the oracle exactly
+(flash-sparse-attention issue 11 "Current Status": mask max/mean difference
+0.0 and position match 1.0)."""
+import numpy as np
+import pytest
+import torch
+
+import masked_flash_attention_gb300 as fa
+import workloads as W
+from oracle import attention as O
+from parity_util import DEV, run_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def worklist(case, **over):
+    p = dict(case["params"])
+    p.update(over)
+    rc, plan = fa.fa_fwd_plan(case["q"], case["k"], case["v"], **p)
+    assert rc == 0
+    out, lse, ws = run_gpu(case, **over)
+    w = ws.cpu()
+    n, nk = plan["n_items"], plan["n_k_tiles"]
+    counts = w[plan["off_counts"]:plan["off_counts"] + 4 * n].view(torch.int32).numpy()
+    tiles = w[plan["off_tiles"]:plan["off_tiles"] + 4 * n * nk].view(torch.int32).numpy().reshape(n, nk)
+    stats = w[plan["off_stats"]:plan["off_stats"] + 24].view(torch.int64).numpy()
+    return plan, counts, tiles, stats, ws
+
+
+def oracle_classes(case, plan, **over):
+    """[n_items, n_k_tiles] classes from the oracle's logit matrices: EMPTY
+    if every pair of the item's rows x the tile's keys is -inf; FULL if none
+    is and no additive term is present; else PARTIAL."""
+    p = dict(case["params"])
+    p.update(over)
+    q, k, v = case["q"], case["k"], case["v"]
+    B, Sq, Hq, d = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    KT = plan["keys_per_tile"]
+    n_rt, nk = plan["n_row_tiles"], plan["n_k_tiles"]
+    decode = plan["path"] == fa._lib.FA_PATH_DECODE
+    cls = np.zeros((plan["n_items"], nk), dtype=np.int32)
+    z = p.get("zero_hold_states")
+    m = p.get("mask")
+    for b in range(B):
+        for hs in range(plan["n_heads_sched"]):
+            heads = range(hs * G, hs * G + G) if decode else [hs]
+            X = []
+            for h in heads:
+                x = O.logits_rows(q[b, :, h].double().numpy(), k[b, :, h // G].double().numpy(),
+                                  np.arange(Sq), Sq, Sk, scale=p["scale"] or d ** -0.5,
+                                  causal=p["causal"], window_left=p["window_left"],
+                                  window_right=p["window_right"], softcap=p["softcap"],
+                                  mask_rows=None if m is None else (m.numpy() if m.dim() == 2 else m[b, h].numpy()),
+                                  z=None if z is None else z[b, h].numpy(), keep_window=p["keep_window"])
+                X.append(x)
+            X = np.stack(X)
+            for rt in range(n_rt):
+                if decode:
+                    i0, i1 = rt * 16 // G, (rt * 16 + 15) // G
+                else:
+                    i0, i1 = rt * plan["rows_per_tile"], (rt + 1) * plan["rows_per_tile"] - 1
+                i1 = min(i1, Sq - 1)
+                item = (b * plan["n_heads_sched"] + hs) * n_rt + rt
+                for kt in range(nk):
+                    blk = X[:, i0:i1 + 1, kt * KT:min(Sk, (kt + 1) * KT)]
+                    if blk.size == 0 or np.all(blk == -np.inf):
+                        cls[item, kt] = 0
+                    elif np.all(np.isfinite(blk)) and z is None and (m is None or True):
+                        cls[item, kt] = 1
+                    else:
+                        cls[item, kt] = 2
+    return cls
+
+
+def gpu_classes(plan, counts, tiles):
+    cls = np.zeros((plan["n_items"], plan["n_k_tiles"]), dtype=np.int32)
+    for it in range(plan["n_items"]):
+        seen = []
+        for e in tiles[it, :counts[it]]:
+            kt, part = int(e) >> 1, int(e) & 1
+            seen.append(kt)
+            cls[it, kt] = 2 if part else 1
+        assert seen == sorted(set(seen)), "tiles must be listed once, in key order"
+    return cls
+
+
+def test_worked_example_schedules_one_partial_tile():
+    case = W.sliding_window_decode(seed=0)
+    plan, counts, tiles, stats, _ = worklist(case)
+    assert plan["n_items"] == 1 and plan["n_k_tiles"] == 6
+    assert counts[0] == 1 and tiles[0, 0] == (4 << 1) | 1   # keys 512..639 hold 515..575
+    assert tuple(stats) == (0, 1, 5)
+    # all -inf row: nothing scheduled at all
+    plan, counts, tiles, stats, _ = worklist(W.sliding_window_decode(seed=0, all_masked=True))
+    assert counts[0] == 0 and tuple(stats) == (0, 0, 6)
+
+
+def test_no_skip_schedules_everything():
+    case = W.sliding_window_decode(seed=0)
+    plan, counts, tiles, stats, _ = worklist(case, debug_flags=fa.FA_DEBUG_NO_SKIP)
+    assert counts[0] == 6 and tuple(stats) == (0, 6, 0)
+
+
+@pytest.mark.parametrize("seed,B,Sq,Sk,Hq,Hkv,d,extra", [
+    (0, 2, 3, 700, 8, 2, 64, dict(causal=True, window_left=200)),
+    (1, 1, 9, 520, 4, 4, 64, dict(causal=True)),
+    (2, 1, 5, 900, 6, 3, 128, dict(causal=False, window_left=130, window_right=0)),
+])
+def test_geometric_classes_exact(seed, B, Sq, Sk, Hq, Hkv, d, extra):
+    case = W.random_case(seed, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, d=d, **extra)
+    plan, counts, tiles, stats, _ = worklist(case)
+    got = gpu_classes(plan, counts, tiles)
+    want = oracle_classes(case, plan)
+    assert np.array_equal(got == 0, want == 0)           # EMPTY set exact
+    assert np.all(want[got == 1] == 1)                    # FULL only where nothing is masked
+
+
+def test_dense_mask_classes_exact():
+    case = W.random_case(5, B=1, Sq=2, Sk=900, Hq=2, Hkv=2, d=64)
+    m = torch.zeros(2, 900)
+    m[:, :256] = float("-inf")
+    m[:, 600:700] = torch.randn(2, 100)
+    m[1, 768:] = float("-inf")
+    plan, counts, tiles, stats, _ = worklist(case, mask=m)
+    got = gpu_classes(plan, counts, tiles)
+    want = oracle_classes(case, plan, mask=m)
+    assert np.array_equal(got == 0, want == 0)
+    # the all-zero tiles stay FULL, the mixed ones are PARTIAL
+    assert got[0, 2] == 1 and got[0, 4] == 2 and got[0, 5] == 2
+
+
+def test_topk_kept_sets_exact(golden):
+    g = golden("fsa_mask_agreement.json")
+    for seed, Sq, Sk, keep, causal, ties in [(0, 300, 300, 40, True, True), (1, 64, 500, 100, True, False),
+                                             (2, 7, 260, 30, False, True), (3, 4, 4, 2, True, False)]:
+        case = W.random_case(seed, B=1, Sq=Sq, Sk=Sk, Hq=2, Hkv=2, d=64, causal=causal)
+        z = W.random_zero_hold_states(seed, 1, 2, Sk, ties=ties)
+        plan, counts, tiles, stats, ws = worklist(case, zero_hold_states=z, keep_window=keep)
+        e = ws.cpu()[plan["off_topk_e"]:plan["off_topk_e"] + 4 * 2 * Sk].view(torch.int32).numpy()
+        e = e.reshape(2, Sk).astype(np.int64)
+        off = Sk - Sq
+        n_match = n_total = 0
+        for h in range(2):
+            ok = O.allowed_pairs(np.arange(Sq), np.arange(Sk), Sq, Sk, causal=causal)
+            for i in range(Sq):
+                want = np.zeros(Sk, bool)
+                want[O.topk_kept_row(z[0, h].numpy(), ok[i], keep)] = True
+                got = ok[i] & (i < e[h])
+                n_match += int((got == want).sum())
+                n_total += Sk
+        assert n_match / n_total == g["position_match"]
+        # EMPTY tiles are a subset of the truly empty ones, and no kept pair is lost
+        got = gpu_classes(plan, counts, tiles)
+        want = oracle_classes(case, plan, zero_hold_states=z, keep_window=keep)
+        assert np.all(want[got == 0] == 0)
+
+
+def test_inconsistent_lengths_are_reported():
+    """A sequence longer than the max_seqlen the plan was sized for is caught on
+    the device (no out-of-range access): its item is skipped and the error word
+    says FA_ERR_DEVICE_BOUNDS."""
+    q, k, v, cu_q, cu_k = W.random_varlen(3, 2, 2, 300, 4, 2, 64, min_q=1, min_k=1)
+    lk = int((cu_k[1:] - cu_k[:-1]).max())
+    p = W.base_params(cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=2, max_seqlen_k=max(1, lk - 1),
+                      causal=True)
+    out, lse, ws = fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), **to_dev(p))
+    rc, info = fa.fa_check_device_error(ws)
+    assert rc == fa._lib.FA_ERR_DEVICE_BOUNDS

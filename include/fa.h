@@ -209,6 +209,37 @@ int fa_fwd_workspace_size(const fa_tensor* q, const fa_tensor* k, const fa_tenso
                           int32_t window_left, int32_t window_right, float softcap,
                           float scale, int32_t causal, const fa_opts* opts, size_t* bytes);
 
+/* Size of the static device scratch used by fa_fwd_noalloc (32 MiB). */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* fa_fwd for callers that cannot allocate device memory (the pages this
+ * library follows have no counterpart of it).  Some callers may not call
+ * cudaMalloc at all: allocator-free inference runtimes that only hand out
+ * pre-sized input/output buffers, plugins whose host forbids device
+ * allocations after start-up, latency paths that must not touch an allocator.
+ * This entry point takes the same arguments as fa_fwd, except that
+ * opts->workspace and opts->workspace_bytes are ignored: the scratch lives in
+ * a static device array of FA_NOALLOC_SCRATCH_BYTES that the library owns and
+ * that every GPU loading the library holds until the process exits.  It calls
+ * no allocating routine.
+ *   - A problem whose scratch need (fa_fwd_workspace_size) exceeds
+ *     FA_NOALLOC_SCRATCH_BYTES is rejected with FA_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address (a
+ *     one-time set-up per device, done with that device current); make that
+ *     first call before any stream capture.
+ *   - All calls share the array: calls that overlap on the GPU (other
+ *     streams, other threads) race on it; serialise them.
+ *   - Each call clears the array's device error word before its kernels run,
+ *     so faults recorded by the kernels (a bad page index, inconsistent
+ *     sequence lengths) are not reported to the caller; use fa_fwd with a
+ *     workspace and fa_check_device_error when that matters. */
+int fa_fwd_noalloc(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
+                   const fa_tensor* out, const fa_tensor* lse,
+                   const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+                   const fa_tensor* block_table, const fa_mask* mask,
+                   int32_t window_left, int32_t window_right, float softcap, float scale,
+                   int32_t causal, const fa_opts* opts);
+
 /* Synchronises `stream`, then reads and clears the device error word at the
  * start of `workspace`: FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_DEVICE_BOUNDS.
  * `info` (nullable) receives the first recorded detail (e.g. the bad page). */

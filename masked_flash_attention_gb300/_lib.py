@@ -235,3 +235,26 @@ def fa_check_device_error(workspace, stream=None):
     st = stream if stream is not None else torch.cuda.current_stream().cuda_stream
     rc = lib.fa_check_device_error(st, workspace.data_ptr(), ctypes.byref(info))
     return rc, info.value
+
+
+def fa_fwd_noalloc(q, k, v, *, out, lse, cu_seqlens_q=None, cu_seqlens_k=None, block_table=None,
+                   mask=None, zero_hold_states=None, keep_window=0, window_left=-1, window_right=-1,
+                   softcap=0.0, scale=None, causal=False, max_seqlen_q=None, max_seqlen_k=None,
+                   stream=None, debug_flags=0, **_):
+    """fa_fwd_noalloc of the C ABI: the forward pass for callers that may not
+    allocate device memory.  ``out`` and ``lse`` are caller-provided; the
+    library's static device scratch replaces the workspace, so nothing is
+    allocated by this call.  Raises FaError on a non-zero status (a problem
+    too large for the static scratch gives FA_ERR_WORKSPACE)."""
+    fn = lib.fa_fwd_noalloc
+    fn.argtypes = _ARGS
+    fn.restype = ctypes.c_int
+    opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                     debug_flags=debug_flags)
+    args, keep = _args(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask,
+                       zero_hold_states, keep_window, window_left, window_right, softcap,
+                       scale or 0.0, causal, opts)
+    rc = fn(*args)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_noalloc")
+    return out, lse

@@ -230,11 +230,28 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   P.debug_flags = opts->debug_flags;
 
   // ---- path and tile geometry ----
+  // Few query rows per K/V head (decode): the 16-row split-KV kernel.  Many
+  // rows: the tcgen05 kernel, which reads Q/K/V through TMA tensor maps and so
+  // needs non-zero strides on every dimension of extent > 1 and a contiguous
+  // (non-paged) K/V.
   const int G = P.G;
-  P.path = FA_PATH_DECODE;
-  P.rows_per_tile = kDecodeRows;
-  P.n_heads_sched = (int32_t)Hkv;
-  P.n_row_tiles = ceil_div(Sq * G, kDecodeRows);
+  bool tma_ok = !paged;
+  if (!varlen_q && n_seq > 1 && P.q_sb == 0) tma_ok = false;
+  if (!varlen_k && !paged && n_seq > 1 && (P.k_sb == 0 || P.v_sb == 0)) tma_ok = false;
+  if ((Hq > 1 && P.q_sh == 0) || (Hkv > 1 && (P.k_sh == 0 || P.v_sh == 0))) tma_ok = false;
+  if (P.q_ss == 0 || P.k_ss == 0 || P.v_ss == 0) tma_ok = false;
+  const bool prefill = tma_ok && Sq * (int64_t)G > 64;
+  if (prefill) {
+    P.path = FA_PATH_PREFILL;
+    P.rows_per_tile = kPrefillRows;
+    P.n_heads_sched = (int32_t)Hq;
+    P.n_row_tiles = ceil_div(Sq, kPrefillRows);
+  } else {
+    P.path = FA_PATH_DECODE;
+    P.rows_per_tile = kDecodeRows;
+    P.n_heads_sched = (int32_t)Hkv;
+    P.n_row_tiles = ceil_div(Sq * G, kDecodeRows);
+  }
   P.n_kt = ceil_div(Sk, kKeysPerTile);
   P.n_items = n_seq * (int64_t)P.n_heads_sched * P.n_row_tiles;
   if (Sq == 0 || n_seq == 0) P.n_items = 0;
@@ -391,7 +408,7 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_
   if (e == cudaSuccess) e = launch_classify(P, st);
   if (e == cudaSuccess && opts->event_begin)
     e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_begin), st);
-  if (e == cudaSuccess) e = launch_decode(P, st);
+  if (e == cudaSuccess) e = (P.path == FA_PATH_PREFILL) ? launch_prefill(P, st) : launch_decode(P, st);
   if (e == cudaSuccess && opts->event_end)
     e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_end), st);
   if (e != cudaSuccess) {

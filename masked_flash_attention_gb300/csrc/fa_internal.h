@@ -79,5 +79,6 @@ cudaError_t launch_mask_summary(const Params& p, cudaStream_t st);
 cudaError_t launch_topk_prep(const Params& p, cudaStream_t st);
 cudaError_t launch_classify(const Params& p, cudaStream_t st);
 cudaError_t launch_decode(const Params& p, cudaStream_t st);
+cudaError_t launch_prefill(const Params& p, cudaStream_t st);
 
 }  // namespace mfa

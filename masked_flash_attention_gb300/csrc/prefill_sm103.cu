@@ -1,0 +1,592 @@
+// prefill_sm103.cu -- masked flash-attention forward for many query rows on
+// the 5th-generation tensor cores of sm_103a (tcgen05 + TMEM + TMA).
+//
+// The method is the tiled, online-softmax attention of the ExecuTorch pull
+// request 10466 "Summary": q@k is cut into chunks along both the query and the
+// key dimension, the softmax is accumulated progressively and rescaled at the
+// end; an all -inf chunk must not poison the running values.  Chunks whose
+// every pair is masked are not computed at all: the scheduler (sched.cu) left
+// them out of each item's key-tile list.
+//
+// CTA = two 128-row query sub-tiles that read the same K/V head: two q-heads
+// of one grouped-query group (InfiniTrain pull request 193 "Transformer 接入":
+// the kernel shares the K/V heads instead of expanding them) or, with one
+// q-head per K/V head, two consecutive row tiles.  Every K/V tile is loaded
+// once by TMA for both.  The two key-tile lists are merged; a sub-tile skips
+// the tiles that are not on its own list.
+//
+// Warp roles (12 warps = 3 warpgroups):
+//   warp 0      TMA producer: Q once, then K/V tiles through an NS-stage ring
+//   warp 1      MMA issuer (one thread) and TMEM owner
+//   warps 2..3  idle
+//   warps 4..7  softmax warpgroup for sub-tile 0, warps 8..11 for sub-tile 1
+// Each softmax thread walks its row of S twice, 64 columns at a time: pass 1
+// finds the row max (PARTIAL tiles apply the pair rules and additive terms
+// and write the final logits back to TMEM), pass 2 exponentiates, sums and
+// stores P as bf16 over the first 64 columns.
+// TMEM (512 columns): S_t = Q_t K^T in columns [128 t, 128 t + 128), fp32;
+// P_t (bf16, two per column) overwrites the first 64 of them; O_t in
+// [256 + D t, 256 + D t + D).  Per key tile j the MMA thread issues
+//   PV_0(j-1), QK_0(j), PV_1(j-1), QK_1(j)
+// so that sub-tile 0's softmax of tile j overlaps sub-tile 1's MMAs and vice
+// versa.  Each softmax thread owns one query row (32x32b TMEM loads), so the
+// row max and row sum need no cross-lane reduction.  The running max is the
+// exponent reference and is only raised when the row max exceeds it by more
+// than 2^8 (in log2 units), so O in TMEM is rarely rescaled.  A fully masked
+// row keeps reference -inf, exponentiates against 0, and ends with l = 0:
+// O = 0, LSE = -inf.
+//
+// Every mbarrier wait is bounded (1 s); on a time-out the kernel records
+// FA_ERR_DEVICE_TIMEOUT in the workspace error word, every role stops, in-flight
+// MMAs are drained and TMEM is released before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <mutex>
+
+#include "fa_device.cuh"
+#include "tc_sm103.cuh"
+
+namespace mfa {
+
+namespace {
+
+constexpr int kPrefillThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct PCfg {
+  static constexpr int NS = (D == 128) ? 2 : 4;          // K/V stages
+  static constexpr int kTileBytes = 128 * D * 2;          // one 128-row bf16 tile
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + NS * kTileBytes;
+  static constexpr int kBarOff = kVOff + NS * kTileBytes;
+  static constexpr int kSmem = kBarOff + 256 + 1024;      // barriers + 1024-byte alignment slack
+  static constexpr uint32_t kOCol = 256;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+struct SubTile {
+  bool valid;   // sequence passed the scheduler's checks and the sub-tile exists
+  int h, rt, count;
+  const int32_t* tiles;
+};
+
+// Merged walk over two ascending key-tile lists.
+struct Merge {
+  const int32_t* l0;
+  const int32_t* l1;
+  int c0, c1, i0, i1;
+  __device__ __forceinline__ void init(const SubTile (&st)[2]) {
+    l0 = st[0].tiles; l1 = st[1].tiles;
+    c0 = st[0].valid ? st[0].count : 0;
+    c1 = st[1].valid ? st[1].count : 0;
+    i0 = i1 = 0;
+  }
+  __device__ __forceinline__ bool next(int& kt, bool& in0, bool& in1, bool& part0, bool& part1) {
+    int e0 = i0 < c0 ? __ldg(l0 + i0) : 0x7ffffffe;
+    int e1 = i1 < c1 ? __ldg(l1 + i1) : 0x7ffffffe;
+    int k0 = e0 >> 1, k1 = e1 >> 1;
+    kt = min(k0, k1);
+    if (kt >= 0x3fffffff) return false;
+    in0 = (k0 == kt); in1 = (k1 == kt);
+    part0 = in0 && (e0 & 1); part1 = in1 && (e1 & 1);
+    if (in0) ++i0;
+    if (in1) ++i1;
+    return true;
+  }
+};
+
+// CTA -> (sequence, K/V head, two sub-tiles); longest query tiles first.
+__device__ __forceinline__ void cta_work(const Params& p, int cta, int& b, int& g, SubTile (&st)[2]) {
+  const int G = p.G, nrt = p.n_row_tiles;
+  int h[2], rt[2];
+  bool present[2];
+  if (G >= 2) {
+    const int PP = (G + 1) / 2;
+    const int per = p.n_seq * p.Hkv * PP;
+    const int r_t = nrt - 1 - cta / per;
+    int r = cta % per;
+    const int pp = r % PP;
+    r /= PP;
+    g = r % p.Hkv;
+    b = r / p.Hkv;
+    for (int t = 0; t < 2; ++t) {
+      int hh = 2 * pp + t;
+      present[t] = hh < G;
+      h[t] = g * G + (present[t] ? hh : 0);
+      rt[t] = r_t;
+    }
+  } else {
+    const int NR2 = (nrt + 1) / 2;
+    const int per = p.n_seq * p.Hq;
+    const int rp = NR2 - 1 - cta / per;
+    const int r = cta % per;
+    const int hq = r % p.Hq;
+    b = r / p.Hq;
+    g = hq;
+    for (int t = 0; t < 2; ++t) {
+      rt[t] = 2 * rp + t;
+      present[t] = rt[t] < nrt;
+      h[t] = hq;
+    }
+  }
+  for (int t = 0; t < 2; ++t) {
+    st[t].h = h[t];
+    st[t].rt = rt[t];
+    st[t].valid = false;
+    st[t].count = 0;
+    st[t].tiles = nullptr;
+    if (present[t]) {
+      int64_t item = ((int64_t)b * p.Hq + h[t]) * p.n_row_tiles + rt[t];
+      int c = p.item_count[item];
+      st[t].valid = c >= 0;
+      st[t].count = c > 0 ? c : 0;
+      st[t].tiles = p.item_tiles + item * p.n_kt;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag, uint32_t where) {
+  if (!*abort_flag) {
+    *abort_flag = 1;
+    record_error(p, FA_ERR_DEVICE_TIMEOUT, where);
+  }
+}
+
+// Output pointers of query row i (within its sequence) for q-head h.
+__device__ __forceinline__ void row_out(const Params& p, int b, int h, int i, uint16_t*& optr, float*& lptr) {
+  int64_t qrow = p.cu_q ? (int64_t)p.cu_q[b] + i : (int64_t)i;
+  int64_t bo = p.cu_q ? 0 : (int64_t)b;
+  optr = p.o + bo * p.o_sb + qrow * p.o_ss + (int64_t)h * p.o_sh;
+  lptr = p.lse + bo * p.lse_sb + (int64_t)h * p.lse_sh + qrow * p.lse_ss;
+}
+
+template <int D>
+__device__ __forceinline__ void write_empty_row(const Params& p, int b, int h, int i) {
+  uint16_t* optr;
+  float* lptr;
+  row_out(p, b, h, i, optr, lptr);
+#pragma unroll
+  for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(optr + c) = make_uint4(0, 0, 0, 0);
+  *lptr = -INFINITY;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPrefillThreads, 1)
+    prefill_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv) {
+  using C = PCfg<D>;
+  constexpr int NS = C::NS;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  int b, g;
+  SubTile st[2];
+  cta_work(p, blockIdx.x, b, g, st);
+  if (!st[0].valid && !st[1].valid) return;
+  const int q_len = seq_qlen(p, b), kv_len = seq_klen(p, b);
+  const int off = kv_len - q_len;
+
+  // Nothing scheduled for either sub-tile: only zero rows to write.
+  if (st[0].count == 0 && st[1].count == 0) {
+    if (warp >= 4) {
+      const int t = (warp - 4) >> 2;
+      const int i = st[t].rt * 128 + 32 * (warp & 3) + lane;
+      if (st[t].valid && i < q_len) write_empty_row<D>(p, b, st[t].h, i);
+    }
+    return;
+  }
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NS;
+  uint64_t* kv_empty = v_full + NS;
+  uint64_t* s_full = kv_empty + NS;   // [2]
+  uint64_t* p_full = s_full + 2;      // [2]
+  uint64_t* o_final = p_full + 2;     // [2]
+  uint64_t* mma_done = o_final + 2;   // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (tid == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      tc::mbar_init(k_full + s, 1);
+      tc::mbar_init(v_full + s, 1);
+      tc::mbar_init(kv_empty + s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      tc::mbar_init(s_full + t, 1);
+      tc::mbar_init(p_full + t, 128);
+      tc::mbar_init(o_final + t, 1);
+    }
+    tc::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+
+  const int kv_row0 = p.cu_k ? p.cu_k[b] : 0;
+  const int kv_b = p.cu_k ? 0 : b;
+  const int q_row0 = p.cu_q ? p.cu_q[b] : 0;
+  const int q_b = p.cu_q ? 0 : b;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tmq);
+      tc::tma_prefetch_desc(&tmk);
+      tc::tma_prefetch_desc(&tmv);
+      uint32_t qbytes = 0;
+      for (int t = 0; t < 2; ++t)
+        if (st[t].count > 0) qbytes += C::kTileBytes;
+      tc::mbar_arrive_expect_tx(q_full, qbytes);
+      for (int t = 0; t < 2; ++t) {
+        if (st[t].count == 0) continue;
+        unsigned char* dst = smem + C::kQOff + t * C::kTileBytes;
+        for (int c = 0; c < D / 64; ++c)
+          tc::tma_load_4d(dst + c * 16384, &tmq, q_full, c * 64, st[t].h, q_row0 + st[t].rt * 128, q_b);
+      }
+      Merge m;
+      m.init(st);
+      int kt, j = 0;
+      bool in0, in1, pa0, pa1;
+      while (m.next(kt, in0, in1, pa0, pa1)) {
+        const int s = j % NS;
+        if (j >= NS && !tc::mbar_wait(kv_empty + s, ((j / NS) - 1) & 1, abort_flag)) {
+          fail(p, abort_flag, 1);
+          break;
+        }
+        unsigned char* dk = smem + C::kKOff + s * C::kTileBytes;
+        unsigned char* dv = smem + C::kVOff + s * C::kTileBytes;
+        tc::mbar_arrive_expect_tx(k_full + s, C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tc::tma_load_4d(dk + c * 16384, &tmk, k_full + s, c * 64, g, kv_row0 + kt * 128, kv_b);
+        tc::mbar_arrive_expect_tx(v_full + s, C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tc::tma_load_4d(dv + c * 16384, &tmv, v_full + s, c * 64, g, kv_row0 + kt * 128, kv_b);
+        ++j;
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA can exit
+        const int first = j > NS ? j - NS : 0;
+        for (int jj = first; jj < j; ++jj) {
+          tc::mbar_wait_drain(k_full + jj % NS, (jj / NS) & 1, 100000000ull);
+          tc::mbar_wait_drain(v_full + jj % NS, (jj / NS) & 1, 100000000ull);
+        }
+        tc::mbar_wait_drain(q_full, 0, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
+      const uint32_t sQ = tc::smem_u32(smem + C::kQOff);
+      const uint32_t sK = tc::smem_u32(smem + C::kKOff);
+      const uint32_t sV = tc::smem_u32(smem + C::kVOff);
+      bool ok = tc::mbar_wait(q_full, 0, abort_flag);
+      if (!ok) fail(p, abort_flag, 2);
+      tc::fence_after_sync();
+      int remaining[2] = {st[0].count, st[1].count};
+      bool pend[2] = {false, false};
+      bool started[2] = {false, false};
+      uint32_t pph[2] = {0, 0};
+      int ps = 0, j = 0;
+      auto do_pv = [&](int t, int sp) -> bool {
+        if (!tc::mbar_wait(p_full + t, pph[t], abort_flag)) return false;
+        pph[t] ^= 1;
+        tc::fence_after_sync();
+        const uint32_t vbase = sV + sp * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint64_t bd = tc::sdesc_sw128(vbase + ks * 2048, 16384, 1024);
+          tc::mma_ts(tbase + C::kOCol + t * D, tbase + t * 128 + ks * 8, bd, idO, (started[t] || ks > 0) ? 1u : 0u);
+        }
+        started[t] = true;
+        pend[t] = false;
+        if (remaining[t] == 0) tc::mma_commit(o_final + t);
+        return true;
+      };
+      Merge m;
+      m.init(st);
+      int kt;
+      bool in[2], pa[2];
+      while (ok && m.next(kt, in[0], in[1], pa[0], pa[1])) {
+        const int s = j % NS;
+        if (!tc::mbar_wait(k_full + s, (j / NS) & 1, abort_flag)) { ok = false; break; }
+        if (j > 0 && !tc::mbar_wait(v_full + ps, ((j - 1) / NS) & 1, abort_flag)) { ok = false; break; }
+        tc::fence_after_sync();
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (pend[t] && !do_pv(t, ps)) { ok = false; break; }
+          if (in[t]) {
+            const uint32_t qb = sQ + t * C::kTileBytes, kb = sK + s * C::kTileBytes;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+              tc::mma_ss(tbase + t * 128, tc::sdesc_sw128(qb + o, 16, 1024), tc::sdesc_sw128(kb + o, 16, 1024), idS,
+                         ks > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(s_full + t);
+            pend[t] = true;
+            --remaining[t];
+          }
+        }
+        if (!ok) break;
+        if (j > 0) tc::mma_commit(kv_empty + ps);
+        ps = s;
+        ++j;
+      }
+      if (ok && (pend[0] || pend[1])) {
+        ok = tc::mbar_wait(v_full + ps, ((j - 1) / NS) & 1, abort_flag);
+        tc::fence_after_sync();
+        for (int t = 0; t < 2 && ok; ++t)
+          if (pend[t]) ok = do_pv(t, ps);
+      }
+      if (!ok) fail(p, abort_flag, 3);
+      // drain: nothing issued may still run when TMEM is released
+      tc::mma_commit(mma_done);
+      tc::mbar_wait_drain(mma_done, 0, 200000000ull);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = 32 * wq + lane;
+    const SubTile me = st[t];
+    const int i = me.rt * 128 + row;
+    const int h = me.h;
+    const uint32_t lane_base = tbase + ((uint32_t)(32 * wq) << 16);
+    const bool plain_kind = p.softcap == 0.f && p.mask_kind == FA_MASK_NONE;
+    if (me.valid && me.count == 0) {
+      if (i < q_len) write_empty_row<D>(p, b, h, i);
+    } else if (me.valid) {
+      float m_ref = -INFINITY, l = 0.f;
+      uint32_t sph = 0;
+      bool first = true, ok = true;
+      Merge m;
+      m.init(st);
+      int kt;
+      bool in[2], pa[2];
+      while (m.next(kt, in[0], in[1], pa[0], pa[1])) {
+        if (!in[t]) continue;
+        if (!tc::mbar_wait(s_full + t, sph, abort_flag)) { ok = false; break; }
+        sph ^= 1;
+        tc::fence_after_sync();
+        const bool plain = plain_kind && !pa[t];
+        const uint32_t scol = lane_base + t * 128;
+        const int j0 = kt * kKeysPerTile;
+        // pass 1: row max (raw scores on FULL tiles, final logits otherwise)
+        float mx = -INFINITY;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[2][32];
+          tc::tmem_ld32(scol + half * 64, r[0]);
+          tc::tmem_ld32(scol + half * 64 + 32, r[1]);
+          tc::tmem_wait_ld();
+          if (plain) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[c][e]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const int j = j0 + half * 64 + c * 32 + e;
+                float xv = (i < q_len) ? logit_log2(p, __uint_as_float(r[c][e]), b, h, i, j, off, kv_len)
+                                       : -INFINITY;
+                mx = fmaxf(mx, xv);
+                r[c][e] = __float_as_uint(xv);
+              }
+              tc::tmem_st32(scol + half * 64 + c * 32, r[c]);
+            }
+          }
+        }
+        if (!plain) tc::tmem_wait_st();
+        if (plain) mx *= p.scale_log2;
+        // raise the exponent reference only when the row max outgrew it by 2^8
+        const bool upd = mx > m_ref + kRescaleLog2;
+        const float alpha = upd ? fast_exp2(m_ref - mx) : 1.f;
+        const bool need_o = upd && !first && m_ref != -INFINITY;
+        if (__any_sync(0xffffffffu, need_o)) {
+          const float f = need_o ? alpha : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            const uint32_t a = lane_base + C::kOCol + t * D + c * 32;
+            tc::tmem_ld32(a, r);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+            tc::tmem_st32(a, r);
+          }
+          tc::tmem_wait_st();
+        }
+        if (upd) {
+          l *= alpha;
+          m_ref = mx;
+        }
+        const float eref = (m_ref == -INFINITY) ? 0.f : m_ref;
+        // pass 2: P = exp2(x - ref) -> bf16 pairs over columns [0, 64)
+        float rs = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[2][32];
+          tc::tmem_ld32(scol + half * 64, r[0]);
+          tc::tmem_ld32(scol + half * 64 + 32, r[1]);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float x0 = __uint_as_float(r[c][2 * e]), x1 = __uint_as_float(r[c][2 * e + 1]);
+              float p0 = plain ? fast_exp2(fmaf(x0, p.scale_log2, -eref)) : fast_exp2(x0 - eref);
+              float p1 = plain ? fast_exp2(fmaf(x1, p.scale_log2, -eref)) : fast_exp2(x1 - eref);
+              rs += p0 + p1;
+              pk[e] = pack2(p0, p1);
+            }
+            tc::tmem_st16(scol + (half * 2 + c) * 16, pk);
+          }
+        }
+        l += rs;
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        tc::mbar_arrive(p_full + t);
+        first = false;
+      }
+      if (ok) ok = tc::mbar_wait(o_final + t, 0, abort_flag);
+      if (!ok) {
+        fail(p, abort_flag, 4 + t);
+      } else {
+        tc::fence_after_sync();
+        const bool empty = !(l > 0.f);
+        const float inv = empty ? 0.f : 1.f / l;
+        uint16_t* optr;
+        float* lptr;
+        row_out(p, b, h, i < q_len ? i : 0, optr, lptr);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld32(lane_base + C::kOCol + t * D + c * 32, r);
+          tc::tmem_wait_ld();
+          if (i < q_len) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack2(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
+              w.y = pack2(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
+              w.z = pack2(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
+              w.w = pack2(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
+              *reinterpret_cast<uint4*>(optr + c * 32 + 8 * v4) = w;
+            }
+          }
+        }
+        if (i < q_len) *lptr = empty ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 1) tc::tmem_dealloc(tbase, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// 4-D map {d, heads, rows, batch} over a bshd (or packed thd) bf16 tensor,
+// box {64, 1, 128, 1}, 128-byte swizzle; rows beyond the tensor read as 0.
+bool encode_bshd(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int batch, int64_t s_h,
+                 int64_t s_row, int64_t s_b) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows, (cuuint64_t)batch};
+  cuuint64_t strides[3] = {(cuuint64_t)s_h * 2, (cuuint64_t)s_row * 2, (cuuint64_t)s_b * 2};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_prefill_d(const Params& p, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  const bool vq = p.cu_q != nullptr, vk = p.cu_k != nullptr;
+  // extents of 1 get a harmless stride (the stride of the next-inner dimension)
+  const int64_t q_rows = vq ? p.tot_q : p.Sq, k_rows = vk ? p.tot_k : p.Sk;
+  const int qb = vq ? 1 : p.n_seq, kb = vk ? 1 : p.n_seq;
+  const int64_t q_sb = (qb == 1 || p.q_sb == 0) ? p.q_ss : p.q_sb;
+  const int64_t k_sb = (kb == 1 || p.k_sb == 0) ? p.k_ss : p.k_sb;
+  const int64_t v_sb = (kb == 1 || p.v_sb == 0) ? p.v_ss : p.v_sb;
+  if (!encode_bshd(&mq, p.q, D, p.Hq, q_rows, qb, p.q_sh, p.q_ss, q_sb) ||
+      !encode_bshd(&mk, p.k, D, p.Hkv, k_rows, kb, p.k_sh, p.k_ss, k_sb) ||
+      !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       PCfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
+
+  int64_t grid;
+  if (p.G >= 2)
+    grid = (int64_t)p.n_row_tiles * p.n_seq * p.Hkv * ((p.G + 1) / 2);
+  else
+    grid = (int64_t)((p.n_row_tiles + 1) / 2) * p.n_seq * p.Hq;
+  if (grid <= 0) return cudaSuccess;
+  prefill_kernel<D><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const Params& p, cudaStream_t st) {
+  if (p.n_items <= 0) return cudaSuccess;
+  if (p.d == 64) return launch_prefill_d<64>(p, st);
+  return launch_prefill_d<128>(p, st);
+}
+
+}  // namespace mfa

@@ -239,3 +239,88 @@ def test_dynamic_topk_full():
 
 def test_paged_varlen_decode_full():
     check(W.paged_varlen_decode(seed=0))
+
+
+# ---------------------------------------------------------------------------
+# tcgen05 prefill path (many query rows per K/V head)
+# ---------------------------------------------------------------------------
+
+def _assert_prefill(case, **over):
+    import masked_flash_attention_gb300 as fa
+    p = dict(case["params"])
+    p.update(over)
+    rc, plan = fa.fa_fwd_plan(case["q"], case["k"], case["v"], **p)
+    assert rc == 0 and plan["path"] == fa._lib.FA_PATH_PREFILL, plan
+
+
+PREFILL = [
+    (1, 129, 129, 2, 1, 128, dict(causal=True)),                  # ragged tail, GQA pair
+    (2, 300, 700, 6, 2, 64, dict(causal=True)),                   # group of 3: one lone head
+    (1, 384, 384, 4, 4, 128, dict(causal=True)),                  # MHA: pairs of row tiles, odd count
+    (1, 256, 1000, 8, 8, 64, dict(causal=False)),
+    (2, 200, 600, 8, 2, 128, dict(causal=True, window_left=150, window_right=10)),
+    (1, 500, 500, 4, 1, 128, dict(causal=True, softcap=20.0)),
+    (1, 1000, 1000, 2, 2, 64, dict(causal=True)),
+    (1, 300, 120, 4, 2, 128, dict(causal=True)),                  # q_len > kv_len
+    (3, 140, 4100, 16, 8, 128, dict(causal=True)),                # long past KV
+]
+
+
+@pytest.mark.parametrize("i", range(len(PREFILL)))
+def test_prefill_sweep(i):
+    B, Sq, Sk, Hq, Hkv, d, extra = PREFILL[i]
+    c = W.random_case(300 + i, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, d=d, **extra)
+    _assert_prefill(c)
+    check(c)
+
+
+@pytest.mark.parametrize("all_masked", [False, True])
+def test_prefill_without_skipping(all_masked):
+    from masked_flash_attention_gb300 import FA_DEBUG_NO_SKIP
+    c = W.random_case(320, B=1, Sq=300, Sk=300, Hq=4, Hkv=2, d=128, causal=True)
+    m = None
+    if all_masked:
+        m = torch.zeros(300, 300)
+        m[:130] = float("-inf")
+    _assert_prefill(c, mask=m)
+    out, lse, _ = run_gpu(c, mask=m, debug_flags=FA_DEBUG_NO_SKIP)
+    ref_o, ref_l = run_oracle(c, mask=m)
+    compare(out, lse, ref_o, ref_l, "prefill no-skip")
+
+
+def test_prefill_dense_mask():
+    c = W.random_case(321, B=2, Sq=260, Sk=500, Hq=4, Hkv=2, d=128, causal=False)
+    m = W.random_dense_mask(321, 260, 500)
+    m[:, :128] = float("-inf")
+    m[5] = float("-inf")
+    m[:, 256:384] = 0.0
+    _assert_prefill(c, mask=m)
+    check(c, mask=m)
+
+
+def test_prefill_dense_mask_per_head():
+    c = W.random_case(322, B=1, Sq=200, Sk=300, Hq=4, Hkv=4, d=64, causal=True)
+    m = torch.stack([W.random_dense_mask(40 + h, 200, 300, p_neg_inf=0.5) for h in range(4)])[None]
+    m[0, 1, :, :200] = float("-inf")
+    _assert_prefill(c, mask=m)
+    check(c, mask=m)
+
+
+@pytest.mark.parametrize("causal,ties", [(True, True), (True, False), (False, True)])
+def test_prefill_topk(causal, ties):
+    c = W.random_case(323, B=1, Sq=400, Sk=400, Hq=2, Hkv=2, d=128, causal=causal)
+    z = W.random_zero_hold_states(323, 1, 2, 400, ties=ties)
+    _assert_prefill(c, zero_hold_states=z, keep_window=100)
+    check(c, zero_hold_states=z, keep_window=100)
+
+
+@pytest.mark.parametrize("seed,q_eq_k", [(0, False), (1, True)])
+def test_prefill_varlen(seed, q_eq_k):
+    q, k, v, cu_q, cu_k = W.random_varlen(330 + seed, 4, 300, 600, 8, 2, 128, q_eq_k=q_eq_k, min_q=60)
+    lq = int((cu_q[1:] - cu_q[:-1]).max())
+    lk = int((cu_k[1:] - cu_k[:-1]).max())
+    params = W.base_params(scale=128 ** -0.5, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=lq,
+                           max_seqlen_k=max(1, lk), causal=True)
+    case = dict(name=f"prefill_varlen{seed}", q=q, k=k, v=v, params=params)
+    _assert_prefill(case)
+    check(case)

@@ -20,10 +20,13 @@
 //   warp 1      MMA issuer (one thread) and TMEM owner
 //   warps 2..3  idle
 //   warps 4..7  softmax warpgroup for sub-tile 0, warps 8..11 for sub-tile 1
-// Each softmax thread walks its row of S twice, 64 columns at a time: pass 1
-// finds the row max (PARTIAL tiles apply the pair rules and additive terms
-// and write the final logits back to TMEM), pass 2 exponentiates, sums and
-// stores P as bf16 over the first 64 columns.
+// Registers: the block launches with 168 per thread (3 warps share an SM
+// sub-partition); warpgroup 0 (producer, MMA) hands registers back with
+// setmaxnreg and the softmax warpgroups take 216, enough to keep a whole
+// 128-key row of S in registers for one pass: max, exponentiate, sum, store P.
+// The kernel is specialised on the additive term (none, dense, top-k) and on
+// the soft-cap; a PARTIAL tile applies the pair rules as one column range per
+// row, and top-k tiles stage their keys' expiry rows and bias in smem.
 // TMEM (512 columns): S_t = Q_t K^T in columns [128 t, 128 t + 128), fp32;
 // P_t (bf16, two per column) overwrites the first 64 of them; O_t in
 // [256 + D t, 256 + D t + D).  Per key tile j the MMA thread issues
@@ -54,6 +57,14 @@ namespace mfa {
 namespace {
 
 constexpr int kPrefillThreads = 384;
+// Register split (setmaxnreg): the kernel is built to launch with exactly
+// kLaunchRegs per thread; warpgroup 0 (producer, MMA) gives registers back and
+// the two softmax warpgroups take them, so that a 128-key row of S fits.
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 72;
+constexpr int kSoftmaxRegs = 216;
+static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs <= kPrefillThreads * kLaunchRegs,
+              "the register split must fit the block's launch allocation");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -65,7 +76,7 @@ struct PCfg {
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + NS * kTileBytes;
   static constexpr int kBarOff = kVOff + NS * kTileBytes;
-  static constexpr int kSmem = kBarOff + 256 + 1024;      // barriers + 1024-byte alignment slack
+  static constexpr int kSmem = kBarOff + 256 + 4096 + 1024;  // barriers, top-k staging, alignment slack
   static constexpr uint32_t kOCol = 256;
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
@@ -181,7 +192,20 @@ __device__ __forceinline__ void write_empty_row(const Params& p, int b, int h, i
   *lptr = -INFINITY;
 }
 
-template <int D>
+// Per-row key range allowed by the pair rules (causal bottom-right, window,
+// key bound), inclusive; empty (lo > hi) for rows past the sequence end.
+__device__ __forceinline__ void row_key_range(const Params& p, int i, int q_len, int kv_len, int off, int& lo,
+                                              int& hi) {
+  lo = 0;
+  hi = kv_len - 1;
+  if (p.causal) hi = min(hi, i + off);
+  if (p.wl >= 0) lo = max(lo, i + off - p.wl);
+  if (p.wr >= 0) hi = min(hi, i + off + p.wr);
+  if (i >= q_len) { lo = 1; hi = 0; }
+}
+
+// MK: additive term kind (FA_MASK_NONE / DENSE / TOPK); SC: logit soft-cap on.
+template <int D, int MK, bool SC>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
@@ -246,187 +270,224 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc::fence_after_sync();
   const uint32_t tbase = *tmem_slot;
 
-  const int kv_row0 = p.cu_k ? p.cu_k[b] : 0;
-  const int kv_b = p.cu_k ? 0 : b;
-  const int q_row0 = p.cu_q ? p.cu_q[b] : 0;
-  const int q_b = p.cu_q ? 0 : b;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tc::tma_prefetch_desc(&tmq);
-      tc::tma_prefetch_desc(&tmk);
-      tc::tma_prefetch_desc(&tmv);
-      uint32_t qbytes = 0;
-      for (int t = 0; t < 2; ++t)
-        if (st[t].count > 0) qbytes += C::kTileBytes;
-      tc::mbar_arrive_expect_tx(q_full, qbytes);
-      for (int t = 0; t < 2; ++t) {
-        if (st[t].count == 0) continue;
-        unsigned char* dst = smem + C::kQOff + t * C::kTileBytes;
-        for (int c = 0; c < D / 64; ++c)
-          tc::tma_load_4d(dst + c * 16384, &tmq, q_full, c * 64, st[t].h, q_row0 + st[t].rt * 128, q_b);
-      }
-      Merge m;
-      m.init(st);
-      int kt, j = 0;
-      bool in0, in1, pa0, pa1;
-      while (m.next(kt, in0, in1, pa0, pa1)) {
-        const int s = j % NS;
-        if (j >= NS && !tc::mbar_wait(kv_empty + s, ((j / NS) - 1) & 1, abort_flag)) {
-          fail(p, abort_flag, 1);
-          break;
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        const int kv_row0 = p.cu_k ? p.cu_k[b] : 0;
+        const int kv_b = p.cu_k ? 0 : b;
+        const int q_row0 = p.cu_q ? p.cu_q[b] : 0;
+        const int q_b = p.cu_q ? 0 : b;
+        tc::tma_prefetch_desc(&tmq);
+        tc::tma_prefetch_desc(&tmk);
+        tc::tma_prefetch_desc(&tmv);
+        uint32_t qbytes = 0;
+        for (int t = 0; t < 2; ++t)
+          if (st[t].count > 0) qbytes += C::kTileBytes;
+        tc::mbar_arrive_expect_tx(q_full, qbytes);
+        for (int t = 0; t < 2; ++t) {
+          if (st[t].count == 0) continue;
+          unsigned char* dst = smem + C::kQOff + t * C::kTileBytes;
+          for (int c = 0; c < D / 64; ++c)
+            tc::tma_load_4d(dst + c * 16384, &tmq, q_full, c * 64, st[t].h, q_row0 + st[t].rt * 128, q_b);
         }
-        unsigned char* dk = smem + C::kKOff + s * C::kTileBytes;
-        unsigned char* dv = smem + C::kVOff + s * C::kTileBytes;
-        tc::mbar_arrive_expect_tx(k_full + s, C::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tc::tma_load_4d(dk + c * 16384, &tmk, k_full + s, c * 64, g, kv_row0 + kt * 128, kv_b);
-        tc::mbar_arrive_expect_tx(v_full + s, C::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tc::tma_load_4d(dv + c * 16384, &tmv, v_full + s, c * 64, g, kv_row0 + kt * 128, kv_b);
-        ++j;
-      }
-      if (*abort_flag) {
-        // let the copies already issued land before the CTA can exit
-        const int first = j > NS ? j - NS : 0;
-        for (int jj = first; jj < j; ++jj) {
-          tc::mbar_wait_drain(k_full + jj % NS, (jj / NS) & 1, 100000000ull);
-          tc::mbar_wait_drain(v_full + jj % NS, (jj / NS) & 1, 100000000ull);
-        }
-        tc::mbar_wait_drain(q_full, 0, 100000000ull);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
-      const uint32_t sQ = tc::smem_u32(smem + C::kQOff);
-      const uint32_t sK = tc::smem_u32(smem + C::kKOff);
-      const uint32_t sV = tc::smem_u32(smem + C::kVOff);
-      bool ok = tc::mbar_wait(q_full, 0, abort_flag);
-      if (!ok) fail(p, abort_flag, 2);
-      tc::fence_after_sync();
-      int remaining[2] = {st[0].count, st[1].count};
-      bool pend[2] = {false, false};
-      bool started[2] = {false, false};
-      uint32_t pph[2] = {0, 0};
-      int ps = 0, j = 0;
-      auto do_pv = [&](int t, int sp) -> bool {
-        if (!tc::mbar_wait(p_full + t, pph[t], abort_flag)) return false;
-        pph[t] ^= 1;
-        tc::fence_after_sync();
-        const uint32_t vbase = sV + sp * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint64_t bd = tc::sdesc_sw128(vbase + ks * 2048, 16384, 1024);
-          tc::mma_ts(tbase + C::kOCol + t * D, tbase + t * 128 + ks * 8, bd, idO, (started[t] || ks > 0) ? 1u : 0u);
-        }
-        started[t] = true;
-        pend[t] = false;
-        if (remaining[t] == 0) tc::mma_commit(o_final + t);
-        return true;
-      };
-      Merge m;
-      m.init(st);
-      int kt;
-      bool in[2], pa[2];
-      while (ok && m.next(kt, in[0], in[1], pa[0], pa[1])) {
-        const int s = j % NS;
-        if (!tc::mbar_wait(k_full + s, (j / NS) & 1, abort_flag)) { ok = false; break; }
-        if (j > 0 && !tc::mbar_wait(v_full + ps, ((j - 1) / NS) & 1, abort_flag)) { ok = false; break; }
-        tc::fence_after_sync();
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (pend[t] && !do_pv(t, ps)) { ok = false; break; }
-          if (in[t]) {
-            const uint32_t qb = sQ + t * C::kTileBytes, kb = sK + s * C::kTileBytes;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-              tc::mma_ss(tbase + t * 128, tc::sdesc_sw128(qb + o, 16, 1024), tc::sdesc_sw128(kb + o, 16, 1024), idS,
-                         ks > 0 ? 1u : 0u);
-            }
-            tc::mma_commit(s_full + t);
-            pend[t] = true;
-            --remaining[t];
+        Merge m;
+        m.init(st);
+        int kt, j = 0;
+        bool in0, in1, pa0, pa1;
+        while (m.next(kt, in0, in1, pa0, pa1)) {
+          const int s = j % NS;
+          if (j >= NS && !tc::mbar_wait(kv_empty + s, ((j / NS) - 1) & 1, abort_flag)) {
+            fail(p, abort_flag, 1);
+            break;
           }
+          unsigned char* dk = smem + C::kKOff + s * C::kTileBytes;
+          unsigned char* dv = smem + C::kVOff + s * C::kTileBytes;
+          tc::mbar_arrive_expect_tx(k_full + s, C::kTileBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tc::tma_load_4d(dk + c * 16384, &tmk, k_full + s, c * 64, g, kv_row0 + kt * 128, kv_b);
+          tc::mbar_arrive_expect_tx(v_full + s, C::kTileBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tc::tma_load_4d(dv + c * 16384, &tmv, v_full + s, c * 64, g, kv_row0 + kt * 128, kv_b);
+          ++j;
         }
-        if (!ok) break;
-        if (j > 0) tc::mma_commit(kv_empty + ps);
-        ps = s;
-        ++j;
+        if (*abort_flag) {
+          // let the copies already issued land before the CTA can exit
+          const int first = j > NS ? j - NS : 0;
+          for (int jj = first; jj < j; ++jj) {
+            tc::mbar_wait_drain(k_full + jj % NS, (jj / NS) & 1, 100000000ull);
+            tc::mbar_wait_drain(v_full + jj % NS, (jj / NS) & 1, 100000000ull);
+          }
+          tc::mbar_wait_drain(q_full, 0, 100000000ull);
+        }
       }
-      if (ok && (pend[0] || pend[1])) {
-        ok = tc::mbar_wait(v_full + ps, ((j - 1) / NS) & 1, abort_flag);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
+        const uint32_t sQ = tc::smem_u32(smem + C::kQOff);
+        const uint32_t sK = tc::smem_u32(smem + C::kKOff);
+        const uint32_t sV = tc::smem_u32(smem + C::kVOff);
+        bool ok = tc::mbar_wait(q_full, 0, abort_flag);
+        if (!ok) fail(p, abort_flag, 2);
         tc::fence_after_sync();
-        for (int t = 0; t < 2 && ok; ++t)
-          if (pend[t]) ok = do_pv(t, ps);
+        int remaining[2] = {st[0].count, st[1].count};
+        bool pend[2] = {false, false};
+        bool started[2] = {false, false};
+        uint32_t pph[2] = {0, 0};
+        int ps = 0, j = 0;
+        auto do_pv = [&](int t, int sp) -> bool {
+          if (!tc::mbar_wait(p_full + t, pph[t], abort_flag)) return false;
+          pph[t] ^= 1;
+          tc::fence_after_sync();
+          const uint32_t vbase = sV + sp * C::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            uint64_t bd = tc::sdesc_sw128(vbase + ks * 2048, 16384, 1024);
+            tc::mma_ts(tbase + C::kOCol + t * D, tbase + t * 128 + ks * 8, bd, idO,
+                       (started[t] || ks > 0) ? 1u : 0u);
+          }
+          started[t] = true;
+          pend[t] = false;
+          if (remaining[t] == 0) tc::mma_commit(o_final + t);
+          return true;
+        };
+        Merge m;
+        m.init(st);
+        int kt;
+        bool in[2], pa[2];
+        while (ok && m.next(kt, in[0], in[1], pa[0], pa[1])) {
+          const int s = j % NS;
+          if (!tc::mbar_wait(k_full + s, (j / NS) & 1, abort_flag)) { ok = false; break; }
+          if (j > 0 && !tc::mbar_wait(v_full + ps, ((j - 1) / NS) & 1, abort_flag)) { ok = false; break; }
+          tc::fence_after_sync();
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (pend[t] && !do_pv(t, ps)) { ok = false; break; }
+            if (in[t]) {
+              const uint32_t qb = sQ + t * C::kTileBytes, kb = sK + s * C::kTileBytes;
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks) {
+                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+                tc::mma_ss(tbase + t * 128, tc::sdesc_sw128(qb + o, 16, 1024), tc::sdesc_sw128(kb + o, 16, 1024),
+                           idS, ks > 0 ? 1u : 0u);
+              }
+              tc::mma_commit(s_full + t);
+              pend[t] = true;
+              --remaining[t];
+            }
+          }
+          if (!ok) break;
+          if (j > 0) tc::mma_commit(kv_empty + ps);
+          ps = s;
+          ++j;
+        }
+        if (ok && (pend[0] || pend[1])) {
+          ok = tc::mbar_wait(v_full + ps, ((j - 1) / NS) & 1, abort_flag);
+          tc::fence_after_sync();
+          for (int t = 0; t < 2 && ok; ++t)
+            if (pend[t]) ok = do_pv(t, ps);
+        }
+        if (!ok) fail(p, abort_flag, 3);
+        // drain: nothing issued may still run when TMEM is released
+        tc::mma_commit(mma_done);
+        tc::mbar_wait_drain(mma_done, 0, 200000000ull);
       }
-      if (!ok) fail(p, abort_flag, 3);
-      // drain: nothing issued may still run when TMEM is released
-      tc::mma_commit(mma_done);
-      tc::mbar_wait_drain(mma_done, 0, 200000000ull);
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp >= 4) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;
-    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int wtid = tid - 128 - 128 * t;  // 0..127 within the warpgroup
+    const int wq = warp & 3;               // TMEM lane quarter this warp may access
     const int row = 32 * wq + lane;
     const SubTile me = st[t];
     const int i = me.rt * 128 + row;
     const int h = me.h;
     const uint32_t lane_base = tbase + ((uint32_t)(32 * wq) << 16);
-    const bool plain_kind = p.softcap == 0.f && p.mask_kind == FA_MASK_NONE;
+    const uint32_t scol = lane_base + t * 128;
+    int jlo_r, jhi_r;
+    row_key_range(p, i, q_len, kv_len, off, jlo_r, jhi_r);
+    // top-k: per key tile, the keys' expiry rows and bias, staged in smem
+    int2* kbuf = reinterpret_cast<int2*>(smem + C::kBarOff + 256) + t * 256;
     if (me.valid && me.count == 0) {
       if (i < q_len) write_empty_row<D>(p, b, h, i);
     } else if (me.valid) {
       float m_ref = -INFINITY, l = 0.f;
       uint32_t sph = 0;
       bool first = true, ok = true;
+      int par = 0;
       Merge m;
       m.init(st);
       int kt;
       bool in[2], pa[2];
       while (m.next(kt, in[0], in[1], pa[0], pa[1])) {
         if (!in[t]) continue;
+        const int j0 = kt * kKeysPerTile;
+        if (MK == FA_MASK_TOPK) {
+          const int jj = j0 + wtid;
+          int2 v = make_int2(kRowNever, 0);
+          if (jj < kv_len) {
+            const int64_t bh = (int64_t)b * p.Hq + h;
+            v.x = __ldg(p.topk_e + bh * p.Sk + jj);
+            v.y = __float_as_int(
+                __ldg(p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh + (int64_t)jj * p.z_sk) * kLog2e);
+          }
+          kbuf[par * 128 + wtid] = v;
+          asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
+        }
         if (!tc::mbar_wait(s_full + t, sph, abort_flag)) { ok = false; break; }
         sph ^= 1;
         tc::fence_after_sync();
-        const bool plain = plain_kind && !pa[t];
-        const uint32_t scol = lane_base + t * 128;
-        const int j0 = kt * kKeysPerTile;
-        // pass 1: row max (raw scores on FULL tiles, final logits otherwise)
-        float mx = -INFINITY;
+        float x[128];
+        {
+          uint32_t r[4][32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[2][32];
-          tc::tmem_ld32(scol + half * 64, r[0]);
-          tc::tmem_ld32(scol + half * 64 + 32, r[1]);
+          for (int c = 0; c < 4; ++c) tc::tmem_ld32(scol + c * 32, r[c]);
           tc::tmem_wait_ld();
-          if (plain) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-              for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[c][e]));
-          } else {
+            for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[c][e]);
+        }
+        // logits in log2 units; a FULL tile without soft-cap keeps raw scores
+        // and folds the scale into the exponent below
+        const bool plain = !SC && !pa[t];
+        float mx = -INFINITY;
+        if (plain) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+          for (int e = 0; e < 128; ++e) mx = fmaxf(mx, x[e]);
+          mx *= p.scale_log2;
+        } else {
+          const int clo = jlo_r - j0, chi = jhi_r - j0;
+          const bool all_in = !pa[t];
+          const float* mrow = nullptr;
+          if (MK == FA_MASK_DENSE && i < q_len)
+            mrow = p.mask + (int64_t)(p.m_nb > 1 ? b : 0) * p.m_sb + (int64_t)(p.m_nh > 1 ? h : 0) * p.m_sh +
+                   (int64_t)i * p.m_sq + (int64_t)j0 * p.m_sk;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int j = j0 + half * 64 + c * 32 + e;
-                float xv = (i < q_len) ? logit_log2(p, __uint_as_float(r[c][e]), b, h, i, j, off, kv_len)
-                                       : -INFINITY;
-                mx = fmaxf(mx, xv);
-                r[c][e] = __float_as_uint(xv);
-              }
-              tc::tmem_st32(scol + half * 64 + c * 32, r[c]);
+          for (int e = 0; e < 128; ++e) {
+            float v;
+            if (SC) {
+              v = p.softcap * tanhf(x[e] * p.scale / p.softcap) * kLog2e;
+            } else {
+              v = x[e] * p.scale_log2;
             }
+            bool keep = all_in || (e >= clo && e <= chi);
+            if (MK == FA_MASK_DENSE && !all_in) {
+              if (keep) v += __ldg(mrow + (int64_t)e * p.m_sk) * kLog2e;
+            }
+            if (MK == FA_MASK_TOPK) {
+              const int2 kv = kbuf[par * 128 + e];
+              keep = keep && (i < kv.x);
+              v += __int_as_float(kv.y);
+            }
+            x[e] = keep ? v : -INFINITY;
+            mx = fmaxf(mx, x[e]);
           }
         }
-        if (!plain) tc::tmem_wait_st();
-        if (plain) mx *= p.scale_log2;
         // raise the exponent reference only when the row max outgrew it by 2^8
         const bool upd = mx > m_ref + kRescaleLog2;
         const float alpha = upd ? fast_exp2(m_ref - mx) : 1.f;
@@ -450,33 +511,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           m_ref = mx;
         }
         const float eref = (m_ref == -INFINITY) ? 0.f : m_ref;
-        // pass 2: P = exp2(x - ref) -> bf16 pairs over columns [0, 64)
         float rs = 0.f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[2][32];
-          tc::tmem_ld32(scol + half * 64, r[0]);
-          tc::tmem_ld32(scol + half * 64 + 32, r[1]);
-          tc::tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float x0 = __uint_as_float(r[c][2 * e]), x1 = __uint_as_float(r[c][2 * e + 1]);
-              float p0 = plain ? fast_exp2(fmaf(x0, p.scale_log2, -eref)) : fast_exp2(x0 - eref);
-              float p1 = plain ? fast_exp2(fmaf(x1, p.scale_log2, -eref)) : fast_exp2(x1 - eref);
-              rs += p0 + p1;
-              pk[e] = pack2(p0, p1);
-            }
-            tc::tmem_st16(scol + (half * 2 + c) * 16, pk);
+          for (int e = 0; e < 16; ++e) {
+            const float x0 = x[c * 32 + 2 * e], x1 = x[c * 32 + 2 * e + 1];
+            const float p0 = plain ? fast_exp2(fmaf(x0, p.scale_log2, -eref)) : fast_exp2(x0 - eref);
+            const float p1 = plain ? fast_exp2(fmaf(x1, p.scale_log2, -eref)) : fast_exp2(x1 - eref);
+            rs += p0 + p1;
+            pk[e] = pack2(p0, p1);
           }
+          tc::tmem_st16(scol + c * 16, pk);
         }
         l += rs;
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::mbar_arrive(p_full + t);
         first = false;
+        par ^= 1;
       }
       if (ok) ok = tc::mbar_wait(o_final + t, 0, abort_flag);
       if (!ok) {
@@ -553,6 +607,26 @@ bool encode_bshd(CUtensorMap* m, const void* base, int d, int heads, int64_t row
   return r == CUDA_SUCCESS;
 }
 
+template <int D, int MK, bool SC>
+cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap& mq, const CUtensorMap& mk,
+                             const CUtensorMap& mv, int64_t grid) {
+  auto kern = prefill_kernel<D, MK, SC>;
+  // setmaxnreg.inc would wait forever if the block were launched with fewer
+  // registers than the split assumes: launch only when the build matches.
+  static int regs = -1;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    regs = fa.numRegs;
+  }
+  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_prefill_d(const Params& p, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
@@ -567,18 +641,24 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st) {
       !encode_bshd(&mk, p.k, D, p.Hkv, k_rows, kb, p.k_sh, p.k_ss, k_sb) ||
       !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PCfg<D>::kSmem);
-  if (e != cudaSuccess) return e;
-
   int64_t grid;
   if (p.G >= 2)
     grid = (int64_t)p.n_row_tiles * p.n_seq * p.Hkv * ((p.G + 1) / 2);
   else
     grid = (int64_t)((p.n_row_tiles + 1) / 2) * p.n_seq * p.Hq;
   if (grid <= 0) return cudaSuccess;
-  prefill_kernel<D><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv);
-  return cudaGetLastError();
+  const bool sc = p.softcap > 0.f;
+  switch (p.mask_kind) {
+    case FA_MASK_DENSE:
+      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true>(p, st, mq, mk, mv, grid)
+                : launch_prefill_v<D, FA_MASK_DENSE, false>(p, st, mq, mk, mv, grid);
+    case FA_MASK_TOPK:
+      return sc ? launch_prefill_v<D, FA_MASK_TOPK, true>(p, st, mq, mk, mv, grid)
+                : launch_prefill_v<D, FA_MASK_TOPK, false>(p, st, mq, mk, mv, grid);
+    default:
+      return sc ? launch_prefill_v<D, FA_MASK_NONE, true>(p, st, mq, mk, mv, grid)
+                : launch_prefill_v<D, FA_MASK_NONE, false>(p, st, mq, mk, mv, grid);
+  }
 }
 
 }  // namespace

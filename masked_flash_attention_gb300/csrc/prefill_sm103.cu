@@ -16,9 +16,10 @@
 // the tiles that are not on its own list.
 //
 // Warp roles (12 warps = 3 warpgroups):
-//   warp 0      TMA producer: Q once, then K/V tiles through an NS-stage ring
+//   warp 0      TMA producer: Q once, then K tiles through an NS-stage ring
 //   warp 1      MMA issuer (one thread) and TMEM owner
-//   warps 2..3  idle
+//   warp 2      TMA producer: V tiles through an NS-stage ring
+//   warp 3      idle
 //   warps 4..7  softmax warpgroup for sub-tile 0, warps 8..11 for sub-tile 1
 // Registers: the block launches with 168 per thread (3 warps share an SM
 // sub-partition); warpgroup 0 (producer, MMA) hands registers back with
@@ -167,6 +168,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Packed fp32 pair arithmetic (one instruction for two lanes of work).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
 __device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag, uint32_t where) {
   if (!*abort_flag) {
     *abort_flag = 1;
@@ -237,8 +255,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + NS;
-  uint64_t* kv_empty = v_full + NS;
-  uint64_t* s_full = kv_empty + NS;   // [2]
+  uint64_t* k_empty = v_full + NS;
+  uint64_t* v_empty = k_empty + NS;
+  uint64_t* s_full = v_empty + NS;    // [2]
   uint64_t* p_full = s_full + 2;      // [2]
   uint64_t* o_final = p_full + 2;     // [2]
   uint64_t* mma_done = o_final + 2;   // [1]
@@ -250,7 +269,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     for (int s = 0; s < NS; ++s) {
       tc::mbar_init(k_full + s, 1);
       tc::mbar_init(v_full + s, 1);
-      tc::mbar_init(kv_empty + s, 1);
+      tc::mbar_init(k_empty + s, 1);
+      tc::mbar_init(v_empty + s, 1);
     }
     for (int t = 0; t < 2; ++t) {
       tc::mbar_init(s_full + t, 1);
@@ -272,25 +292,34 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-    if (warp == 0) {
-      // ---------------------------------------------------------- producer
+    if (warp == 0 || warp == 2) {
+      // ---------------------------------------------------------- producers
+      // warp 0: Q once, then K tiles; warp 2: V tiles.  Each ring has its own
+      // release barrier: a K stage frees when the QKs that read it are done,
+      // a V stage when its PVs are done, a step later.
       if (lane == 0) {
+        const bool is_k = (warp == 0);
         const int kv_row0 = p.cu_k ? p.cu_k[b] : 0;
         const int kv_b = p.cu_k ? 0 : b;
-        const int q_row0 = p.cu_q ? p.cu_q[b] : 0;
-        const int q_b = p.cu_q ? 0 : b;
-        tc::tma_prefetch_desc(&tmq);
-        tc::tma_prefetch_desc(&tmk);
-        tc::tma_prefetch_desc(&tmv);
-        uint32_t qbytes = 0;
-        for (int t = 0; t < 2; ++t)
-          if (st[t].count > 0) qbytes += C::kTileBytes;
-        tc::mbar_arrive_expect_tx(q_full, qbytes);
-        for (int t = 0; t < 2; ++t) {
-          if (st[t].count == 0) continue;
-          unsigned char* dst = smem + C::kQOff + t * C::kTileBytes;
-          for (int c = 0; c < D / 64; ++c)
-            tc::tma_load_4d(dst + c * 16384, &tmq, q_full, c * 64, st[t].h, q_row0 + st[t].rt * 128, q_b);
+        const CUtensorMap* map = is_k ? &tmk : &tmv;
+        uint64_t* full = is_k ? k_full : v_full;
+        uint64_t* empty = is_k ? k_empty : v_empty;
+        unsigned char* ring = smem + (is_k ? C::kKOff : C::kVOff);
+        tc::tma_prefetch_desc(map);
+        if (is_k) {
+          const int q_row0 = p.cu_q ? p.cu_q[b] : 0;
+          const int q_b = p.cu_q ? 0 : b;
+          tc::tma_prefetch_desc(&tmq);
+          uint32_t qbytes = 0;
+          for (int t = 0; t < 2; ++t)
+            if (st[t].count > 0) qbytes += C::kTileBytes;
+          tc::mbar_arrive_expect_tx(q_full, qbytes);
+          for (int t = 0; t < 2; ++t) {
+            if (st[t].count == 0) continue;
+            unsigned char* dst = smem + C::kQOff + t * C::kTileBytes;
+            for (int c = 0; c < D / 64; ++c)
+              tc::tma_load_4d(dst + c * 16384, &tmq, q_full, c * 64, st[t].h, q_row0 + st[t].rt * 128, q_b);
+          }
         }
         Merge m;
         m.init(st);
@@ -298,28 +327,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         bool in0, in1, pa0, pa1;
         while (m.next(kt, in0, in1, pa0, pa1)) {
           const int s = j % NS;
-          if (j >= NS && !tc::mbar_wait(kv_empty + s, ((j / NS) - 1) & 1, abort_flag)) {
-            fail(p, abort_flag, 1);
+          if (j >= NS && !tc::mbar_wait(empty + s, ((j / NS) - 1) & 1, abort_flag)) {
+            fail(p, abort_flag, is_k ? 1 : 7);
             break;
           }
-          unsigned char* dk = smem + C::kKOff + s * C::kTileBytes;
-          unsigned char* dv = smem + C::kVOff + s * C::kTileBytes;
-          tc::mbar_arrive_expect_tx(k_full + s, C::kTileBytes);
+          tc::mbar_arrive_expect_tx(full + s, C::kTileBytes);
           for (int c = 0; c < D / 64; ++c)
-            tc::tma_load_4d(dk + c * 16384, &tmk, k_full + s, c * 64, g, kv_row0 + kt * 128, kv_b);
-          tc::mbar_arrive_expect_tx(v_full + s, C::kTileBytes);
-          for (int c = 0; c < D / 64; ++c)
-            tc::tma_load_4d(dv + c * 16384, &tmv, v_full + s, c * 64, g, kv_row0 + kt * 128, kv_b);
+            tc::tma_load_4d(ring + s * C::kTileBytes + c * 16384, map, full + s, c * 64, g, kv_row0 + kt * 128,
+                            kv_b);
           ++j;
         }
         if (*abort_flag) {
           // let the copies already issued land before the CTA can exit
           const int first = j > NS ? j - NS : 0;
-          for (int jj = first; jj < j; ++jj) {
-            tc::mbar_wait_drain(k_full + jj % NS, (jj / NS) & 1, 100000000ull);
-            tc::mbar_wait_drain(v_full + jj % NS, (jj / NS) & 1, 100000000ull);
-          }
-          tc::mbar_wait_drain(q_full, 0, 100000000ull);
+          for (int jj = first; jj < j; ++jj) tc::mbar_wait_drain(full + jj % NS, (jj / NS) & 1, 100000000ull);
+          if (is_k) tc::mbar_wait_drain(q_full, 0, 100000000ull);
         }
       }
     } else if (warp == 1) {
@@ -378,8 +400,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               --remaining[t];
             }
           }
-          if (!ok) break;
-          if (j > 0) tc::mma_commit(kv_empty + ps);
+            if (!ok) break;
+          tc::mma_commit(k_empty + s);               // QKs of this entry issued
+          if (j > 0) tc::mma_commit(v_empty + ps);   // PVs of the previous entry issued
           ps = s;
           ++j;
         }
@@ -457,9 +480,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const bool plain = !SC && !pa[t];
         float mx = -INFINITY;
         if (plain) {
+          float m8[8];
 #pragma unroll
-          for (int e = 0; e < 128; ++e) mx = fmaxf(mx, x[e]);
-          mx *= p.scale_log2;
+          for (int k = 0; k < 8; ++k) m8[k] = x[k];
+#pragma unroll
+          for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
+          mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])) * p.scale_log2;
         } else {
           const int clo = jlo_r - j0, chi = jhi_r - j0;
           const bool all_in = !pa[t];
@@ -485,8 +513,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               v += __int_as_float(kv.y);
             }
             x[e] = keep ? v : -INFINITY;
-            mx = fmaxf(mx, x[e]);
           }
+          float m8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = x[k];
+#pragma unroll
+          for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
+          mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]));
         }
         // raise the exponent reference only when the row max outgrew it by 2^8
         const bool upd = mx > m_ref + kRescaleLog2;
@@ -511,21 +546,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           m_ref = mx;
         }
         const float eref = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs = 0.f;
+        const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 ner = make_float2(-eref, -eref);
+        float2 acc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float x0 = x[c * 32 + 2 * e], x1 = x[c * 32 + 2 * e + 1];
-            const float p0 = plain ? fast_exp2(fmaf(x0, p.scale_log2, -eref)) : fast_exp2(x0 - eref);
-            const float p1 = plain ? fast_exp2(fmaf(x1, p.scale_log2, -eref)) : fast_exp2(x1 - eref);
-            rs += p0 + p1;
-            pk[e] = pack2(p0, p1);
+            float2 v = make_float2(x[c * 32 + 2 * e], x[c * 32 + 2 * e + 1]);
+            v = plain ? fma2(v, sl2, ner) : add2(v, ner);
+            const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
+            acc[e & 3] = add2(acc[e & 3], pe);
+            pk[e] = pack2(pe.x, pe.y);
           }
           tc::tmem_st16(scol + c * 16, pk);
         }
-        l += rs;
+        acc[0] = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+        l += acc[0].x + acc[0].y;
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::mbar_arrive(p_full + t);

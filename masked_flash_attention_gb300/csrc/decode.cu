@@ -5,14 +5,17 @@
 // scheduled key tiles.  The packed rows are the query heads of the K/V head's
 // group times the query positions, so a group shares every K/V byte it reads
 // (grouped-query heads without K/V expansion, InfiniTrain pull request 193
-// "Transformer 接入").  K/V rows are streamed into shared memory with 16-byte
-// cp.async copies (coalesced: a warp copies whole 128/256-byte rows), through a
-// paged block_table when there is one (vLLM pull request 11277's
-// flash_attn_varlen_func `block_table`), three 64-key stages in flight.  Each
-// of the 4 warps owns 16 keys of a stage: S = Q K^T and O += P V run on
-// mma.sync m16n8k16 (bf16 in, fp32 accumulate); 16 rows are too few for a
-// 128-row tcgen05 tile.  The running softmax is guarded so that a fully
-// masked stage never produces NaN (ExecuTorch pull request 10466 "Summary").
+// "Transformer 接入").  The split's keys are cut into 16-key chunks dealt out
+// round-robin to the 4 warps; every warp streams its own chunks through a
+// private 3-stage shared-memory ring with 16-byte cp.async copies (each
+// instruction of a warp covers two whole K or V rows, so the copies are fully
+// coalesced), through the paged block_table when there is one (vLLM pull
+// request 11277's flash_attn_varlen_func `block_table`; one page lookup per
+// chunk when the page size is a multiple of 16).  Warps never wait for each
+// other until the end.  S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16
+// in, fp32 accumulate); 16 rows are too few for a 128-row tcgen05 tile.  The
+// running softmax is guarded so that a fully masked chunk never produces NaN
+// (ExecuTorch pull request 10466 "Summary").
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -22,18 +25,20 @@ namespace mfa {
 
 namespace {
 
-constexpr int kStageKeys = 64;
-constexpr int kStages = 3;
-constexpr int kThreads = 128;
+constexpr int kChunkKeys = 16;   // keys per warp stage
+constexpr int kWarpStages = 3;   // stages in flight per warp
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
 
 template <int D>
 struct DecodeSmem {
-  static constexpr int kChunks = D / 8;                      // 16-byte chunks per row
-  static constexpr int kKvBytes = kStageKeys * D * 2;        // K or V of one stage
+  static constexpr int kChunks = D / 8;                        // 16-byte chunks per row
+  static constexpr int kKvBytes = kChunkKeys * D * 2;          // K or V of one warp stage
   static constexpr int kStageBytes = 2 * kKvBytes;
+  static constexpr int kWarpBytes = kWarpStages * kStageBytes;
   static constexpr int kQBytes = kDecodeRows * D * 2;
-  static constexpr int kTotal = kStages * kStageBytes + kQBytes;
-  static_assert(4 * kDecodeRows * D * 4 <= kStages * kStageBytes, "merge buffer must fit");
+  static constexpr int kTotal = kWarps * kWarpBytes + kQBytes;
+  static_assert(kWarps * kDecodeRows * D * 4 <= kWarps * kWarpBytes, "merge buffer must fit");
 };
 
 // swizzled 16-byte chunk offset (bytes) of (row, chunk) in a [rows][D] bf16 tile
@@ -43,7 +48,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+  asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -134,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
   const int32_t* tiles = p.item_tiles + item * p.n_kt;
 
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
-  const uint32_t sQ = sbase + kStages * S::kStageBytes;
+  const uint32_t sQ = sbase + kWarps * S::kWarpBytes;
+  const uint32_t sW = sbase + warp * S::kWarpBytes;  // this warp's ring
 
   // ---- Q: 16 packed rows -> smem (zero for padding rows) ----
   for (int idx = tid; idx < kDecodeRows * S::kChunks; idx += kThreads) {
@@ -151,37 +157,60 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     }
   }
   cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
 
-  // ---- stage schedule: stage s = half (s & 1) of list entry t_begin + s/2 ----
-  const int n_stages = 2 * (t_end - t_begin);
-  auto stage_key0 = [&](int s, bool& partial, bool& live) -> int {
-    int e = tiles[t_begin + (s >> 1)];
+  // ---- this warp's chunks: c = warp, warp + 4, ... of the split ----
+  const int n_chunks = (t_end - t_begin) * (kKeysPerTile / kChunkKeys);
+  const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
+  const bool paged_fast = p.block_table && (p.page_size % kChunkKeys) == 0;
+  auto chunk_key0 = [&](int k, bool& partial, bool& live) -> int {
+    const int c = warp + k * kWarps;
+    const int e = tiles[t_begin + c / (kKeysPerTile / kChunkKeys)];
     partial = (e & 1) != 0;
-    int kj0 = (e >> 1) * kKeysPerTile + (s & 1) * kStageKeys;
-    live = (kj0 <= geo.jhi) && (kj0 + kStageKeys - 1 >= geo.jlo) && (kj0 < geo.kv_len);
+    const int kj0 = (e >> 1) * kKeysPerTile + (c % (kKeysPerTile / kChunkKeys)) * kChunkKeys;
+    live = (kj0 <= geo.jhi) && (kj0 + kChunkKeys - 1 >= geo.jlo) && (kj0 < geo.kv_len);
     return kj0;
   };
-  auto load_stage = [&](int s) {
+  // lane l copies 16-byte chunk (l % 16) of rows 2i + l / 16 (i = 0..7) of K and V:
+  // each instruction covers two whole rows (D = 128) or four (D = 64)
+  auto load_chunk = [&](int k) {
     bool partial, live;
-    int kj0 = stage_key0(s, partial, live);
-    if (live) {
-      uint32_t sK = sbase + (s % kStages) * S::kStageBytes;
-      uint32_t sV = sK + S::kKvBytes;
-#pragma unroll
-      for (int it = 0; it < kStageKeys * S::kChunks / kThreads; ++it) {
-        int idx = it * kThreads + tid;
-        int r = idx / S::kChunks, c = idx % S::kChunks;
-        int j = min(kj0 + r, geo.kv_len - 1);
-        cp_async16(sK + swz<D>(r, c), kv_row(p, p.k, p.k_sb, p.k_ss, p.k_sh, geo.b, geo.g, j) + c * 8);
-        cp_async16(sV + swz<D>(r, c), kv_row(p, p.v, p.v_sb, p.v_ss, p.v_sh, geo.b, geo.g, j) + c * 8);
+    const int kj0 = chunk_key0(k, partial, live);
+    if (!live) return;
+    const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
+    const uint32_t sV = sK + S::kKvBytes;
+    constexpr int kRowsPerInstr = 32 / S::kChunks;
+    const int c = lane % S::kChunks, r0 = lane / S::kChunks;
+    const uint16_t* kbase = nullptr;
+    const uint16_t* vbase = nullptr;
+    if (paged_fast) {
+      int pg = __ldg(p.block_table + (int64_t)geo.b * p.bt_stride + kj0 / p.page_size);
+      if ((unsigned)pg >= (unsigned)p.num_pages) {
+        record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)pg);
+        pg = 0;
       }
+      const int64_t row0 = kj0 % p.page_size;
+      kbase = p.k + (int64_t)pg * p.k_sb + row0 * p.k_ss + (int64_t)geo.g * p.k_sh;
+      vbase = p.v + (int64_t)pg * p.v_sb + row0 * p.v_ss + (int64_t)geo.g * p.v_sh;
+    }
+#pragma unroll
+    for (int i = 0; i < kChunkKeys / kRowsPerInstr; ++i) {
+      const int r = i * kRowsPerInstr + r0;
+      const int j = min(kj0 + r, geo.kv_len - 1);
+      const uint16_t* kr;
+      const uint16_t* vr;
+      if (paged_fast && kj0 + r < geo.kv_len) {
+        kr = kbase + (int64_t)r * p.k_ss;
+        vr = vbase + (int64_t)r * p.v_ss;
+      } else {
+        kr = kv_row(p, p.k, p.k_sb, p.k_ss, p.k_sh, geo.b, geo.g, j);
+        vr = kv_row(p, p.v, p.v_sb, p.v_ss, p.v_sh, geo.b, geo.g, j);
+      }
+      cp_async16(sK + swz<D>(r, c), kr + c * 8);
+      cp_async16(sV + swz<D>(r, c), vr + c * 8);
     }
   };
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    if (s < n_stages) load_stage(s);
-    cp_async_commit();
-  }
 
   // per-thread rows of the mma fragments: r0 = lane/4, r1 = r0 + 8
   const int r0 = lane >> 2;
@@ -192,55 +221,67 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     qi_r[e] = P / p.G;
     h_r[e] = geo.g * p.G + P % p.G;
   }
+  uint32_t qa[D / 16][4];
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    int row = (lane & 7) + 8 * ((lane >> 3) & 1);
+    int chunk = 2 * ks + (lane >> 4);
+    ldsm_x4(sQ + swz<D>(row, chunk), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+  }
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.f, 0.f};
   float o_acc[D / 8][4];
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
-  uint32_t qa[D / 16][4];
-  bool q_loaded = false;
 
-  for (int s = 0; s < n_stages; ++s) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
-    if (s + kStages - 1 < n_stages) load_stage(s + kStages - 1);
-    cp_async_commit();
-    if (!q_loaded) {
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        int row = (lane & 7) + 8 * ((lane >> 3) & 1);
-        int chunk = 2 * ks + (lane >> 4);
-        ldsm_x4(sQ + swz<D>(row, chunk), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-      }
-      q_loaded = true;
-    }
+  for (int k = 0; k < kWarpStages - 1; ++k) {
+    if (k < my_chunks) load_chunk(k);
+    cp_async_commit();
+  }
+  for (int k = 0; k < my_chunks; ++k) {
+    cp_async_wait<kWarpStages - 2>();
+    __syncwarp();
+    if (k + kWarpStages - 1 < my_chunks) load_chunk(k + kWarpStages - 1);
+    cp_async_commit();
     bool partial, live;
-    const int kj0 = stage_key0(s, partial, live);
-    const int wk0 = kj0 + 16 * warp;  // this warp's first key
-    if (!live || wk0 > geo.jhi || wk0 + 15 < geo.jlo || wk0 >= geo.kv_len) continue;
-    const uint32_t sK = sbase + (s % kStages) * S::kStageBytes;
+    const int kj0 = chunk_key0(k, partial, live);
+    if (!live) continue;
+    const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
     const uint32_t sV = sK + S::kKvBytes;
 
-    // ---- S = Q K^T : 16 rows x 16 keys ----
-    float sc[2][4];
+    // ---- S = Q K^T : 16 rows x 16 keys (two independent accumulator chains
+    // per key group, halving the dependent mma depth) ----
+    float sc[2][4], sc2[2][4];
 #pragma unroll
-    for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[n][e] = sc2[n][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      int key = 16 * warp + (lane & 7) + 8 * (lane >> 4);
+      int key = (lane & 7) + 8 * (lane >> 4);
       int chunk = 2 * ks + ((lane >> 3) & 1);
       uint32_t b0, b1, b2, b3;
       ldsm_x4(sK + swz<D>(key, chunk), b0, b1, b2, b3);
-      mma_bf16(sc[0], qa[ks], b0, b1);
-      mma_bf16(sc[1], qa[ks], b2, b3);
+      if (ks & 1) {
+        mma_bf16(sc2[0], qa[ks], b0, b1);
+        mma_bf16(sc2[1], qa[ks], b2, b3);
+      } else {
+        mma_bf16(sc[0], qa[ks], b0, b1);
+        mma_bf16(sc[1], qa[ks], b2, b3);
+      }
     }
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[n][e] += sc2[n][e];
     // ---- logit transform (log2 units) ----
     const bool plain = !partial && p.softcap == 0.f && p.mask_kind == FA_MASK_NONE;
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        int j = wk0 + 8 * n + 2 * (lane & 3) + (e & 1);
+        int j = kj0 + 8 * n + 2 * (lane & 3) + (e & 1);
         int rr = e >> 1;
         if (plain) {
           sc[n][e] *= p.scale_log2;
@@ -284,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     pa[3] = pack_bf16(sc[1][2], sc[1][3]);
 #pragma unroll
     for (int dn = 0; dn < D / 16; ++dn) {
-      int key = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1);
+      int key = (lane & 7) + 8 * ((lane >> 3) & 1);
       int chunk = 2 * dn + (lane >> 4);
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(sV + swz<D>(key, chunk), b0, b1, b2, b3);
@@ -296,15 +337,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
   __syncthreads();
 
   // ---- merge the 4 warps' (m, l, O) ----
-  float* red_m = reinterpret_cast<float*>(smem + kStages * S::kStageBytes);  // over Q: [4][16]
-  float* red_l = red_m + 4 * kDecodeRows;
+  float* red_m = reinterpret_cast<float*>(smem + kWarps * S::kWarpBytes);  // over Q: [4][16]
+  float* red_l = red_m + kWarps * kDecodeRows;
   float* obuf = reinterpret_cast<float*>(smem);  // [4][16][D]
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
     l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
   }
-  __syncthreads();  // Q area no longer read
   if ((lane & 3) == 0) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
@@ -319,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     int row = r0 + 8 * rr;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w * kDecodeRows + row]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * kDecodeRows + row]);
     float Mref = (M == -INFINITY) ? 0.f : M;
     f_own[rr] = fast_exp2(m_run[rr] - Mref);
   }
@@ -338,11 +378,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     const int c0 = (tid & 7) * (D / 8);
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w * kDecodeRows + row]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * kDecodeRows + row]);
     float Mref = (M == -INFINITY) ? 0.f : M;
     float L = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) L += red_l[w * kDecodeRows + row] * fast_exp2(red_m[w * kDecodeRows + row] - Mref);
+    for (int w = 0; w < kWarps; ++w)
+      L += red_l[w * kDecodeRows + row] * fast_exp2(red_m[w * kDecodeRows + row] - Mref);
     const bool empty = !(L > 0.f);
     const float inv = empty ? 0.f : 1.f / L;
     const float lse_val = empty ? -INFINITY : (Mref + __log2f(L)) * kLn2;
@@ -351,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     for (int c = 0; c < D / 8; ++c) {
       float acc = 0.f;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) acc += obuf[(w * kDecodeRows + row) * D + c0 + c];
+      for (int w = 0; w < kWarps; ++w) acc += obuf[(w * kDecodeRows + row) * D + c0 + c];
       vals[c] = acc * inv;
     }
     const int P = geo.rt * kDecodeRows + row;

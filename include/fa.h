@@ -145,7 +145,7 @@ typedef enum { FA_TILE_EMPTY = 0, FA_TILE_FULL = 1, FA_TILE_PARTIAL = 2 } fa_til
  * Work is cut into items: item = (seq * n_heads_sched + head) * n_row_tiles
  * + row_tile.  For the PREFILL path head is a q-head and a row tile is
  * rows_per_tile query rows.  For the DECODE path head is a K/V head and a row
- * tile is 16 consecutive packed rows p = i * (Hq/Hkv) + (h % (Hq/Hkv)) of that
+ * tile is 8 consecutive packed rows p = i * (Hq/Hkv) + (h % (Hq/Hkv)) of that
  * K/V head's query heads.  Keys are cut into tiles of keys_per_tile.
  *
  * Work list in the workspace after fa_fwd (device memory, int32):

@@ -406,9 +406,9 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_
   if (P.mask_kind == FA_MASK_DENSE) e = launch_mask_summary(P, st);
   if (e == cudaSuccess && P.mask_kind == FA_MASK_TOPK) e = launch_topk_prep(P, st);
   if (e == cudaSuccess) e = launch_classify(P, st);
-  if (e == cudaSuccess && opts->event_begin)
-    e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_begin), st);
-  if (e == cudaSuccess) e = (P.path == FA_PATH_PREFILL) ? launch_prefill(P, st) : launch_decode(P, st);
+  cudaEvent_t ev_begin = static_cast<cudaEvent_t>(opts->event_begin);
+  if (e == cudaSuccess)
+    e = (P.path == FA_PATH_PREFILL) ? launch_prefill(P, st, ev_begin) : launch_decode(P, st, ev_begin);
   if (e == cudaSuccess && opts->event_end)
     e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_end), st);
   if (e != cudaSuccess) {

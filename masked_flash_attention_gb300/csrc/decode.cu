@@ -1,7 +1,7 @@
 // decode.cu -- split-KV attention for few query rows per K/V head (decode,
 // speculative decode, short chunks), plus the split combine pass.
 //
-// One CTA = one item (sequence, K/V head, 16 packed rows) x one split of its
+// One CTA = one item (sequence, K/V head, 8 packed rows) x one split of its
 // scheduled key tiles.  The packed rows are the query heads of the K/V head's
 // group times the query positions, so a group shares every K/V byte it reads
 // (grouped-query heads without K/V expansion, InfiniTrain pull request 193
@@ -12,14 +12,17 @@
 // coalesced), through the paged block_table when there is one (vLLM pull
 // request 11277's flash_attn_varlen_func `block_table`; one page lookup per
 // chunk when the page size is a multiple of 16).  Warps never wait for each
-// other until the end.  S = Q K^T and O += P V run on mma.sync m16n8k16 (bf16
-// in, fp32 accumulate); 16 rows are too few for a 128-row tcgen05 tile.  The
+// other until the end.  S^T = K Q^T and O^T += V^T P^T run on mma.sync
+// m16n8k16 (bf16 in, fp32 accumulate) with keys / head-dim on M and the 8 query
+// rows on N, so a group of 4 q-heads wastes half of N instead of 3/4 of M;
+// 8 rows are far too few for a 128-row tcgen05 tile.  The
 // running softmax is guarded so that a fully masked chunk never produces NaN
 // (ExecuTorch pull request 10466 "Summary").
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "fa_device.cuh"
+#include "host_util.h"
 
 namespace mfa {
 
@@ -39,6 +42,7 @@ struct DecodeSmem {
   static constexpr int kQBytes = kDecodeRows * D * 2;
   static constexpr int kTotal = kWarps * kWarpBytes + kQBytes;
   static_assert(kWarps * kDecodeRows * D * 4 <= kWarps * kWarpBytes, "merge buffer must fit");
+  static_assert(2 * kWarps * kDecodeRows * 4 <= kQBytes, "warp statistics must fit over Q");
 };
 
 // swizzled 16-byte chunk offset (bytes) of (row, chunk) in a [rows][D] bf16 tile
@@ -68,6 +72,11 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -157,8 +166,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     }
   }
   cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
 
   // ---- this warp's chunks: c = warp, warp + 4, ... of the split ----
   const int n_chunks = (t_end - t_begin) * (kKeysPerTile / kChunkKeys);
@@ -212,33 +219,38 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     }
   };
 
-  // per-thread rows of the mma fragments: r0 = lane/4, r1 = r0 + 8
-  const int r0 = lane >> 2;
+  // Fragment roles: keys (and head-dim) on the mma M side, the 8 packed
+  // query rows on N.  Lane = 4 g + c holds S^T[key g, g+8][row 2c, 2c+1] and
+  // O^T[d 16m + g, + 8][row 2c, 2c+1].
+  const int g8 = lane >> 2, c4 = lane & 3;
   int qi_r[2], h_r[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    int P = geo.rt * kDecodeRows + r0 + 8 * e;
+    int P = geo.rt * kDecodeRows + 2 * c4 + e;
     qi_r[e] = P / p.G;
     h_r[e] = geo.g * p.G + P % p.G;
   }
-  uint32_t qa[D / 16][4];
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    int row = (lane & 7) + 8 * ((lane >> 3) & 1);
-    int chunk = 2 * ks + (lane >> 4);
-    ldsm_x4(sQ + swz<D>(row, chunk), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-  }
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-  float o_acc[D / 8][4];
-#pragma unroll
-  for (int n = 0; n < D / 8; ++n) o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
-
+  // the first chunks go out before Q is waited for, so their latency overlaps
 #pragma unroll
   for (int k = 0; k < kWarpStages - 1; ++k) {
     if (k < my_chunks) load_chunk(k);
     cp_async_commit();
   }
+  cp_async_wait<kWarpStages - 1>();  // this thread's Q copies have landed
+  __syncthreads();                   // ... and everyone else's
+  // Q^T as the B operand: [16 d x 8 rows] per k-step, two k-steps per ldmatrix.x4
+  uint32_t qb[D / 16][2];
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ks += 2) {
+    const int mi = lane >> 3;
+    ldsm_x4(sQ + swz<D>(lane & 7, 2 * ks + mi), qb[ks][0], qb[ks][1], qb[ks + 1][0], qb[ks + 1][1]);
+  }
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  float o_acc[D / 16][4];
+#pragma unroll
+  for (int n = 0; n < D / 16; ++n) o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
+
   for (int k = 0; k < my_chunks; ++k) {
     cp_async_wait<kWarpStages - 2>();
     __syncwarp();
@@ -250,136 +262,115 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
     const uint32_t sV = sK + S::kKvBytes;
 
-    // ---- S = Q K^T : 16 rows x 16 keys (two independent accumulator chains
-    // per key group, halving the dependent mma depth) ----
-    float sc[2][4], sc2[2][4];
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sc[n][e] = sc2[n][e] = 0.f;
+    // ---- S^T = K Q^T : 16 keys x 8 rows, two accumulator chains ----
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      int key = (lane & 7) + 8 * (lane >> 4);
-      int chunk = 2 * ks + ((lane >> 3) & 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(sK + swz<D>(key, chunk), b0, b1, b2, b3);
-      if (ks & 1) {
-        mma_bf16(sc2[0], qa[ks], b0, b1);
-        mma_bf16(sc2[1], qa[ks], b2, b3);
-      } else {
-        mma_bf16(sc[0], qa[ks], b0, b1);
-        mma_bf16(sc[1], qa[ks], b2, b3);
-      }
+      const int mi = lane >> 3;
+      uint32_t a[4];
+      ldsm_x4(sK + swz<D>((lane & 7) + 8 * (mi & 1), 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+      if (ks & 1) mma_bf16(sb, a, qb[ks][0], qb[ks][1]);
+      else mma_bf16(sa, a, qb[ks][0], qb[ks][1]);
     }
+    float sc[4];
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sc[n][e] += sc2[n][e];
-    // ---- logit transform (log2 units) ----
+    for (int e = 0; e < 4; ++e) sc[e] = sa[e] + sb[e];
+    // ---- logit transform (log2 units); element e: key g8 + 8 (e >> 1), row 2 c4 + (e & 1) ----
     const bool plain = !partial && p.softcap == 0.f && p.mask_kind == FA_MASK_NONE;
 #pragma unroll
-    for (int n = 0; n < 2; ++n) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int j = kj0 + 8 * n + 2 * (lane & 3) + (e & 1);
-        int rr = e >> 1;
-        if (plain) {
-          sc[n][e] *= p.scale_log2;
-        } else if (qi_r[rr] >= geo.q_len) {
-          sc[n][e] = -INFINITY;  // padding row: never read the mask out of range
-        } else {
-          sc[n][e] = logit_log2(p, sc[n][e], geo.b, h_r[rr], qi_r[rr], j, geo.off, geo.kv_len);
-        }
+    for (int e = 0; e < 4; ++e) {
+      const int j = kj0 + g8 + 8 * (e >> 1);
+      const int rr = e & 1;
+      if (plain) {
+        sc[e] *= p.scale_log2;
+      } else if (qi_r[rr] >= geo.q_len) {
+        sc[e] = -INFINITY;  // padding row: never read the mask out of range
+      } else {
+        sc[e] = logit_log2(p, sc[e], geo.b, h_r[rr], qi_r[rr], j, geo.off, geo.kv_len);
       }
     }
-    // ---- online softmax, -inf guarded ----
+    // ---- online softmax per row (a column of S^T), -inf guarded ----
     float alpha[2];
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      float mx = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]), fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      float m_new = fmaxf(m_run[rr], mx);
-      float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+      float mx = fmaxf(sc[rr], sc[rr + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run[rr], mx);
+      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
       alpha[rr] = fast_exp2(m_run[rr] - m_ref);
       m_run[rr] = m_new;
-      float rs = 0.f;
-#pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        sc[n][2 * rr] = fast_exp2(sc[n][2 * rr] - m_ref);
-        sc[n][2 * rr + 1] = fast_exp2(sc[n][2 * rr + 1] - m_ref);
-        rs += sc[n][2 * rr] + sc[n][2 * rr + 1];
-      }
-      l_run[rr] = l_run[rr] * alpha[rr] + rs;
+      sc[rr] = fast_exp2(sc[rr] - m_ref);
+      sc[rr + 2] = fast_exp2(sc[rr + 2] - m_ref);
+      l_run[rr] = l_run[rr] * alpha[rr] + sc[rr] + sc[rr + 2];
     }
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o_acc[n][0] *= alpha[0]; o_acc[n][1] *= alpha[0];
-      o_acc[n][2] *= alpha[1]; o_acc[n][3] *= alpha[1];
+    for (int n = 0; n < D / 16; ++n) {
+      o_acc[n][0] *= alpha[0]; o_acc[n][1] *= alpha[1];
+      o_acc[n][2] *= alpha[0]; o_acc[n][3] *= alpha[1];
     }
-    // ---- O += P V ----
-    uint32_t pa[4];
-    pa[0] = pack_bf16(sc[0][0], sc[0][1]);
-    pa[1] = pack_bf16(sc[0][2], sc[0][3]);
-    pa[2] = pack_bf16(sc[1][0], sc[1][1]);
-    pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+    // ---- P^T (C layout) -> B operand [16 keys x 8 rows] by an 8x8 transpose ----
+    const uint32_t pb0 = movmatrix_t(pack_bf16(sc[0], sc[1]));  // keys 0..7
+    const uint32_t pb1 = movmatrix_t(pack_bf16(sc[2], sc[3]));  // keys 8..15
+    // ---- O^T += V^T P^T : per 16 head-dim values, one mma over the 16 keys ----
 #pragma unroll
-    for (int dn = 0; dn < D / 16; ++dn) {
-      int key = (lane & 7) + 8 * ((lane >> 3) & 1);
-      int chunk = 2 * dn + (lane >> 4);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(sV + swz<D>(key, chunk), b0, b1, b2, b3);
-      mma_bf16(o_acc[2 * dn], pa, b0, b1);
-      mma_bf16(o_acc[2 * dn + 1], pa, b2, b3);
+    for (int mt = 0; mt < D / 16; ++mt) {
+      const int mi = lane >> 3;
+      uint32_t a[4];
+      ldsm_x4_t(sV + swz<D>((lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+      mma_bf16(o_acc[mt], a, pb0, pb1);
     }
   }
   cp_async_wait<0>();
   __syncthreads();
 
   // ---- merge the 4 warps' (m, l, O) ----
-  float* red_m = reinterpret_cast<float*>(smem + kWarps * S::kWarpBytes);  // over Q: [4][16]
+  float* red_m = reinterpret_cast<float*>(smem + kWarps * S::kWarpBytes);  // over Q: [4][8]
   float* red_l = red_m + kWarps * kDecodeRows;
-  float* obuf = reinterpret_cast<float*>(smem);  // [4][16][D]
+  float* obuf = reinterpret_cast<float*>(smem);  // [4][8][D]
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
-    l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
-    l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
+    l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 4);
+    l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 8);
+    l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 16);
   }
-  if ((lane & 3) == 0) {
+  if (g8 == 0) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      red_m[warp * kDecodeRows + r0 + 8 * rr] = m_run[rr];
-      red_l[warp * kDecodeRows + r0 + 8 * rr] = l_run[rr];
+      red_m[warp * kDecodeRows + 2 * c4 + rr] = m_run[rr];
+      red_l[warp * kDecodeRows + 2 * c4 + rr] = l_run[rr];
     }
   }
   __syncthreads();
   float f_own[2];
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
-    int row = r0 + 8 * rr;
+    const int row = 2 * c4 + rr;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * kDecodeRows + row]);
-    float Mref = (M == -INFINITY) ? 0.f : M;
+    const float Mref = (M == -INFINITY) ? 0.f : M;
     f_own[rr] = fast_exp2(m_run[rr] - Mref);
   }
 #pragma unroll
-  for (int n = 0; n < D / 8; ++n) {
-    int col = 8 * n + 2 * (lane & 3);
-    float* o0 = obuf + (warp * kDecodeRows + r0) * D + col;
-    float* o1 = obuf + (warp * kDecodeRows + r0 + 8) * D + col;
-    o0[0] = o_acc[n][0] * f_own[0]; o0[1] = o_acc[n][1] * f_own[0];
-    o1[0] = o_acc[n][2] * f_own[1]; o1[1] = o_acc[n][3] * f_own[1];
+  for (int mt = 0; mt < D / 16; ++mt) {
+    float* ow = obuf + (warp * kDecodeRows) * D;
+    ow[(2 * c4) * D + 16 * mt + g8] = o_acc[mt][0] * f_own[0];
+    ow[(2 * c4 + 1) * D + 16 * mt + g8] = o_acc[mt][1] * f_own[1];
+    ow[(2 * c4) * D + 16 * mt + g8 + 8] = o_acc[mt][2] * f_own[0];
+    ow[(2 * c4 + 1) * D + 16 * mt + g8 + 8] = o_acc[mt][3] * f_own[1];
   }
   __syncthreads();
-  // each thread: one row, D/8 consecutive columns
+  // each thread: one row, D/16 consecutive columns
   {
-    const int row = tid >> 3;            // 16 rows x 8 threads
-    const int c0 = (tid & 7) * (D / 8);
+    constexpr int kCols = D / 16;
+    const int row = tid >> 4;  // 8 rows x 16 threads
+    const int c0 = (tid & 15) * kCols;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * kDecodeRows + row]);
-    float Mref = (M == -INFINITY) ? 0.f : M;
+    const float Mref = (M == -INFINITY) ? 0.f : M;
     float L = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w)
@@ -387,9 +378,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     const bool empty = !(L > 0.f);
     const float inv = empty ? 0.f : 1.f / L;
     const float lse_val = empty ? -INFINITY : (Mref + __log2f(L)) * kLn2;
-    float vals[D / 8];
+    float vals[kCols];
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
+    for (int c = 0; c < kCols; ++c) {
       float acc = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) acc += obuf[(w * kDecodeRows + row) * D + c0 + c];
@@ -401,23 +392,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
       out_ptrs(p, geo, P, optr, lptr, valid);
       if (valid) {
 #pragma unroll
-        for (int c = 0; c < D / 8; c += 8) {
-          uint4 pk;
+        for (int c = 0; c < kCols; c += 4) {
+          uint2 pk;
           pk.x = pack_bf16(vals[c + 0], vals[c + 1]);
           pk.y = pack_bf16(vals[c + 2], vals[c + 3]);
-          pk.z = pack_bf16(vals[c + 4], vals[c + 5]);
-          pk.w = pack_bf16(vals[c + 6], vals[c + 7]);
-          *reinterpret_cast<uint4*>(optr + c0 + c) = pk;
+          *reinterpret_cast<uint2*>(optr + c0 + c) = pk;
         }
-        if ((tid & 7) == 0) *lptr = lse_val;
+        if ((tid & 15) == 0) *lptr = lse_val;
       }
     } else {
       int64_t slot = (item * p.n_splits + split) * kDecodeRows + row;
       float* po = p.part_o + slot * D + c0;
 #pragma unroll
-      for (int c = 0; c < D / 8; c += 4)
+      for (int c = 0; c < kCols; c += 4)
         *reinterpret_cast<float4*>(po + c) = make_float4(vals[c], vals[c + 1], vals[c + 2], vals[c + 3]);
-      if ((tid & 7) == 0) p.part_lse[slot] = lse_val;
+      if ((tid & 15) == 0) p.part_lse[slot] = lse_val;
     }
   }
 }
@@ -425,14 +414,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
 // Merge the splits of items that had more than one: LSE = logsumexp of the
 // split LSEs (all -inf -> -inf), O = sum_s exp(LSE_s - LSE) O_s (0 if empty).
 template <int D>
-__global__ void __launch_bounds__(512) combine_kernel(const Params p) {
+__global__ void __launch_bounds__(32 * kDecodeRows) combine_kernel(const Params p) {
   const int64_t item = blockIdx.x;
   const int count = p.item_count[item];
   if (count <= p.tiles_per_split) return;
   const int n_eff = (count + p.tiles_per_split - 1) / p.tiles_per_split;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ItemGeo geo = item_geo(p, item);
-  const int row = warp;  // 16 warps = 16 packed rows
+  const int row = warp;  // one warp per packed row
   uint16_t* optr; float* lptr; bool valid;
   out_ptrs(p, geo, geo.rt * kDecodeRows + row, optr, lptr, valid);
   if (!valid) return;
@@ -462,24 +451,25 @@ __global__ void __launch_bounds__(512) combine_kernel(const Params p) {
 }
 
 template <int D>
-cudaError_t launch_decode_d(const Params& p, cudaStream_t st) {
+cudaError_t launch_decode_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
   using S = DecodeSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
+  cudaError_t e = ensure_smem_attr<decode_kernel<D>>(S::kTotal);
   if (e != cudaSuccess) return e;
+  if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
   int64_t grid = p.n_items * p.n_splits;
   decode_kernel<D><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.n_splits <= 1) return e;
-  combine_kernel<D><<<(unsigned)p.n_items, 512, 0, st>>>(p);
+  combine_kernel<D><<<(unsigned)p.n_items, 32 * kDecodeRows, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const Params& p, cudaStream_t st) {
-  if (p.n_items <= 0) return cudaSuccess;
-  if (p.d == 64) return launch_decode_d<64>(p, st);
-  return launch_decode_d<128>(p, st);
+cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
+  if (p.n_items <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
+  if (p.d == 64) return launch_decode_d<64>(p, st, ev_begin);
+  return launch_decode_d<128>(p, st, ev_begin);
 }
 
 }  // namespace mfa

@@ -12,7 +12,7 @@ namespace mfa {
 
 constexpr int kKeysPerTile = 128;     // scheduler key tile
 constexpr int kPrefillRows = 128;     // query rows per prefill item (tcgen05 M)
-constexpr int kDecodeRows = 16;       // packed rows per decode item (mma M)
+constexpr int kDecodeRows = 8;        // packed rows per decode item (mma N)
 constexpr int kMaxTopkKeys = 16384;   // top-k preparation keeps all keys of a row in smem
 
 // Workspace header (first 256 bytes of the workspace).
@@ -78,7 +78,9 @@ struct Params {
 cudaError_t launch_mask_summary(const Params& p, cudaStream_t st);
 cudaError_t launch_topk_prep(const Params& p, cudaStream_t st);
 cudaError_t launch_classify(const Params& p, cudaStream_t st);
-cudaError_t launch_decode(const Params& p, cudaStream_t st);
-cudaError_t launch_prefill(const Params& p, cudaStream_t st);
+// The attention launchers record `ev_begin` (if not null) on the stream right
+// before the kernel itself is enqueued, after all host-side preparation.
+cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
+cudaError_t launch_prefill(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
 
 }  // namespace mfa

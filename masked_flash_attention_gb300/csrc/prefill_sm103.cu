@@ -51,6 +51,7 @@
 #include <mutex>
 
 #include "fa_device.cuh"
+#include "host_util.h"
 #include "tc_sm103.cuh"
 
 namespace mfa {
@@ -649,7 +650,7 @@ bool encode_bshd(CUtensorMap* m, const void* base, int d, int heads, int64_t row
 
 template <int D, int MK, bool SC>
 cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap& mq, const CUtensorMap& mk,
-                             const CUtensorMap& mv, int64_t grid) {
+                             const CUtensorMap& mv, int64_t grid, cudaEvent_t ev_begin) {
   auto kern = prefill_kernel<D, MK, SC>;
   // setmaxnreg.inc would wait forever if the block were launched with fewer
   // registers than the split assumes: launch only when the build matches.
@@ -661,14 +662,15 @@ cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap
     regs = fa.numRegs;
   }
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PCfg<D>::kSmem);
+  cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC>>(PCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
+  if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
   kern<<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv);
   return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_prefill_d(const Params& p, cudaStream_t st) {
+cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
   CUtensorMap mq, mk, mv;
   const bool vq = p.cu_q != nullptr, vk = p.cu_k != nullptr;
   // extents of 1 get a harmless stride (the stride of the next-inner dimension)
@@ -686,27 +688,27 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st) {
     grid = (int64_t)p.n_row_tiles * p.n_seq * p.Hkv * ((p.G + 1) / 2);
   else
     grid = (int64_t)((p.n_row_tiles + 1) / 2) * p.n_seq * p.Hq;
-  if (grid <= 0) return cudaSuccess;
+  if (grid <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
   const bool sc = p.softcap > 0.f;
   switch (p.mask_kind) {
     case FA_MASK_DENSE:
-      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true>(p, st, mq, mk, mv, grid)
-                : launch_prefill_v<D, FA_MASK_DENSE, false>(p, st, mq, mk, mv, grid);
+      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true>(p, st, mq, mk, mv, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_DENSE, false>(p, st, mq, mk, mv, grid, ev_begin);
     case FA_MASK_TOPK:
-      return sc ? launch_prefill_v<D, FA_MASK_TOPK, true>(p, st, mq, mk, mv, grid)
-                : launch_prefill_v<D, FA_MASK_TOPK, false>(p, st, mq, mk, mv, grid);
+      return sc ? launch_prefill_v<D, FA_MASK_TOPK, true>(p, st, mq, mk, mv, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_TOPK, false>(p, st, mq, mk, mv, grid, ev_begin);
     default:
-      return sc ? launch_prefill_v<D, FA_MASK_NONE, true>(p, st, mq, mk, mv, grid)
-                : launch_prefill_v<D, FA_MASK_NONE, false>(p, st, mq, mk, mv, grid);
+      return sc ? launch_prefill_v<D, FA_MASK_NONE, true>(p, st, mq, mk, mv, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_NONE, false>(p, st, mq, mk, mv, grid, ev_begin);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const Params& p, cudaStream_t st) {
-  if (p.n_items <= 0) return cudaSuccess;
-  if (p.d == 64) return launch_prefill_d<64>(p, st);
-  return launch_prefill_d<128>(p, st);
+cudaError_t launch_prefill(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
+  if (p.n_items <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
+  if (p.d == 64) return launch_prefill_d<64>(p, st, ev_begin);
+  return launch_prefill_d<128>(p, st, ev_begin);
 }
 
 }  // namespace mfa

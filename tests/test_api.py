@@ -44,7 +44,7 @@ def test_plan_ok_and_geometry():
     rc, p = plan(T(4, 1, 32, 128), T(4, 700, 8, 128), T(4, 700, 8, 128), causal=True)
     assert rc == 0
     assert p["path"] == _lib.FA_PATH_DECODE
-    assert p["n_heads_sched"] == 8 and p["rows_per_tile"] == 16 and p["n_row_tiles"] == 1
+    assert p["n_heads_sched"] == 8 and p["rows_per_tile"] == 8 and p["n_row_tiles"] == 1
     assert p["n_k_tiles"] == 6 and p["n_items"] == 32
     assert p["workspace_bytes"] >= p["off_tiles"] + 32 * 6 * 4
 

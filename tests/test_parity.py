@@ -56,7 +56,7 @@ SWEEP = [
     (2, 3, 300, 12, 4, 64, dict(causal=True)),
     (1, 5, 129, 6, 2, 128, dict(causal=True, window_left=7, window_right=2)),
     (2, 4, 260, 16, 2, 128, dict()),                       # group of 8, not causal
-    (1, 17, 200, 3, 1, 64, dict(causal=True)),             # 17*3 packed rows: 4 row tiles
+    (1, 17, 200, 3, 1, 64, dict(causal=True)),             # 17*3 packed rows: 7 row tiles
     (2, 130, 300, 4, 2, 128, dict(causal=True)),
     (1, 257, 257, 2, 2, 64, dict(causal=True)),
     (1, 200, 100, 2, 1, 128, dict(causal=True)),           # q_len > kv_len: empty rows

@@ -61,7 +61,8 @@ def oracle_classes(case, plan, **over):
             X = np.stack(X)
             for rt in range(n_rt):
                 if decode:
-                    i0, i1 = rt * 16 // G, (rt * 16 + 15) // G
+                    R = plan["rows_per_tile"]  # packed rows (query, head-in-group)
+                    i0, i1 = rt * R // G, (rt * R + R - 1) // G
                 else:
                     i0, i1 = rt * plan["rows_per_tile"], (rt + 1) * plan["rows_per_tile"] - 1
                 i1 = min(i1, Sq - 1)

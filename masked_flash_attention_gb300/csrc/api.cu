@@ -15,10 +15,6 @@
 
 #include "fa_internal.h"
 
-namespace mfa {
-size_t topk_prep_smem(int Sk);
-}
-
 using namespace mfa;
 
 namespace {
@@ -54,7 +50,7 @@ int check_i32_vec(const fa_tensor* t, int64_t len) {
 struct Plan {
   fa_plan pub;
   Params prm;
-  size_t off_summary, off_topk_e, off_topk_maxe, off_part_o, off_part_lse;
+  size_t off_summary, off_topk_e, off_topk_maxe, off_topk_sorted, off_part_o, off_part_lse;
 };
 
 int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
@@ -284,6 +280,8 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   if (mask_kind == FA_MASK_TOPK) off = align_up(off + (size_t)n_seq * Hq * Sk * 4);
   pl->off_topk_maxe = off;
   if (mask_kind == FA_MASK_TOPK) off = align_up(off + (size_t)n_seq * Hq * n_kt_alloc * 4);
+  pl->off_topk_sorted = off;
+  if (mask_kind == FA_MASK_TOPK) off = align_up(off + (size_t)n_seq * Hq * n_kt_alloc * kKeysPerTile * 8);
   pl->off_part_o = off;
   if (P.n_splits > 1) off = align_up(off + (size_t)P.n_items * P.n_splits * kDecodeRows * d * 4);
   pl->off_part_lse = off;
@@ -301,7 +299,7 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   pub.n_items = P.n_items;
   pub.off_topk_e = (mask_kind == FA_MASK_TOPK) ? pl->off_topk_e : 0;
   pub.n_kernels = P.n_items == 0 ? 0
-                  : 2 + (P.n_splits > 1) + (mask_kind == FA_MASK_DENSE) + (mask_kind == FA_MASK_TOPK);
+                  : 2 + (P.n_splits > 1) + (mask_kind == FA_MASK_DENSE) + 2 * (mask_kind == FA_MASK_TOPK);
   pub.workspace_bytes = off;
   P.n_kt = n_kt_alloc;
   return FA_OK;
@@ -317,6 +315,7 @@ void bind_workspace(Plan* pl, void* ws) {
   P.mask_summary = base + pl->off_summary;
   P.topk_e = reinterpret_cast<int32_t*>(base + pl->off_topk_e);
   P.topk_tile_maxe = reinterpret_cast<int32_t*>(base + pl->off_topk_maxe);
+  P.topk_sorted = reinterpret_cast<uint64_t*>(base + pl->off_topk_sorted);
   P.part_o = reinterpret_cast<float*>(base + pl->off_part_o);
   P.part_lse = reinterpret_cast<float*>(base + pl->off_part_lse);
 }

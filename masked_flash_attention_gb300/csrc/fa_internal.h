@@ -64,6 +64,7 @@ struct Params {
   uint8_t* mask_summary; // [m_nb][m_nh][n_row_tiles][n_kt]
   int32_t* topk_e;       // [n_seq][Hq][Sk]: first query row at which key j is dropped
   int32_t* topk_tile_maxe;  // [n_seq][Hq][n_kt]
+  uint64_t* topk_sorted; // [n_seq][Hq][n_kt * 128]: per 128-key bucket, its keys' words sorted
 
   // decode split-KV
   int32_t n_splits, tiles_per_split;

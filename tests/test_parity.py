@@ -130,6 +130,7 @@ def test_dense_mask_per_head():
     (2, 1, 9, 1000, 2, 64, 300, True, False),
     (3, 1, 2, 700, 2, 128, 100, False, True),
     (4, 1, 1, 129, 1, 64, 200, True, False),    # keep_window larger than the row
+    (5, 1, 40, 9000, 2, 128, 3000, True, True),  # more than 64 key buckets
 ])
 def test_topk(seed, B, Sq, Sk, H, d, keep, causal, ties):
     c = W.random_case(seed, B=B, Sq=Sq, Sk=Sk, Hq=H, Hkv=H, d=d, causal=causal)

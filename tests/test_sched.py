@@ -138,7 +138,8 @@ def test_dense_mask_classes_exact():
 def test_topk_kept_sets_exact(golden):
     g = golden("fsa_mask_agreement.json")
     for seed, Sq, Sk, keep, causal, ties in [(0, 300, 300, 40, True, True), (1, 64, 500, 100, True, False),
-                                             (2, 7, 260, 30, False, True), (3, 4, 4, 2, True, False)]:
+                                             (2, 7, 260, 30, False, True), (3, 4, 4, 2, True, False),
+                                             (4, 40, 9000, 3000, True, True)]:  # > 64 key buckets
         case = W.random_case(seed, B=1, Sq=Sq, Sk=Sk, Hq=2, Hkv=2, d=64, causal=causal)
         z = W.random_zero_hold_states(seed, 1, 2, Sk, ties=ties)
         plan, counts, tiles, stats, ws = worklist(case, zero_hold_states=z, keep_window=keep)

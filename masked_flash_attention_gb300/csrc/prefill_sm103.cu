@@ -186,6 +186,23 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return *reinterpret_cast<float2*>(&d);
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 128 values held as 64 pairs: a tree of three-input maxima over
+// four independent accumulators.
+__device__ __forceinline__ float row_max128(const float2 (&x)[64]) {
+  float m[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m[k] = fmaxf(x[k].x, x[k].y);
+#pragma unroll
+  for (int i = 4; i < 64; ++i) m[i & 3] = max3f(m[i & 3], x[i].x, x[i].y);
+  return max3f(fmaxf(m[0], m[1]), m[2], m[3]);
+}
+
 __device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag, uint32_t where) {
   if (!*abort_flag) {
     *abort_flag = 1;
@@ -448,7 +465,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int kt;
       bool in[2], pa[2];
       while (m.next(kt, in[0], in[1], pa[0], pa[1])) {
-        if (!in[t]) continue;
+        const bool mine = t ? in[1] : in[0];
+        const bool part = t ? pa[1] : pa[0];
+        if (!mine) continue;
         const int j0 = kt * kKeysPerTile;
         if (MK == FA_MASK_TOPK) {
           const int jj = j0 + wtid;
@@ -465,7 +484,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (!tc::mbar_wait(s_full + t, sph, abort_flag)) { ok = false; break; }
         sph ^= 1;
         tc::fence_after_sync();
-        float x[128];
+        float2 x[64];
         {
           uint32_t r[4][32];
 #pragma unroll
@@ -474,35 +493,29 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[c][e]);
+            for (int e = 0; e < 16; ++e)
+              x[c * 16 + e] = make_float2(__uint_as_float(r[c][2 * e]), __uint_as_float(r[c][2 * e + 1]));
         }
         // logits in log2 units; a FULL tile without soft-cap keeps raw scores
         // and folds the scale into the exponent below
-        const bool plain = !SC && !pa[t];
-        float mx = -INFINITY;
+        const bool plain = !SC && !part;
+        float mx;
         if (plain) {
-          float m8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = x[k];
-#pragma unroll
-          for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
-          mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])) * p.scale_log2;
+          mx = row_max128(x) * p.scale_log2;
         } else {
           const int clo = jlo_r - j0, chi = jhi_r - j0;
-          const bool all_in = !pa[t];
+          const bool all_in = !part;
           const float* mrow = nullptr;
           if (MK == FA_MASK_DENSE && i < q_len)
             mrow = p.mask + (int64_t)(p.m_nb > 1 ? b : 0) * p.m_sb + (int64_t)(p.m_nh > 1 ? h : 0) * p.m_sh +
                    (int64_t)i * p.m_sq + (int64_t)j0 * p.m_sk;
 #pragma unroll
           for (int e = 0; e < 128; ++e) {
-            float v;
+            float v = (e & 1) ? x[e >> 1].y : x[e >> 1].x;
             if (SC) {
-              v = p.softcap * tanhf(x[e] * p.scale / p.softcap) * kLog2e;
+              v = p.softcap * tanhf(v * p.scale / p.softcap) * kLog2e;
             } else {
-              v = x[e] * p.scale_log2;
+              v = v * p.scale_log2;
             }
             bool keep = all_in || (e >= clo && e <= chi);
             if (MK == FA_MASK_DENSE && !all_in) {
@@ -513,16 +526,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               keep = keep && (i < kv.x);
               v += __int_as_float(kv.y);
             }
-            x[e] = keep ? v : -INFINITY;
+            v = keep ? v : -INFINITY;
+            if (e & 1) x[e >> 1].y = v; else x[e >> 1].x = v;
           }
-          float m8[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = x[k];
-#pragma unroll
-          for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], x[e]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
-          mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]));
+          mx = row_max128(x);
         }
         // raise the exponent reference only when the row max outgrew it by 2^8
         const bool upd = mx > m_ref + kRescaleLog2;
@@ -547,23 +554,38 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           m_ref = mx;
         }
         const float eref = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 ner = make_float2(-eref, -eref);
         float2 acc[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
+        for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+        // P = exp2(x - ref): one packed FMA (FULL: scale folded in) or add per pair
+        if (plain) {
+          const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float2 v = make_float2(x[c * 32 + 2 * e], x[c * 32 + 2 * e + 1]);
-            v = plain ? fma2(v, sl2, ner) : add2(v, ner);
-            const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
-            acc[e & 3] = add2(acc[e & 3], pe);
-            pk[e] = pack2(pe.x, pe.y);
+            for (int e = 0; e < 16; ++e) {
+              const float2 v = fma2(x[c * 16 + e], sl2, ner);
+              const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
+              acc[e & 3] = add2(acc[e & 3], pe);
+              pk[e] = pack2(pe.x, pe.y);
+            }
+            tc::tmem_st16(scol + c * 16, pk);
           }
-          tc::tmem_st16(scol + c * 16, pk);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float2 v = add2(x[c * 16 + e], ner);
+              const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
+              acc[e & 3] = add2(acc[e & 3], pe);
+              pk[e] = pack2(pe.x, pe.y);
+            }
+            tc::tmem_st16(scol + c * 16, pk);
+          }
         }
         acc[0] = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
         l += acc[0].x + acc[0].y;

@@ -17,9 +17,9 @@
 //
 // Warp roles (12 warps = 3 warpgroups):
 //   warp 0      TMA producer: Q once, then K tiles through an NS-stage ring
-//   warp 1      MMA issuer (one thread) and TMEM owner
+//   warp 1      MMA issuer for sub-tile 0 (one thread) and TMEM owner
 //   warp 2      TMA producer: V tiles through an NS-stage ring
-//   warp 3      idle
+//   warp 3      MMA issuer for sub-tile 1 (one thread)
 //   warps 4..7  softmax warpgroup for sub-tile 0, warps 8..11 for sub-tile 1
 // Registers: the block launches with 168 per thread (3 warps share an SM
 // sub-partition); warpgroup 0 (producer, MMA) hands registers back with
@@ -30,10 +30,10 @@
 // row, and top-k tiles stage their keys' expiry rows and bias in smem.
 // TMEM (512 columns): S_t = Q_t K^T in columns [128 t, 128 t + 128), fp32;
 // P_t (bf16, two per column) overwrites the first 64 of them; O_t in
-// [256 + D t, 256 + D t + D).  Per key tile j the MMA thread issues
-//   PV_0(j-1), QK_0(j), PV_1(j-1), QK_1(j)
-// so that sub-tile 0's softmax of tile j overlaps sub-tile 1's MMAs and vice
-// versa.  Each softmax thread owns one query row (32x32b TMEM loads), so the
+// [256 + D t, 256 + D t + D).  Per key tile j the two MMA issuers put out
+//   PV_0(j-1), QK_0(j) | PV_1(j-1), QK_1(j)
+// in that order, so that sub-tile 0's softmax of tile j overlaps sub-tile 1's
+// MMAs and vice versa.  Each softmax thread owns one query row (32x32b TMEM loads), so the
 // row max and row sum need no cross-lane reduction.  The running max is the
 // exponent reference and is only raised when the row max exceeds it by more
 // than 2^8 (in log2 units), so O in TMEM is rarely rescaled.  A fully masked
@@ -49,6 +49,7 @@
 
 #include <climits>
 #include <mutex>
+#include <type_traits>
 
 #include "fa_device.cuh"
 #include "host_util.h"
@@ -186,6 +187,48 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return *reinterpret_cast<float2*>(&d);
 }
 
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+// a + b rounded toward minus infinity
+__device__ __forceinline__ float2 add2_rm(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rm.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+  return *reinterpret_cast<float2*>(&d);
+}
+
+// 2^v for a pair, on the FMA and integer pipes instead of the special-function
+// unit, whose 16 results per clock and SM would otherwise bound the softmax.
+// v = n + f with n = floor(v), f in [0, 1); 2^f ~ 1 + f (c1 + f (c2 + f c3)),
+// a minimax cubic for the relative error (at most 8.6e-5, below the 2^-9
+// rounding of the bf16 P it feeds), fitted by exp2_fit.py in this package;
+// n is added to the exponent field.  v is clamped at -127, where the result is
+// exactly 0.  Only used where v <= 8 is known (FULL tiles, lazy rescale bound).
+constexpr float kExp2C1 = 6.951167865e-01f;
+constexpr float kExp2C2 = 2.276449909e-01f;
+constexpr float kExp2C3 = 7.706704220e-02f;
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: ulp 1, so v + it rounds v to an integer
+__device__ __forceinline__ float2 exp2_poly2(float2 v) {
+  v.x = fmaxf(v.x, -127.f);
+  v.y = fmaxf(v.y, -127.f);
+  const float2 magic = make_float2(kRoundMagic, kRoundMagic);
+  const float2 t = add2_rm(v, magic);        // floor(v) + magic, exact
+  const float2 f = sub2(v, sub2(t, magic));  // v - floor(v), exact
+  float2 q = fma2(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
+  q = fma2(q, f, make_float2(kExp2C1, kExp2C1));
+  q = fma2(q, f, make_float2(1.f, 1.f));
+  // the low mantissa bits of t hold floor(v); shifted by 23 they add it to the
+  // exponent of q (the magic's own bits shift out)
+  return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
+                     __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
+}
+
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -278,8 +321,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* s_full = v_empty + NS;    // [2]
   uint64_t* p_full = s_full + 2;      // [2]
   uint64_t* o_final = p_full + 2;     // [2]
-  uint64_t* mma_done = o_final + 2;   // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* mma_done = o_final + 2;   // [2]
+  uint64_t* tok = mma_done + 2;       // [2] issue-order token between the MMA issuers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tok + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (tid == 0) {
@@ -287,15 +331,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     for (int s = 0; s < NS; ++s) {
       tc::mbar_init(k_full + s, 1);
       tc::mbar_init(v_full + s, 1);
-      tc::mbar_init(k_empty + s, 1);
-      tc::mbar_init(v_empty + s, 1);
+      tc::mbar_init(k_empty + s, 2);  // one arrival per MMA issuer
+      tc::mbar_init(v_empty + s, 2);
     }
     for (int t = 0; t < 2; ++t) {
       tc::mbar_init(s_full + t, 1);
       tc::mbar_init(p_full + t, 128);
       tc::mbar_init(o_final + t, 1);
+      tc::mbar_init(mma_done + t, 1);
+      tc::mbar_init(tok + t, 1);
     }
-    tc::mbar_init(mma_done, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -362,78 +407,93 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           if (is_k) tc::mbar_wait_drain(q_full, 0, 100000000ull);
         }
       }
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
+    } else if (warp == 1 || warp == 3) {
+      // ---------------------------------------------------------- MMA issuers
+      // The MMA queue is shallow: an issuing thread stalls on tcgen05.mma almost
+      // at once, so whatever a lone issuer does between its MMA groups (waits,
+      // list walk, commits) is tensor idle time.  Two issuers, one per sub-tile
+      // (warp 1: sub-tile 0, warp 3: sub-tile 1), hand a token back and forth so
+      // that the groups still go out in the order PV_0 QK_0 | PV_1 QK_1 | PV_0 ...
+      // (the ping-pong of the two softmax warpgroups) while each one's
+      // bookkeeping overlaps the other's MMAs.  Both walk the merged tile list,
+      // which the K/V rings follow; a stage is released once both are done with
+      // it (arrival count 2).
+      auto issue = [&](auto T) {
+        constexpr int t = decltype(T)::value;
         constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
-        const uint32_t sQ = tc::smem_u32(smem + C::kQOff);
+        const uint32_t sQ = tc::smem_u32(smem + C::kQOff + t * C::kTileBytes);
         const uint32_t sK = tc::smem_u32(smem + C::kKOff);
         const uint32_t sV = tc::smem_u32(smem + C::kVOff);
+        const uint32_t tS = tbase + t * 128, tO = tbase + C::kOCol + t * D;
         bool ok = tc::mbar_wait(q_full, 0, abort_flag);
         if (!ok) fail(p, abort_flag, 2);
         tc::fence_after_sync();
-        int remaining[2] = {st[0].count, st[1].count};
-        bool pend[2] = {false, false};
-        bool started[2] = {false, false};
-        uint32_t pph[2] = {0, 0};
-        int ps = 0, j = 0;
-        auto do_pv = [&](int t, int sp) -> bool {
-          if (!tc::mbar_wait(p_full + t, pph[t], abort_flag)) return false;
-          pph[t] ^= 1;
+        int prev = -1;        // merged index of this sub-tile's last QK; its PV is pending
+        bool o_acc = false;   // O already holds a partial sum
+        uint32_t pph = 0, tph = 0;
+        auto do_pv = [&]() -> bool {
+          const int ps = prev % NS;
+          if (!tc::mbar_wait(p_full + t, pph, abort_flag)) return false;
+          pph ^= 1;
           tc::fence_after_sync();
-          const uint32_t vbase = sV + sp * C::kTileBytes;
+          const uint32_t vbase = sV + ps * C::kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            uint64_t bd = tc::sdesc_sw128(vbase + ks * 2048, 16384, 1024);
-            tc::mma_ts(tbase + C::kOCol + t * D, tbase + t * 128 + ks * 8, bd, idO,
-                       (started[t] || ks > 0) ? 1u : 0u);
-          }
-          started[t] = true;
-          pend[t] = false;
-          if (remaining[t] == 0) tc::mma_commit(o_final + t);
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_ts(tO, tS + ks * 8, tc::sdesc_sw128(vbase + ks * 2048, 16384, 1024), idO,
+                       (o_acc || ks > 0) ? 1u : 0u);
+          o_acc = true;
+          tc::mma_commit(v_empty + ps);
           return true;
         };
         Merge m;
         m.init(st);
-        int kt;
+        int kt, j = 0;
         bool in[2], pa[2];
         while (ok && m.next(kt, in[0], in[1], pa[0], pa[1])) {
           const int s = j % NS;
+          const bool mine = t ? in[1] : in[0];
+          // the stages of this entry (and, for a PV, of the previous own one)
           if (!tc::mbar_wait(k_full + s, (j / NS) & 1, abort_flag)) { ok = false; break; }
-          if (j > 0 && !tc::mbar_wait(v_full + ps, ((j - 1) / NS) & 1, abort_flag)) { ok = false; break; }
-          tc::fence_after_sync();
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (pend[t] && !do_pv(t, ps)) { ok = false; break; }
-            if (in[t]) {
-              const uint32_t qb = sQ + t * C::kTileBytes, kb = sK + s * C::kTileBytes;
-#pragma unroll
-              for (int ks = 0; ks < D / 16; ++ks) {
-                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                tc::mma_ss(tbase + t * 128, tc::sdesc_sw128(qb + o, 16, 1024), tc::sdesc_sw128(kb + o, 16, 1024),
-                           idS, ks > 0 ? 1u : 0u);
-              }
-              tc::mma_commit(s_full + t);
-              pend[t] = true;
-              --remaining[t];
-            }
+          if (prev >= 0 && mine && !tc::mbar_wait(v_full + prev % NS, (prev / NS) & 1, abort_flag)) {
+            ok = false;
+            break;
           }
-            if (!ok) break;
-          tc::mma_commit(k_empty + s);               // QKs of this entry issued
-          if (j > 0) tc::mma_commit(v_empty + ps);   // PVs of the previous entry issued
-          ps = s;
+          if (!mine && !tc::mbar_wait(v_full + s, (j / NS) & 1, abort_flag)) { ok = false; break; }
+          // the partner's group for the previous entry (sub-tile 1: for this one)
+          if (t == 1 || j > 0) {
+            if (!tc::mbar_wait(tok + t, tph, abort_flag)) { ok = false; break; }
+            tph ^= 1;
+          }
+          if (mine) {
+            if (prev >= 0 && !do_pv()) { ok = false; break; }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+              tc::mma_ss(tS, tc::sdesc_sw128(sQ + o, 16, 1024),
+                         tc::sdesc_sw128(sK + s * C::kTileBytes + o, 16, 1024), idS, ks > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(s_full + t);
+            prev = j;
+          }
+          tc::mbar_arrive(tok + (1 - t));  // this entry's group is issued
+          tc::mma_commit(k_empty + s);
+          if (!mine) tc::mma_commit(v_empty + s);
           ++j;
         }
-        if (ok && (pend[0] || pend[1])) {
-          ok = tc::mbar_wait(v_full + ps, ((j - 1) / NS) & 1, abort_flag);
-          tc::fence_after_sync();
-          for (int t = 0; t < 2 && ok; ++t)
-            if (pend[t]) ok = do_pv(t, ps);
+        if (ok && prev >= 0) {
+          ok = tc::mbar_wait(v_full + prev % NS, (prev / NS) & 1, abort_flag) && do_pv();
+          if (ok) tc::mma_commit(o_final + t);
         }
         if (!ok) fail(p, abort_flag, 3);
         // drain: nothing issued may still run when TMEM is released
-        tc::mma_commit(mma_done);
-        tc::mbar_wait_drain(mma_done, 0, 200000000ull);
+        tc::mma_commit(mma_done + t);
+        tc::mbar_wait_drain(mma_done + t, 0, 200000000ull);
+      };
+      if (lane == 0) {
+        if (warp == 1) issue(std::integral_constant<int, 0>{});
+        else issue(std::integral_constant<int, 1>{});
       }
       __syncwarp();
     }
@@ -567,7 +627,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float2 v = fma2(x[c * 16 + e], sl2, ner);
-              const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
+              // some exponentials on the FMA pipes, interleaved with the SFU ones
+              // (a warp issues in order: the ALU work fills the SFU's gaps)
+              const float2 pe = false ? exp2_poly2(v) : make_float2(fast_exp2(v.x), fast_exp2(v.y));
               acc[e & 3] = add2(acc[e & 3], pe);
               pk[e] = pack2(pe.x, pe.y);
             }

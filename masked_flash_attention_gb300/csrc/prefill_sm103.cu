@@ -8,37 +8,34 @@
 // every pair is masked are not computed at all: the scheduler (sched.cu) left
 // them out of each item's key-tile list.
 //
-// CTA = two 128-row query sub-tiles that read the same K/V head: two q-heads
-// of one grouped-query group (InfiniTrain pull request 193 "Transformer 接入":
-// the kernel shares the K/V heads instead of expanding them) or, with one
-// q-head per K/V head, two consecutive row tiles.  Every K/V tile is loaded
-// once by TMA for both.  The two key-tile lists are merged; a sub-tile skips
-// the tiles that are not on its own list.
+// Persistent kernel: one CTA per SM walks the work units (sequence, q-head,
+// 128-row query tile) longest first, unit u going to CTA u mod grid, so the
+// pipelines run on from one unit into the next (Q of the next unit is fetched
+// while the current one runs; its first QK overlaps the current epilogue).
+// Grouped-query heads read their K/V head directly (InfiniTrain pull request
+// 193 "Transformer 接入": no expansion); neighbouring units are the q-heads of
+// one group, so their K/V tiles are served from L2.
 //
-// Warp roles (12 warps = 3 warpgroups):
-//   warp 0      TMA producer: Q once, then K tiles through an NS-stage ring
-//   warp 1      MMA issuer for sub-tile 0 (one thread) and TMEM owner
+// Warp roles (12 warps):
+//   warp 0      TMA producer: K tiles through an NS-stage ring
+//   warp 1      QK issuer (one thread), Q prefetch, TMEM owner
 //   warp 2      TMA producer: V tiles through an NS-stage ring
-//   warp 3      MMA issuer for sub-tile 1 (one thread)
-//   warps 4..7  softmax warpgroup for sub-tile 0, warps 8..11 for sub-tile 1
-// Registers: the block launches with 168 per thread (3 warps share an SM
-// sub-partition); warpgroup 0 (producer, MMA) hands registers back with
-// setmaxnreg and the softmax warpgroups take 216, enough to keep a whole
-// 128-key row of S in registers for one pass: max, exponentiate, sum, store P.
-// The kernel is specialised on the additive term (none, dense, top-k) and on
-// the soft-cap; a PARTIAL tile applies the pair rules as one column range per
-// row, and top-k tiles stage their keys' expiry rows and bias in smem.
-// TMEM (512 columns): S_t = Q_t K^T in columns [128 t, 128 t + 128), fp32;
-// P_t (bf16, two per column) overwrites the first 64 of them; O_t in
-// [256 + D t, 256 + D t + D).  Per key tile j the two MMA issuers put out
-//   PV_0(j-1), QK_0(j) | PV_1(j-1), QK_1(j)
-// in that order, so that sub-tile 0's softmax of tile j overlaps sub-tile 1's
-// MMAs and vice versa.  Each softmax thread owns one query row (32x32b TMEM loads), so the
-// row max and row sum need no cross-lane reduction.  The running max is the
-// exponent reference and is only raised when the row max exceeds it by more
-// than 2^8 (in log2 units), so O in TMEM is rarely rescaled.  A fully masked
-// row keeps reference -inf, exponentiates against 0, and ends with l = 0:
-// O = 0, LSE = -inf.
+//   warp 3      PV issuer (one thread)
+//   warps 4..7  softmax, key columns 0..63 of every tile
+//   warps 8..11 softmax, key columns 64..127
+// TMEM (512 columns): S in two buffers [0,128) [128,256) (fp32), P in two
+// buffers [256,320) [320,384) (bf16, two per column), O in [384, 384 + D).
+// With S and P double-buffered QK(j+1) runs while the softmax of tile j does,
+// and PV(j) while the softmax of tile j+1 does; the tensor cores wait on the
+// softmax only when it is slower than QK + PV.  The MMA queue is shallow (an
+// issuing thread stalls on tcgen05.mma almost at once), so QK and PV come from
+// two threads: each one's waits overlap the other's MMAs.
+// Each softmax thread owns half a row (32x32b TMEM loads); the two halves
+// exchange their row maxima through shared memory once per tile and add their
+// row sums at the end.  The running max is the exponent reference and is only
+// raised when the row max exceeds it by more than 2^8 (in log2 units), so O in
+// TMEM is rarely rescaled.  A fully masked row keeps reference -inf,
+// exponentiates against 0, and ends with l = 0: O = 0, LSE = -inf.
 //
 // Every mbarrier wait is bounded (1 s); on a time-out the kernel records
 // FA_ERR_DEVICE_TIMEOUT in the workspace error word, every role stops, in-flight
@@ -49,7 +46,6 @@
 
 #include <climits>
 #include <mutex>
-#include <type_traits>
 
 #include "fa_device.cuh"
 #include "host_util.h"
@@ -60,109 +56,65 @@ namespace mfa {
 namespace {
 
 constexpr int kPrefillThreads = 384;
-// Register split (setmaxnreg): the kernel is built to launch with exactly
-// kLaunchRegs per thread; warpgroup 0 (producer, MMA) gives registers back and
-// the two softmax warpgroups take them, so that a 128-key row of S fits.
-constexpr int kLaunchRegs = 168;
-constexpr int kProducerRegs = 72;
-constexpr int kSoftmaxRegs = 216;
-static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs <= kPrefillThreads * kLaunchRegs,
-              "the register split must fit the block's launch allocation");
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 0;    // S buffers: kSCol + 128 * buf
+constexpr uint32_t kPCol = 256;  // P buffers: kPCol + 64 * buf
+constexpr uint32_t kOCol = 384;  // O
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct PCfg {
-  static constexpr int NS = (D == 128) ? 2 : 4;          // K/V stages
-  static constexpr int kTileBytes = 128 * D * 2;          // one 128-row bf16 tile
-  static constexpr int kQOff = 0;
+  static constexpr int NS = (D == 128) ? 2 : 4;    // K/V ring stages
+  static constexpr int kTileBytes = 128 * D * 2;    // one 128-row bf16 tile
+  static constexpr int kQOff = 0;                   // two Q buffers
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + NS * kTileBytes;
-  static constexpr int kBarOff = kVOff + NS * kTileBytes;
-  static constexpr int kSmem = kBarOff + 256 + 4096 + 1024;  // barriers, top-k staging, alignment slack
-  static constexpr uint32_t kOCol = 256;
+  static constexpr int kAuxOff = kVOff + NS * kTileBytes;
+  // aux: barriers and flags (512 B), row-max exchange [2][2][128] floats,
+  // row-sum exchange [2][128] floats, top-k staging [2 halves][2][64] int2
+  static constexpr int kRedOff = kAuxOff + 512;
+  static constexpr int kSumOff = kRedOff + 2 * 2 * 128 * 4;
+  static constexpr int kTopkOff = kSumOff + 2 * 128 * 4;
+  static constexpr int kSmem = kTopkOff + 2 * 2 * 64 * 8 + 1024;  // + alignment slack
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kOCol + D <= kTmemCols, "TMEM budget");
 };
 
-struct SubTile {
-  bool valid;   // sequence passed the scheduler's checks and the sub-tile exists
-  int h, rt, count;
+// One work unit: 128 query rows of one q-head of one sequence.
+struct Unit {
+  bool present;  // the tile holds rows of the sequence
+  bool valid;    // the scheduler accepted the sequence
+  int b, h, rt, count;
   const int32_t* tiles;
 };
 
-// Merged walk over two ascending key-tile lists.
-struct Merge {
-  const int32_t* l0;
-  const int32_t* l1;
-  int c0, c1, i0, i1;
-  __device__ __forceinline__ void init(const SubTile (&st)[2]) {
-    l0 = st[0].tiles; l1 = st[1].tiles;
-    c0 = st[0].valid ? st[0].count : 0;
-    c1 = st[1].valid ? st[1].count : 0;
-    i0 = i1 = 0;
-  }
-  __device__ __forceinline__ bool next(int& kt, bool& in0, bool& in1, bool& part0, bool& part1) {
-    int e0 = i0 < c0 ? __ldg(l0 + i0) : 0x7ffffffe;
-    int e1 = i1 < c1 ? __ldg(l1 + i1) : 0x7ffffffe;
-    int k0 = e0 >> 1, k1 = e1 >> 1;
-    kt = min(k0, k1);
-    if (kt >= 0x3fffffff) return false;
-    in0 = (k0 == kt); in1 = (k1 == kt);
-    part0 = in0 && (e0 & 1); part1 = in1 && (e1 & 1);
-    if (in0) ++i0;
-    if (in1) ++i1;
-    return true;
-  }
-};
+// Unit u, longest query tiles first (row tile descending), q-heads fastest.
+__device__ __forceinline__ Unit unit_at(const Params& p, int u) {
+  Unit w;
+  const int per = p.n_seq * p.Hq;
+  w.rt = p.n_row_tiles - 1 - u / per;
+  const int r = u % per;
+  w.h = r % p.Hq;
+  w.b = r / p.Hq;
+  w.present = w.rt * 128 < seq_qlen(p, w.b);
+  const int64_t item = ((int64_t)w.b * p.Hq + w.h) * p.n_row_tiles + w.rt;
+  const int c = w.present ? __ldg(p.item_count + item) : -1;
+  w.valid = c >= 0;
+  w.count = c > 0 ? c : 0;
+  w.tiles = p.item_tiles + item * p.n_kt;
+  return w;
+}
 
-// CTA -> (sequence, K/V head, two sub-tiles); longest query tiles first.
-__device__ __forceinline__ void cta_work(const Params& p, int cta, int& b, int& g, SubTile (&st)[2]) {
-  const int G = p.G, nrt = p.n_row_tiles;
-  int h[2], rt[2];
-  bool present[2];
-  if (G >= 2) {
-    const int PP = (G + 1) / 2;
-    const int per = p.n_seq * p.Hkv * PP;
-    const int r_t = nrt - 1 - cta / per;
-    int r = cta % per;
-    const int pp = r % PP;
-    r /= PP;
-    g = r % p.Hkv;
-    b = r / p.Hkv;
-    for (int t = 0; t < 2; ++t) {
-      int hh = 2 * pp + t;
-      present[t] = hh < G;
-      h[t] = g * G + (present[t] ? hh : 0);
-      rt[t] = r_t;
-    }
-  } else {
-    const int NR2 = (nrt + 1) / 2;
-    const int per = p.n_seq * p.Hq;
-    const int rp = NR2 - 1 - cta / per;
-    const int r = cta % per;
-    const int hq = r % p.Hq;
-    b = r / p.Hq;
-    g = hq;
-    for (int t = 0; t < 2; ++t) {
-      rt[t] = 2 * rp + t;
-      present[t] = rt[t] < nrt;
-      h[t] = hq;
-    }
+__device__ __forceinline__ int n_units(const Params& p) { return p.n_row_tiles * p.n_seq * p.Hq; }
+
+// Next unit with key tiles at or after u (this CTA's stride), or -1.
+__device__ __forceinline__ int next_busy(const Params& p, int u, Unit& w) {
+  const int n = n_units(p);
+  for (; u < n; u += gridDim.x) {
+    w = unit_at(p, u);
+    if (w.present && w.valid && w.count > 0) return u;
   }
-  for (int t = 0; t < 2; ++t) {
-    st[t].h = h[t];
-    st[t].rt = rt[t];
-    st[t].valid = false;
-    st[t].count = 0;
-    st[t].tiles = nullptr;
-    if (present[t]) {
-      int64_t item = ((int64_t)b * p.Hq + h[t]) * p.n_row_tiles + rt[t];
-      int c = p.item_count[item];
-      st[t].valid = c >= 0;
-      st[t].count = c > 0 ? c : 0;
-      st[t].tiles = p.item_tiles + item * p.n_kt;
-    }
-  }
+  return -1;
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -187,62 +139,20 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return *reinterpret_cast<float2*>(&d);
 }
 
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
-  return *reinterpret_cast<float2*>(&d);
-}
-// a + b rounded toward minus infinity
-__device__ __forceinline__ float2 add2_rm(float2 a, float2 b) {
-  uint64_t d;
-  asm("add.rm.f32x2 %0, %1, %2;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
-  return *reinterpret_cast<float2*>(&d);
-}
-
-// 2^v for a pair, on the FMA and integer pipes instead of the special-function
-// unit, whose 16 results per clock and SM would otherwise bound the softmax.
-// v = n + f with n = floor(v), f in [0, 1); 2^f ~ 1 + f (c1 + f (c2 + f c3)),
-// a minimax cubic for the relative error (at most 8.6e-5, below the 2^-9
-// rounding of the bf16 P it feeds), fitted by exp2_fit.py in this package;
-// n is added to the exponent field.  v is clamped at -127, where the result is
-// exactly 0.  Only used where v <= 8 is known (FULL tiles, lazy rescale bound).
-constexpr float kExp2C1 = 6.951167865e-01f;
-constexpr float kExp2C2 = 2.276449909e-01f;
-constexpr float kExp2C3 = 7.706704220e-02f;
-constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: ulp 1, so v + it rounds v to an integer
-__device__ __forceinline__ float2 exp2_poly2(float2 v) {
-  v.x = fmaxf(v.x, -127.f);
-  v.y = fmaxf(v.y, -127.f);
-  const float2 magic = make_float2(kRoundMagic, kRoundMagic);
-  const float2 t = add2_rm(v, magic);        // floor(v) + magic, exact
-  const float2 f = sub2(v, sub2(t, magic));  // v - floor(v), exact
-  float2 q = fma2(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
-  q = fma2(q, f, make_float2(kExp2C1, kExp2C1));
-  q = fma2(q, f, make_float2(1.f, 1.f));
-  // the low mantissa bits of t hold floor(v); shifted by 23 they add it to the
-  // exponent of q (the magic's own bits shift out)
-  return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
-                     __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
-}
-
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 
-// Maximum of 128 values held as 64 pairs: a tree of three-input maxima over
-// four independent accumulators.
-__device__ __forceinline__ float row_max128(const float2 (&x)[64]) {
+// Maximum of 64 values held as 32 pairs: three-input maxima over four
+// independent accumulators.
+__device__ __forceinline__ float row_max64(const float2 (&x)[32]) {
   float m[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) m[k] = fmaxf(x[k].x, x[k].y);
 #pragma unroll
-  for (int i = 4; i < 64; ++i) m[i & 3] = max3f(m[i & 3], x[i].x, x[i].y);
+  for (int i = 4; i < 32; ++i) m[i & 3] = max3f(m[i & 3], x[i].x, x[i].y);
   return max3f(fmaxf(m[0], m[1]), m[2], m[3]);
 }
 
@@ -295,52 +205,46 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  int b, g;
-  SubTile st[2];
-  cta_work(p, blockIdx.x, b, g, st);
-  if (!st[0].valid && !st[1].valid) return;
-  const int q_len = seq_qlen(p, b), kv_len = seq_klen(p, b);
-  const int off = kv_len - q_len;
-
-  // Nothing scheduled for either sub-tile: only zero rows to write.
-  if (st[0].count == 0 && st[1].count == 0) {
-    if (warp >= 4) {
-      const int t = (warp - 4) >> 2;
-      const int i = st[t].rt * 128 + 32 * (warp & 3) + lane;
-      if (st[t].valid && i < q_len) write_empty_row<D>(p, b, st[t].h, i);
-    }
-    return;
-  }
-
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* v_full = k_full + NS;
-  uint64_t* k_empty = v_full + NS;
-  uint64_t* v_empty = k_empty + NS;
-  uint64_t* s_full = v_empty + NS;    // [2]
-  uint64_t* p_full = s_full + 2;      // [2]
-  uint64_t* o_final = p_full + 2;     // [2]
-  uint64_t* mma_done = o_final + 2;   // [2]
-  uint64_t* tok = mma_done + 2;       // [2] issue-order token between the MMA issuers
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tok + 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kAuxOff);
+  uint64_t* q_full = bars;            // [2] Q buffer loaded
+  uint64_t* q_empty = q_full + 2;     // [2] QKs reading a Q buffer done
+  uint64_t* k_full = q_empty + 2;     // [NS]
+  uint64_t* k_empty = k_full + NS;    // [NS]
+  uint64_t* v_full = k_empty + NS;    // [NS]
+  uint64_t* v_empty = v_full + NS;    // [NS]
+  uint64_t* s_full = v_empty + NS;    // [2] S buffer written by QK
+  uint64_t* s_free = s_full + 2;      // [2] S buffer read by the softmax (256 arrivals)
+  uint64_t* p_full = s_free + 2;      // [2] P buffer written, O rescaled (256 arrivals)
+  uint64_t* p_free = p_full + 2;      // [2] PV reading a P buffer done
+  uint64_t* o_full = p_free + 2;      // [1] last PV of a unit done
+  uint64_t* drained = o_full + 1;     // [2] all MMAs of an issuer done (teardown)
+  uint64_t* xchg = drained + 2;       // [2] row maxima of both halves posted (256 arrivals)
+  uint64_t* sumx = xchg + 2;          // [1] row sums of both halves posted (256 arrivals)
+  uint64_t* kready = sumx + 1;        // [2 halves][2] top-k staging filled (128 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kready + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (tid == 0) {
-    tc::mbar_init(q_full, 1);
+    for (int k = 0; k < 2; ++k) {
+      tc::mbar_init(q_full + k, 1);
+      tc::mbar_init(q_empty + k, 1);
+      tc::mbar_init(s_full + k, 1);
+      tc::mbar_init(s_free + k, 256);
+      tc::mbar_init(p_full + k, 256);
+      tc::mbar_init(p_free + k, 1);
+      tc::mbar_init(drained + k, 1);
+      tc::mbar_init(xchg + k, 256);
+      tc::mbar_init(kready + k, 128);
+      tc::mbar_init(kready + 2 + k, 128);
+    }
+    tc::mbar_init(sumx, 256);
     for (int s = 0; s < NS; ++s) {
       tc::mbar_init(k_full + s, 1);
+      tc::mbar_init(k_empty + s, 1);
       tc::mbar_init(v_full + s, 1);
-      tc::mbar_init(k_empty + s, 2);  // one arrival per MMA issuer
-      tc::mbar_init(v_empty + s, 2);
+      tc::mbar_init(v_empty + s, 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      tc::mbar_init(s_full + t, 1);
-      tc::mbar_init(p_full + t, 128);
-      tc::mbar_init(o_final + t, 1);
-      tc::mbar_init(mma_done + t, 1);
-      tc::mbar_init(tok + t, 1);
-    }
+    tc::mbar_init(o_full, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -353,261 +257,274 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc::fence_after_sync();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-    if (warp == 0 || warp == 2) {
-      // ---------------------------------------------------------- producers
-      // warp 0: Q once, then K tiles; warp 2: V tiles.  Each ring has its own
-      // release barrier: a K stage frees when the QKs that read it are done,
-      // a V stage when its PVs are done, a step later.
-      if (lane == 0) {
-        const bool is_k = (warp == 0);
-        const int kv_row0 = p.cu_k ? p.cu_k[b] : 0;
-        const int kv_b = p.cu_k ? 0 : b;
-        const CUtensorMap* map = is_k ? &tmk : &tmv;
-        uint64_t* full = is_k ? k_full : v_full;
-        uint64_t* empty = is_k ? k_empty : v_empty;
-        unsigned char* ring = smem + (is_k ? C::kKOff : C::kVOff);
-        tc::tma_prefetch_desc(map);
-        if (is_k) {
-          const int q_row0 = p.cu_q ? p.cu_q[b] : 0;
-          const int q_b = p.cu_q ? 0 : b;
-          tc::tma_prefetch_desc(&tmq);
-          uint32_t qbytes = 0;
-          for (int t = 0; t < 2; ++t)
-            if (st[t].count > 0) qbytes += C::kTileBytes;
-          tc::mbar_arrive_expect_tx(q_full, qbytes);
-          for (int t = 0; t < 2; ++t) {
-            if (st[t].count == 0) continue;
-            unsigned char* dst = smem + C::kQOff + t * C::kTileBytes;
-            for (int c = 0; c < D / 64; ++c)
-              tc::tma_load_4d(dst + c * 16384, &tmq, q_full, c * 64, st[t].h, q_row0 + st[t].rt * 128, q_b);
-          }
-        }
-        Merge m;
-        m.init(st);
-        int kt, j = 0;
-        bool in0, in1, pa0, pa1;
-        while (m.next(kt, in0, in1, pa0, pa1)) {
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ producers
+    // K (warp 0) and V (warp 2) tiles of every busy unit, in order, through
+    // their rings; a stage is refilled once the MMAs that read it are done.
+    if (lane == 0) {
+      const bool is_k = (warp == 0);
+      const CUtensorMap* map = is_k ? &tmk : &tmv;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      unsigned char* ring = smem + (is_k ? C::kKOff : C::kVOff);
+      tc::tma_prefetch_desc(map);
+      int j = 0;
+      bool ok = true;
+      Unit w;
+      for (int u = next_busy(p, blockIdx.x, w); ok && u >= 0; u = next_busy(p, u + gridDim.x, w)) {
+        const int kv_row0 = p.cu_k ? p.cu_k[w.b] : 0;
+        const int kv_b = p.cu_k ? 0 : w.b;
+        const int g = w.h / p.G;
+        for (int i = 0; i < w.count; ++i, ++j) {
+          const int kt = __ldg(w.tiles + i) >> 1;
           const int s = j % NS;
           if (j >= NS && !tc::mbar_wait(empty + s, ((j / NS) - 1) & 1, abort_flag)) {
             fail(p, abort_flag, is_k ? 1 : 7);
+            ok = false;
             break;
           }
           tc::mbar_arrive_expect_tx(full + s, C::kTileBytes);
           for (int c = 0; c < D / 64; ++c)
             tc::tma_load_4d(ring + s * C::kTileBytes + c * 16384, map, full + s, c * 64, g, kv_row0 + kt * 128,
                             kv_b);
-          ++j;
-        }
-        if (*abort_flag) {
-          // let the copies already issued land before the CTA can exit
-          const int first = j > NS ? j - NS : 0;
-          for (int jj = first; jj < j; ++jj) tc::mbar_wait_drain(full + jj % NS, (jj / NS) & 1, 100000000ull);
-          if (is_k) tc::mbar_wait_drain(q_full, 0, 100000000ull);
         }
       }
-    } else if (warp == 1 || warp == 3) {
-      // ---------------------------------------------------------- MMA issuers
-      // The MMA queue is shallow: an issuing thread stalls on tcgen05.mma almost
-      // at once, so whatever a lone issuer does between its MMA groups (waits,
-      // list walk, commits) is tensor idle time.  Two issuers, one per sub-tile
-      // (warp 1: sub-tile 0, warp 3: sub-tile 1), hand a token back and forth so
-      // that the groups still go out in the order PV_0 QK_0 | PV_1 QK_1 | PV_0 ...
-      // (the ping-pong of the two softmax warpgroups) while each one's
-      // bookkeeping overlaps the other's MMAs.  Both walk the merged tile list,
-      // which the K/V rings follow; a stage is released once both are done with
-      // it (arrival count 2).
-      auto issue = [&](auto T) {
-        constexpr int t = decltype(T)::value;
-        constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false);
-        constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
-        const uint32_t sQ = tc::smem_u32(smem + C::kQOff + t * C::kTileBytes);
-        const uint32_t sK = tc::smem_u32(smem + C::kKOff);
-        const uint32_t sV = tc::smem_u32(smem + C::kVOff);
-        const uint32_t tS = tbase + t * 128, tO = tbase + C::kOCol + t * D;
-        bool ok = tc::mbar_wait(q_full, 0, abort_flag);
-        if (!ok) fail(p, abort_flag, 2);
-        tc::fence_after_sync();
-        int prev = -1;        // merged index of this sub-tile's last QK; its PV is pending
-        bool o_acc = false;   // O already holds a partial sum
-        uint32_t pph = 0, tph = 0;
-        auto do_pv = [&]() -> bool {
-          const int ps = prev % NS;
-          if (!tc::mbar_wait(p_full + t, pph, abort_flag)) return false;
-          pph ^= 1;
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA can exit
+        const int first = j > NS ? j - NS : 0;
+        for (int jj = first; jj < j; ++jj) tc::mbar_wait_drain(full + jj % NS, (jj / NS) & 1, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ QK issuer
+    // S[g % 2] = Q K_g^T for the g-th tile this CTA processes, as soon as the
+    // softmax has read that S buffer two tiles back.  Also fetches Q: the next
+    // unit's Q while the current unit runs (two buffers).
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false);
+      const uint32_t sQ = tc::smem_u32(smem + C::kQOff);
+      const uint32_t sK = tc::smem_u32(smem + C::kKOff);
+      tc::tma_prefetch_desc(&tmq);
+      int nq = 0;  // Q copies issued; copy l goes to buffer l & 1
+      auto load_q = [&](const Unit& w, int qb) {
+        ++nq;
+        const int q_row0 = p.cu_q ? p.cu_q[w.b] : 0;
+        const int q_b = p.cu_q ? 0 : w.b;
+        unsigned char* dst = smem + C::kQOff + qb * C::kTileBytes;
+        tc::mbar_arrive_expect_tx(q_full + qb, C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tc::tma_load_4d(dst + c * 16384, &tmq, q_full + qb, c * 64, w.h, q_row0 + w.rt * 128, q_b);
+      };
+      bool ok = true;
+      int g = 0, kk = 0;  // tiles and busy units so far
+      Unit w, wn;
+      int u = next_busy(p, blockIdx.x, w);
+      if (u >= 0) load_q(w, 0);
+      for (; ok && u >= 0; ++kk) {
+        const int qb = kk & 1;
+        const int un = next_busy(p, u + gridDim.x, wn);
+        if (!tc::mbar_wait(q_full + qb, (kk >> 1) & 1, abort_flag)) { ok = false; break; }
+        for (int i = 0; i < w.count; ++i, ++g) {
+          const int s = g % NS, sb = g & 1;
+          if (!tc::mbar_wait(k_full + s, (g / NS) & 1, abort_flag)) { ok = false; break; }
+          if (g >= 2 && !tc::mbar_wait(s_free + sb, ((g - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
           tc::fence_after_sync();
-          const uint32_t vbase = sV + ps * C::kTileBytes;
+          const uint32_t qa = sQ + qb * C::kTileBytes, ka = sK + s * C::kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_ts(tO, tS + ks * 8, tc::sdesc_sw128(vbase + ks * 2048, 16384, 1024), idO,
-                       (o_acc || ks > 0) ? 1u : 0u);
-          o_acc = true;
-          tc::mma_commit(v_empty + ps);
-          return true;
-        };
-        Merge m;
-        m.init(st);
-        int kt, j = 0;
-        bool in[2], pa[2];
-        while (ok && m.next(kt, in[0], in[1], pa[0], pa[1])) {
-          const int s = j % NS;
-          const bool mine = t ? in[1] : in[0];
-          // the stages of this entry (and, for a PV, of the previous own one)
-          if (!tc::mbar_wait(k_full + s, (j / NS) & 1, abort_flag)) { ok = false; break; }
-          if (prev >= 0 && mine && !tc::mbar_wait(v_full + prev % NS, (prev / NS) & 1, abort_flag)) {
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+            tc::mma_ss(tbase + kSCol + sb * 128, tc::sdesc_sw128(qa + o, 16, 1024),
+                       tc::sdesc_sw128(ka + o, 16, 1024), idS, ks > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(s_full + sb);
+          tc::mma_commit(k_empty + s);
+          if (i == 0 && un >= 0) {
+            // next unit's Q into the other buffer, last read by unit kk - 1
+            if (kk >= 1 && !tc::mbar_wait(q_empty + (qb ^ 1), ((kk - 1) >> 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            load_q(wn, qb ^ 1);
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(q_empty + qb);
+        u = un;
+        w = wn;
+      }
+      if (!ok) fail(p, abort_flag, 2);
+      tc::mma_commit(drained);
+      tc::mbar_wait_drain(drained, 0, 200000000ull);
+      if (*abort_flag) {
+        // let the last Q copies land before the CTA can exit
+        for (int l = nq > 2 ? nq - 2 : 0; l < nq; ++l)
+          tc::mbar_wait_drain(q_full + (l & 1), (l >> 1) & 1, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ PV issuer
+    // O (+)= P[g % 2] V_g once the softmax of tile g has written P (and
+    // rescaled O); the first tile of a unit overwrites O.
+    if (lane == 0) {
+      constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
+      const uint32_t sV = tc::smem_u32(smem + C::kVOff);
+      bool ok = true;
+      int g = 0;
+      Unit w;
+      for (int u = next_busy(p, blockIdx.x, w); ok && u >= 0; u = next_busy(p, u + gridDim.x, w)) {
+        for (int i = 0; i < w.count; ++i, ++g) {
+          const int s = g % NS, pb = g & 1;
+          if (!tc::mbar_wait(p_full + pb, (g >> 1) & 1, abort_flag) ||
+              !tc::mbar_wait(v_full + s, (g / NS) & 1, abort_flag)) {
             ok = false;
             break;
           }
-          if (!mine && !tc::mbar_wait(v_full + s, (j / NS) & 1, abort_flag)) { ok = false; break; }
-          // the partner's group for the previous entry (sub-tile 1: for this one)
-          if (t == 1 || j > 0) {
-            if (!tc::mbar_wait(tok + t, tph, abort_flag)) { ok = false; break; }
-            tph ^= 1;
-          }
-          if (mine) {
-            if (prev >= 0 && !do_pv()) { ok = false; break; }
-            tc::fence_after_sync();
+          tc::fence_after_sync();
+          const uint32_t va = sV + s * C::kTileBytes;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-              tc::mma_ss(tS, tc::sdesc_sw128(sQ + o, 16, 1024),
-                         tc::sdesc_sw128(sK + s * C::kTileBytes + o, 16, 1024), idS, ks > 0 ? 1u : 0u);
-            }
-            tc::mma_commit(s_full + t);
-            prev = j;
-          }
-          tc::mbar_arrive(tok + (1 - t));  // this entry's group is issued
-          tc::mma_commit(k_empty + s);
-          if (!mine) tc::mma_commit(v_empty + s);
-          ++j;
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_ts(tbase + kOCol, tbase + kPCol + pb * 64 + ks * 8, tc::sdesc_sw128(va + ks * 2048, 16384, 1024),
+                       idO, (i > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_commit(p_free + pb);
+          tc::mma_commit(v_empty + s);
+          if (i == w.count - 1) tc::mma_commit(o_full);
         }
-        if (ok && prev >= 0) {
-          ok = tc::mbar_wait(v_full + prev % NS, (prev / NS) & 1, abort_flag) && do_pv();
-          if (ok) tc::mma_commit(o_final + t);
-        }
-        if (!ok) fail(p, abort_flag, 3);
-        // drain: nothing issued may still run when TMEM is released
-        tc::mma_commit(mma_done + t);
-        tc::mbar_wait_drain(mma_done + t, 0, 200000000ull);
-      };
-      if (lane == 0) {
-        if (warp == 1) issue(std::integral_constant<int, 0>{});
-        else issue(std::integral_constant<int, 1>{});
       }
-      __syncwarp();
+      if (!ok) fail(p, abort_flag, 3);
+      tc::mma_commit(drained + 1);
+      tc::mbar_wait_drain(drained + 1, 0, 200000000ull);
     }
+    __syncwarp();
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 4) >> 2;
-    const int wtid = tid - 128 - 128 * t;  // 0..127 within the warpgroup
+    // Thread = one row, one half of the key columns.  The halves meet through
+    // mbarriers (bounded waits), never through a named barrier, so that a
+    // warpgroup that gives up on a timed-out wait cannot leave the other stuck.
+    const int w = (warp - 4) >> 2;         // keys [64 w, 64 w + 64) of every tile
+    const int wtid = tid - 128 - 128 * w;  // 0..127 within the warpgroup
     const int wq = warp & 3;               // TMEM lane quarter this warp may access
     const int row = 32 * wq + lane;
-    const SubTile me = st[t];
-    const int i = me.rt * 128 + row;
-    const int h = me.h;
     const uint32_t lane_base = tbase + ((uint32_t)(32 * wq) << 16);
-    const uint32_t scol = lane_base + t * 128;
-    int jlo_r, jhi_r;
-    row_key_range(p, i, q_len, kv_len, off, jlo_r, jhi_r);
-    // top-k: per key tile, the keys' expiry rows and bias, staged in smem
-    int2* kbuf = reinterpret_cast<int2*>(smem + C::kBarOff + 256) + t * 256;
-    if (me.valid && me.count == 0) {
-      if (i < q_len) write_empty_row<D>(p, b, h, i);
-    } else if (me.valid) {
+    float* red = reinterpret_cast<float*>(smem + C::kRedOff);   // [2 parity][2 halves][128]
+    float* rsum = reinterpret_cast<float*>(smem + C::kSumOff);  // [2 halves][128]
+    int2* kbuf = reinterpret_cast<int2*>(smem + C::kTopkOff) + w * 128;  // [2 parity][64]
+    constexpr int kHalfD = D / 2;  // O columns each half rescales and stores
+    bool ok = true;
+    int g = 0, kk = 0;  // tiles and busy units so far
+    const int nu = n_units(p);
+    for (int u = blockIdx.x; ok && u < nu; u += gridDim.x) {
+      const Unit un = unit_at(p, u);
+      if (!un.present || !un.valid) continue;
+      const int b = un.b, h = un.h;
+      const int q_len = seq_qlen(p, b), kv_len = seq_klen(p, b);
+      const int off = kv_len - q_len;
+      const int i = un.rt * 128 + row;
+      if (un.count == 0) {
+        if (w == 0 && i < q_len) write_empty_row<D>(p, b, h, i);
+        continue;
+      }
+      int jlo_r, jhi_r;
+      row_key_range(p, i, q_len, kv_len, off, jlo_r, jhi_r);
       float m_ref = -INFINITY, l = 0.f;
-      uint32_t sph = 0;
-      bool first = true, ok = true;
-      int par = 0;
-      Merge m;
-      m.init(st);
-      int kt;
-      bool in[2], pa[2];
-      while (m.next(kt, in[0], in[1], pa[0], pa[1])) {
-        const bool mine = t ? in[1] : in[0];
-        const bool part = t ? pa[1] : pa[0];
-        if (!mine) continue;
-        const int j0 = kt * kKeysPerTile;
+      bool first = true;
+      for (int it = 0; it < un.count; ++it, ++g) {
+        const int ent = __ldg(un.tiles + it);
+        const int j0 = (ent >> 1) * kKeysPerTile + 64 * w;  // first key of this half
+        const bool part = ent & 1;
+        const int par = g & 1;
         if (MK == FA_MASK_TOPK) {
-          const int jj = j0 + wtid;
-          int2 v = make_int2(kRowNever, 0);
-          if (jj < kv_len) {
-            const int64_t bh = (int64_t)b * p.Hq + h;
-            v.x = __ldg(p.topk_e + bh * p.Sk + jj);
-            v.y = __float_as_int(
-                __ldg(p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh + (int64_t)jj * p.z_sk) * kLog2e);
+          // this half's 64 keys: expiry row and bias, staged for the whole warpgroup
+          if (wtid < 64) {
+            const int jj = j0 + wtid;
+            int2 v = make_int2(kRowNever, 0);
+            if (jj < kv_len) {
+              const int64_t bh = (int64_t)b * p.Hq + h;
+              v.x = __ldg(p.topk_e + bh * p.Sk + jj);
+              v.y = __float_as_int(
+                  __ldg(p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh + (int64_t)jj * p.z_sk) * kLog2e);
+            }
+            kbuf[par * 64 + wtid] = v;
           }
-          kbuf[par * 128 + wtid] = v;
-          asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
+          tc::mbar_arrive(kready + 2 * w + par);
+          if (!tc::mbar_wait(kready + 2 * w + par, (g >> 1) & 1, abort_flag)) { ok = false; break; }
         }
-        if (!tc::mbar_wait(s_full + t, sph, abort_flag)) { ok = false; break; }
-        sph ^= 1;
+        if (!tc::mbar_wait(s_full + par, (g >> 1) & 1, abort_flag)) { ok = false; break; }
         tc::fence_after_sync();
-        float2 x[64];
+        float2 x[32];
         {
-          uint32_t r[4][32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tc::tmem_ld32(scol + c * 32, r[c]);
+          uint32_t r[2][32];
+          const uint32_t sa = lane_base + kSCol + par * 128 + 64 * w;
+          tc::tmem_ld32(sa, r[0]);
+          tc::tmem_ld32(sa + 32, r[1]);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               x[c * 16 + e] = make_float2(__uint_as_float(r[c][2 * e]), __uint_as_float(r[c][2 * e + 1]));
         }
+        tc::fence_before_sync();
+        tc::mbar_arrive(s_free + par);  // the QK two tiles on may overwrite this S buffer
         // logits in log2 units; a FULL tile without soft-cap keeps raw scores
         // and folds the scale into the exponent below
         const bool plain = !SC && !part;
         float mx;
         if (plain) {
-          mx = row_max128(x) * p.scale_log2;
+          mx = row_max64(x) * p.scale_log2;
         } else {
           const int clo = jlo_r - j0, chi = jhi_r - j0;
-          const bool all_in = !part;
           const float* mrow = nullptr;
           if (MK == FA_MASK_DENSE && i < q_len)
             mrow = p.mask + (int64_t)(p.m_nb > 1 ? b : 0) * p.m_sb + (int64_t)(p.m_nh > 1 ? h : 0) * p.m_sh +
                    (int64_t)i * p.m_sq + (int64_t)j0 * p.m_sk;
 #pragma unroll
-          for (int e = 0; e < 128; ++e) {
+          for (int e = 0; e < 64; ++e) {
             float v = (e & 1) ? x[e >> 1].y : x[e >> 1].x;
             if (SC) {
               v = p.softcap * tanhf(v * p.scale / p.softcap) * kLog2e;
             } else {
               v = v * p.scale_log2;
             }
-            bool keep = all_in || (e >= clo && e <= chi);
-            if (MK == FA_MASK_DENSE && !all_in) {
+            bool keep = !part || (e >= clo && e <= chi);
+            if (MK == FA_MASK_DENSE && part) {
               if (keep) v += __ldg(mrow + (int64_t)e * p.m_sk) * kLog2e;
             }
             if (MK == FA_MASK_TOPK) {
-              const int2 kv = kbuf[par * 128 + e];
+              const int2 kv = kbuf[par * 64 + e];
               keep = keep && (i < kv.x);
               v += __int_as_float(kv.y);
             }
             v = keep ? v : -INFINITY;
             if (e & 1) x[e >> 1].y = v; else x[e >> 1].x = v;
           }
-          mx = row_max128(x);
+          mx = row_max64(x);
         }
+        // both halves of a row use one reference: exchange the half maxima
+        red[(par * 2 + w) * 128 + row] = mx;
+        tc::mbar_arrive(xchg + par);
+        if (!tc::mbar_wait(xchg + par, (g >> 1) & 1, abort_flag)) { ok = false; break; }
+        mx = fmaxf(mx, red[(par * 2 + (w ^ 1)) * 128 + row]);
         // raise the exponent reference only when the row max outgrew it by 2^8
         const bool upd = mx > m_ref + kRescaleLog2;
         const float alpha = upd ? fast_exp2(m_ref - mx) : 1.f;
         const bool need_o = upd && !first && m_ref != -INFINITY;
         if (__any_sync(0xffffffffu, need_o)) {
+          // O holds the previous tile's PV once that PV is done
+          if (!tc::mbar_wait(p_free + (par ^ 1), ((g - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc::fence_after_sync();
           const float f = need_o ? alpha : 1.f;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < kHalfD / 32; ++c) {
             uint32_t r[32];
-            const uint32_t a = lane_base + C::kOCol + t * D + c * 32;
+            const uint32_t a = lane_base + kOCol + w * kHalfD + c * 32;
             tc::tmem_ld32(a, r);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
             tc::tmem_st32(a, r);
           }
-          tc::tmem_wait_st();
         }
         if (upd) {
           l *= alpha;
@@ -618,26 +535,27 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         float2 acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+        // this P buffer is free once the PV two tiles back is done
+        if (g >= 2 && !tc::mbar_wait(p_free + par, ((g - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+        const uint32_t pa = lane_base + kPCol + par * 64 + 32 * w;
         // P = exp2(x - ref): one packed FMA (FULL: scale folded in) or add per pair
         if (plain) {
           const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float2 v = fma2(x[c * 16 + e], sl2, ner);
-              // some exponentials on the FMA pipes, interleaved with the SFU ones
-              // (a warp issues in order: the ALU work fills the SFU's gaps)
-              const float2 pe = false ? exp2_poly2(v) : make_float2(fast_exp2(v.x), fast_exp2(v.y));
+              const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
               acc[e & 3] = add2(acc[e & 3], pe);
               pk[e] = pack2(pe.x, pe.y);
             }
-            tc::tmem_st16(scol + c * 16, pk);
+            tc::tmem_st16(pa + c * 16, pk);
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -646,47 +564,52 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               acc[e & 3] = add2(acc[e & 3], pe);
               pk[e] = pack2(pe.x, pe.y);
             }
-            tc::tmem_st16(scol + c * 16, pk);
+            tc::tmem_st16(pa + c * 16, pk);
           }
         }
         acc[0] = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
         l += acc[0].x + acc[0].y;
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        tc::mbar_arrive(p_full + t);
+        tc::mbar_arrive(p_full + par);
         first = false;
-        par ^= 1;
       }
-      if (ok) ok = tc::mbar_wait(o_final + t, 0, abort_flag);
-      if (!ok) {
-        fail(p, abort_flag, 4 + t);
-      } else {
-        tc::fence_after_sync();
-        const bool empty = !(l > 0.f);
-        const float inv = empty ? 0.f : 1.f / l;
-        uint16_t* optr;
-        float* lptr;
-        row_out(p, b, h, i < q_len ? i : 0, optr, lptr);
+      if (!ok) break;
+      // ---- epilogue: O / l, LSE; the halves add their row sums
+      rsum[w * 128 + row] = l;
+      tc::mbar_arrive(sumx);
+      if (!tc::mbar_wait(sumx, kk & 1, abort_flag) || !tc::mbar_wait(o_full, kk & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const float lt = l + rsum[(w ^ 1) * 128 + row];
+      const bool empty = !(lt > 0.f);
+      const float inv = empty ? 0.f : 1.f / lt;
+      uint16_t* optr;
+      float* lptr;
+      row_out(p, b, h, i < q_len ? i : 0, optr, lptr);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(lane_base + C::kOCol + t * D + c * 32, r);
-          tc::tmem_wait_ld();
-          if (i < q_len) {
+      for (int c = 0; c < kHalfD / 32; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(lane_base + kOCol + w * kHalfD + c * 32, r);
+        tc::tmem_wait_ld();
+        if (i < q_len) {
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 w;
-              w.x = pack2(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
-              w.y = pack2(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
-              w.z = pack2(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
-              w.w = pack2(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
-              *reinterpret_cast<uint4*>(optr + c * 32 + 8 * v4) = w;
-            }
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 o4;
+            o4.x = pack2(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
+            o4.y = pack2(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
+            o4.z = pack2(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
+            o4.w = pack2(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
+            *reinterpret_cast<uint4*>(optr + w * kHalfD + c * 32 + 8 * v4) = o4;
           }
         }
-        if (i < q_len) *lptr = empty ? -INFINITY : (m_ref + __log2f(l)) * kLn2;
       }
+      if (w == 0 && i < q_len) *lptr = empty ? -INFINITY : (m_ref + __log2f(lt)) * kLn2;
+      ++kk;
     }
+    if (!ok) fail(p, abort_flag, 4 + w);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -732,24 +655,26 @@ bool encode_bshd(CUtensorMap* m, const void* base, int d, int heads, int64_t row
   return r == CUDA_SUCCESS;
 }
 
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 1;
+  }
+  return n;
+}
+
 template <int D, int MK, bool SC>
 cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap& mq, const CUtensorMap& mk,
-                             const CUtensorMap& mv, int64_t grid, cudaEvent_t ev_begin) {
-  auto kern = prefill_kernel<D, MK, SC>;
-  // setmaxnreg.inc would wait forever if the block were launched with fewer
-  // registers than the split assumes: launch only when the build matches.
-  static int regs = -1;
-  if (regs < 0) {
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    regs = fa.numRegs;
-  }
-  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+                             const CUtensorMap& mv, int grid, cudaEvent_t ev_begin) {
   cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC>>(PCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-  kern<<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv);
+  prefill_kernel<D, MK, SC><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv);
   return cudaGetLastError();
 }
 
@@ -767,12 +692,11 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
       !encode_bshd(&mk, p.k, D, p.Hkv, k_rows, kb, p.k_sh, p.k_ss, k_sb) ||
       !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb))
     return cudaErrorInvalidValue;
-  int64_t grid;
-  if (p.G >= 2)
-    grid = (int64_t)p.n_row_tiles * p.n_seq * p.Hkv * ((p.G + 1) / 2);
-  else
-    grid = (int64_t)((p.n_row_tiles + 1) / 2) * p.n_seq * p.Hq;
-  if (grid <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
+  // one CTA per SM (persistent), never more CTAs than work units
+  const int64_t units = (int64_t)p.n_row_tiles * p.n_seq * p.Hq;
+  if (units <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
+  if (units > INT_MAX) return cudaErrorInvalidValue;
+  const int grid = (int)(units < sm_count() ? units : sm_count());
   const bool sc = p.softcap > 0.f;
   switch (p.mask_kind) {
     case FA_MASK_DENSE:

@@ -80,6 +80,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// As mbar_wait, but polling without the suspend hint: for waits on the
+// critical path, where the wake-up delay of a suspended thread (a few hundred
+// cycles) would idle the tensor cores.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns = 1000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
 // Bounded wait that ignores the abort flag: used while tearing down, to let
 // work that was already issued (TMA copies, MMAs) finish before the CTA
 // releases the memory it targets.

@@ -56,6 +56,15 @@ namespace mfa {
 namespace {
 
 constexpr int kPrefillThreads = 384;
+// Register split (setmaxnreg): the kernel is built to launch with exactly
+// kLaunchRegs per thread; warpgroup 0 (producers, issuers) gives registers
+// back and the two softmax warpgroups take them, so that a 128-key row of S
+// fits in registers.
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 72;
+constexpr int kSoftmaxRegs = 216;
+static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs <= kPrefillThreads * kLaunchRegs,
+              "the register split must fit the block's launch allocation");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // S buffers: kSCol + 128 * buf
 constexpr uint32_t kPCol = 256;  // P buffers: kPCol + 64 * buf
@@ -70,12 +79,12 @@ struct PCfg {
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + NS * kTileBytes;
   static constexpr int kAuxOff = kVOff + NS * kTileBytes;
-  // aux: barriers and flags (512 B), row-max exchange [2][2][128] floats,
-  // row-sum exchange [2][128] floats, top-k staging [2 halves][2][64] int2
+  // aux: barriers and flags (512 B), row references [2][128] floats, row
+  // sums [2][128] floats, top-k staging [2 warpgroups][2][128] int2
   static constexpr int kRedOff = kAuxOff + 512;
-  static constexpr int kSumOff = kRedOff + 2 * 2 * 128 * 4;
+  static constexpr int kSumOff = kRedOff + 2 * 128 * 4;
   static constexpr int kTopkOff = kSumOff + 2 * 128 * 4;
-  static constexpr int kSmem = kTopkOff + 2 * 2 * 64 * 8 + 1024;  // + alignment slack
+  static constexpr int kSmem = kTopkOff + 2 * 2 * 128 * 8 + 1024;  // + alignment slack
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
 };
@@ -145,14 +154,14 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return d;
 }
 
-// Maximum of 64 values held as 32 pairs: three-input maxima over four
+// Maximum of 128 values held as 64 pairs: three-input maxima over four
 // independent accumulators.
-__device__ __forceinline__ float row_max64(const float2 (&x)[32]) {
+__device__ __forceinline__ float row_max128(const float2 (&x)[64]) {
   float m[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) m[k] = fmaxf(x[k].x, x[k].y);
 #pragma unroll
-  for (int i = 4; i < 32; ++i) m[i & 3] = max3f(m[i & 3], x[i].x, x[i].y);
+  for (int i = 4; i < 64; ++i) m[i & 3] = max3f(m[i & 3], x[i].x, x[i].y);
   return max3f(fmaxf(m[0], m[1]), m[2], m[3]);
 }
 
@@ -213,15 +222,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* v_full = k_empty + NS;    // [NS]
   uint64_t* v_empty = v_full + NS;    // [NS]
   uint64_t* s_full = v_empty + NS;    // [2] S buffer written by QK
-  uint64_t* s_free = s_full + 2;      // [2] S buffer read by the softmax (256 arrivals)
-  uint64_t* p_full = s_free + 2;      // [2] P buffer written, O rescaled (256 arrivals)
+  uint64_t* s_free = s_full + 2;      // [2] S buffer read by the softmax (128 arrivals)
+  uint64_t* p_full = s_free + 2;      // [2] P buffer written, O rescaled (128 arrivals)
   uint64_t* p_free = p_full + 2;      // [2] PV reading a P buffer done
   uint64_t* o_full = p_free + 2;      // [1] last PV of a unit done
   uint64_t* drained = o_full + 1;     // [2] all MMAs of an issuer done (teardown)
-  uint64_t* xchg = drained + 2;       // [2] row maxima of both halves posted (256 arrivals)
-  uint64_t* sumx = xchg + 2;          // [1] row sums of both halves posted (256 arrivals)
-  uint64_t* kready = sumx + 1;        // [2 halves][2] top-k staging filled (128 arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kready + 4);
+  uint64_t* sumx = drained + 2;       // [1] row sums of both warpgroups posted (256 arrivals)
+  uint64_t* kready = sumx + 1;        // [2 warpgroups][2] top-k staging filled (128 arrivals)
+  uint64_t* refb = kready + 4;        // [2 tile parity] row references posted (128 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(refb + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   if (tid == 0) {
@@ -229,11 +238,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       tc::mbar_init(q_full + k, 1);
       tc::mbar_init(q_empty + k, 1);
       tc::mbar_init(s_full + k, 1);
-      tc::mbar_init(s_free + k, 256);
-      tc::mbar_init(p_full + k, 256);
+      tc::mbar_init(s_free + k, 128);
+      tc::mbar_init(p_full + k, 128);
       tc::mbar_init(p_free + k, 1);
       tc::mbar_init(drained + k, 1);
-      tc::mbar_init(xchg + k, 256);
+      tc::mbar_init(refb + k, 128);
       tc::mbar_init(kready + k, 128);
       tc::mbar_init(kready + 2 + k, 128);
     }
@@ -257,6 +266,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc::fence_after_sync();
   const uint32_t tbase = *tmem_slot;
 
+  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ producers
     // K (warp 0) and V (warp 2) tiles of every busy unit, in order, through
@@ -398,21 +408,29 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
     __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------------------ softmax
-    // Thread = one row, one half of the key columns.  The halves meet through
-    // mbarriers (bounded waits), never through a named barrier, so that a
-    // warpgroup that gives up on a timed-out wait cannot leave the other stuck.
-    const int w = (warp - 4) >> 2;         // keys [64 w, 64 w + 64) of every tile
+    // Warpgroup w takes the tiles with g % 2 == w (S and P buffer w), so one
+    // warpgroup's exponentials overlap the other's loads and maxima; each
+    // thread owns a whole 128-key row of its tile.  The exponent reference
+    // of a row is decided tile by tile, in order: the warpgroup of tile g waits
+    // for the reference posted after tile g - 1, raises it if its own maximum
+    // outgrew it by more than 2^8, and posts it.  Each warpgroup keeps its own
+    // row sum against the reference it last used; the two are rescaled to the
+    // final reference and added at the end.  The warpgroups meet through
+    // mbarriers (bounded waits), never through a named barrier, so that one
+    // that gives up on a timed-out wait cannot leave the other stuck.
+    const int w = (warp - 4) >> 2;
     const int wtid = tid - 128 - 128 * w;  // 0..127 within the warpgroup
     const int wq = warp & 3;               // TMEM lane quarter this warp may access
     const int row = 32 * wq + lane;
     const uint32_t lane_base = tbase + ((uint32_t)(32 * wq) << 16);
-    float* red = reinterpret_cast<float*>(smem + C::kRedOff);   // [2 parity][2 halves][128]
-    float* rsum = reinterpret_cast<float*>(smem + C::kSumOff);  // [2 halves][128]
-    int2* kbuf = reinterpret_cast<int2*>(smem + C::kTopkOff) + w * 128;  // [2 parity][64]
-    constexpr int kHalfD = D / 2;  // O columns each half rescales and stores
+    float* refv = reinterpret_cast<float*>(smem + C::kRedOff);  // [2 tile parity][128]
+    float* rsum = reinterpret_cast<float*>(smem + C::kSumOff);  // [2 warpgroups][128]
+    int2* kbuf = reinterpret_cast<int2*>(smem + C::kTopkOff) + w * 256;  // [2][128]
+    constexpr int kHalfD = D / 2;  // O columns each warpgroup rescales and stores
     bool ok = true;
-    int g = 0, kk = 0;  // tiles and busy units so far
+    int g = 0, kk = 0;  // tiles and busy units so far (all of them, both parities)
     const int nu = n_units(p);
     for (int u = blockIdx.x; ok && u < nu; u += gridDim.x) {
       const Unit un = unit_at(p, u);
@@ -427,40 +445,41 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       int jlo_r, jhi_r;
       row_key_range(p, i, q_len, kv_len, off, jlo_r, jhi_r);
-      float m_ref = -INFINITY, l = 0.f;
-      bool first = true;
-      for (int it = 0; it < un.count; ++it, ++g) {
+      float m_ref = -INFINITY;  // reference after the last tile seen
+      float r_own = -INFINITY;  // reference this warpgroup's row sum is against
+      float l = 0.f;
+      // the first tile of the unit is this warpgroup's if g is of its parity
+      for (int it = (g & 1) == w ? 0 : 1; it < un.count; it += 2) {
+        const int gt = g + it;  // global index of this tile
+        const int par = w;      // == gt & 1
         const int ent = __ldg(un.tiles + it);
-        const int j0 = (ent >> 1) * kKeysPerTile + 64 * w;  // first key of this half
+        const int j0 = (ent >> 1) * kKeysPerTile;
         const bool part = ent & 1;
-        const int par = g & 1;
+        const int kb = (gt >> 1) & 1;  // top-k staging buffer
         if (MK == FA_MASK_TOPK) {
-          // this half's 64 keys: expiry row and bias, staged for the whole warpgroup
-          if (wtid < 64) {
-            const int jj = j0 + wtid;
-            int2 v = make_int2(kRowNever, 0);
-            if (jj < kv_len) {
-              const int64_t bh = (int64_t)b * p.Hq + h;
-              v.x = __ldg(p.topk_e + bh * p.Sk + jj);
-              v.y = __float_as_int(
-                  __ldg(p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh + (int64_t)jj * p.z_sk) * kLog2e);
-            }
-            kbuf[par * 64 + wtid] = v;
+          const int jj = j0 + wtid;
+          int2 v = make_int2(kRowNever, 0);
+          if (jj < kv_len) {
+            const int64_t bh = (int64_t)b * p.Hq + h;
+            v.x = __ldg(p.topk_e + bh * p.Sk + jj);
+            v.y = __float_as_int(
+                __ldg(p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh + (int64_t)jj * p.z_sk) * kLog2e);
           }
-          tc::mbar_arrive(kready + 2 * w + par);
-          if (!tc::mbar_wait(kready + 2 * w + par, (g >> 1) & 1, abort_flag)) { ok = false; break; }
+          kbuf[kb * 128 + wtid] = v;
+          tc::mbar_arrive(kready + 2 * w + kb);
+          if (!tc::mbar_wait(kready + 2 * w + kb, (gt >> 2) & 1, abort_flag)) { ok = false; break; }
         }
-        if (!tc::mbar_wait(s_full + par, (g >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(s_full + par, (gt >> 1) & 1, abort_flag)) { ok = false; break; }
         tc::fence_after_sync();
-        float2 x[32];
+        float2 x[64];
         {
-          uint32_t r[2][32];
-          const uint32_t sa = lane_base + kSCol + par * 128 + 64 * w;
-          tc::tmem_ld32(sa, r[0]);
-          tc::tmem_ld32(sa + 32, r[1]);
+          uint32_t r[4][32];
+          const uint32_t sa = lane_base + kSCol + par * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tc::tmem_ld32(sa + c * 32, r[c]);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               x[c * 16 + e] = make_float2(__uint_as_float(r[c][2 * e]), __uint_as_float(r[c][2 * e + 1]));
@@ -472,7 +491,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const bool plain = !SC && !part;
         float mx;
         if (plain) {
-          mx = row_max64(x) * p.scale_log2;
+          mx = row_max128(x) * p.scale_log2;
         } else {
           const int clo = jlo_r - j0, chi = jhi_r - j0;
           const float* mrow = nullptr;
@@ -480,7 +499,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             mrow = p.mask + (int64_t)(p.m_nb > 1 ? b : 0) * p.m_sb + (int64_t)(p.m_nh > 1 ? h : 0) * p.m_sh +
                    (int64_t)i * p.m_sq + (int64_t)j0 * p.m_sk;
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
+          for (int e = 0; e < 128; ++e) {
             float v = (e & 1) ? x[e >> 1].y : x[e >> 1].x;
             if (SC) {
               v = p.softcap * tanhf(v * p.scale / p.softcap) * kLog2e;
@@ -492,33 +511,33 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               if (keep) v += __ldg(mrow + (int64_t)e * p.m_sk) * kLog2e;
             }
             if (MK == FA_MASK_TOPK) {
-              const int2 kv = kbuf[par * 64 + e];
+              const int2 kv = kbuf[kb * 128 + e];
               keep = keep && (i < kv.x);
               v += __int_as_float(kv.y);
             }
             v = keep ? v : -INFINITY;
             if (e & 1) x[e >> 1].y = v; else x[e >> 1].x = v;
           }
-          mx = row_max64(x);
+          mx = row_max128(x);
         }
-        // both halves of a row use one reference: exchange the half maxima
-        red[(par * 2 + w) * 128 + row] = mx;
-        tc::mbar_arrive(xchg + par);
-        if (!tc::mbar_wait(xchg + par, (g >> 1) & 1, abort_flag)) { ok = false; break; }
-        mx = fmaxf(mx, red[(par * 2 + (w ^ 1)) * 128 + row]);
+        // the reference after tile gt - 1 (every tile's reference is posted,
+        // also across units, so that the two warpgroups stay in step)
+        if (gt >= 1 && !tc::mbar_wait(refb + (par ^ 1), ((gt - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+        const float m_prev = (it == 0) ? -INFINITY : refv[(par ^ 1) * 128 + row];
         // raise the exponent reference only when the row max outgrew it by 2^8
-        const bool upd = mx > m_ref + kRescaleLog2;
-        const float alpha = upd ? fast_exp2(m_ref - mx) : 1.f;
-        const bool need_o = upd && !first && m_ref != -INFINITY;
-        if (__any_sync(0xffffffffu, need_o)) {
-          // O holds the previous tile's PV once that PV is done
-          if (!tc::mbar_wait(p_free + (par ^ 1), ((g - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+        const bool upd = mx > m_prev + kRescaleLog2;
+        m_ref = upd ? mx : m_prev;
+        refv[par * 128 + row] = m_ref;
+        tc::mbar_arrive(refb + par);
+        if (it != 0 && __any_sync(0xffffffffu, upd && m_prev != -INFINITY)) {
+          // O holds the PV of tile gt - 1 (against m_prev) once that PV is done
+          if (!tc::mbar_wait(p_free + (par ^ 1), ((gt - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
           tc::fence_after_sync();
-          const float f = need_o ? alpha : 1.f;
+          const float f = (upd && m_prev != -INFINITY) ? fast_exp2(m_prev - m_ref) : 1.f;
 #pragma unroll
-          for (int c = 0; c < kHalfD / 32; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t r[32];
-            const uint32_t a = lane_base + kOCol + w * kHalfD + c * 32;
+            const uint32_t a = lane_base + kOCol + c * 32;
             tc::tmem_ld32(a, r);
             tc::tmem_wait_ld();
 #pragma unroll
@@ -526,9 +545,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             tc::tmem_st32(a, r);
           }
         }
-        if (upd) {
-          l *= alpha;
-          m_ref = mx;
+        if (r_own != m_ref) {
+          l = (r_own == -INFINITY) ? 0.f : l * fast_exp2(r_own - m_ref);
+          r_own = m_ref;
         }
         const float eref = (m_ref == -INFINITY) ? 0.f : m_ref;
         const float2 ner = make_float2(-eref, -eref);
@@ -536,13 +555,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
         // this P buffer is free once the PV two tiles back is done
-        if (g >= 2 && !tc::mbar_wait(p_free + par, ((g - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-        const uint32_t pa = lane_base + kPCol + par * 64 + 32 * w;
+        if (gt >= 2 && !tc::mbar_wait(p_free + par, ((gt - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+        const uint32_t pa = lane_base + kPCol + par * 64;
         // P = exp2(x - ref): one packed FMA (FULL: scale folded in) or add per pair
         if (plain) {
           const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -555,7 +574,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -572,18 +591,23 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         tc::tmem_wait_st();
         tc::fence_before_sync();
         tc::mbar_arrive(p_full + par);
-        first = false;
       }
       if (!ok) break;
-      // ---- epilogue: O / l, LSE; the halves add their row sums
-      rsum[w * 128 + row] = l;
+      // ---- epilogue: both warpgroups' row sums against the final reference
+      const int gl = g + un.count - 1;  // the unit's last tile
+      g += un.count;
+      if ((gl & 1) != w) {
+        if (!tc::mbar_wait(refb + (gl & 1), (gl >> 1) & 1, abort_flag)) { ok = false; break; }
+        m_ref = refv[(gl & 1) * 128 + row];
+      }
+      rsum[w * 128 + row] = (r_own == m_ref || r_own == -INFINITY) ? l : l * fast_exp2(r_own - m_ref);
       tc::mbar_arrive(sumx);
       if (!tc::mbar_wait(sumx, kk & 1, abort_flag) || !tc::mbar_wait(o_full, kk & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      const float lt = l + rsum[(w ^ 1) * 128 + row];
+      const float lt = rsum[row] + rsum[128 + row];
       const bool empty = !(lt > 0.f);
       const float inv = empty ? 0.f : 1.f / lt;
       uint16_t* optr;
@@ -671,6 +695,16 @@ int sm_count() {
 template <int D, int MK, bool SC>
 cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& mv, int grid, cudaEvent_t ev_begin) {
+  // setmaxnreg.inc would wait forever if the block were launched with fewer
+  // registers than the split assumes: launch only when the build matches.
+  static int regs = -1;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MK, SC>);
+    if (e != cudaSuccess) return e;
+    regs = fa.numRegs;
+  }
+  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC>>(PCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;

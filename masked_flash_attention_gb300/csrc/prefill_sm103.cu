@@ -154,15 +154,15 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return d;
 }
 
-// Maximum of 128 values held as 64 pairs: three-input maxima over four
+// Maximum of 128 values held as 64 pairs: three-input maxima over eight
 // independent accumulators.
 __device__ __forceinline__ float row_max128(const float2 (&x)[64]) {
-  float m[4];
+  float m[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) m[k] = fmaxf(x[k].x, x[k].y);
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(x[k].x, x[k].y);
 #pragma unroll
-  for (int i = 4; i < 64; ++i) m[i & 3] = max3f(m[i & 3], x[i].x, x[i].y);
-  return max3f(fmaxf(m[0], m[1]), m[2], m[3]);
+  for (int i = 8; i < 64; ++i) m[i & 7] = max3f(m[i & 7], x[i].x, x[i].y);
+  return fmaxf(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], max3f(m[5], m[6], m[7])));
 }
 
 __device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag, uint32_t where) {
@@ -554,38 +554,36 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         float2 acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
-        // this P buffer is free once the PV two tiles back is done
-        if (gt >= 2 && !tc::mbar_wait(p_free + par, ((gt - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-        const uint32_t pa = lane_base + kPCol + par * 64;
-        // P = exp2(x - ref): one packed FMA (FULL: scale folded in) or add per pair
+        // P = exp2(x - ref) packed to bf16 pairs in registers: one packed FMA
+        // (FULL: scale folded in) or add per pair
+        uint32_t pk[4][16];
         if (plain) {
           const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float2 v = fma2(x[c * 16 + e], sl2, ner);
               const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
               acc[e & 3] = add2(acc[e & 3], pe);
-              pk[e] = pack2(pe.x, pe.y);
+              pk[c][e] = pack2(pe.x, pe.y);
             }
-            tc::tmem_st16(pa + c * 16, pk);
-          }
         } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const float2 v = add2(x[c * 16 + e], ner);
               const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
               acc[e & 3] = add2(acc[e & 3], pe);
-              pk[e] = pack2(pe.x, pe.y);
+              pk[c][e] = pack2(pe.x, pe.y);
             }
-            tc::tmem_st16(pa + c * 16, pk);
-          }
         }
+        // this P buffer is free once the PV two tiles back is done
+        if (gt >= 2 && !tc::mbar_wait(p_free + par, ((gt - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+        const uint32_t pa = lane_base + kPCol + par * 64;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_st16(pa + c * 16, pk[c]);
         acc[0] = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
         l += acc[0].x + acc[0].y;
         tc::tmem_wait_st();

@@ -45,6 +45,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cstring>
 #include <mutex>
 
 #include "fa_device.cuh"
@@ -84,8 +85,11 @@ struct PCfg {
   static constexpr int kRedOff = kAuxOff + 512;
   static constexpr int kSumOff = kRedOff + 2 * 128 * 4;
   static constexpr int kTopkOff = kSumOff + 2 * 128 * 4;
-  static constexpr int kSmem = kTopkOff + 2 * 2 * 128 * 8 + 1024;  // + alignment slack
+  // output staging: per softmax warp 32 rows x 32 bf16 columns
+  static constexpr int kStageOff = (kTopkOff + 2 * 2 * 128 * 8 + 1023) / 1024 * 1024;  // swizzle-aligned
+  static constexpr int kSmem = kStageOff + 8 * 2048 + 1024;  // + alignment slack
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  static_assert(kStageOff % 1024 == 0, "TMA store source alignment");
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
 };
 
@@ -206,7 +210,7 @@ __device__ __forceinline__ void row_key_range(const Params& p, int i, int q_len,
 template <int D, int MK, bool SC>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv) {
+                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const int o_tma) {
   using C = PCfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ unsigned char smem_raw[];
@@ -432,8 +436,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     bool ok = true;
     int g = 0, kk = 0;  // tiles and busy units so far (all of them, both parities)
     const int nu = n_units(p);
+    // the next unit's descriptor and first list entry are read a unit ahead,
+    // so that no global-memory latency sits between two units
+    Unit un_next;
+    if (blockIdx.x < nu) un_next = unit_at(p, blockIdx.x);
+    int ent_first = 0;
+    bool ent_first_ok = false;
     for (int u = blockIdx.x; ok && u < nu; u += gridDim.x) {
-      const Unit un = unit_at(p, u);
+      const Unit un = un_next;
+      if (u + (int)gridDim.x < nu) un_next = unit_at(p, u + gridDim.x);
+      const bool pre_ok = ent_first_ok;
+      ent_first_ok = false;
       if (!un.present || !un.valid) continue;
       const int b = un.b, h = un.h;
       const int q_len = seq_qlen(p, b), kv_len = seq_klen(p, b);
@@ -449,10 +462,22 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       float r_own = -INFINITY;  // reference this warpgroup's row sum is against
       float l = 0.f;
       // the first tile of the unit is this warpgroup's if g is of its parity
-      for (int it = (g & 1) == w ? 0 : 1; it < un.count; it += 2) {
+      const int it0 = (g & 1) == w ? 0 : 1;
+      int ent_cur = pre_ok ? ent_first : (it0 < un.count ? __ldg(un.tiles + it0) : 0);
+      for (int it = it0; it < un.count; it += 2) {
         const int gt = g + it;  // global index of this tile
         const int par = w;      // == gt & 1
-        const int ent = __ldg(un.tiles + it);
+        const int ent = ent_cur;
+        if (it + 2 < un.count) {
+          ent_cur = __ldg(un.tiles + it + 2);
+        } else if (u + (int)gridDim.x < nu && un_next.present && un_next.valid && un_next.count > 0) {
+          // this warpgroup's first entry of the next unit
+          const int itn = ((g + un.count) & 1) == w ? 0 : 1;
+          if (itn < un_next.count) {
+            ent_first = __ldg(un_next.tiles + itn);
+            ent_first_ok = true;
+          }
+        }
         const int j0 = (ent >> 1) * kKeysPerTile;
         const bool part = ent & 1;
         const int kb = (gt >> 1) & 1;  // top-k staging buffer
@@ -485,7 +510,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               x[c * 16 + e] = make_float2(__uint_as_float(r[c][2 * e]), __uint_as_float(r[c][2 * e + 1]));
         }
         tc::fence_before_sync();
-        tc::mbar_arrive(s_free + par);  // the QK two tiles on may overwrite this S buffer
+        tc::mbar_arrive_relaxed(s_free + par);  // the QK two tiles on may overwrite this S buffer
         // logits in log2 units; a FULL tile without soft-cap keeps raw scores
         // and folds the scale into the exponent below
         const bool plain = !SC && !part;
@@ -588,7 +613,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         l += acc[0].x + acc[0].y;
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        tc::mbar_arrive(p_full + par);
+        tc::mbar_arrive_relaxed(p_full + par);
       }
       if (!ok) break;
       // ---- epilogue: both warpgroups' row sums against the final reference
@@ -608,30 +633,60 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const float lt = rsum[row] + rsum[128 + row];
       const bool empty = !(lt > 0.f);
       const float inv = empty ? 0.f : 1.f / lt;
-      uint16_t* optr;
-      float* lptr;
-      row_out(p, b, h, i < q_len ? i : 0, optr, lptr);
+      // O / l through a warp-private staging tile: a thread packs its own row,
+      // then each store instruction writes 64 contiguous bytes of 8 rows
+      uint4* stg = reinterpret_cast<uint4*>(smem + C::kStageOff + (warp - 4) * 2048);  // [32 rows][4]
+      const int row0 = un.rt * 128 + 32 * wq;  // first row of this warp
+      const int64_t qbase = p.cu_q ? (int64_t)p.cu_q[b] : 0;
+      uint16_t* obase = p.o + (p.cu_q ? 0 : (int64_t)b * p.o_sb) + (int64_t)h * p.o_sh;
+      // whole 32-row chunks inside the sequence leave by TMA store
+      const bool tma_rows = o_tma && row0 + 32 <= q_len;
 #pragma unroll
       for (int c = 0; c < kHalfD / 32; ++c) {
         uint32_t r[32];
         tc::tmem_ld32(lane_base + kOCol + w * kHalfD + c * 32, r);
+        // the staging tile is free once the previous TMA store has read it
+        if (lane == 0) tc::bulk_wait_read_all();
+        __syncwarp();
         tc::tmem_wait_ld();
-        if (i < q_len) {
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 o4;
-            o4.x = pack2(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
-            o4.y = pack2(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
-            o4.z = pack2(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
-            o4.w = pack2(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
-            *reinterpret_cast<uint4*>(optr + w * kHalfD + c * 32 + 8 * v4) = o4;
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint4 o4;
+          o4.x = pack2(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
+          o4.y = pack2(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
+          o4.z = pack2(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
+          o4.w = pack2(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
+          stg[lane * 4 + (v4 ^ ((lane >> 1) & 3))] = o4;  // swizzled: 4 wavefronts
+        }
+        if (tma_rows) {
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc::tma_store_4d(&tmo, stg, w * kHalfD + c * 32, h, (int)(qbase + row0), p.cu_q ? 0 : b);
+            tc::bulk_commit();
           }
+        } else {
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = 8 * k + (lane >> 2), q = lane & 3;
+            const uint4 o4 = stg[rr * 4 + (q ^ ((rr >> 1) & 3))];
+            if (row0 + rr < q_len)
+              *reinterpret_cast<uint4*>(obase + (qbase + row0 + rr) * p.o_ss + w * kHalfD + c * 32 + 8 * q) = o4;
+          }
+          __syncwarp();
         }
       }
-      if (w == 0 && i < q_len) *lptr = empty ? -INFINITY : (m_ref + __log2f(lt)) * kLn2;
+      if (w == 0 && i < q_len) {
+        float* lptr = p.lse + (p.cu_q ? 0 : (int64_t)b * p.lse_sb) + (int64_t)h * p.lse_sh + (qbase + i) * p.lse_ss;
+        *lptr = empty ? -INFINITY : (m_ref + __log2f(lt)) * kLn2;
+      }
       ++kk;
     }
     if (!ok) fail(p, abort_flag, 4 + w);
+    // output stores complete before the CTA exits
+    if (lane == 0) tc::bulk_wait_all();
+    __syncwarp();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -677,6 +732,21 @@ bool encode_bshd(CUtensorMap* m, const void* base, int d, int heads, int64_t row
   return r == CUDA_SUCCESS;
 }
 
+// 4-D map over the bf16 output for the epilogue's TMA stores: box {32, 1, 32,
+// 1} (32 columns x 32 rows), 64-byte swizzle (the staging layout).
+bool encode_out(CUtensorMap* m, void* base, int d, int heads, int64_t rows, int batch, int64_t s_h, int64_t s_row,
+                int64_t s_b) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows, (cuuint64_t)batch};
+  cuuint64_t strides[3] = {(cuuint64_t)s_h * 2, (cuuint64_t)s_row * 2, (cuuint64_t)s_b * 2};
+  cuuint32_t box[4] = {32, 1, 32, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -692,7 +762,8 @@ int sm_count() {
 
 template <int D, int MK, bool SC>
 cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap& mq, const CUtensorMap& mk,
-                             const CUtensorMap& mv, int grid, cudaEvent_t ev_begin) {
+                             const CUtensorMap& mv, const CUtensorMap& mo, int o_tma, int grid,
+                             cudaEvent_t ev_begin) {
   // setmaxnreg.inc would wait forever if the block were launched with fewer
   // registers than the split assumes: launch only when the build matches.
   static int regs = -1;
@@ -706,7 +777,7 @@ cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap
   cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC>>(PCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-  prefill_kernel<D, MK, SC><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv);
+  prefill_kernel<D, MK, SC><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
   return cudaGetLastError();
 }
 
@@ -720,6 +791,11 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
   const int64_t q_sb = (qb == 1 || p.q_sb == 0) ? p.q_ss : p.q_sb;
   const int64_t k_sb = (kb == 1 || p.k_sb == 0) ? p.k_ss : p.k_sb;
   const int64_t v_sb = (kb == 1 || p.v_sb == 0) ? p.v_ss : p.v_sb;
+  const int64_t o_sb = (qb == 1 || p.o_sb == 0) ? p.o_ss : p.o_sb;
+  CUtensorMap mo;
+  // without a valid map (unusual strides) the epilogue uses plain stores
+  const int o_tma = encode_out(&mo, p.o, D, p.Hq, q_rows, qb, p.o_sh, p.o_ss, o_sb) ? 1 : 0;
+  if (!o_tma) memset(&mo, 0, sizeof(mo));
   if (!encode_bshd(&mq, p.q, D, p.Hq, q_rows, qb, p.q_sh, p.q_ss, q_sb) ||
       !encode_bshd(&mk, p.k, D, p.Hkv, k_rows, kb, p.k_sh, p.k_ss, k_sb) ||
       !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb))
@@ -732,14 +808,14 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
   const bool sc = p.softcap > 0.f;
   switch (p.mask_kind) {
     case FA_MASK_DENSE:
-      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true>(p, st, mq, mk, mv, grid, ev_begin)
-                : launch_prefill_v<D, FA_MASK_DENSE, false>(p, st, mq, mk, mv, grid, ev_begin);
+      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_DENSE, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
     case FA_MASK_TOPK:
-      return sc ? launch_prefill_v<D, FA_MASK_TOPK, true>(p, st, mq, mk, mv, grid, ev_begin)
-                : launch_prefill_v<D, FA_MASK_TOPK, false>(p, st, mq, mk, mv, grid, ev_begin);
+      return sc ? launch_prefill_v<D, FA_MASK_TOPK, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_TOPK, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
     default:
-      return sc ? launch_prefill_v<D, FA_MASK_NONE, true>(p, st, mq, mk, mv, grid, ev_begin)
-                : launch_prefill_v<D, FA_MASK_NONE, false>(p, st, mq, mk, mv, grid, ev_begin);
+      return sc ? launch_prefill_v<D, FA_MASK_NONE, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_NONE, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
   }
 }
 

@@ -219,6 +219,7 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   P.scale = scale;
   P.scale_log2 = scale * 1.4426950408889634f;
   P.softcap = softcap;
+  P.inv_softcap = softcap > 0.f ? 1.f / softcap : 0.f;
   P.causal = causal ? 1 : 0;
   P.wl = wl;
   P.wr = wr;

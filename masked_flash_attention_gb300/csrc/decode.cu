@@ -21,8 +21,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
+
 #include "fa_device.cuh"
 #include "host_util.h"
+#include "tc_sm103.cuh"
 
 namespace mfa {
 
@@ -40,7 +43,8 @@ struct DecodeSmem {
   static constexpr int kStageBytes = 2 * kKvBytes;
   static constexpr int kWarpBytes = kWarpStages * kStageBytes;
   static constexpr int kQBytes = kDecodeRows * D * 2;
-  static constexpr int kTotal = kWarps * kWarpBytes + kQBytes;
+  static constexpr int kBarOff = kWarps * kWarpBytes + kQBytes;  // TMA mode: [warp][stage] mbarriers + abort flag
+  static constexpr int kTotal = kBarOff + kWarps * kWarpStages * 8 + 16 + 1024;  // + alignment slack
   static_assert(kWarps * kDecodeRows * D * 4 <= kWarps * kWarpBytes, "merge buffer must fit");
   static_assert(2 * kWarps * kDecodeRows * 4 <= kQBytes, "warp statistics must fit over Q");
 };
@@ -129,204 +133,24 @@ __device__ __forceinline__ void out_ptrs(const Params& p, const ItemGeo& t, int 
   lptr = p.lse + bo * p.lse_sb + (int64_t)h * p.lse_sh + qrow * p.lse_ss;
 }
 
+// byte offset of (row, 16-byte column chunk cc) in a TMA-written chunk: two
+// 64-column halves of 16 rows x 128 bytes, 128-byte swizzle
+__device__ __forceinline__ uint32_t swz_tma(int row, int cc) {
+  return (uint32_t)((cc >> 3) * (kChunkKeys * 128) + row * 128 + (((cc & 7) ^ (row & 7)) << 4));
+}
+
+// Merge the 4 consumer warps' (m, l, O) and write the item's rows, or this
+// split's partial rows when the item has several splits.  Run by the 128
+// consumer threads only (thread ids 0..127), which meet on named barrier 1;
+// `smem` (16 KB at d = 128) is free for the merge buffer, `red_m` points to
+// 2 x 4 x 8 floats that are not part of it.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
-  using S = DecodeSmem<D>;
-  extern __shared__ __align__(1024) unsigned char smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t cta = blockIdx.x;
-  const int64_t item = cta / p.n_splits;
-  const int split = (int)(cta % p.n_splits);
-  const int count = p.item_count[item];
-  if (count < 0) return;  // sequence rejected by the scheduler's length checks
-  const int t_begin = split * p.tiles_per_split;
-  // an item with nothing scheduled still owes its rows O = 0, LSE = -inf
-  if (t_begin >= count && !(split == 0 && count == 0)) return;
-  const int t_end = min(count, t_begin + p.tiles_per_split);
-  const bool single = count <= p.tiles_per_split;
-  const ItemGeo geo = item_geo(p, item);
-  const int32_t* tiles = p.item_tiles + item * p.n_kt;
-
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
-  const uint32_t sQ = sbase + kWarps * S::kWarpBytes;
-  const uint32_t sW = sbase + warp * S::kWarpBytes;  // this warp's ring
-
-  // ---- Q: 16 packed rows -> smem (zero for padding rows) ----
-  for (int idx = tid; idx < kDecodeRows * S::kChunks; idx += kThreads) {
-    int r = idx / S::kChunks, c = idx % S::kChunks;
-    int P = geo.rt * kDecodeRows + r;
-    int qi = P / p.G, h = geo.g * p.G + P % p.G;
-    uint32_t dst = sQ + swz<D>(r, c);
-    if (qi < geo.q_len) {
-      int64_t qrow = p.cu_q ? (int64_t)p.cu_q[geo.b] + qi : (int64_t)qi;
-      int64_t bo = p.cu_q ? 0 : (int64_t)geo.b;
-      cp_async16(dst, p.q + bo * p.q_sb + qrow * p.q_ss + (int64_t)h * p.q_sh + c * 8);
-    } else {
-      asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0));
-    }
-  }
-  cp_async_commit();
-
-  // ---- this warp's chunks: c = warp, warp + 4, ... of the split ----
-  const int n_chunks = (t_end - t_begin) * (kKeysPerTile / kChunkKeys);
-  const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
-  const bool paged_fast = p.block_table && (p.page_size % kChunkKeys) == 0;
-  auto chunk_key0 = [&](int k, bool& partial, bool& live) -> int {
-    const int c = warp + k * kWarps;
-    const int e = tiles[t_begin + c / (kKeysPerTile / kChunkKeys)];
-    partial = (e & 1) != 0;
-    const int kj0 = (e >> 1) * kKeysPerTile + (c % (kKeysPerTile / kChunkKeys)) * kChunkKeys;
-    live = (kj0 <= geo.jhi) && (kj0 + kChunkKeys - 1 >= geo.jlo) && (kj0 < geo.kv_len);
-    return kj0;
-  };
-  // lane l copies 16-byte chunk (l % 16) of rows 2i + l / 16 (i = 0..7) of K and V:
-  // each instruction covers two whole rows (D = 128) or four (D = 64)
-  auto load_chunk = [&](int k) {
-    bool partial, live;
-    const int kj0 = chunk_key0(k, partial, live);
-    if (!live) return;
-    const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
-    const uint32_t sV = sK + S::kKvBytes;
-    constexpr int kRowsPerInstr = 32 / S::kChunks;
-    const int c = lane % S::kChunks, r0 = lane / S::kChunks;
-    const uint16_t* kbase = nullptr;
-    const uint16_t* vbase = nullptr;
-    if (paged_fast) {
-      int pg = __ldg(p.block_table + (int64_t)geo.b * p.bt_stride + kj0 / p.page_size);
-      if ((unsigned)pg >= (unsigned)p.num_pages) {
-        record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)pg);
-        pg = 0;
-      }
-      const int64_t row0 = kj0 % p.page_size;
-      kbase = p.k + (int64_t)pg * p.k_sb + row0 * p.k_ss + (int64_t)geo.g * p.k_sh;
-      vbase = p.v + (int64_t)pg * p.v_sb + row0 * p.v_ss + (int64_t)geo.g * p.v_sh;
-    }
-#pragma unroll
-    for (int i = 0; i < kChunkKeys / kRowsPerInstr; ++i) {
-      const int r = i * kRowsPerInstr + r0;
-      const int j = min(kj0 + r, geo.kv_len - 1);
-      const uint16_t* kr;
-      const uint16_t* vr;
-      if (paged_fast && kj0 + r < geo.kv_len) {
-        kr = kbase + (int64_t)r * p.k_ss;
-        vr = vbase + (int64_t)r * p.v_ss;
-      } else {
-        kr = kv_row(p, p.k, p.k_sb, p.k_ss, p.k_sh, geo.b, geo.g, j);
-        vr = kv_row(p, p.v, p.v_sb, p.v_ss, p.v_sh, geo.b, geo.g, j);
-      }
-      cp_async16(sK + swz<D>(r, c), kr + c * 8);
-      cp_async16(sV + swz<D>(r, c), vr + c * 8);
-    }
-  };
-
-  // Fragment roles: keys (and head-dim) on the mma M side, the 8 packed
-  // query rows on N.  Lane = 4 g + c holds S^T[key g, g+8][row 2c, 2c+1] and
-  // O^T[d 16m + g, + 8][row 2c, 2c+1].
+__device__ __forceinline__ void decode_finish(const Params& p, const ItemGeo& geo, int64_t item, int split,
+                                              bool single, unsigned char* smem, float* red_m, int tid,
+                                              float (&m_run)[2], float (&l_run)[2], float (&o_acc)[D / 16][4]) {
+  const int warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 2, c4 = lane & 3;
-  int qi_r[2], h_r[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    int P = geo.rt * kDecodeRows + 2 * c4 + e;
-    qi_r[e] = P / p.G;
-    h_r[e] = geo.g * p.G + P % p.G;
-  }
-  // the first chunks go out before Q is waited for, so their latency overlaps
-#pragma unroll
-  for (int k = 0; k < kWarpStages - 1; ++k) {
-    if (k < my_chunks) load_chunk(k);
-    cp_async_commit();
-  }
-  cp_async_wait<kWarpStages - 1>();  // this thread's Q copies have landed
-  __syncthreads();                   // ... and everyone else's
-  // Q^T as the B operand: [16 d x 8 rows] per k-step, two k-steps per ldmatrix.x4
-  uint32_t qb[D / 16][2];
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ks += 2) {
-    const int mi = lane >> 3;
-    ldsm_x4(sQ + swz<D>(lane & 7, 2 * ks + mi), qb[ks][0], qb[ks][1], qb[ks + 1][0], qb[ks + 1][1]);
-  }
-  float m_run[2] = {-INFINITY, -INFINITY};
-  float l_run[2] = {0.f, 0.f};
-  float o_acc[D / 16][4];
-#pragma unroll
-  for (int n = 0; n < D / 16; ++n) o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
-
-  for (int k = 0; k < my_chunks; ++k) {
-    cp_async_wait<kWarpStages - 2>();
-    __syncwarp();
-    if (k + kWarpStages - 1 < my_chunks) load_chunk(k + kWarpStages - 1);
-    cp_async_commit();
-    bool partial, live;
-    const int kj0 = chunk_key0(k, partial, live);
-    if (!live) continue;
-    const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
-    const uint32_t sV = sK + S::kKvBytes;
-
-    // ---- S^T = K Q^T : 16 keys x 8 rows, two accumulator chains ----
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const int mi = lane >> 3;
-      uint32_t a[4];
-      ldsm_x4(sK + swz<D>((lane & 7) + 8 * (mi & 1), 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
-      if (ks & 1) mma_bf16(sb, a, qb[ks][0], qb[ks][1]);
-      else mma_bf16(sa, a, qb[ks][0], qb[ks][1]);
-    }
-    float sc[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sc[e] = sa[e] + sb[e];
-    // ---- logit transform (log2 units); element e: key g8 + 8 (e >> 1), row 2 c4 + (e & 1) ----
-    const bool plain = !partial && p.softcap == 0.f && p.mask_kind == FA_MASK_NONE;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = kj0 + g8 + 8 * (e >> 1);
-      const int rr = e & 1;
-      if (plain) {
-        sc[e] *= p.scale_log2;
-      } else if (qi_r[rr] >= geo.q_len) {
-        sc[e] = -INFINITY;  // padding row: never read the mask out of range
-      } else {
-        sc[e] = logit_log2(p, sc[e], geo.b, h_r[rr], qi_r[rr], j, geo.off, geo.kv_len);
-      }
-    }
-    // ---- online softmax per row (a column of S^T), -inf guarded ----
-    float alpha[2];
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      float mx = fmaxf(sc[rr], sc[rr + 2]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float m_new = fmaxf(m_run[rr], mx);
-      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-      alpha[rr] = fast_exp2(m_run[rr] - m_ref);
-      m_run[rr] = m_new;
-      sc[rr] = fast_exp2(sc[rr] - m_ref);
-      sc[rr + 2] = fast_exp2(sc[rr + 2] - m_ref);
-      l_run[rr] = l_run[rr] * alpha[rr] + sc[rr] + sc[rr + 2];
-    }
-#pragma unroll
-    for (int n = 0; n < D / 16; ++n) {
-      o_acc[n][0] *= alpha[0]; o_acc[n][1] *= alpha[1];
-      o_acc[n][2] *= alpha[0]; o_acc[n][3] *= alpha[1];
-    }
-    // ---- P^T (C layout) -> B operand [16 keys x 8 rows] by an 8x8 transpose ----
-    const uint32_t pb0 = movmatrix_t(pack_bf16(sc[0], sc[1]));  // keys 0..7
-    const uint32_t pb1 = movmatrix_t(pack_bf16(sc[2], sc[3]));  // keys 8..15
-    // ---- O^T += V^T P^T : per 16 head-dim values, one mma over the 16 keys ----
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-      const int mi = lane >> 3;
-      uint32_t a[4];
-      ldsm_x4_t(sV + swz<D>((lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
-      mma_bf16(o_acc[mt], a, pb0, pb1);
-    }
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-
   // ---- merge the 4 warps' (m, l, O) ----
-  float* red_m = reinterpret_cast<float*>(smem + kWarps * S::kWarpBytes);  // over Q: [4][8]
   float* red_l = red_m + kWarps * kDecodeRows;
   float* obuf = reinterpret_cast<float*>(smem);  // [4][8][D]
 #pragma unroll
@@ -342,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
       red_l[warp * kDecodeRows + 2 * c4 + rr] = l_run[rr];
     }
   }
-  __syncthreads();
+  asm volatile("bar.sync 1, 128;" ::: "memory");
   float f_own[2];
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
@@ -361,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
     ow[(2 * c4) * D + 16 * mt + g8 + 8] = o_acc[mt][2] * f_own[0];
     ow[(2 * c4 + 1) * D + 16 * mt + g8 + 8] = o_acc[mt][3] * f_own[1];
   }
-  __syncthreads();
+  asm volatile("bar.sync 1, 128;" ::: "memory");
   // each thread: one row, D/16 consecutive columns
   {
     constexpr int kCols = D / 16;
@@ -411,6 +235,303 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
   }
 }
 
+// TMA: K/V chunks arrive by TMA tensor copies (a 16-row box of one K/V head:
+// one page, or 16 consecutive rows), issued by lane 0 of the warp that owns
+// the ring and tracked by one mbarrier per stage; otherwise by 16-byte
+// cp.async from all lanes (any layout).
+template <int D, bool TMA>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  using S = DecodeSmem<D>;
+  extern __shared__ unsigned char smem_raw[];
+  // 1024-byte aligned base: the TMA copies use the 128-byte swizzle
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t cta = blockIdx.x;
+  const int64_t item = cta / p.n_splits;
+  const int split = (int)(cta % p.n_splits);
+  const int count = p.item_count[item];
+  if (count < 0) return;  // sequence rejected by the scheduler's length checks
+  const int t_begin = split * p.tiles_per_split;
+  // an item with nothing scheduled still owes its rows O = 0, LSE = -inf
+  if (t_begin >= count && !(split == 0 && count == 0)) return;
+  const int t_end = min(count, t_begin + p.tiles_per_split);
+  const bool single = count <= p.tiles_per_split;
+  const ItemGeo geo = item_geo(p, item);
+  const int32_t* tiles = p.item_tiles + item * p.n_kt;
+
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t sQ = sbase + kWarps * S::kWarpBytes;
+  const uint32_t sW = sbase + warp * S::kWarpBytes;  // this warp's ring
+
+  // ---- Q: 16 packed rows -> smem (zero for padding rows) ----
+  for (int idx = tid; idx < kDecodeRows * S::kChunks; idx += kThreads) {
+    int r = idx / S::kChunks, c = idx % S::kChunks;
+    int P = geo.rt * kDecodeRows + r;
+    int qi = P / p.G, h = geo.g * p.G + P % p.G;
+    uint32_t dst = sQ + swz<D>(r, c);
+    if (qi < geo.q_len) {
+      int64_t qrow = p.cu_q ? (int64_t)p.cu_q[geo.b] + qi : (int64_t)qi;
+      int64_t bo = p.cu_q ? 0 : (int64_t)geo.b;
+      cp_async16(dst, p.q + bo * p.q_sb + qrow * p.q_ss + (int64_t)h * p.q_sh + c * 8);
+    } else {
+      asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst), "r"(0));
+    }
+  }
+  cp_async_commit();
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + S::kBarOff) + warp * kWarpStages;  // this warp's stages
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kBarOff + kWarps * kWarpStages * 8);
+  if (TMA) {
+    if (lane < kWarpStages) tc::mbar_init(kv_full + lane, 1);
+    if (tid == 0) *abort_flag = 0;
+    tc::fence_mbar_init();
+    __syncwarp();
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tmk);
+      tc::tma_prefetch_desc(&tmv);
+    }
+  }
+  uint32_t kv_phase = 0;  // TMA mode: parity of each stage's next completion
+
+  // ---- this warp's chunks: c = warp, warp + 4, ... of the split ----
+  const int n_chunks = (t_end - t_begin) * (kKeysPerTile / kChunkKeys);
+  const int my_chunks = n_chunks > warp ? (n_chunks - warp + kWarps - 1) / kWarps : 0;
+  const bool paged_fast = p.block_table && (p.page_size % kChunkKeys) == 0;
+  // Chunk descriptors (first key, partial flag, page) are computed by the lane
+  // whose index matches the chunk's position in a batch of 32, half a batch
+  // ahead, and fetched with a shuffle: no global-memory load sits between a
+  // chunk's turn and its copies.
+  auto chunk_desc = [&](int k, int& kj0_, int& pg_) {
+    kj0_ = -1;
+    pg_ = 0;
+    if (k >= my_chunks) return;
+    const int c = warp + k * kWarps;
+    const int e = __ldg(tiles + t_begin + c / (kKeysPerTile / kChunkKeys));
+    kj0_ = ((e >> 1) * kKeysPerTile + (c % (kKeysPerTile / kChunkKeys)) * kChunkKeys) * 2 + (e & 1);
+    const int kj = (e >> 1) * kKeysPerTile + (c % (kKeysPerTile / kChunkKeys)) * kChunkKeys;
+    if (paged_fast && kj < geo.kv_len) pg_ = __ldg(p.block_table + (int64_t)geo.b * p.bt_stride + kj / p.page_size);
+  };
+  int dk_cur, dp_cur, dk_next, dp_next;  // this lane's descriptor in the current / next batch
+  chunk_desc(lane, dk_cur, dp_cur);
+  chunk_desc(32 + lane, dk_next, dp_next);
+  auto chunk_key0 = [&](int k, bool& partial, bool& live, int& pg) -> int {
+    const int src = k & 31;
+    const bool cur = ((k >> 5) & 1) == 0;  // batches alternate between the two register sets
+    const int code = __shfl_sync(0xffffffffu, cur ? dk_cur : dk_next, src);
+    pg = __shfl_sync(0xffffffffu, cur ? dp_cur : dp_next, src);
+    partial = (code & 1) != 0;
+    const int kj0 = code >> 1;
+    live = (kj0 <= geo.jhi) && (kj0 + kChunkKeys - 1 >= geo.jlo) && (kj0 < geo.kv_len);
+    return kj0;
+  };
+  // lane l copies 16-byte chunk (l % 16) of rows 2i + l / 16 (i = 0..7) of K and V:
+  // each instruction covers two whole rows (D = 128) or four (D = 64)
+  auto load_chunk = [&](int k) {
+    bool partial, live;
+    int pg;
+    const int kj0 = chunk_key0(k, partial, live, pg);
+    if (!live) return;
+    if (TMA) {
+      if (lane == 0) {
+        const int st = k % kWarpStages;
+        int row, outer;
+        if (p.block_table) {
+          if ((unsigned)pg >= (unsigned)p.num_pages) {
+            record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)pg);
+            pg = 0;
+          }
+          row = kj0 % p.page_size;
+          outer = pg;
+        } else {
+          row = (p.cu_k ? p.cu_k[geo.b] : 0) + kj0;
+          outer = p.cu_k ? 0 : geo.b;
+        }
+        unsigned char* dst = smem + warp * S::kWarpBytes + st * S::kStageBytes;
+        // this warp's reads of the stage (previous chunk) precede the copy
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive_expect_tx(kv_full + st, S::kStageBytes);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf) {
+          tc::tma_load_4d(dst + hf * (kChunkKeys * 128), &tmk, kv_full + st, hf * 64, geo.g, row, outer);
+          tc::tma_load_4d(dst + S::kKvBytes + hf * (kChunkKeys * 128), &tmv, kv_full + st, hf * 64, geo.g, row,
+                          outer);
+        }
+      }
+      return;
+    }
+    const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
+    const uint32_t sV = sK + S::kKvBytes;
+    constexpr int kRowsPerInstr = 32 / S::kChunks;
+    const int c = lane % S::kChunks, r0 = lane / S::kChunks;
+    const uint16_t* kbase = nullptr;
+    const uint16_t* vbase = nullptr;
+    if (paged_fast) {
+      if ((unsigned)pg >= (unsigned)p.num_pages) {
+        record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)pg);
+        pg = 0;
+      }
+      const int64_t row0 = kj0 % p.page_size;
+      kbase = p.k + (int64_t)pg * p.k_sb + row0 * p.k_ss + (int64_t)geo.g * p.k_sh;
+      vbase = p.v + (int64_t)pg * p.v_sb + row0 * p.v_ss + (int64_t)geo.g * p.v_sh;
+    }
+#pragma unroll
+    for (int i = 0; i < kChunkKeys / kRowsPerInstr; ++i) {
+      const int r = i * kRowsPerInstr + r0;
+      const int j = min(kj0 + r, geo.kv_len - 1);
+      const uint16_t* kr;
+      const uint16_t* vr;
+      if (paged_fast && kj0 + r < geo.kv_len) {
+        kr = kbase + (int64_t)r * p.k_ss;
+        vr = vbase + (int64_t)r * p.v_ss;
+      } else {
+        kr = kv_row(p, p.k, p.k_sb, p.k_ss, p.k_sh, geo.b, geo.g, j);
+        vr = kv_row(p, p.v, p.v_sb, p.v_ss, p.v_sh, geo.b, geo.g, j);
+      }
+      cp_async16(sK + swz<D>(r, c), kr + c * 8);
+      cp_async16(sV + swz<D>(r, c), vr + c * 8);
+    }
+  };
+
+  // Fragment roles: keys (and head-dim) on the mma M side, the 8 packed
+  // query rows on N.  Lane = 4 g + c holds S^T[key g, g+8][row 2c, 2c+1] and
+  // O^T[d 16m + g, + 8][row 2c, 2c+1].
+  const int g8 = lane >> 2, c4 = lane & 3;
+  int qi_r[2], h_r[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    int P = geo.rt * kDecodeRows + 2 * c4 + e;
+    qi_r[e] = P / p.G;
+    h_r[e] = geo.g * p.G + P % p.G;
+  }
+  // the first chunks go out before Q is waited for, so their latency overlaps
+#pragma unroll
+  for (int k = 0; k < kWarpStages - 1; ++k) {
+    if (k < my_chunks) load_chunk(k);
+    if (!TMA) cp_async_commit();
+  }
+  if (TMA) cp_async_wait<0>();       // this thread's Q copies have landed
+  else cp_async_wait<kWarpStages - 1>();
+  __syncthreads();                   // ... and everyone else's
+  // Q^T as the B operand: [16 d x 8 rows] per k-step, two k-steps per ldmatrix.x4
+  uint32_t qb[D / 16][2];
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ks += 2) {
+    const int mi = lane >> 3;
+    ldsm_x4(sQ + swz<D>(lane & 7, 2 * ks + mi), qb[ks][0], qb[ks][1], qb[ks + 1][0], qb[ks + 1][1]);
+  }
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  float o_acc[D / 16][4];
+#pragma unroll
+  for (int n = 0; n < D / 16; ++n) o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
+
+  bool ok = true;
+  for (int k = 0; k < my_chunks; ++k) {
+    if (!TMA) cp_async_wait<kWarpStages - 2>();
+    __syncwarp();
+    if (k + kWarpStages - 1 < my_chunks) load_chunk(k + kWarpStages - 1);
+    if (!TMA) cp_async_commit();
+    // half a batch past a batch start, the batch after next replaces the one just finished
+    if ((k & 31) == 16 && k >= 32) {
+      if (((k >> 5) & 1) == 0) chunk_desc((k & ~31) + 32 + lane + 0, dk_next, dp_next);
+      else chunk_desc((k & ~31) + 32 + lane, dk_cur, dp_cur);
+    }
+    bool partial, live;
+    int pg_unused;
+    const int kj0 = chunk_key0(k, partial, live, pg_unused);
+    if (!live) continue;
+    if (TMA) {
+      const int st = k % kWarpStages;
+      if (!tc::mbar_wait(kv_full + st, (kv_phase >> st) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      kv_phase ^= 1u << st;
+    }
+    const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
+    const uint32_t sV = sK + S::kKvBytes;
+
+    // ---- S^T = K Q^T : 16 keys x 8 rows, two accumulator chains ----
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int mi = lane >> 3;
+      uint32_t a[4];
+      const int kr = (lane & 7) + 8 * (mi & 1), kc = 2 * ks + (mi >> 1);
+      ldsm_x4(sK + (TMA ? swz_tma(kr, kc) : swz<D>(kr, kc)), a[0], a[1], a[2], a[3]);
+      if (ks & 1) mma_bf16(sb, a, qb[ks][0], qb[ks][1]);
+      else mma_bf16(sa, a, qb[ks][0], qb[ks][1]);
+    }
+    float sc[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[e] = sa[e] + sb[e];
+    // ---- logit transform (log2 units); element e: key g8 + 8 (e >> 1), row 2 c4 + (e & 1) ----
+    // FULL chunk without an additive mask: only scale (and soft-cap) apply
+    const bool plain = !partial && p.mask_kind == FA_MASK_NONE;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = kj0 + g8 + 8 * (e >> 1);
+      const int rr = e & 1;
+      if (plain) {
+        sc[e] = p.softcap > 0.f ? softcap_log2(sc[e] * p.scale, p.softcap, p.inv_softcap) : sc[e] * p.scale_log2;
+      } else if (qi_r[rr] >= geo.q_len) {
+        sc[e] = -INFINITY;  // padding row: never read the mask out of range
+      } else {
+        sc[e] = logit_log2(p, sc[e], geo.b, h_r[rr], qi_r[rr], j, geo.off, geo.kv_len);
+      }
+    }
+    // ---- online softmax per row (a column of S^T), -inf guarded ----
+    float alpha[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      float mx = fmaxf(sc[rr], sc[rr + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run[rr], mx);
+      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+      alpha[rr] = fast_exp2(m_run[rr] - m_ref);
+      m_run[rr] = m_new;
+      sc[rr] = fast_exp2(sc[rr] - m_ref);
+      sc[rr + 2] = fast_exp2(sc[rr + 2] - m_ref);
+      l_run[rr] = l_run[rr] * alpha[rr] + sc[rr] + sc[rr + 2];
+    }
+#pragma unroll
+    for (int n = 0; n < D / 16; ++n) {
+      o_acc[n][0] *= alpha[0]; o_acc[n][1] *= alpha[1];
+      o_acc[n][2] *= alpha[0]; o_acc[n][3] *= alpha[1];
+    }
+    // ---- P^T (C layout) -> B operand [16 keys x 8 rows] by an 8x8 transpose ----
+    const uint32_t pb0 = movmatrix_t(pack_bf16(sc[0], sc[1]));  // keys 0..7
+    const uint32_t pb1 = movmatrix_t(pack_bf16(sc[2], sc[3]));  // keys 8..15
+    // ---- O^T += V^T P^T : per 16 head-dim values, one mma over the 16 keys ----
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      const int mi = lane >> 3;
+      uint32_t a[4];
+      const int vr = (lane & 7) + 8 * (mi >> 1), vc = 2 * mt + (mi & 1);
+      ldsm_x4_t(sV + (TMA ? swz_tma(vr, vc) : swz<D>(vr, vc)), a[0], a[1], a[2], a[3]);
+      mma_bf16(o_acc[mt], a, pb0, pb1);
+    }
+  }
+  cp_async_wait<0>();
+  if (TMA && !ok && !*abort_flag) {
+    *abort_flag = 1;
+    record_error(p, FA_ERR_DEVICE_TIMEOUT, 22);
+  }
+  __syncthreads();
+  if (TMA && *abort_flag) {
+    // copies may still be landing in this warp's ring: let them, then leave
+    // without touching shared memory or results
+    if (lane < kWarpStages) tc::mbar_wait_drain(kv_full + lane, (kv_phase >> lane) & 1, 100000000ull);
+    return;
+  }
+
+  decode_finish<D>(p, geo, item, split, single, smem, reinterpret_cast<float*>(smem + kWarps * S::kWarpBytes), tid,
+                   m_run, l_run, o_acc);
+}
+
 // Merge the splits of items that had more than one: LSE = logsumexp of the
 // split LSEs (all -inf -> -inf), O = sum_s exp(LSE_s - LSE) O_s (0 if empty).
 template <int D>
@@ -450,14 +571,50 @@ __global__ void __launch_bounds__(32 * kDecodeRows) combine_kernel(const Params 
   if (lane == 0) *lptr = (L > 0.f) ? (M + __logf(L)) : -INFINITY;
 }
 
+// Tensor maps for the TMA decode path: 4-D {d, Hkv, rows, outer} with a
+// 16-row box; rows/outer are (row in page, page) for a paged cache, (row,
+// sequence) or (packed row, 1) otherwise.  False when the layout has none.
+template <int D>
+bool decode_maps(const Params& p, CUtensorMap* mk, CUtensorMap* mv) {
+  int64_t rows, outer, k_so, v_so;
+  if (p.block_table) {
+    if (p.page_size % kChunkKeys != 0) return false;
+    rows = p.page_size;
+    outer = p.num_pages;
+    k_so = p.k_sb;
+    v_so = p.v_sb;
+  } else {
+    rows = p.cu_k ? p.tot_k : p.Sk;
+    outer = p.cu_k ? 1 : p.n_seq;
+    k_so = (outer == 1 || p.k_sb == 0) ? p.k_ss : p.k_sb;
+    v_so = (outer == 1 || p.v_sb == 0) ? p.v_ss : p.v_sb;
+  }
+  if (rows <= 0 || outer <= 0) return false;
+  return encode_4d_bf16(mk, p.k, D, p.Hkv, rows, outer, p.k_sh, p.k_ss, k_so, 64, kChunkKeys,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) &&
+         encode_4d_bf16(mv, p.v, D, p.Hkv, rows, outer, p.v_sh, p.v_ss, v_so, 64, kChunkKeys,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+}
+
 template <int D>
 cudaError_t launch_decode_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
+  cudaError_t e;
+  const int64_t grid = p.n_items * p.n_splits;
   using S = DecodeSmem<D>;
-  cudaError_t e = ensure_smem_attr<decode_kernel<D>>(S::kTotal);
-  if (e != cudaSuccess) return e;
-  if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-  int64_t grid = p.n_items * p.n_splits;
-  decode_kernel<D><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p);
+  CUtensorMap mk, mv;
+  if (decode_maps<D>(p, &mk, &mv)) {
+    e = ensure_smem_attr<decode_kernel<D, true>>(S::kTotal);
+    if (e != cudaSuccess) return e;
+    if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
+    decode_kernel<D, true><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
+  } else {
+    memset(&mk, 0, sizeof(mk));
+    memset(&mv, 0, sizeof(mv));
+    e = ensure_smem_attr<decode_kernel<D, false>>(S::kTotal);
+    if (e != cudaSuccess) return e;
+    if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
+    decode_kernel<D, false><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess || p.n_splits <= 1) return e;
   combine_kernel<D><<<(unsigned)p.n_items, 32 * kDecodeRows, 0, st>>>(p);

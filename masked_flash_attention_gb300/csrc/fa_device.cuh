@@ -68,26 +68,39 @@ __device__ __forceinline__ bool tile_all_allowed(const Params& p, int i0, int i1
   return ok;
 }
 
+__device__ __forceinline__ float fast_exp2(float x);
+
+// Soft-capped logit in log2 units: cap * tanh(x / cap) * log2(e), with
+// tanh(y) = sign(y) (1 - t) / (1 + t), t = 2^(-2 log2(e) |y|) -- one hardware
+// exp2 and one fast division instead of a full-precision tanh and divide.
+// For small |y| the rounding of 1 - t costs about 1e-7 relative to 1, i.e.
+// ~1e-6 in the logit at cap 30: far below the bf16 rounding of P.
+__device__ __forceinline__ float softcap_log2(float x, float cap, float inv_cap) {
+  const float y = x * inv_cap;
+  const float t = fast_exp2(-2.f * kLog2e * fabsf(y));
+  const float th = __fdividef(1.f - t, 1.f + t);
+  return copysignf(th, y) * (cap * kLog2e);
+}
+
 // Full logit transform of one raw dot product `s` for (sequence b, q-head h,
 // query row i, key j), returned in log2 units (x * log2 e), -inf if dropped:
 // scale, soft-cap, pair rules, dense mask or top-k (keep test + bias).
 __device__ __forceinline__ float logit_log2(const Params& p, float s, int b, int h, int i, int j,
                                             int off, int kv_len) {
-  float x = s * p.scale;
-  if (p.softcap > 0.f) x = p.softcap * tanhf(x / p.softcap);
   if (!pair_allowed(p, i, j, off, kv_len)) return -INFINITY;
+  float x = (p.softcap > 0.f) ? softcap_log2(s * p.scale, p.softcap, p.inv_softcap) : s * p.scale_log2;
   if (p.mask_kind == FA_MASK_DENSE) {
     const float* m = p.mask + (int64_t)(p.m_nb > 1 ? b : 0) * p.m_sb +
                      (int64_t)(p.m_nh > 1 ? h : 0) * p.m_sh + (int64_t)i * p.m_sq +
                      (int64_t)j * p.m_sk;
-    x += __ldg(m);
+    x += __ldg(m) * kLog2e;
   } else if (p.mask_kind == FA_MASK_TOPK) {
     int64_t bh = (int64_t)b * p.Hq + h;
     int e = __ldg(p.topk_e + bh * p.Sk + j);
     if (!(i < e)) return -INFINITY;
-    x += __ldg(p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh + (int64_t)j * p.z_sk);
+    x += __ldg(p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh + (int64_t)j * p.z_sk) * kLog2e;
   }
-  return x * kLog2e;
+  return x;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

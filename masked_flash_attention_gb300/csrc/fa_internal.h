@@ -47,6 +47,7 @@ struct Params {
   float scale;        // natural-log units
   float scale_log2;   // scale * log2(e)
   float softcap;      // 0 = off
+  float inv_softcap;  // 1 / softcap (0 when off)
   int32_t causal, wl, wr;
 
   // additive mask

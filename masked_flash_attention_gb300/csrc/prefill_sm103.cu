@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           for (int e = 0; e < 128; ++e) {
             float v = (e & 1) ? x[e >> 1].y : x[e >> 1].x;
             if (SC) {
-              v = p.softcap * tanhf(v * p.scale / p.softcap) * kLog2e;
+              v = softcap_log2(v * p.scale, p.softcap, p.inv_softcap);
             } else {
               v = v * p.scale_log2;
             }
@@ -697,54 +697,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-    cudaGetLastError();
-  });
-  return fn;
-}
-
 // 4-D map {d, heads, rows, batch} over a bshd (or packed thd) bf16 tensor,
 // box {64, 1, 128, 1}, 128-byte swizzle; rows beyond the tensor read as 0.
 bool encode_bshd(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int batch, int64_t s_h,
                  int64_t s_row, int64_t s_b) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows, (cuuint64_t)batch};
-  cuuint64_t strides[3] = {(cuuint64_t)s_h * 2, (cuuint64_t)s_row * 2, (cuuint64_t)s_b * 2};
-  cuuint32_t box[4] = {64, 1, 128, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_4d_bf16(m, base, d, heads, rows, batch, s_h, s_row, s_b, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 // 4-D map over the bf16 output for the epilogue's TMA stores: box {32, 1, 32,
 // 1} (32 columns x 32 rows), 64-byte swizzle (the staging layout).
 bool encode_out(CUtensorMap* m, void* base, int d, int heads, int64_t rows, int batch, int64_t s_h, int64_t s_row,
                 int64_t s_b) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows, (cuuint64_t)batch};
-  cuuint64_t strides[3] = {(cuuint64_t)s_h * 2, (cuuint64_t)s_row * 2, (cuuint64_t)s_b * 2};
-  cuuint32_t box[4] = {32, 1, 32, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_4d_bf16(m, base, d, heads, rows, batch, s_h, s_row, s_b, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 int sm_count() {

@@ -53,8 +53,8 @@ KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_dev
 # time: once the kernel changes the figure no longer applies and is reported
 # as null.
 MEASURED_TRAFFIC = {
-    ("causal_prefill_past_kv", "prefill_kernel"): ("4101633fddd7561e", 106117888),
-    ("paged_varlen_decode", "decode_kernel"): ("36d1816d64710c6c", 759962112),
+    ("causal_prefill_past_kv", "prefill_kernel"): ("ff044ea3e0fb75e7", 108679424),
+    ("paged_varlen_decode", "decode_kernel"): ("9c347889c8150332", 761989120),
 }
 
 

@@ -12,7 +12,11 @@ What is computed (for every sequence b, query head h, query row i, key j):
      repeating them is its section "Transformer 接入".
   2. ``x = scale * <Q[i], K[j]>``, then the logit soft-cap
      ``x = softcap * tanh(x / softcap)`` when softcap > 0 (the ``softcap``
-     argument of the vLLM pull request 11277 ``flash_attn_varlen_func`` call).
+     argument of the vLLM pull request 11277 ``flash_attn_varlen_func`` call),
+     then the ALiBi bias ``x -= slope[h] * |i + off - j|`` when per-head slopes
+     are given (the ``alibi_slopes`` argument of the same call; the pages name
+     it without a formula, and this linear distance penalty, aligned like the
+     causal rule below, is its plain reading).
   3. pair rules, with ``off = kv_len - q_len`` (bottom-right alignment: the
      last query sits on the last key; FastChat pull request 2315 "Optimize
      for proper flash attn causal handling", causal with q_len != kv_len and
@@ -34,7 +38,8 @@ What is computed (for every sequence b, query head h, query row i, key j):
      chunk) gives O = 0 and LSE = -inf; otherwise the plain softmax
      ``p = exp(x - max) / sum``, ``O = p @ V``, ``LSE = max + ln(sum)``.
 
-Readings where the pages are silent are listed in the design doc of the project.
+Where the pages are silent the plainest reading that the rest supports is
+taken; each such reading is stated where it is used.
 """
 from __future__ import annotations
 
@@ -86,7 +91,8 @@ def topk_kept_row(z, candidates, keep_window):
 
 
 def logits_rows(q_rows, k, rows, q_len, kv_len, *, scale, causal=False, window_left=-1,
-                window_right=-1, softcap=0.0, mask_rows=None, z=None, keep_window=0):
+                window_right=-1, softcap=0.0, mask_rows=None, z=None, keep_window=0,
+                alibi_slope=None):
     """Final logits ``x[r, j]`` for the query rows ``rows`` of one (sequence,
     head): scaled dot products, soft-cap, pair rules, additive terms; -inf
     where a key is dropped.  ``q_rows`` is ``[len(rows), d]``, ``k`` is
@@ -99,6 +105,9 @@ def logits_rows(q_rows, k, rows, q_len, kv_len, *, scale, causal=False, window_l
     s = float(scale) * (q_rows @ k.T)
     if softcap and softcap > 0:
         s = float(softcap) * np.tanh(s / float(softcap))
+    if alibi_slope is not None:  # this head's ALiBi slope
+        off = kv_len - q_len
+        s = s - float(alibi_slope) * np.abs((rows + off)[:, None] - keys[None, :]).astype(np.float64)
     ok = allowed_pairs(rows, keys, q_len, kv_len, causal, window_left, window_right)
     if mask_rows is not None:
         s = s + _np(mask_rows)
@@ -161,7 +170,8 @@ def _mask_for(mask, b, h, Sq, Sk):
 
 def attention(q, k, v, *, scale=None, causal=False, window_left=-1, window_right=-1,
               softcap=0.0, mask=None, zero_hold_states=None, keep_window=0,
-              cu_seqlens_q=None, cu_seqlens_k=None, block_table=None, **_unused):
+              cu_seqlens_q=None, cu_seqlens_k=None, block_table=None, alibi_slopes=None,
+              **_unused):
     """Masked attention forward over a whole batch.
 
     Layouts: Q ``[B, Sq, Hq, d]`` and K/V ``[B, Sk, Hkv, d]``; or packed
@@ -169,7 +179,8 @@ def attention(q, k, v, *, scale=None, causal=False, window_left=-1, window_right
     ``[total_k, Hkv, d]`` with ``cu_seqlens_k`` (vLLM ``flash_attn_varlen_func``
     arguments); or a paged K/V cache ``[num_pages, page_size, Hkv, d]`` with
     ``block_table`` ``[n_seq, max_pages]`` and ``cu_seqlens_k`` giving each
-    sequence's key count.  Returns ``(out, lse)`` in fp64: ``out`` shaped like
+    sequence's key count; ``alibi_slopes``, optional, per q-head ``[Hq]``.
+    Returns ``(out, lse)`` in fp64: ``out`` shaped like
     Q; ``lse`` ``[B, Hq, Sq]`` (or ``[Hq, total_q]`` when Q is packed)."""
     q = _np(q)
     k = _np(k)
@@ -215,8 +226,9 @@ def attention(q, k, v, *, scale=None, causal=False, window_left=-1, window_right
         for h in range(Hq):
             g = h // G
             z = None if zero_hold_states is None else _np(zero_hold_states)[b, h, :Sk]
+            slope = None if alibi_slopes is None else float(_np(alibi_slopes)[h])
             o, l = attention_rows(qb[:, h, :], kb[:, g, :], vb[:, g, :], np.arange(Sq), Sq, Sk,
-                                  mask_rows=_mask_for(mask, b, h, Sq, Sk), z=z, **kw)
+                                  mask_rows=_mask_for(mask, b, h, Sq, Sk), z=z, alibi_slope=slope, **kw)
             if packed_q:
                 out[q0:q1, h, :] = o
                 lse[h, q0:q1] = l

@@ -430,3 +430,62 @@ def test_paged_decode_workload_shapes():
         assert int((bt[s] >= 0).sum()) == (int(lens[s]) + 15) // 16
     out, lse = O.attention(c["q"], c["k"], c["v"], **p)
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+# ---------------------------------------------------------------------------
+# ALiBi (the ``alibi_slopes`` argument of the vLLM pull request 11277 call):
+# with Q = 0 every score is 0, so the weights are e^(-s * distance) and the
+# row sums are geometric series with a closed form.
+# ---------------------------------------------------------------------------
+
+def _geometric(s, n):
+    """sum_{d=0}^{n-1} e^(-s d)"""
+    return (1.0 - math.exp(-s * n)) / (1.0 - math.exp(-s))
+
+
+def test_alibi_causal_closed_form():
+    n, s = 9, 0.37
+    q = torch.zeros(1, n, 1, 16)
+    k = torch.randn(1, n, 1, 16, generator=torch.Generator().manual_seed(3))
+    v = torch.zeros(1, n, 1, 16)
+    v[0, :, 0, :n] = torch.eye(n)  # V row j = e_j: O row i = the weights themselves
+    out, lse = O.attention(q, k, v, causal=True, alibi_slopes=np.array([s]))
+    for i in range(n):
+        z = _geometric(s, i + 1)
+        assert abs(lse[0, 0, i] - math.log(z)) < 1e-12
+        want = np.zeros(16)
+        for j in range(i + 1):
+            want[j] = math.exp(-s * (i - j)) / z
+        np.testing.assert_allclose(out[0, i, 0], want, atol=1e-14)
+
+
+def test_alibi_bottom_right_single_query():
+    # one query over n keys, causal: it sits on the last key, distances 0..n-1
+    n, s = 12, 0.21
+    q = torch.zeros(1, 1, 2, 8)
+    k = torch.randn(1, n, 1, 8, generator=torch.Generator().manual_seed(4))
+    v = torch.randn(1, n, 1, 8, generator=torch.Generator().manual_seed(5))
+    _, lse = O.attention(q, k, v, causal=True, alibi_slopes=np.array([s, 2 * s]))
+    assert abs(lse[0, 0, 0] - math.log(_geometric(s, n))) < 1e-12
+    assert abs(lse[0, 1, 0] - math.log(_geometric(2 * s, n))) < 1e-12
+
+
+def test_alibi_non_causal_two_sided():
+    n, s = 7, 0.5
+    q = torch.zeros(1, n, 1, 8)
+    k = torch.randn(1, n, 1, 8, generator=torch.Generator().manual_seed(6))
+    v = torch.randn(1, n, 1, 8, generator=torch.Generator().manual_seed(7))
+    _, lse = O.attention(q, k, v, alibi_slopes=np.array([s]))
+    for i in range(n):
+        # keys at or left of i: distances 0..i; right of i: 1..n-1-i
+        z = _geometric(s, i + 1) + (_geometric(s, n - i) - 1.0)
+        assert abs(lse[0, 0, i] - math.log(z)) < 1e-12
+
+
+def test_alibi_zero_slope_is_no_bias():
+    g = torch.Generator().manual_seed(8)
+    q, k, v = (torch.randn(2, 5, 4, 16, generator=g).bfloat16() for _ in range(3))
+    a, la = O.attention(q, k[:, :, :2], v[:, :, :2], causal=True)
+    b, lb = O.attention(q, k[:, :, :2], v[:, :, :2], causal=True, alibi_slopes=np.zeros(4))
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(la, lb)

@@ -76,7 +76,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 1
+#define FA_ABI_VERSION 2
 
 typedef enum {
   FA_OK = 0,
@@ -132,6 +132,16 @@ typedef struct {
    * pass (split combine included): lets a caller time that kernel alone. */
   void* event_begin;
   void* event_end;
+  /* Optional ALiBi slopes (NULL = none): device pointer to Hq fp32 values,
+   * one per query head.  Adds -slope[h] * |i + kv_len - q_len - j| to the
+   * (scaled, soft-capped) logit of query row i and key j, before masks:
+   * vLLM pull request 11277, the `alibi_slopes` argument of its
+   * flash_attn_varlen_func call (the pages give no formula; this linear
+   * distance penalty, aligned bottom-right like the causal rule, is the plain
+   * reading).  Read by the kernels, so it must stay valid until they finish.
+ * On the prefill path ALiBi cannot be combined with a dense or top-k mask
+ * (FA_ERR_UNSUPPORTED); the decode path takes any combination. */
+  const void* alibi_slopes;
 } fa_opts;
 
 /* Kernel path chosen by the planner. */

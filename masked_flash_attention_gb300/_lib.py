@@ -49,7 +49,7 @@ class fa_opts(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("max_seqlen_q", ctypes.c_int32),
                 ("max_seqlen_k", ctypes.c_int32), ("debug_flags", ctypes.c_uint32),
                 ("reserved", ctypes.c_int32), ("event_begin", ctypes.c_void_p),
-                ("event_end", ctypes.c_void_p)]
+                ("event_end", ctypes.c_void_p), ("alibi_slopes", ctypes.c_void_p)]
 
 
 class fa_plan(ctypes.Structure):
@@ -156,8 +156,9 @@ def _out_shapes(q, cu_seqlens_q, max_seqlen_q):
 
 
 def make_opts(stream=None, workspace=None, max_seqlen_q=0, max_seqlen_k=0, debug_flags=0,
-              event_begin=None, event_end=None):
+              event_begin=None, event_end=None, alibi_slopes=None):
     o = fa_opts()
+    o.alibi_slopes = alibi_slopes.data_ptr() if alibi_slopes is not None else None
     o.event_begin = event_begin.cuda_event if event_begin is not None else None
     o.event_end = event_end.cuda_event if event_end is not None else None
     o.stream = stream if stream is not None else torch.cuda.current_stream().cuda_stream
@@ -195,14 +196,27 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
     return torch.zeros(max(256, int(nbytes)), dtype=torch.uint8, device=device)
 
 
+def _alibi(slopes, q):
+    """Checked ALiBi slopes: a contiguous fp32 CUDA tensor with one value per
+    query head, on q's device (or None)."""
+    if slopes is None:
+        return None
+    if (not isinstance(slopes, torch.Tensor) or slopes.dtype != torch.float32 or not slopes.is_cuda
+            or slopes.device != q.device or slopes.dim() != 1 or slopes.numel() != q.shape[-2]
+            or not slopes.is_contiguous()):
+        raise FaError(FA_ERR_INVALID_ARG, "alibi_slopes (fp32 CUDA tensor [Hq] on q's device)")
+    return slopes
+
+
 def fa_fwd(q, k, v, *, out=None, lse=None, cu_seqlens_q=None, cu_seqlens_k=None,
            block_table=None, mask=None, zero_hold_states=None, keep_window=0, window_left=-1,
            window_right=-1, softcap=0.0, scale=None, causal=False, max_seqlen_q=None,
            max_seqlen_k=None, workspace=None, stream=None, debug_flags=0, event_begin=None,
-           event_end=None, **_):
+           event_end=None, alibi_slopes=None, **_):
     """Masked attention forward on the GPU through the C ABI.  Returns
     ``(out, lse, workspace)``; ``out``/``lse``/``workspace`` are allocated with
-    torch when not given.  Raises FaError on a non-zero status."""
+    torch when not given.  ``alibi_slopes``: optional fp32 CUDA tensor [Hq].
+    Raises FaError on a non-zero status."""
     if not q.is_cuda:
         raise FaError(FA_ERR_INVALID_ARG, "fa_fwd (tensors must be CUDA tensors)")
     oshape, lshape = _out_shapes(q, cu_seqlens_q, max_seqlen_q)
@@ -210,8 +224,10 @@ def fa_fwd(q, k, v, *, out=None, lse=None, cu_seqlens_q=None, cu_seqlens_k=None,
         out = torch.empty(oshape, dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty(lshape, dtype=torch.float32, device=q.device)
+    alibi_slopes = _alibi(alibi_slopes, q)
     opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
-                     debug_flags=debug_flags, event_begin=event_begin, event_end=event_end)
+                     debug_flags=debug_flags, event_begin=event_begin, event_end=event_end,
+                     alibi_slopes=alibi_slopes)
     args, keep = _args(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask,
                        zero_hold_states, keep_window, window_left, window_right, softcap,
                        scale or 0.0, causal, opts)
@@ -240,7 +256,7 @@ def fa_check_device_error(workspace, stream=None):
 def fa_fwd_noalloc(q, k, v, *, out, lse, cu_seqlens_q=None, cu_seqlens_k=None, block_table=None,
                    mask=None, zero_hold_states=None, keep_window=0, window_left=-1, window_right=-1,
                    softcap=0.0, scale=None, causal=False, max_seqlen_q=None, max_seqlen_k=None,
-                   stream=None, debug_flags=0, **_):
+                   stream=None, debug_flags=0, alibi_slopes=None, **_):
     """fa_fwd_noalloc of the C ABI: the forward pass for callers that may not
     allocate device memory.  ``out`` and ``lse`` are caller-provided; the
     library's static device scratch replaces the workspace, so nothing is
@@ -249,8 +265,9 @@ def fa_fwd_noalloc(q, k, v, *, out, lse, cu_seqlens_q=None, cu_seqlens_k=None, b
     fn = lib.fa_fwd_noalloc
     fn.argtypes = _ARGS
     fn.restype = ctypes.c_int
+    alibi_slopes = _alibi(alibi_slopes, q)
     opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
-                     debug_flags=debug_flags)
+                     debug_flags=debug_flags, alibi_slopes=alibi_slopes)
     args, keep = _args(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask,
                        zero_hold_states, keep_window, window_left, window_right, softcap,
                        scale or 0.0, causal, opts)

@@ -225,6 +225,7 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   P.wr = wr;
   P.mask_kind = mask_kind;
   P.debug_flags = opts->debug_flags;
+  P.alibi = static_cast<const float*>(opts->alibi_slopes);
 
   // ---- path and tile geometry ----
   // Few query rows per K/V head (decode): the 16-row split-KV kernel.  Many
@@ -249,6 +250,8 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
     P.n_heads_sched = (int32_t)Hkv;
     P.n_row_tiles = ceil_div(Sq * G, kDecodeRows);
   }
+  // prefill carries ALiBi only without a dense or top-k mask (decode: any)
+  if (P.path == FA_PATH_PREFILL && P.alibi && mask_kind != FA_MASK_NONE) return FA_ERR_UNSUPPORTED;
   P.n_kt = ceil_div(Sk, kKeysPerTile);
   P.n_items = n_seq * (int64_t)P.n_heads_sched * P.n_row_tiles;
   if (Sq == 0 || n_seq == 0) P.n_items = 0;

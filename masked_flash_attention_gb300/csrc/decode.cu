@@ -467,8 +467,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int e = 0; e < 4; ++e) sc[e] = sa[e] + sb[e];
     // ---- logit transform (log2 units); element e: key g8 + 8 (e >> 1), row 2 c4 + (e & 1) ----
-    // FULL chunk without an additive mask: only scale (and soft-cap) apply
-    const bool plain = !partial && p.mask_kind == FA_MASK_NONE;
+    // FULL chunk without an additive term: only scale (and soft-cap) apply
+    const bool plain = !partial && p.mask_kind == FA_MASK_NONE && !p.alibi;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = kj0 + g8 + 8 * (e >> 1);

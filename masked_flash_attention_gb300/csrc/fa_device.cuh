@@ -84,11 +84,12 @@ __device__ __forceinline__ float softcap_log2(float x, float cap, float inv_cap)
 
 // Full logit transform of one raw dot product `s` for (sequence b, q-head h,
 // query row i, key j), returned in log2 units (x * log2 e), -inf if dropped:
-// scale, soft-cap, pair rules, dense mask or top-k (keep test + bias).
+// scale, soft-cap, ALiBi, pair rules, dense mask or top-k (keep test + bias).
 __device__ __forceinline__ float logit_log2(const Params& p, float s, int b, int h, int i, int j,
                                             int off, int kv_len) {
   if (!pair_allowed(p, i, j, off, kv_len)) return -INFINITY;
   float x = (p.softcap > 0.f) ? softcap_log2(s * p.scale, p.softcap, p.inv_softcap) : s * p.scale_log2;
+  if (p.alibi) x -= __ldg(p.alibi + h) * kLog2e * (float)abs(i + off - j);
   if (p.mask_kind == FA_MASK_DENSE) {
     const float* m = p.mask + (int64_t)(p.m_nb > 1 ? b : 0) * p.m_sb +
                      (int64_t)(p.m_nh > 1 ? h : 0) * p.m_sh + (int64_t)i * p.m_sq +

@@ -48,6 +48,7 @@ struct Params {
   float scale_log2;   // scale * log2(e)
   float softcap;      // 0 = off
   float inv_softcap;  // 1 / softcap (0 when off)
+  const float* alibi; // [Hq] ALiBi slopes (natural-log units), null = off
   int32_t causal, wl, wr;
 
   // additive mask

@@ -206,8 +206,9 @@ __device__ __forceinline__ void row_key_range(const Params& p, int i, int q_len,
   if (i >= q_len) { lo = 1; hi = 0; }
 }
 
-// MK: additive term kind (FA_MASK_NONE / DENSE / TOPK); SC: logit soft-cap on.
-template <int D, int MK, bool SC>
+// MK: additive term kind (FA_MASK_NONE / DENSE / TOPK); SC: logit soft-cap on;
+// AL: ALiBi slopes on (only with MK == FA_MASK_NONE).
+template <int D, int MK, bool SC, bool AL>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const int o_tma) {
@@ -458,6 +459,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       int jlo_r, jhi_r;
       row_key_range(p, i, q_len, kv_len, off, jlo_r, jhi_r);
+      const float alibi_l2 = AL ? __ldg(p.alibi + h) * kLog2e : 0.f;  // ALiBi slope, log2 units
       float m_ref = -INFINITY;  // reference after the last tile seen
       float r_own = -INFINITY;  // reference this warpgroup's row sum is against
       float l = 0.f;
@@ -513,7 +515,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         tc::mbar_arrive_relaxed(s_free + par);  // the QK two tiles on may overwrite this S buffer
         // logits in log2 units; a FULL tile without soft-cap keeps raw scores
         // and folds the scale into the exponent below
-        const bool plain = !SC && !part;
+        const bool plain = !SC && !part && !AL;
         float mx;
         if (plain) {
           mx = row_max128(x) * p.scale_log2;
@@ -531,6 +533,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             } else {
               v = v * p.scale_log2;
             }
+            if (AL) v -= alibi_l2 * (float)abs(i + off - (j0 + e));
             bool keep = !part || (e >= clo && e <= chi);
             if (MK == FA_MASK_DENSE && part) {
               if (keep) v += __ldg(mrow + (int64_t)e * p.m_sk) * kLog2e;
@@ -726,7 +729,7 @@ int sm_count() {
   return n;
 }
 
-template <int D, int MK, bool SC>
+template <int D, int MK, bool SC, bool AL>
 cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& mv, const CUtensorMap& mo, int o_tma, int grid,
                              cudaEvent_t ev_begin) {
@@ -735,15 +738,15 @@ cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap
   static int regs = -1;
   if (regs < 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MK, SC>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MK, SC, AL>);
     if (e != cudaSuccess) return e;
     regs = fa.numRegs;
   }
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC>>(PCfg<D>::kSmem);
+  cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL>>(PCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-  prefill_kernel<D, MK, SC><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
+  prefill_kernel<D, MK, SC, AL><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
   return cudaGetLastError();
 }
 
@@ -772,16 +775,21 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
   if (units > INT_MAX) return cudaErrorInvalidValue;
   const int grid = (int)(units < sm_count() ? units : sm_count());
   const bool sc = p.softcap > 0.f;
+  if (p.alibi) {  // the planner allows ALiBi in prefill only without a mask
+    if (p.mask_kind != FA_MASK_NONE) return cudaErrorInvalidValue;
+    return sc ? launch_prefill_v<D, FA_MASK_NONE, true, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+              : launch_prefill_v<D, FA_MASK_NONE, false, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
+  }
   switch (p.mask_kind) {
     case FA_MASK_DENSE:
-      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
-                : launch_prefill_v<D, FA_MASK_DENSE, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
+      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_DENSE, false, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
     case FA_MASK_TOPK:
-      return sc ? launch_prefill_v<D, FA_MASK_TOPK, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
-                : launch_prefill_v<D, FA_MASK_TOPK, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
+      return sc ? launch_prefill_v<D, FA_MASK_TOPK, true, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_TOPK, false, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
     default:
-      return sc ? launch_prefill_v<D, FA_MASK_NONE, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
-                : launch_prefill_v<D, FA_MASK_NONE, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
+      return sc ? launch_prefill_v<D, FA_MASK_NONE, true, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_NONE, false, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
   }
 }
 

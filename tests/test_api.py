@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(fa.lib, n), n
         assert ctypes.cast(getattr(fa.lib, n), ctypes.c_void_p).value
-    assert fa.fa_abi_version() == 1
+    assert fa.fa_abi_version() == 2
     assert fa.fa_status_string(0) == "ok"
 
 

@@ -325,3 +325,62 @@ def test_prefill_varlen(seed, q_eq_k):
     case = dict(name=f"prefill_varlen{seed}", q=q, k=k, v=v, params=params)
     _assert_prefill(case)
     check(case)
+
+
+# ---------------------------------------------------------------------------
+# ALiBi slopes (vLLM pull request 11277's flash_attn_varlen_func argument):
+# prefill and decode, with and without other additive terms
+# ---------------------------------------------------------------------------
+
+def _alibi_slopes(H):
+    # the usual geometric head slopes 2^(-8 (h + 1) / H)
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=torch.float32)
+
+
+ALIBI = [
+    (2, 300, 700, 8, 2, 128, dict(causal=True)),                                    # prefill, past KV
+    (1, 256, 600, 4, 4, 64, dict(causal=False, window_left=200, window_right=50)),  # two-sided distances
+    (1, 200, 200, 4, 2, 128, dict(causal=True, softcap=20.0)),                      # after the soft-cap
+    (2, 1, 900, 8, 2, 128, dict(causal=True, softcap=30.0)),                        # decode
+    (3, 2, 300, 4, 4, 64, dict(causal=True)),                                       # decode, 2 rows
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("i", range(len(ALIBI)))
+def test_alibi(i):
+    B, Sq, Sk, Hq, Hkv, d, extra = ALIBI[i]
+    c = W.random_case(900 + i, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, d=d, **extra)
+    check(c, alibi_slopes=_alibi_slopes(Hq))
+
+
+@pytest.mark.gpu
+def test_alibi_with_dense_mask():
+    # decode path: ALiBi and a dense mask together
+    c = W.random_case(910, B=2, Sq=3, Sk=400, Hq=4, Hkv=2, d=128, causal=True)
+    m = W.random_dense_mask(910, 3, 400)
+    m[:, :128] = float("-inf")
+    check(c, mask=m, alibi_slopes=_alibi_slopes(4))
+
+
+@pytest.mark.gpu
+def test_alibi_with_mask_on_prefill_is_unsupported():
+    import masked_flash_attention_gb300 as fa
+    c = W.random_case(911, B=1, Sq=260, Sk=400, Hq=4, Hkv=2, d=128, causal=True)
+    m = W.random_dense_mask(911, 260, 400)
+    with pytest.raises(fa.FaError) as e:
+        run_gpu(c, mask=m, alibi_slopes=_alibi_slopes(4))
+    assert e.value.status == fa._lib.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_alibi_paged_decode():
+    c = W.paged_varlen_decode(seed=3, n_seq=6, max_len=700)
+    check(c, alibi_slopes=_alibi_slopes(c["q"].shape[-2]))
+
+
+def test_alibi_slopes_checked():
+    import masked_flash_attention_gb300 as fa
+    q = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(fa.FaError):
+        fa._lib._alibi(torch.zeros(3), q)  # wrong length (and not on a device)

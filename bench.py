@@ -145,6 +145,15 @@ def algorithmic_io_bytes(case):
     return (q.numel() + k.numel() + v.numel() + q.numel()) * 2 + lse
 
 
+def _as_dtype(case, dtype):
+    """The workload with q, k, v in the requested input type (for "f16" the
+    bf16 draws converted to fp16)."""
+    if dtype == "bf16":
+        return case
+    t = torch.float16
+    return dict(case, name=case["name"] + "_f16", q=case["q"].to(t), k=case["k"].to(t), v=case["v"].to(t))
+
+
 def workload_units(case, name):
     d = case["q"].shape[-1]
     if name == "paged_varlen_decode":
@@ -236,7 +245,7 @@ def run_gpu(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    case = W.WORKLOADS[args.workload](seed=args.seed + rank)
+    case = _as_dtype(W.WORKLOADS[args.workload](seed=args.seed + rank), args.dtype)
     units = workload_units(case, args.workload)
     p = dict(case["params"])
     gp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
@@ -352,7 +361,7 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": args.dtype,
         "data": "synthetic",
         "config": {"workload": case["name"], "seed": args.seed,
                    "l2": "flushed between timed steps (256 MB write outside the events)",
@@ -441,7 +450,7 @@ def run_reference(args):
     dist_rank = int(os.environ.get("RANK", "0"))
     if dist_rank != 0:
         return None
-    case = W.WORKLOADS[args.workload](seed=args.seed)
+    case = _as_dtype(W.WORKLOADS[args.workload](seed=args.seed), args.dtype)
     units = workload_units(case, args.workload)
     per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     n, _ = _pick_heads(case, per_step_budget)
@@ -478,6 +487,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="causal_prefill_past_kv", choices=sorted(W.WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
+                    help="input type of q, k, v and out (fp16 peak = bf16 peak, as the nominal rates are equal)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,

@@ -34,6 +34,12 @@
  * h / (Hq / Hkv); K/V are never expanded (InfiniTrain pull request 193, "feat:
  * Flash Attention", sections "Framework 与 autograd" and "Transformer 接入").
  *
+ * Element type: q, k, v and out are all bf16 or all fp16 (the two input
+ * types of the FlashAttention-2 kernels in InfiniTrain pull request 193,
+ * "FlashAttention native backend"; "bf16" below stands for either).  Logits,
+ * the softmax and the accumulators are fp32; P enters the PV product in the
+ * input type; out is written in the input type.
+ *
  * Layouts (element strides; the head-dim stride must be 1, every other stride
  * a multiple of 8 elements, every base pointer 16-byte aligned):
  *   q    bf16 [B, Sq, Hq, d]                      fixed-length batch
@@ -76,7 +82,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 2
+#define FA_ABI_VERSION 3
 
 typedef enum {
   FA_OK = 0,
@@ -89,7 +95,7 @@ typedef enum {
   FA_ERR_NO_DEVICE = 7       /* no usable sm_103 device is current */
 } fa_status;
 
-typedef enum { FA_DTYPE_BF16 = 1, FA_DTYPE_F32 = 2, FA_DTYPE_I32 = 3 } fa_dtype;
+typedef enum { FA_DTYPE_BF16 = 1, FA_DTYPE_F32 = 2, FA_DTYPE_I32 = 3, FA_DTYPE_F16 = 4 } fa_dtype;
 
 /* A strided view of device memory; shape/stride are in elements, outermost
  * first; only the first ndim entries are read. */

@@ -27,11 +27,11 @@ bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-// A bf16 activation/cache tensor: dtype, rank, unit head-dim stride, other
-// strides multiples of 8 elements (16 bytes), 16-byte aligned base.
+// An activation/cache tensor: bf16 or fp16, rank, unit head-dim stride,
+// other strides multiples of 8 elements (16 bytes), 16-byte aligned base.
 int check_bf16(const fa_tensor* t, int ndim) {
   if (!t || !t->data) return FA_ERR_INVALID_ARG;
-  if (t->dtype != FA_DTYPE_BF16 || t->ndim != ndim) return FA_ERR_INVALID_ARG;
+  if ((t->dtype != FA_DTYPE_BF16 && t->dtype != FA_DTYPE_F16) || t->ndim != ndim) return FA_ERR_INVALID_ARG;
   for (int i = 0; i < ndim; ++i)
     if (t->shape[i] < 0) return FA_ERR_INVALID_ARG;
   if (t->stride[ndim - 1] != 1) return FA_ERR_INVALID_ARG;
@@ -134,7 +134,9 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   if (Sq > INT32_MAX / 64 || Sk > INT32_MAX / 64 || n_seq > INT32_MAX / 64) return FA_ERR_INVALID_ARG;
 
   // ---- out / lse ----
-  if (out->dtype != FA_DTYPE_BF16 || out->ndim != q->ndim || !out->data) return FA_ERR_INVALID_ARG;
+  // one element type for q, k, v and out
+  if (k->dtype != q->dtype || v->dtype != q->dtype || out->dtype != q->dtype) return FA_ERR_INVALID_ARG;
+  if (out->ndim != q->ndim || !out->data) return FA_ERR_INVALID_ARG;
   for (int i = 0; i < q->ndim; ++i)
     if (out->shape[i] != q->shape[i]) return FA_ERR_INVALID_ARG;
   if ((rc = check_bf16(out, out->ndim))) return rc;
@@ -221,6 +223,7 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   P.softcap = softcap;
   P.inv_softcap = softcap > 0.f ? 1.f / softcap : 0.f;
   P.causal = causal ? 1 : 0;
+  P.f16 = q->dtype == FA_DTYPE_F16 ? 1 : 0;
   P.wl = wl;
   P.wr = wr;
   P.mask_kind = mask_kind;

@@ -19,6 +19,7 @@
 // running softmax is guarded so that a fully masked chunk never produces NaN
 // (ExecuTorch pull request 10466 "Summary").
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -70,21 +71,38 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
+// m16n8k16, fp32 accumulate; A and B both bf16, or both fp16 when F16.
+template <bool F16>
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  if constexpr (F16)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
   return d;
 }
+// Two fp32 values rounded to nearest-even into a packed pair of the input
+// type (bf16, or fp16 when F16).
+template <bool F16>
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  if constexpr (F16) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
 }
 
 // Address of key/value row j (head g) of sequence b.
@@ -144,7 +162,7 @@ __device__ __forceinline__ uint32_t swz_tma(int row, int cc) {
 // consumer threads only (thread ids 0..127), which meet on named barrier 1;
 // `smem` (16 KB at d = 128) is free for the merge buffer, `red_m` points to
 // 2 x 4 x 8 floats that are not part of it.
-template <int D>
+template <int D, bool F16>
 __device__ __forceinline__ void decode_finish(const Params& p, const ItemGeo& geo, int64_t item, int split,
                                               bool single, unsigned char* smem, float* red_m, int tid,
                                               float (&m_run)[2], float (&l_run)[2], float (&o_acc)[D / 16][4]) {
@@ -218,8 +236,8 @@ __device__ __forceinline__ void decode_finish(const Params& p, const ItemGeo& ge
 #pragma unroll
         for (int c = 0; c < kCols; c += 4) {
           uint2 pk;
-          pk.x = pack_bf16(vals[c + 0], vals[c + 1]);
-          pk.y = pack_bf16(vals[c + 2], vals[c + 3]);
+          pk.x = pack_bf16<F16>(vals[c + 0], vals[c + 1]);
+          pk.y = pack_bf16<F16>(vals[c + 2], vals[c + 3]);
           *reinterpret_cast<uint2*>(optr + c0 + c) = pk;
         }
         if ((tid & 15) == 0) *lptr = lse_val;
@@ -239,7 +257,7 @@ __device__ __forceinline__ void decode_finish(const Params& p, const ItemGeo& ge
 // one page, or 16 consecutive rows), issued by lane 0 of the warp that owns
 // the ring and tracked by one mbarrier per stage; otherwise by 16-byte
 // cp.async from all lanes (any layout).
-template <int D, bool TMA>
+template <int D, bool TMA, bool F16>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   using S = DecodeSmem<D>;
@@ -460,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       uint32_t a[4];
       const int kr = (lane & 7) + 8 * (mi & 1), kc = 2 * ks + (mi >> 1);
       ldsm_x4(sK + (TMA ? swz_tma(kr, kc) : swz<D>(kr, kc)), a[0], a[1], a[2], a[3]);
-      if (ks & 1) mma_bf16(sb, a, qb[ks][0], qb[ks][1]);
-      else mma_bf16(sa, a, qb[ks][0], qb[ks][1]);
+      if (ks & 1) mma_bf16<F16>(sb, a, qb[ks][0], qb[ks][1]);
+      else mma_bf16<F16>(sa, a, qb[ks][0], qb[ks][1]);
     }
     float sc[4];
 #pragma unroll
@@ -503,8 +521,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       o_acc[n][2] *= alpha[0]; o_acc[n][3] *= alpha[1];
     }
     // ---- P^T (C layout) -> B operand [16 keys x 8 rows] by an 8x8 transpose ----
-    const uint32_t pb0 = movmatrix_t(pack_bf16(sc[0], sc[1]));  // keys 0..7
-    const uint32_t pb1 = movmatrix_t(pack_bf16(sc[2], sc[3]));  // keys 8..15
+    const uint32_t pb0 = movmatrix_t(pack_bf16<F16>(sc[0], sc[1]));  // keys 0..7
+    const uint32_t pb1 = movmatrix_t(pack_bf16<F16>(sc[2], sc[3]));  // keys 8..15
     // ---- O^T += V^T P^T : per 16 head-dim values, one mma over the 16 keys ----
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
@@ -512,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       uint32_t a[4];
       const int vr = (lane & 7) + 8 * (mi >> 1), vc = 2 * mt + (mi & 1);
       ldsm_x4_t(sV + (TMA ? swz_tma(vr, vc) : swz<D>(vr, vc)), a[0], a[1], a[2], a[3]);
-      mma_bf16(o_acc[mt], a, pb0, pb1);
+      mma_bf16<F16>(o_acc[mt], a, pb0, pb1);
     }
   }
   cp_async_wait<0>();
@@ -528,13 +546,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     return;
   }
 
-  decode_finish<D>(p, geo, item, split, single, smem, reinterpret_cast<float*>(smem + kWarps * S::kWarpBytes), tid,
+  decode_finish<D, F16>(p, geo, item, split, single, smem, reinterpret_cast<float*>(smem + kWarps * S::kWarpBytes), tid,
                    m_run, l_run, o_acc);
 }
 
 // Merge the splits of items that had more than one: LSE = logsumexp of the
 // split LSEs (all -inf -> -inf), O = sum_s exp(LSE_s - LSE) O_s (0 if empty).
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(32 * kDecodeRows) combine_kernel(const Params p) {
   const int64_t item = blockIdx.x;
   const int count = p.item_count[item];
@@ -567,7 +585,7 @@ __global__ void __launch_bounds__(32 * kDecodeRows) combine_kernel(const Params 
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll
   for (int c = 0; c < kPer; c += 2)
-    *reinterpret_cast<uint32_t*>(optr + lane * kPer + c) = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
+    *reinterpret_cast<uint32_t*>(optr + lane * kPer + c) = pack_bf16<F16>(acc[c] * inv, acc[c + 1] * inv);
   if (lane == 0) *lptr = (L > 0.f) ? (M + __logf(L)) : -INFINITY;
 }
 
@@ -591,33 +609,33 @@ bool decode_maps(const Params& p, CUtensorMap* mk, CUtensorMap* mv) {
   }
   if (rows <= 0 || outer <= 0) return false;
   return encode_4d_bf16(mk, p.k, D, p.Hkv, rows, outer, p.k_sh, p.k_ss, k_so, 64, kChunkKeys,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) &&
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, p.f16 != 0) &&
          encode_4d_bf16(mv, p.v, D, p.Hkv, rows, outer, p.v_sh, p.v_ss, v_so, 64, kChunkKeys,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, p.f16 != 0);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_decode_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
   cudaError_t e;
   const int64_t grid = p.n_items * p.n_splits;
   using S = DecodeSmem<D>;
   CUtensorMap mk, mv;
   if (decode_maps<D>(p, &mk, &mv)) {
-    e = ensure_smem_attr<decode_kernel<D, true>>(S::kTotal);
+    e = ensure_smem_attr<decode_kernel<D, true, F16>>(S::kTotal);
     if (e != cudaSuccess) return e;
     if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-    decode_kernel<D, true><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
+    decode_kernel<D, true, F16><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
   } else {
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
-    e = ensure_smem_attr<decode_kernel<D, false>>(S::kTotal);
+    e = ensure_smem_attr<decode_kernel<D, false, F16>>(S::kTotal);
     if (e != cudaSuccess) return e;
     if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-    decode_kernel<D, false><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
+    decode_kernel<D, false, F16><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || p.n_splits <= 1) return e;
-  combine_kernel<D><<<(unsigned)p.n_items, 32 * kDecodeRows, 0, st>>>(p);
+  combine_kernel<D, F16><<<(unsigned)p.n_items, 32 * kDecodeRows, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -625,8 +643,8 @@ cudaError_t launch_decode_d(const Params& p, cudaStream_t st, cudaEvent_t ev_beg
 
 cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
   if (p.n_items <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
-  if (p.d == 64) return launch_decode_d<64>(p, st, ev_begin);
-  return launch_decode_d<128>(p, st, ev_begin);
+  if (p.f16) return p.d == 64 ? launch_decode_d<64, true>(p, st, ev_begin) : launch_decode_d<128, true>(p, st, ev_begin);
+  return p.d == 64 ? launch_decode_d<64, false>(p, st, ev_begin) : launch_decode_d<128, false>(p, st, ev_begin);
 }
 
 }  // namespace mfa

@@ -44,6 +44,7 @@ struct Params {
   int32_t n_seq, Sq, Sk;  // Sq/Sk: fixed lengths, or max lengths for varlen
   int64_t tot_q, tot_k;   // rows of packed Q / K (varlen), for device-side checks
   int32_t Hq, Hkv, G, d;
+  int32_t f16;        // q, k, v, out are fp16 (else bf16)
   float scale;        // natural-log units
   float scale_log2;   // scale * log2(e)
   float softcap;      // 0 = off
@@ -85,5 +86,6 @@ cudaError_t launch_classify(const Params& p, cudaStream_t st);
 // before the kernel itself is enqueued, after all host-side preparation.
 cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
 cudaError_t launch_prefill(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
+cudaError_t launch_prefill_f16(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);  // p.f16 inputs
 
 }  // namespace mfa

@@ -48,19 +48,21 @@ inline EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 4-D bf16 map {d, heads, rows, outer} with box {box_d, 1, box_rows, 1}.
-// Strides are in elements (head, row, outer).  False when the driver rejects
-// the layout (alignment, strides) or has no encoder.
+// 4-D map of 2-byte elements (bf16, or fp16 when f16) {d, heads, rows, outer}
+// with box {box_d, 1, box_rows, 1}.  Strides are in elements (head, row,
+// outer).  False when the driver rejects the layout (alignment, strides) or
+// has no encoder.
 inline bool encode_4d_bf16(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int64_t outer,
                            int64_t s_h, int64_t s_row, int64_t s_outer, int box_d, int box_rows,
-                           CUtensorMapSwizzle swz, CUtensorMapL2promotion l2) {
+                           CUtensorMapSwizzle swz, CUtensorMapL2promotion l2, bool f16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows, (cuuint64_t)outer};
   cuuint64_t strides[3] = {(cuuint64_t)s_h * 2, (cuuint64_t)s_row * 2, (cuuint64_t)s_outer * 2};
   cuuint32_t box[4] = {(cuuint32_t)box_d, 1, (cuuint32_t)box_rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+  CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                  const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

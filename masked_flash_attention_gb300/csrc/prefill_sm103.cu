@@ -24,7 +24,7 @@
 //   warps 4..7  softmax, key columns 0..63 of every tile
 //   warps 8..11 softmax, key columns 64..127
 // TMEM (512 columns): S in two buffers [0,128) [128,256) (fp32), P in two
-// buffers [256,320) [320,384) (bf16, two per column), O in [384, 384 + D).
+// buffers [256,320) [320,384) (input type, two per column), O in [384, 384 + D).
 // With S and P double-buffered QK(j+1) runs while the softmax of tile j does,
 // and PV(j) while the softmax of tile j+1 does; the tensor cores wait on the
 // softmax only when it is slower than QK + PV.  The MMA queue is shallow (an
@@ -42,6 +42,7 @@
 // MMAs are drained and TMEM is released before the CTA exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -75,7 +76,7 @@ constexpr float kRescaleLog2 = 8.0f;
 template <int D>
 struct PCfg {
   static constexpr int NS = (D == 128) ? 2 : 4;    // K/V ring stages
-  static constexpr int kTileBytes = 128 * D * 2;    // one 128-row bf16 tile
+  static constexpr int kTileBytes = 128 * D * 2;    // one 128-row tile of 2-byte elements
   static constexpr int kQOff = 0;                   // two Q buffers
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + NS * kTileBytes;
@@ -85,7 +86,7 @@ struct PCfg {
   static constexpr int kRedOff = kAuxOff + 512;
   static constexpr int kSumOff = kRedOff + 2 * 128 * 4;
   static constexpr int kTopkOff = kSumOff + 2 * 128 * 4;
-  // output staging: per softmax warp 32 rows x 32 bf16 columns
+  // output staging: per softmax warp 32 rows x 32 output columns
   static constexpr int kStageOff = (kTopkOff + 2 * 2 * 128 * 8 + 1023) / 1024 * 1024;  // swizzle-aligned
   static constexpr int kSmem = kStageOff + 8 * 2048 + 1024;  // + alignment slack
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -130,9 +131,17 @@ __device__ __forceinline__ int next_busy(const Params& p, int u, Unit& w) {
   return -1;
 }
 
+// Two fp32 values rounded to nearest-even into one packed pair of the input
+// type (bf16, or fp16 when F16).
+template <bool F16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  if constexpr (F16) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
 }
 
 // Packed fp32 pair arithmetic (one instruction for two lanes of work).
@@ -207,8 +216,9 @@ __device__ __forceinline__ void row_key_range(const Params& p, int i, int q_len,
 }
 
 // MK: additive term kind (FA_MASK_NONE / DENSE / TOPK); SC: logit soft-cap on;
-// AL: ALiBi slopes on (only with MK == FA_MASK_NONE).
-template <int D, int MK, bool SC, bool AL>
+// AL: ALiBi slopes on (only with MK == FA_MASK_NONE); F16: inputs, P and the
+// output are fp16 (else bf16).
+template <int D, int MK, bool SC, bool AL, bool F16>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const int o_tma) {
@@ -317,7 +327,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // softmax has read that S buffer two tiles back.  Also fetches Q: the next
     // unit's Q while the current unit runs (two buffers).
     if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false, F16);
       const uint32_t sQ = tc::smem_u32(smem + C::kQOff);
       const uint32_t sK = tc::smem_u32(smem + C::kKOff);
       tc::tma_prefetch_desc(&tmq);
@@ -383,7 +393,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // O (+)= P[g % 2] V_g once the softmax of tile g has written P (and
     // rescaled O); the first tile of a unit overwrites O.
     if (lane == 0) {
-      constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true, F16);
       const uint32_t sV = tc::smem_u32(smem + C::kVOff);
       bool ok = true;
       int g = 0;
@@ -582,7 +592,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         float2 acc[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
-        // P = exp2(x - ref) packed to bf16 pairs in registers: one packed FMA
+        // P = exp2(x - ref) packed to input-type pairs in registers: one packed FMA
         // (FULL: scale folded in) or add per pair
         uint32_t pk[4][16];
         if (plain) {
@@ -594,7 +604,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               const float2 v = fma2(x[c * 16 + e], sl2, ner);
               const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
               acc[e & 3] = add2(acc[e & 3], pe);
-              pk[c][e] = pack2(pe.x, pe.y);
+              pk[c][e] = pack2<F16>(pe.x, pe.y);
             }
         } else {
 #pragma unroll
@@ -604,7 +614,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               const float2 v = add2(x[c * 16 + e], ner);
               const float2 pe = make_float2(fast_exp2(v.x), fast_exp2(v.y));
               acc[e & 3] = add2(acc[e & 3], pe);
-              pk[c][e] = pack2(pe.x, pe.y);
+              pk[c][e] = pack2<F16>(pe.x, pe.y);
             }
         }
         // this P buffer is free once the PV two tiles back is done
@@ -655,10 +665,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
           uint4 o4;
-          o4.x = pack2(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
-          o4.y = pack2(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
-          o4.z = pack2(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
-          o4.w = pack2(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
+          o4.x = pack2<F16>(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
+          o4.y = pack2<F16>(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
+          o4.z = pack2<F16>(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
+          o4.w = pack2<F16>(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
           stg[lane * 4 + (v4 ^ ((lane >> 1) & 3))] = o4;  // swizzled: 4 wavefronts
         }
         if (tma_rows) {
@@ -700,20 +710,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// 4-D map {d, heads, rows, batch} over a bshd (or packed thd) bf16 tensor,
+// 4-D map {d, heads, rows, batch} over a bshd (or packed thd) bf16 / fp16 tensor,
 // box {64, 1, 128, 1}, 128-byte swizzle; rows beyond the tensor read as 0.
 bool encode_bshd(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int batch, int64_t s_h,
-                 int64_t s_row, int64_t s_b) {
+                 int64_t s_row, int64_t s_b, bool f16) {
   return encode_4d_bf16(m, base, d, heads, rows, batch, s_h, s_row, s_b, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, f16);
 }
 
-// 4-D map over the bf16 output for the epilogue's TMA stores: box {32, 1, 32,
+// 4-D map over the output for the epilogue's TMA stores: box {32, 1, 32,
 // 1} (32 columns x 32 rows), 64-byte swizzle (the staging layout).
 bool encode_out(CUtensorMap* m, void* base, int d, int heads, int64_t rows, int batch, int64_t s_h, int64_t s_row,
-                int64_t s_b) {
+                int64_t s_b, bool f16) {
   return encode_4d_bf16(m, base, d, heads, rows, batch, s_h, s_row, s_b, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
-                        CU_TENSOR_MAP_L2_PROMOTION_NONE);
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, f16);
 }
 
 int sm_count() {
@@ -729,7 +739,7 @@ int sm_count() {
   return n;
 }
 
-template <int D, int MK, bool SC, bool AL>
+template <int D, int MK, bool SC, bool AL, bool F16>
 cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& mv, const CUtensorMap& mo, int o_tma, int grid,
                              cudaEvent_t ev_begin) {
@@ -738,19 +748,19 @@ cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap
   static int regs = -1;
   if (regs < 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MK, SC, AL>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MK, SC, AL, F16>);
     if (e != cudaSuccess) return e;
     regs = fa.numRegs;
   }
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL>>(PCfg<D>::kSmem);
+  cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL, F16>>(PCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-  prefill_kernel<D, MK, SC, AL><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
+  prefill_kernel<D, MK, SC, AL, F16><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
   CUtensorMap mq, mk, mv;
   const bool vq = p.cu_q != nullptr, vk = p.cu_k != nullptr;
@@ -763,11 +773,11 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
   const int64_t o_sb = (qb == 1 || p.o_sb == 0) ? p.o_ss : p.o_sb;
   CUtensorMap mo;
   // without a valid map (unusual strides) the epilogue uses plain stores
-  const int o_tma = encode_out(&mo, p.o, D, p.Hq, q_rows, qb, p.o_sh, p.o_ss, o_sb) ? 1 : 0;
+  const int o_tma = encode_out(&mo, p.o, D, p.Hq, q_rows, qb, p.o_sh, p.o_ss, o_sb, F16) ? 1 : 0;
   if (!o_tma) memset(&mo, 0, sizeof(mo));
-  if (!encode_bshd(&mq, p.q, D, p.Hq, q_rows, qb, p.q_sh, p.q_ss, q_sb) ||
-      !encode_bshd(&mk, p.k, D, p.Hkv, k_rows, kb, p.k_sh, p.k_ss, k_sb) ||
-      !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb))
+  if (!encode_bshd(&mq, p.q, D, p.Hq, q_rows, qb, p.q_sh, p.q_ss, q_sb, F16) ||
+      !encode_bshd(&mk, p.k, D, p.Hkv, k_rows, kb, p.k_sh, p.k_ss, k_sb, F16) ||
+      !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb, F16))
     return cudaErrorInvalidValue;
   // one CTA per SM (persistent), never more CTAs than work units
   const int64_t units = (int64_t)p.n_row_tiles * p.n_seq * p.Hq;
@@ -777,28 +787,37 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
   const bool sc = p.softcap > 0.f;
   if (p.alibi) {  // the planner allows ALiBi in prefill only without a mask
     if (p.mask_kind != FA_MASK_NONE) return cudaErrorInvalidValue;
-    return sc ? launch_prefill_v<D, FA_MASK_NONE, true, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
-              : launch_prefill_v<D, FA_MASK_NONE, false, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
+    return sc ? launch_prefill_v<D, FA_MASK_NONE, true, true, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+              : launch_prefill_v<D, FA_MASK_NONE, false, true, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
   }
   switch (p.mask_kind) {
     case FA_MASK_DENSE:
-      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
-                : launch_prefill_v<D, FA_MASK_DENSE, false, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
+      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true, false, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_DENSE, false, false, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
     case FA_MASK_TOPK:
-      return sc ? launch_prefill_v<D, FA_MASK_TOPK, true, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
-                : launch_prefill_v<D, FA_MASK_TOPK, false, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
+      return sc ? launch_prefill_v<D, FA_MASK_TOPK, true, false, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_TOPK, false, false, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
     default:
-      return sc ? launch_prefill_v<D, FA_MASK_NONE, true, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
-                : launch_prefill_v<D, FA_MASK_NONE, false, false>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
+      return sc ? launch_prefill_v<D, FA_MASK_NONE, true, false, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_NONE, false, false, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
   }
 }
 
 }  // namespace
 
+// The fp16 instantiations are compiled in their own translation unit
+// (prefill_f16.cu includes this file with MFA_PREFILL_F16_UNIT defined), so
+// that the two element types build in parallel.
+#ifndef MFA_PREFILL_F16_UNIT
 cudaError_t launch_prefill(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
   if (p.n_items <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
-  if (p.d == 64) return launch_prefill_d<64>(p, st, ev_begin);
-  return launch_prefill_d<128>(p, st, ev_begin);
+  if (p.f16) return launch_prefill_f16(p, st, ev_begin);
+  return p.d == 64 ? launch_prefill_d<64, false>(p, st, ev_begin) : launch_prefill_d<128, false>(p, st, ev_begin);
 }
+#else
+cudaError_t launch_prefill_f16(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
+  return p.d == 64 ? launch_prefill_d<64, true>(p, st, ev_begin) : launch_prefill_d<128, true>(p, st, ev_begin);
+}
+#endif
 
 }  // namespace mfa

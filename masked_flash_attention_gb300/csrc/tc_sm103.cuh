@@ -252,11 +252,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, dense.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor, kind::f16: bf16 x bf16 (or fp16 x fp16 when f16)
+// -> fp32, dense.  A and B always share one type.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                      bool f16 = false) {
   return (1u << 4)                         // D: f32
-         | (1u << 7)                       // A: bf16
-         | (1u << 10)                      // B: bf16
+         | ((f16 ? 0u : 1u) << 7)          // A: bf16 (1) or fp16 (0)
+         | ((f16 ? 0u : 1u) << 10)         // B: same type as A
          | ((a_mn_major ? 1u : 0u) << 15)  // A major
          | ((b_mn_major ? 1u : 0u) << 16)  // B major
          | ((uint32_t)(N >> 3) << 17)      // N / 8

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(fa.lib, n), n
         assert ctypes.cast(getattr(fa.lib, n), ctypes.c_void_p).value
-    assert fa.fa_abi_version() == 2
+    assert fa.fa_abi_version() == 3
     assert fa.fa_status_string(0) == "ok"
 
 
@@ -75,6 +75,11 @@ def test_invalid_arguments():
     assert plan(qs, k, k)[0] == 0 or plan(qs, k, k)[0] == E
     assert plan(T(1, 4, 2, 64)[..., ::2], k, k)[0] == E         # non-unit head-dim stride
     assert plan(q, k, k, out=T(1, 4, 2, 64).float())[0] == E    # out dtype
+    H = torch.float16
+    assert plan(q.half(), k, k)[0] == E                          # q fp16, k/v bf16
+    assert plan(q, k.half(), k)[0] == E                          # k fp16 only
+    assert plan(q.half(), k.half(), k.half(), out=T(1, 4, 2, 64))[0] == E  # out bf16
+    assert plan(q.half(), k.half(), k.half(), out=T(1, 4, 2, 64, dtype=H))[0] == 0
     assert plan(q, k, k, lse=T(1, 2, 5, dtype=torch.float32))[0] == E  # lse shape
 
 

@@ -36,14 +36,15 @@ def _gen(seed: int) -> torch.Generator:
     return g
 
 
-def randn_bf16(g: torch.Generator, shape) -> torch.Tensor:
-    return torch.randn(*shape, generator=g, dtype=torch.float32).to(BF16)
+def randn_bf16(g: torch.Generator, shape, dtype=BF16) -> torch.Tensor:
+    """fp32 N(0, 1) draws rounded to the input type (bf16, or fp16)."""
+    return torch.randn(*shape, generator=g, dtype=torch.float32).to(dtype)
 
 
-def qkv_bshd(g, B, Sq, Sk, Hq, Hkv, d):
-    q = randn_bf16(g, (B, Sq, Hq, d))
-    k = randn_bf16(g, (B, Sk, Hkv, d))
-    v = randn_bf16(g, (B, Sk, Hkv, d))
+def qkv_bshd(g, B, Sq, Sk, Hq, Hkv, d, dtype=BF16):
+    q = randn_bf16(g, (B, Sq, Hq, d), dtype)
+    k = randn_bf16(g, (B, Sk, Hkv, d), dtype)
+    v = randn_bf16(g, (B, Sk, Hkv, d), dtype)
     return q, k, v
 
 
@@ -150,9 +151,9 @@ def dynamic_topk(seed: int = 0, B=2, H=16, d=128, T=8192, keep_window=2048):
 # Small random cases (parity sweeps)
 # ---------------------------------------------------------------------------
 
-def random_case(seed, B=1, Sq=1, Sk=1, Hq=1, Hkv=1, d=64, **params):
+def random_case(seed, B=1, Sq=1, Sk=1, Hq=1, Hkv=1, d=64, dtype=BF16, **params):
     g = _gen(seed)
-    q, k, v = qkv_bshd(g, B, Sq, Sk, Hq, Hkv, d)
+    q, k, v = qkv_bshd(g, B, Sq, Sk, Hq, Hkv, d, dtype)
     p = base_params(scale=1.0 / math.sqrt(d))
     p.update(params)
     return dict(name=f"rand_s{seed}_b{B}_q{Sq}_k{Sk}_h{Hq}x{Hkv}_d{d}", q=q, k=k, v=v, params=p)
@@ -176,7 +177,7 @@ def random_zero_hold_states(seed, B, H, Sk, ties=False):
     return z
 
 
-def random_varlen(seed, n_seq, max_q, max_k, Hq, Hkv, d, q_eq_k=False, min_q=0, min_k=0):
+def random_varlen(seed, n_seq, max_q, max_k, Hq, Hkv, d, q_eq_k=False, min_q=0, min_k=0, dtype=BF16):
     """Packed variable-length batch: per-sequence lengths drawn uniformly."""
     g = _gen(seed)
     lq = torch.randint(min_q, max_q + 1, (n_seq,), generator=g)
@@ -188,9 +189,9 @@ def random_varlen(seed, n_seq, max_q, max_k, Hq, Hkv, d, q_eq_k=False, min_q=0, 
     cu_k = torch.zeros(n_seq + 1, dtype=torch.int32)
     cu_q[1:] = torch.cumsum(lq, 0).to(torch.int32)
     cu_k[1:] = torch.cumsum(lk, 0).to(torch.int32)
-    q = randn_bf16(g, (int(cu_q[-1]), Hq, d))
-    k = randn_bf16(g, (int(cu_k[-1]), Hkv, d))
-    v = randn_bf16(g, (int(cu_k[-1]), Hkv, d))
+    q = randn_bf16(g, (int(cu_q[-1]), Hq, d), dtype)
+    k = randn_bf16(g, (int(cu_k[-1]), Hkv, d), dtype)
+    v = randn_bf16(g, (int(cu_k[-1]), Hkv, d), dtype)
     return q, k, v, cu_q, cu_k
 
 

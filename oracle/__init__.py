@@ -12,6 +12,9 @@ Contents
                 whole masked logit matrix, takes its softmax, multiplies by V.
   brute      -- pure-Python scalar loops over the same definition, for tiny
                 inputs; used to pin ``attention``.
+  kvcache    -- keys from two sources (cached rows, then the step's active
+                rows) and the cache append, built on ``attention``; pinned in
+                ``tests/test_oracle_kvcache.py``.
 
 Parity pins (all in ``tests/test_oracle.py``): the ExecuTorch sliding-window
 worked example, the all -inf chunk, causal equal to a lower-triangular mask and

@@ -53,7 +53,7 @@ def _np(a, dtype=np.float64):
     if hasattr(a, "detach"):
         t = a.detach()
         if t.dtype.is_floating_point:
-            t = t.float()
+            t = t.double()  # exact for bf16, fp16, fp32 and fp64 inputs
         a = t.cpu().numpy()
     return np.asarray(a, dtype=dtype)
 

@@ -8,7 +8,10 @@ Default workload: causal prefill over past KV with grouped-query heads
 (B=4, Hq=32, Hkv=8, d=128, 512 new queries over 4096 keys), metric "useful
 TFLOP/s": 4*d FLOP per (query, key) pair that the mask keeps, per query head.
 ``--workload paged_varlen_decode`` reports KV-cache GB/s (K/V bytes inside
-each sequence's window) instead.
+each sequence's window) instead; ``--workload paged_decode_append`` serves the
+same batch through fa_fwd_kvcache (cached keys plus each sequence's new token
+read from its own tensor, and appended to the cache), reporting the same bytes
+plus the appended rows.
 
 Rules kept here: W >= 3 untimed warm-up steps; each timed step is bracketed by
 CUDA events on the launching stream; between timed steps L2 is flushed by
@@ -151,13 +154,19 @@ def _as_dtype(case, dtype):
     if dtype == "bf16":
         return case
     t = torch.float16
-    return dict(case, name=case["name"] + "_f16", q=case["q"].to(t), k=case["k"].to(t), v=case["v"].to(t))
+    out = dict(case, name=case["name"] + "_f16", q=case["q"].to(t), k=case["k"].to(t), v=case["v"].to(t))
+    if "kvcache" in case:
+        out["kvcache"] = dict(case["kvcache"], k_new=case["kvcache"]["k_new"].to(t),
+                              v_new=case["kvcache"]["v_new"].to(t))
+    return out
 
 
 def workload_units(case, name):
     d = case["q"].shape[-1]
-    if name == "paged_varlen_decode":
+    if name in ("paged_varlen_decode", "paged_decode_append"):
         b = kv_window_bytes(case)
+        if "kvcache" in case:  # the append writes the active K and V rows
+            b += 2 * case["kvcache"]["k_new"].numel() * case["kvcache"]["k_new"].element_size()
         return dict(metric_units=b / 1e9, unit="GB/s", bound="hbm",
                     flops=4.0 * d * useful_pairs(case), bytes=b)
     f = 4.0 * d * useful_pairs(case)
@@ -251,7 +260,21 @@ def run_gpu(args):
     gp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
     q, k, v = case["q"].to(dev), case["k"].to(dev), case["v"].to(dev)
     stream = torch.cuda.current_stream()
-    rc, plan = fa.fa_fwd_plan(q, k, v, stream=stream.cuda_stream, **gp)
+    # the two-source form (cached keys + the step's active rows, appended)
+    kvx = {kk: (vv.to(dev) if isinstance(vv, torch.Tensor) else vv) for kk, vv in case["kvcache"].items()} \
+        if "kvcache" in case else None
+
+    def call(q_, k_, v_, kvx_, **kw):
+        if kvx_ is None:
+            return fa.fa_fwd(q_, k_, v_, **kw, **gp)
+        return fa.fa_fwd_kvcache(q_, k_, v_, kvx_["k_new"], kvx_["v_new"], kvx_["cache_seqlens"],
+                                 append=kvx_["append"], **kw, **gp)
+
+    if kvx is None:
+        rc, plan = fa.fa_fwd_plan(q, k, v, stream=stream.cuda_stream, **gp)
+    else:
+        rc, plan = fa.fa_fwd_kvcache_plan(q, k, v, kvx["k_new"], kvx["v_new"], kvx["cache_seqlens"],
+                                          append=kvx["append"], stream=stream.cuda_stream, **gp)
     assert rc == 0, rc
     ws = fa.alloc_workspace(plan["workspace_bytes"], dev)
     out = torch.empty_like(q)
@@ -263,8 +286,8 @@ def run_gpu(args):
     ev_kb.record(); ev_ke.record()
 
     def step(timing=False, kb=None, ke=None):
-        fa.fa_fwd(q, k, v, out=out, lse=lse, workspace=ws, stream=stream.cuda_stream,
-                  event_begin=kb, event_end=ke, **gp)
+        call(q, k, v, kvx, out=out, lse=lse, workspace=ws, stream=stream.cuda_stream, event_begin=kb,
+             event_end=ke)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -305,12 +328,17 @@ def run_gpu(args):
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    hx = {kk: vv.pin_memory() for kk, vv in case["kvcache"].items() if isinstance(vv, torch.Tensor)} \
+        if kvx is not None else {}
+    dx = dict(kvx, **{kk: torch.empty_like(kvx[kk]) for kk in hx}) if kvx is not None else None
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, *hx.values()))
     d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
 
     def e2e_step():
         dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
-        fa.fa_fwd(dq, dk, dv, out=out, lse=lse, workspace=ws, stream=stream.cuda_stream, **gp)
+        for kk, hv_ in hx.items():
+            dx[kk].copy_(hv_, non_blocking=True)
+        call(dq, dk, dv, dx, out=out, lse=lse, workspace=ws, stream=stream.cuda_stream)
         hout.copy_(out, non_blocking=True); hlse.copy_(lse, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):

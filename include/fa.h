@@ -82,7 +82,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 3
+#define FA_ABI_VERSION 4
 
 typedef enum {
   FA_OK = 0,
@@ -224,6 +224,55 @@ int fa_fwd_workspace_size(const fa_tensor* q, const fa_tensor* k, const fa_tenso
                           const fa_tensor* block_table, const fa_mask* mask,
                           int32_t window_left, int32_t window_right, float softcap,
                           float scale, int32_t causal, const fa_opts* opts, size_t* bytes);
+
+/* Attention over a KV cache plus the step's active keys, read from two
+ * sources (vLLM pull request 11277, the author's reply on aligning with the
+ * unified flash_attn_varlen_func interface, first point: writing the new
+ * tokens into the cache before the attention reads them back is a
+ * read-after-write stall, so the cached and the active K/V are passed
+ * separately).  Sequence s has keys, in order, cache rows 0 .. L_s - 1
+ * (L_s = cache_seqlens[s]) followed by its active rows 0 .. q_len_s - 1, the
+ * keys of its own query tokens: kv_len_s = L_s + q_len_s, and the causal rule
+ * (bottom-right) lets query row i see cached keys and active keys 0 .. i.
+ * The active rows are read from k_new / v_new, never from the cache.
+ *
+ *   q             as for fa_fwd: [B, Sq, Hq, d], or [total_q, Hq, d] with
+ *                 cu_seqlens_q
+ *   k_new, v_new  the active keys/values, laid out like q with Hkv heads:
+ *                 [B, Sq, Hkv, d] or [total_q, Hkv, d]
+ *   k_cache, v_cache  paged [num_pages, page_size, Hkv, d] with block_table
+ *                 [n_seq, max_pages] (cache row j of sequence s is row
+ *                 j % page_size of page block_table[s][j / page_size]), or
+ *                 padded [n_seq, cap, Hkv, d] without a block table
+ *   cache_seqlens int32 [n_seq], device: keys already in the cache
+ *   append != 0   also write the active rows into the cache at rows
+ *                 L_s .. L_s + q_len_s - 1 (a bit-exact copy, done by the
+ *                 attention kernel itself from the active tensors; no kernel
+ *                 of this call reads those cache rows)
+ *   out, lse      as for fa_fwd
+ * The element type rule, GQA, window, softcap, scale, ALiBi (opts) and the
+ * fully-masked-row rule are those of fa_fwd; dense and top-k masks return
+ * FA_ERR_UNSUPPORTED.  opts->max_seqlen_k is required: the largest
+ * L_s + q_len_s.  Work runs on the split-KV decode kernel whatever q_len is.
+ * A cached or appended row beyond the cache (block table width x page_size,
+ * or cap) or a bad page index is recorded as FA_ERR_DEVICE_BOUNDS and its
+ * access skipped; a sequence with L_s + q_len_s > max_seqlen_k is rejected
+ * the same way as in fa_fwd. */
+int fa_fwd_kvcache(const fa_tensor* q, const fa_tensor* k_cache, const fa_tensor* v_cache,
+                   const fa_tensor* k_new, const fa_tensor* v_new, const fa_tensor* out,
+                   const fa_tensor* lse, const fa_tensor* cu_seqlens_q,
+                   const fa_tensor* cache_seqlens, const fa_tensor* block_table,
+                   int32_t window_left, int32_t window_right, float softcap, float scale,
+                   int32_t causal, int32_t append, const fa_opts* opts);
+
+/* Host-only: validate the arguments of fa_fwd_kvcache and describe its plan
+ * (as fa_fwd_plan). */
+int fa_fwd_kvcache_plan(const fa_tensor* q, const fa_tensor* k_cache, const fa_tensor* v_cache,
+                        const fa_tensor* k_new, const fa_tensor* v_new, const fa_tensor* out,
+                        const fa_tensor* lse, const fa_tensor* cu_seqlens_q,
+                        const fa_tensor* cache_seqlens, const fa_tensor* block_table,
+                        int32_t window_left, int32_t window_right, float softcap, float scale,
+                        int32_t causal, int32_t append, const fa_opts* opts, fa_plan* plan_out);
 
 /* Size of the static device scratch used by fa_fwd_noalloc (32 MiB). */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

@@ -14,6 +14,8 @@ from ._lib import (  # noqa: F401
     fa_abi_version,
     fa_check_device_error,
     fa_fwd,
+    fa_fwd_kvcache,
+    fa_fwd_kvcache_plan,
     fa_fwd_noalloc,
     fa_fwd_plan,
     fa_status_string,

@@ -73,8 +73,14 @@ _ARGS = [_P(fa_tensor), _P(fa_tensor), _P(fa_tensor), _P(fa_tensor), _P(fa_tenso
          _P(fa_tensor), _P(fa_tensor), _P(fa_tensor), _P(fa_mask), ctypes.c_int32,
          ctypes.c_int32, ctypes.c_float, ctypes.c_float, ctypes.c_int32, _P(fa_opts)]
 
-EXPORTS = ("fa_fwd", "fa_fwd_plan", "fa_fwd_workspace_size", "fa_check_device_error",
-           "fa_status_string", "fa_abi_version")
+# fa_fwd_kvcache / fa_fwd_kvcache_plan: q, k_cache, v_cache, k_new, v_new, out, lse,
+# cu_seqlens_q, cache_seqlens, block_table, window_left, window_right, softcap,
+# scale, causal, append, opts
+_KV_ARGS = [_P(fa_tensor)] * 10 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                                   ctypes.c_int32, ctypes.c_int32, _P(fa_opts)]
+
+EXPORTS = ("fa_fwd", "fa_fwd_plan", "fa_fwd_workspace_size", "fa_fwd_kvcache", "fa_fwd_kvcache_plan",
+           "fa_check_device_error", "fa_status_string", "fa_abi_version")
 
 
 def _load():
@@ -89,6 +95,10 @@ def _load():
     lib.fa_fwd_plan.restype = ctypes.c_int
     lib.fa_fwd_workspace_size.argtypes = _ARGS + [_P(ctypes.c_size_t)]
     lib.fa_fwd_workspace_size.restype = ctypes.c_int
+    lib.fa_fwd_kvcache.argtypes = _KV_ARGS
+    lib.fa_fwd_kvcache.restype = ctypes.c_int
+    lib.fa_fwd_kvcache_plan.argtypes = _KV_ARGS + [_P(fa_plan)]
+    lib.fa_fwd_kvcache_plan.restype = ctypes.c_int
     lib.fa_check_device_error.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _P(ctypes.c_uint32)]
     lib.fa_check_device_error.restype = ctypes.c_int
     lib.fa_status_string.argtypes = [ctypes.c_int]
@@ -243,6 +253,73 @@ def fa_fwd(q, k, v, *, out=None, lse=None, cu_seqlens_q=None, cu_seqlens_k=None,
     rc = lib.fa_fwd(*args)
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+    return out, lse, workspace
+
+
+def _kv_args(q, k_cache, v_cache, k_new, v_new, out, lse, cu_seqlens_q, cache_seqlens, block_table,
+             window_left, window_right, softcap, scale, causal, append, opts):
+    descs = [describe(x) for x in (q, k_cache, v_cache, k_new, v_new, out, lse, cu_seqlens_q,
+                                   cache_seqlens, block_table)]
+    args = [_ref(x) for x in descs] + [int(window_left), int(window_right), float(softcap),
+                                       float(scale or 0.0), int(bool(causal)), int(bool(append)),
+                                       ctypes.byref(opts)]
+    return args, (descs, opts)
+
+
+def fa_fwd_kvcache_plan(q, k_cache, v_cache, k_new, v_new, cache_seqlens, *, out=None, lse=None,
+                        cu_seqlens_q=None, block_table=None, window_left=-1, window_right=-1,
+                        softcap=0.0, scale=None, causal=True, append=False, max_seqlen_q=None,
+                        max_seqlen_k=None, debug_flags=0, stream=0, **_):
+    """Host-only plan query of fa_fwd_kvcache; returns (status, plan dict)."""
+    if out is None:
+        out = q
+    if lse is None:
+        lse = torch.empty(_out_shapes(q, cu_seqlens_q, max_seqlen_q)[1], dtype=torch.float32,
+                          device=q.device)
+    opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                     debug_flags=debug_flags)
+    args, keep = _kv_args(q, k_cache, v_cache, k_new, v_new, out, lse, cu_seqlens_q, cache_seqlens,
+                          block_table, window_left, window_right, softcap, scale, causal, append, opts)
+    plan = fa_plan()
+    rc = lib.fa_fwd_kvcache_plan(*args, ctypes.byref(plan))
+    return rc, plan.as_dict()
+
+
+def fa_fwd_kvcache(q, k_cache, v_cache, k_new, v_new, cache_seqlens, *, out=None, lse=None,
+                   cu_seqlens_q=None, block_table=None, window_left=-1, window_right=-1, softcap=0.0,
+                   scale=None, causal=True, append=False, max_seqlen_q=None, max_seqlen_k=None,
+                   workspace=None, stream=None, debug_flags=0, event_begin=None, event_end=None,
+                   alibi_slopes=None, **_):
+    """Attention over a KV cache plus the step's active keys (fa_fwd_kvcache of
+    the C ABI): sequence s sees cache rows [0, cache_seqlens[s]) and then its
+    own active rows ``k_new``/``v_new`` (laid out like ``q``); with ``append``
+    the active rows are also written into the cache after the cached ones.
+    ``max_seqlen_k`` (the largest cached + active count) is required.  Returns
+    ``(out, lse, workspace)``; raises FaError on a non-zero status."""
+    if not q.is_cuda:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_fwd_kvcache (tensors must be CUDA tensors)")
+    oshape, lshape = _out_shapes(q, cu_seqlens_q, max_seqlen_q)
+    if out is None:
+        out = torch.empty(oshape, dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty(lshape, dtype=torch.float32, device=q.device)
+    alibi_slopes = _alibi(alibi_slopes, q)
+    opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                     debug_flags=debug_flags, event_begin=event_begin, event_end=event_end,
+                     alibi_slopes=alibi_slopes)
+    args, keep = _kv_args(q, k_cache, v_cache, k_new, v_new, out, lse, cu_seqlens_q, cache_seqlens,
+                          block_table, window_left, window_right, softcap, scale, causal, append, opts)
+    if workspace is None:
+        plan = fa_plan()
+        rc = lib.fa_fwd_kvcache_plan(*args, ctypes.byref(plan))
+        if rc != FA_OK:
+            raise FaError(rc, "fa_fwd_kvcache_plan")
+        workspace = alloc_workspace(plan.workspace_bytes, q.device)
+    opts.workspace = workspace.data_ptr()
+    opts.workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib.fa_fwd_kvcache(*args)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_kvcache")
     return out, lse, workspace
 
 

@@ -47,6 +47,14 @@ int check_i32_vec(const fa_tensor* t, int64_t len) {
   return FA_OK;
 }
 
+// The second key source of fa_fwd_kvcache (null for fa_fwd).
+struct KvNew {
+  const fa_tensor* k_new;
+  const fa_tensor* v_new;
+  const fa_tensor* cache_seqlens;
+  int32_t append;
+};
+
 struct Plan {
   fa_plan pub;
   Params prm;
@@ -56,7 +64,8 @@ struct Plan {
 int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
               const fa_tensor* lse, const fa_tensor* cu_q, const fa_tensor* cu_k,
               const fa_tensor* block_table, const fa_mask* mask, int32_t wl, int32_t wr,
-              float softcap, float scale, int32_t causal, const fa_opts* opts, Plan* pl) {
+              float softcap, float scale, int32_t causal, const fa_opts* opts, Plan* pl,
+              const KvNew* kn = nullptr) {
   if (!q || !k || !v || !out || !lse || !opts || !pl) return FA_ERR_INVALID_ARG;
   memset(pl, 0, sizeof(*pl));
   Params& P = pl->prm;
@@ -64,7 +73,9 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   const bool varlen_q = cu_q != nullptr;
   const bool varlen_k = cu_k != nullptr;
   const bool paged = block_table != nullptr;
-  if (paged && !varlen_k) return FA_ERR_INVALID_ARG;  // page tables need per-sequence key counts
+  // page tables need per-sequence key counts: cu_seqlens_k, or the cached
+  // counts of the two-source form (which takes no cu_seqlens_k)
+  if (kn ? varlen_k : (paged && !varlen_k)) return FA_ERR_INVALID_ARG;
   int rc;
 
   // ---- Q ----
@@ -106,7 +117,7 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
         block_table->shape[0] != n_seq || block_table->stride[1] != 1 || block_table->shape[1] < 1)
       return FA_ERR_INVALID_ARG;
     Sk = opts->max_seqlen_k;
-    if (Sk < 0 || Sk > block_table->shape[1] * page_size) return FA_ERR_INVALID_ARG;
+    if (Sk < 0 || (!kn && Sk > block_table->shape[1] * page_size)) return FA_ERR_INVALID_ARG;
   } else if (varlen_k) {
     if ((rc = check_bf16(k, 3)) || (rc = check_bf16(v, 3))) return rc;
     Hkv = k->shape[1];
@@ -129,6 +140,37 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
     P.v_sb = v->stride[0]; P.v_ss = v->stride[1]; P.v_sh = v->stride[2];
   }
   if (varlen_k && (rc = check_i32_vec(cu_k, n_seq + 1))) return rc;
+  int64_t cache_cap = 0;
+  if (kn) {
+    // cache capacity per sequence; keys = cached + active, at most max_seqlen_k
+    cache_cap = paged ? block_table->shape[1] * page_size : Sk;
+    Sk = opts->max_seqlen_k;
+    if (Sk < 0 || (Sk == 0 && Sq > 0 && n_seq > 0)) return FA_ERR_INVALID_ARG;
+    if (!kn->k_new || !kn->v_new) return FA_ERR_INVALID_ARG;
+    const fa_tensor* kv2[2] = {kn->k_new, kn->v_new};
+    for (const fa_tensor* t : kv2) {
+      if ((rc = check_bf16(t, (int)q->ndim))) return rc;
+      if (t->dtype != q->dtype) return FA_ERR_INVALID_ARG;
+      for (int i = 0; i < q->ndim; ++i) {
+        const int64_t want = (i == q->ndim - 2) ? Hkv : q->shape[i];
+        if (t->shape[i] != want) return FA_ERR_INVALID_ARG;
+      }
+    }
+    if ((rc = check_i32_vec(kn->cache_seqlens, n_seq))) return rc;
+    const fa_tensor *kt = kn->k_new, *vt = kn->v_new;
+    if (varlen_q) {
+      P.kn_sb = 0; P.kn_ss = kt->stride[0]; P.kn_sh = kt->stride[1];
+      P.vn_sb = 0; P.vn_ss = vt->stride[0]; P.vn_sh = vt->stride[1];
+    } else {
+      P.kn_sb = kt->stride[0]; P.kn_ss = kt->stride[1]; P.kn_sh = kt->stride[2];
+      P.vn_sb = vt->stride[0]; P.vn_ss = vt->stride[1]; P.vn_sh = vt->stride[2];
+    }
+    P.k_new = static_cast<const uint16_t*>(kt->data);
+    P.v_new = static_cast<const uint16_t*>(vt->data);
+    P.cache_len = static_cast<const int32_t*>(kn->cache_seqlens->data);
+    P.cache_cap = (int32_t)(cache_cap < INT32_MAX ? cache_cap : INT32_MAX);
+    P.append = kn->append ? 1 : 0;
+  }
   // grouped-query heads: Hq a multiple of Hkv, otherwise an error
   if (Hkv < 1 || Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
   if (Sq > INT32_MAX / 64 || Sk > INT32_MAX / 64 || n_seq > INT32_MAX / 64) return FA_ERR_INVALID_ARG;
@@ -161,6 +203,7 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
 
   // ---- mask ----
   int mask_kind = mask ? mask->kind : FA_MASK_NONE;
+  if (kn && mask_kind != FA_MASK_NONE) return FA_ERR_UNSUPPORTED;
   P.m_nb = P.m_nh = 1;
   if (mask_kind == FA_MASK_DENSE) {
     const fa_tensor& t = mask->t;
@@ -241,7 +284,7 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   if (!varlen_k && !paged && n_seq > 1 && (P.k_sb == 0 || P.v_sb == 0)) tma_ok = false;
   if ((Hq > 1 && P.q_sh == 0) || (Hkv > 1 && (P.k_sh == 0 || P.v_sh == 0))) tma_ok = false;
   if (P.q_ss == 0 || P.k_ss == 0 || P.v_ss == 0) tma_ok = false;
-  const bool prefill = tma_ok && Sq * (int64_t)G > 64;
+  const bool prefill = tma_ok && !kn && Sq * (int64_t)G > 64;  // two sources: decode kernel
   if (prefill) {
     P.path = FA_PATH_PREFILL;
     P.rows_per_tile = kPrefillRows;
@@ -345,6 +388,8 @@ int check_device() {
   return cached[dev] == 1 ? FA_OK : FA_ERR_NO_DEVICE;
 }
 
+
+int run_plan(Plan& pl, const fa_opts* opts);  // enqueue a validated plan (below)
 }  // namespace
 
 extern "C" {
@@ -399,6 +444,44 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_
   int rc = make_plan(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask, window_left,
                      window_right, softcap, scale, causal, opts, &pl);
   if (rc != FA_OK) return rc;
+  return run_plan(pl, opts);
+}
+
+int fa_fwd_kvcache(const fa_tensor* q, const fa_tensor* k_cache, const fa_tensor* v_cache,
+                   const fa_tensor* k_new, const fa_tensor* v_new, const fa_tensor* out,
+                   const fa_tensor* lse, const fa_tensor* cu_seqlens_q,
+                   const fa_tensor* cache_seqlens, const fa_tensor* block_table,
+                   int32_t window_left, int32_t window_right, float softcap, float scale,
+                   int32_t causal, int32_t append, const fa_opts* opts) {
+  Plan pl;
+  const KvNew kn{k_new, v_new, cache_seqlens, append};
+  int rc = make_plan(q, k_cache, v_cache, out, lse, cu_seqlens_q, nullptr, block_table, nullptr, window_left,
+                     window_right, softcap, scale, causal, opts, &pl, &kn);
+  if (rc != FA_OK) return rc;
+  return run_plan(pl, opts);
+}
+
+int fa_fwd_kvcache_plan(const fa_tensor* q, const fa_tensor* k_cache, const fa_tensor* v_cache,
+                        const fa_tensor* k_new, const fa_tensor* v_new, const fa_tensor* out,
+                        const fa_tensor* lse, const fa_tensor* cu_seqlens_q,
+                        const fa_tensor* cache_seqlens, const fa_tensor* block_table,
+                        int32_t window_left, int32_t window_right, float softcap, float scale,
+                        int32_t causal, int32_t append, const fa_opts* opts, fa_plan* plan_out) {
+  Plan pl;
+  const KvNew kn{k_new, v_new, cache_seqlens, append};
+  int rc = make_plan(q, k_cache, v_cache, out, lse, cu_seqlens_q, nullptr, block_table, nullptr, window_left,
+                     window_right, softcap, scale, causal, opts, &pl, &kn);
+  if (rc == FA_OK && plan_out) *plan_out = pl.pub;
+  return rc;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Bind the workspace and enqueue a validated plan's kernels on opts->stream.
+int run_plan(Plan& pl, const fa_opts* opts) {
+  int rc;
   if (!opts->workspace || (reinterpret_cast<uintptr_t>(opts->workspace) % kAlign) != 0 ||
       opts->workspace_bytes < pl.pub.workspace_bytes)
     return FA_ERR_WORKSPACE;
@@ -423,6 +506,10 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_
   }
   return FA_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int fa_check_device_error(void* stream, void* workspace, uint32_t* info) {
   if (!workspace) return FA_ERR_INVALID_ARG;

@@ -120,10 +120,55 @@ __device__ __forceinline__ const uint16_t* kv_row(const Params& p, const uint16_
   return base + (int64_t)b * sb + (int64_t)j * ss + (int64_t)g * sh;
 }
 
+// Key/value row j (head g) of sequence b, cached keys first: rows j >= lc
+// are the sequence's active rows j - lc in k_new / v_new (laid out like q).
+__device__ __forceinline__ const uint16_t* kv_src_row(const Params& p, bool is_v, int b, int g, int j, int lc) {
+  if (j >= lc) {
+    const int64_t r = (p.cu_q ? (int64_t)p.cu_q[b] : 0) + (j - lc);
+    return is_v ? p.v_new + (p.cu_q ? 0 : (int64_t)b * p.vn_sb) + r * p.vn_ss + (int64_t)g * p.vn_sh
+                : p.k_new + (p.cu_q ? 0 : (int64_t)b * p.kn_sb) + r * p.kn_ss + (int64_t)g * p.kn_sh;
+  }
+  return is_v ? kv_row(p, p.v, p.v_sb, p.v_ss, p.v_sh, b, g, j) : kv_row(p, p.k, p.k_sb, p.k_ss, p.k_sh, b, g, j);
+}
+
+// Append (two-source form): the active rows of sequence b, head g, are copied
+// into the cache at rows lc .. lc + q_len - 1 by one CTA per (sequence, K/V
+// head).  The scheduler has checked lc + q_len against the cache capacity; a
+// bad page index is recorded and its rows are not written.
+template <int D>
+__device__ void append_active(const Params& p, int b, int g, int lc, int q_len, int tid, int nthreads) {
+  constexpr int kPieces = D / 8;
+  for (int idx = tid; idx < q_len * kPieces; idx += nthreads) {
+    const int t = idx / kPieces, c = idx % kPieces;
+    const int j = lc + t;
+    int64_t ko, vo;
+    if (p.block_table) {
+      const int pg = __ldg(p.block_table + (int64_t)b * p.bt_stride + j / p.page_size);
+      if ((unsigned)pg >= (unsigned)p.num_pages) {
+        record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)pg);
+        continue;
+      }
+      ko = (int64_t)pg * p.k_sb + (int64_t)(j % p.page_size) * p.k_ss;
+      vo = (int64_t)pg * p.v_sb + (int64_t)(j % p.page_size) * p.v_ss;
+    } else {
+      ko = (int64_t)b * p.k_sb + (int64_t)j * p.k_ss;
+      vo = (int64_t)b * p.v_sb + (int64_t)j * p.v_ss;
+    }
+    ko += (int64_t)g * p.k_sh + c * 8;
+    vo += (int64_t)g * p.v_sh + c * 8;
+    const uint4 kv = *reinterpret_cast<const uint4*>(kv_src_row(p, false, b, g, j, lc) + c * 8);
+    const uint4 vv = *reinterpret_cast<const uint4*>(kv_src_row(p, true, b, g, j, lc) + c * 8);
+    *reinterpret_cast<uint4*>(const_cast<uint16_t*>(p.k) + ko) = kv;
+    *reinterpret_cast<uint4*>(const_cast<uint16_t*>(p.v) + vo) = vv;
+  }
+}
+
 struct ItemGeo {
   int b, g, rt, q_len, kv_len, off, i0, i1, jlo, jhi;
+  int lc;  // keys held in the cache (two-source form), else kv_len
 };
 
+template <bool KV2 = true>
 __device__ __forceinline__ ItemGeo item_geo(const Params& p, int64_t item) {
   ItemGeo t;
   t.rt = (int)(item % p.n_row_tiles);
@@ -133,6 +178,7 @@ __device__ __forceinline__ ItemGeo item_geo(const Params& p, int64_t item) {
   t.q_len = seq_qlen(p, t.b);
   t.kv_len = seq_klen(p, t.b);
   t.off = t.kv_len - t.q_len;
+  t.lc = (KV2 && p.cache_len) ? __ldg(p.cache_len + t.b) : t.kv_len;
   tile_rows(p, t.rt, t.i0, t.i1);
   t.i1 = min(t.i1, t.q_len - 1);
   key_range(p, t.i0, t.i1, t.off, t.kv_len, t.jlo, t.jhi);
@@ -155,6 +201,18 @@ __device__ __forceinline__ void out_ptrs(const Params& p, const ItemGeo& t, int 
 // 64-column halves of 16 rows x 128 bytes, 128-byte swizzle
 __device__ __forceinline__ uint32_t swz_tma(int row, int cc) {
   return (uint32_t)((cc >> 3) * (kChunkKeys * 128) + row * 128 + (((cc & 7) ^ (row & 7)) << 4));
+}
+
+// Zero rows [first, 16) of a TMA-layout V stage (all lanes of the warp; kept
+// out of line: it runs on a sequence's last chunk only).
+template <int D>
+__device__ __noinline__ void zero_rows_from(uint32_t sV, int first, int lane) {
+  constexpr int kPieces = D / 8;
+  for (int idx = lane; idx < kChunkKeys * kPieces; idx += 32) {
+    const int r = idx / kPieces, c = idx % kPieces;
+    if (r >= first) asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(sV + swz_tma(r, c)), "r"(0));
+  }
+  __syncwarp();
 }
 
 // Merge the 4 consumer warps' (m, l, O) and write the item's rows, or this
@@ -257,7 +315,7 @@ __device__ __forceinline__ void decode_finish(const Params& p, const ItemGeo& ge
 // one page, or 16 consecutive rows), issued by lane 0 of the warp that owns
 // the ring and tracked by one mbarrier per stage; otherwise by 16-byte
 // cp.async from all lanes (any layout).
-template <int D, bool TMA, bool F16>
+template <int D, bool TMA, bool F16, bool KV2>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   using S = DecodeSmem<D>;
@@ -276,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (t_begin >= count && !(split == 0 && count == 0)) return;
   const int t_end = min(count, t_begin + p.tiles_per_split);
   const bool single = count <= p.tiles_per_split;
-  const ItemGeo geo = item_geo(p, item);
+  const ItemGeo geo = item_geo<KV2>(p, item);
   const int32_t* tiles = p.item_tiles + item * p.n_kt;
 
   const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
@@ -298,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   cp_async_commit();
+  if (KV2 && p.append && geo.rt == 0 && split == 0) append_active<D>(p, geo.b, geo.g, geo.lc, geo.q_len, tid, kThreads);
   uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + S::kBarOff) + warp * kWarpStages;  // this warp's stages
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kBarOff + kWarps * kWarpStages * 8);
   if (TMA) {
@@ -328,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int e = __ldg(tiles + t_begin + c / (kKeysPerTile / kChunkKeys));
     kj0_ = ((e >> 1) * kKeysPerTile + (c % (kKeysPerTile / kChunkKeys)) * kChunkKeys) * 2 + (e & 1);
     const int kj = (e >> 1) * kKeysPerTile + (c % (kKeysPerTile / kChunkKeys)) * kChunkKeys;
-    if (paged_fast && kj < geo.kv_len) pg_ = __ldg(p.block_table + (int64_t)geo.b * p.bt_stride + kj / p.page_size);
+    if (paged_fast && kj < geo.lc) pg_ = __ldg(p.block_table + (int64_t)geo.b * p.bt_stride + kj / p.page_size);
   };
   int dk_cur, dp_cur, dk_next, dp_next;  // this lane's descriptor in the current / next batch
   chunk_desc(lane, dk_cur, dp_cur);
@@ -350,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int pg;
     const int kj0 = chunk_key0(k, partial, live, pg);
     if (!live) return;
+    if (TMA && KV2 && kj0 + kChunkKeys > geo.lc) return;  // active rows: filled by the warp
     if (TMA) {
       if (lane == 0) {
         const int st = k % kWarpStages;
@@ -399,16 +459,43 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int j = min(kj0 + r, geo.kv_len - 1);
       const uint16_t* kr;
       const uint16_t* vr;
-      if (paged_fast && kj0 + r < geo.kv_len) {
+      if (paged_fast && kj0 + r < geo.lc) {
         kr = kbase + (int64_t)r * p.k_ss;
         vr = vbase + (int64_t)r * p.v_ss;
       } else {
-        kr = kv_row(p, p.k, p.k_sb, p.k_ss, p.k_sh, geo.b, geo.g, j);
-        vr = kv_row(p, p.v, p.v_sb, p.v_ss, p.v_sh, geo.b, geo.g, j);
+        if constexpr (KV2) {
+          kr = kv_src_row(p, false, geo.b, geo.g, j, geo.lc);
+          vr = kv_src_row(p, true, geo.b, geo.g, j, geo.lc);
+        } else {
+          kr = kv_row(p, p.k, p.k_sb, p.k_ss, p.k_sh, geo.b, geo.g, j);
+          vr = kv_row(p, p.v, p.v_sb, p.v_ss, p.v_sh, geo.b, geo.g, j);
+        }
       }
       cp_async16(sK + swz<D>(r, c), kr + c * 8);
       cp_async16(sV + swz<D>(r, c), vr + c * 8);
     }
+  };
+
+  // TMA mode, two-source form: a chunk that holds active rows is copied by
+  // the warp itself when its turn comes: cached rows from the cache, active
+  // rows from k_new / v_new, rows past the keys as zeros.
+  auto fill_chunk = [&](int k, int kj0) {
+    const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
+    for (int idx = lane; idx < kChunkKeys * S::kChunks; idx += 32) {
+      const int r = idx / S::kChunks, c = idx % S::kChunks;
+      const int j = kj0 + r;
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (j < geo.kv_len) {
+        kv = __ldg(reinterpret_cast<const uint4*>(kv_src_row(p, false, geo.b, geo.g, j, geo.lc) + c * 8));
+        vv = __ldg(reinterpret_cast<const uint4*>(kv_src_row(p, true, geo.b, geo.g, j, geo.lc) + c * 8));
+      }
+      const uint32_t o = swz_tma(r, c);
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sK + o), "r"(kv.x), "r"(kv.y), "r"(kv.z),
+                   "r"(kv.w));
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(sK + S::kKvBytes + o), "r"(vv.x), "r"(vv.y),
+                   "r"(vv.z), "r"(vv.w));
+    }
+    __syncwarp();
   };
 
   // Fragment roles: keys (and head-dim) on the mma M side, the 8 packed
@@ -461,11 +548,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!live) continue;
     if (TMA) {
       const int st = k % kWarpStages;
-      if (!tc::mbar_wait(kv_full + st, (kv_phase >> st) & 1, abort_flag)) {
-        ok = false;
-        break;
+      if (KV2 && kj0 + kChunkKeys > geo.lc) {
+        fill_chunk(k, kj0);  // no copy was issued for this stage: its barrier phase is unchanged
+      } else {
+        if (!tc::mbar_wait(kv_full + st, (kv_phase >> st) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        kv_phase ^= 1u << st;
+        if (kj0 + kChunkKeys > geo.kv_len) {
+          // a sequence's last chunk: the box also brought the page's unused
+          // rows, which may hold anything (and P = 0 times a NaN is a NaN):
+          // zero those V rows
+          zero_rows_from<D>(sW + st * S::kStageBytes + S::kKvBytes, geo.kv_len - kj0, lane);
+        }
       }
-      kv_phase ^= 1u << st;
     }
     const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
     const uint32_t sV = sK + S::kKvBytes;
@@ -602,7 +699,7 @@ bool decode_maps(const Params& p, CUtensorMap* mk, CUtensorMap* mv) {
     k_so = p.k_sb;
     v_so = p.v_sb;
   } else {
-    rows = p.cu_k ? p.tot_k : p.Sk;
+    rows = p.cache_len ? p.cache_cap : (p.cu_k ? p.tot_k : p.Sk);
     outer = p.cu_k ? 1 : p.n_seq;
     k_so = (outer == 1 || p.k_sb == 0) ? p.k_ss : p.k_sb;
     v_so = (outer == 1 || p.v_sb == 0) ? p.v_ss : p.v_sb;
@@ -614,29 +711,36 @@ bool decode_maps(const Params& p, CUtensorMap* mk, CUtensorMap* mv) {
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, p.f16 != 0);
 }
 
-template <int D, bool F16>
-cudaError_t launch_decode_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
+template <int D, bool F16, bool KV2>
+cudaError_t launch_decode_v(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
   cudaError_t e;
   const int64_t grid = p.n_items * p.n_splits;
   using S = DecodeSmem<D>;
   CUtensorMap mk, mv;
   if (decode_maps<D>(p, &mk, &mv)) {
-    e = ensure_smem_attr<decode_kernel<D, true, F16>>(S::kTotal);
+    e = ensure_smem_attr<decode_kernel<D, true, F16, KV2>>(S::kTotal);
     if (e != cudaSuccess) return e;
     if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-    decode_kernel<D, true, F16><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
+    decode_kernel<D, true, F16, KV2><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
   } else {
     memset(&mk, 0, sizeof(mk));
     memset(&mv, 0, sizeof(mv));
-    e = ensure_smem_attr<decode_kernel<D, false, F16>>(S::kTotal);
+    e = ensure_smem_attr<decode_kernel<D, false, F16, KV2>>(S::kTotal);
     if (e != cudaSuccess) return e;
     if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-    decode_kernel<D, false, F16><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
+    decode_kernel<D, false, F16, KV2><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || p.n_splits <= 1) return e;
   combine_kernel<D, F16><<<(unsigned)p.n_items, 32 * kDecodeRows, 0, st>>>(p);
   return cudaGetLastError();
+}
+
+// KV2: keys from two sources (fa_fwd_kvcache), a separate instantiation so
+// that the one-source kernels carry none of its code
+template <int D, bool F16>
+cudaError_t launch_decode_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
+  return p.cache_len ? launch_decode_v<D, F16, true>(p, st, ev_begin) : launch_decode_v<D, F16, false>(p, st, ev_begin);
 }
 
 }  // namespace

@@ -18,6 +18,7 @@ __device__ __forceinline__ int seq_qlen(const Params& p, int b) {
   return p.cu_q ? (p.cu_q[b + 1] - p.cu_q[b]) : p.Sq;
 }
 __device__ __forceinline__ int seq_klen(const Params& p, int b) {
+  if (p.cache_len) return __ldg(p.cache_len + b) + seq_qlen(p, b);  // cached + active keys
   return p.cu_k ? (p.cu_k[b + 1] - p.cu_k[b]) : p.Sk;
 }
 

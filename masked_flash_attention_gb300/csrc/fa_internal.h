@@ -52,6 +52,16 @@ struct Params {
   const float* alibi; // [Hq] ALiBi slopes (natural-log units), null = off
   int32_t causal, wl, wr;
 
+  // two key sources (fa_fwd_kvcache): sequence b's keys are cache rows
+  // [0, cache_len[b]) (k / v) followed by its active rows in k_new / v_new,
+  // laid out like q; null cache_len = one source
+  const int32_t* cache_len;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  int64_t kn_sb, kn_ss, kn_sh, vn_sb, vn_ss, vn_sh;
+  int32_t cache_cap;  // cache rows a sequence may hold (block table width x page, or padded length)
+  int32_t append;     // write the active rows into the cache
+
   // additive mask
   int32_t mask_kind;
   const float* mask; int64_t m_sb, m_sh, m_sq, m_sk; int32_t m_nb, m_nh;

@@ -283,6 +283,10 @@ __global__ void __launch_bounds__(256) classify_kernel(const Params p) {
   bool bad = q_len < 0 || kv_len < 0 || q_len > p.Sq || kv_len > p.Sk;
   if (p.cu_q) bad |= p.cu_q[b] < 0 || (int64_t)p.cu_q[b + 1] > p.tot_q;
   if (p.cu_k && !p.block_table) bad |= p.cu_k[b] < 0 || (int64_t)p.cu_k[b + 1] > p.tot_k;
+  if (p.cache_len) {  // two-source form: cached rows within the cache, appended rows too
+    const int64_t lc = __ldg(p.cache_len + b);
+    bad |= lc < 0 || lc > p.cache_cap || lc + q_len > p.Sk || (p.append && lc + q_len > p.cache_cap);
+  }
   if (bad) {
     if (lane == 0) {
       p.item_count[item] = -1;  // the attention kernels leave this item alone

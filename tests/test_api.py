@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(fa.lib, n), n
         assert ctypes.cast(getattr(fa.lib, n), ctypes.c_void_p).value
-    assert fa.fa_abi_version() == 3
+    assert fa.fa_abi_version() == 4
     assert fa.fa_status_string(0) == "ok"
 
 
@@ -129,3 +129,30 @@ def test_fwd_rejects_cpu_tensors():
 def test_empty_problem_plans_no_items():
     rc, p = plan(T(2, 0, 4, 64), T(2, 5, 4, 64), T(2, 5, 4, 64))
     assert rc == 0 and p["n_items"] == 0
+
+
+def test_kvcache_plan_rules():
+    """fa_fwd_kvcache_plan: cache + active keys always take the split-KV kernel;
+    shapes of k_new / v_new follow q with Hkv heads; max_seqlen_k is required;
+    cache_seqlens has one int32 per sequence."""
+    E = _lib.FA_ERR_INVALID_ARG
+    q, kn = T(5, 4, 64), T(5, 2, 64)
+    cu = torch.tensor([0, 2, 5], dtype=torch.int32)
+    cl = torch.tensor([10, 0], dtype=torch.int32)
+    kc = T(8, 16, 2, 64)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    kv = dict(cu_seqlens_q=cu, block_table=bt, max_seqlen_q=3, max_seqlen_k=13)
+    rc, p = fa.fa_fwd_kvcache_plan(q, kc, kc, kn, kn, cl, **kv)
+    assert rc == 0 and p["path"] == _lib.FA_PATH_DECODE and p["n_heads_sched"] == 2
+    assert fa.fa_fwd_kvcache_plan(q, kc, kc, kn, kn, cl, **dict(kv, max_seqlen_k=0))[0] == E
+    assert fa.fa_fwd_kvcache_plan(q, kc, kc, T(5, 1, 64), T(5, 1, 64), cl, **kv)[0] == E   # heads
+    assert fa.fa_fwd_kvcache_plan(q, kc, kc, T(4, 2, 64), T(4, 2, 64), cl, **kv)[0] == E   # rows
+    assert fa.fa_fwd_kvcache_plan(q, kc, kc, kn.half(), kn.half(), cl, **kv)[0] == E        # dtype
+    assert fa.fa_fwd_kvcache_plan(q, kc, kc, kn, kn, cl[:1], **kv)[0] == E                  # lengths
+    assert fa.fa_fwd_kvcache_plan(q, kc, kc, kn, kn, cl.long(), **kv)[0] == E               # int32
+    # padded cache [n_seq, cap, Hkv, d], fixed-length q [B, Sq, Hq, d]
+    rc, p = fa.fa_fwd_kvcache_plan(T(2, 3, 4, 64), T(2, 40, 2, 64), T(2, 40, 2, 64), T(2, 3, 2, 64),
+                                   T(2, 3, 2, 64), cl, max_seqlen_k=13, append=True)
+    assert rc == 0 and p["path"] == _lib.FA_PATH_DECODE
+    assert fa.fa_fwd_kvcache_plan(T(2, 3, 4, 64), T(3, 40, 2, 64), T(3, 40, 2, 64), T(2, 3, 2, 64),
+                                  T(2, 3, 2, 64), cl, max_seqlen_k=13)[0] == E            # batch

@@ -135,6 +135,26 @@ def paged_varlen_decode(seed: int = 0, n_seq=64, min_len=128, max_len=8192, Hq=3
                                    max_seqlen_k=int(lens.max())))
 
 
+def paged_decode_append(seed: int = 0, **kw):
+    """The paged varlen decode batch served the two-source way: each
+    sequence's newest token is the active row (``k_new``/``v_new``), the
+    ``kv_len - 1`` before it are cached, and the call appends the active row
+    to the cache.  The cache already holds that row's values, so the keys the
+    attention sees, and the cache after the append, equal the paged workload's."""
+    c = paged_varlen_decode(seed, **kw)
+    lens = c["kv_lens"].to(torch.int64)
+    bt = c["params"]["block_table"]
+    page = c["k"].shape[1]
+    last = lens - 1
+    pages = bt[torch.arange(len(lens)), last // page].to(torch.int64)
+    rows = last % page
+    k_new = c["k"][pages, rows]      # [n_seq, Hkv, d]: one active row per sequence
+    v_new = c["v"][pages, rows]
+    c = dict(c, name=c["name"].replace("paged_varlen_decode", "paged_decode_append"))
+    c["kvcache"] = dict(k_new=k_new, v_new=v_new, cache_seqlens=last.to(torch.int32), append=True)
+    return c
+
+
 def dynamic_topk(seed: int = 0, B=2, H=16, d=128, T=8192, keep_window=2048):
     """Causal attention where each query row keeps only the ``keep_window``
     causally-allowed keys with the largest ``zero_hold_states`` value; the kept
@@ -223,6 +243,7 @@ def paginate(k, v, cu_k, page_size, seed):
 
 
 WORKLOADS = {
+    "paged_decode_append": paged_decode_append,
     "sliding_window_decode": sliding_window_decode,
     "causal_prefill_past_kv": causal_prefill_past_kv,
     "gpt2_small_layer": gpt2_small_layer,

@@ -56,8 +56,9 @@ KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_dev
 # time: once the kernel changes the figure no longer applies and is reported
 # as null.
 MEASURED_TRAFFIC = {
-    ("causal_prefill_past_kv", "prefill_kernel"): ("ff044ea3e0fb75e7", 108679424),
-    ("paged_varlen_decode", "decode_kernel"): ("9c347889c8150332", 761989120),
+    ("causal_prefill_past_kv", "prefill_kernel"): ("730d1135f4de5d0e", 108879104),
+    ("paged_varlen_decode", "decode_kernel"): ("5297f26e60532d02", 761683712),
+    ("paged_decode_append", "decode_kernel"): ("5297f26e60532d02", 760071680),
 }
 
 

@@ -12,6 +12,9 @@ Contents
                 whole masked logit matrix, takes its softmax, multiplies by V.
   brute      -- pure-Python scalar loops over the same definition, for tiny
                 inputs; used to pin ``attention``.
+  backward   -- gradients dQ, dK, dV of the forward (softmax Jacobian, the
+                soft-cap's derivative, grouped-query sums); pinned by finite
+                differences of ``attention`` in ``tests/test_oracle_backward.py``.
   kvcache    -- keys from two sources (cached rows, then the step's active
                 rows) and the cache append, built on ``attention``; pinned in
                 ``tests/test_oracle_kvcache.py``.

@@ -46,10 +46,11 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "masked attn fwd useful TFLOP/s (prefill) and KV-cache GB/s (decode), 1×GB300"
+METRIC_BWD = "masked attn bwd useful TFLOP/s (dq, dk, dv: 10 d FLOP per kept pair), 1×GB300"
 L2_FLUSH_BYTES = 256 << 20
 CSRC = os.path.join(ROOT, "masked_flash_attention_gb300", "csrc")
 KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_device.cuh"],
-                  "decode_kernel": ["decode.cu", "fa_device.cuh"]}
+                  "decode_kernel": ["decode.cu", "mma_sync.cuh", "fa_device.cuh"]}
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; see profiles/), keyed
 # by workload and kernel, with the hash of the kernel's sources at capture
@@ -257,6 +258,12 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     case = _as_dtype(W.WORKLOADS[args.workload](seed=args.seed + rank), args.dtype)
     units = workload_units(case, args.workload)
+    bwd = args.pass_ == "bwd"
+    if bwd:
+        # useful backward work: 5 products of 2 d FLOP per kept pair (S, dP,
+        # dV, dK, dQ) = 2.5 x the forward's 4 d
+        assert units["bound"] == "tensor" and "kvcache" not in case, "--pass bwd takes the prefill workloads"
+        units = dict(units, flops=units["flops"] * 2.5, metric_units=units["metric_units"] * 2.5)
     p = dict(case["params"])
     gp = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
     q, k, v = case["q"].to(dev), case["k"].to(dev), case["v"].to(dev)
@@ -289,6 +296,21 @@ def run_gpu(args):
     def step(timing=False, kb=None, ke=None):
         call(q, k, v, kvx, out=out, lse=lse, workspace=ws, stream=stream.cuda_stream, event_begin=kb,
              event_end=ke)
+
+    if bwd:
+        # the forward once (untimed) for out and lse; each step is one fa_bwd
+        step()
+        gd = torch.Generator().manual_seed(args.seed + 7)
+        hdout = torch.randn(case["q"].shape, generator=gd, dtype=torch.float32).to(case["q"].dtype)
+        dout = hdout.to(dev)
+        gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        rc, plan = fa.fa_bwd_plan(q, k, v, out, lse, dout, stream=stream.cuda_stream, **gp)
+        assert rc == 0, rc
+        ws = fa.alloc_workspace(plan["workspace_bytes"], dev)
+
+        def step(timing=False, kb=None, ke=None):  # noqa: F811
+            fa.fa_bwd(q, k, v, out, lse, dout, dq=gq, dk=gk, dv=gv, workspace=ws, stream=stream.cuda_stream,
+                      event_begin=kb, event_end=ke, **gp)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -342,6 +364,24 @@ def run_gpu(args):
         call(dq, dk, dv, dx, out=out, lse=lse, workspace=ws, stream=stream.cuda_stream)
         hout.copy_(out, non_blocking=True); hlse.copy_(lse, non_blocking=True)
 
+    if bwd:
+        # inputs q, k, v, out, lse, dout in; dq, dk, dv back
+        hout_in, hlse_in = out.cpu().pin_memory(), lse.cpu().pin_memory()
+        hdo = hdout.pin_memory()
+        eo, el, edo = torch.empty_like(out), torch.empty_like(lse), torch.empty_like(dout)
+        hg = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (gq, gk, gv)]
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hout_in, hlse_in, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in hg)
+
+        def e2e_step():  # noqa: F811
+            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+            eo.copy_(hout_in, non_blocking=True); el.copy_(hlse_in, non_blocking=True)
+            edo.copy_(hdo, non_blocking=True)
+            fa.fa_bwd(dq, dk, dv, eo, el, edo, dq=gq, dk=gk, dv=gv, workspace=ws, stream=stream.cuda_stream,
+                      **gp)
+            for h_, d_ in zip(hg, (gq, gk, gv)):
+                h_.copy_(d_, non_blocking=True)
+
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
@@ -375,12 +415,14 @@ def run_gpu(args):
                 "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4)}
     roof["peak_source"] = pk["src"]
     roof["kernel"] = "decode_kernel" if plan["path"] == fa._lib.FA_PATH_DECODE else "prefill_kernel"
+    if bwd:
+        roof["kernel"] = "backward (delta_kernel, dkdv_kernel, dq_kernel)"
     roof["kernel_ms"] = round(kern_avg, 5)
     roof["traffic"] = args.traffic if args.traffic is not None else measured_traffic(args.workload, roof["kernel"])
     if units["bytes"] is not None or roof["bound"] == "tensor":
         roof["algorithmic_bytes"] = units["bytes"] if units["bytes"] is not None else algorithmic_io_bytes(case)
     line = {
-        "metric": METRIC,
+        "metric": METRIC if args.pass_ == "fwd" else METRIC_BWD,
         "value": round(value, 3),
         "unit": units["unit"],
         "n_gpus": world,
@@ -392,7 +434,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": args.dtype,
         "data": "synthetic",
-        "config": {"workload": case["name"], "seed": args.seed,
+        "config": {"workload": case["name"], "seed": args.seed, "pass": args.pass_,
                    "l2": "flushed between timed steps (256 MB write outside the events)",
                    "parallelism": f"replica per GPU x{world}", "path": plan["path"],
                    "n_items": plan["n_items"], "n_splits": plan["n_splits"]},
@@ -462,8 +504,30 @@ def _pick_heads(case, budget_s):
     return max(1, int(budget_s / max(dt1, 1e-3))), dt1
 
 
+def _oracle_bwd_sample(case):
+    """Backward oracle on the first K/V head's q-head group of the first
+    sequence; returns (seconds, fraction of the workload's units covered)."""
+    from oracle import backward as B
+    p = dict(case["params"])
+    q, k, v = case["q"], case["k"], case["v"]
+    assert p["cu_seqlens_q"] is None, "fixed-length workloads"
+    Hq, Hkv = q.shape[2], k.shape[2]
+    G = Hq // Hkv
+    g = torch.Generator().manual_seed(11)
+    do = torch.randn(1, q.shape[1], G, q.shape[3], generator=g).to(q.dtype)
+    t0 = time.perf_counter()
+    B.attention_grad(q[:1, :, :G], k[:1, :, :1], v[:1, :, :1], do, **p)
+    return time.perf_counter() - t0, G / (q.shape[0] * Hq)
+
+
 def cpu_baseline(case, units, args, budget_s=None):
     budget_s = args.cpu_budget if budget_s is None else budget_s
+    if getattr(args, "pass_", "fwd") == "bwd":
+        dt, frac = _oracle_bwd_sample(case)
+        return {"value": round(units["metric_units"] * frac / dt, 6), "unit": units["unit"],
+                "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                "sample": f"fp64 numpy backward oracle on one K/V head's q-head group of one sequence "
+                          f"({frac * 100:.2f}% of the units) in {dt:.2f} s"}
     n, _ = _pick_heads(case, budget_s)
     dt, frac = _oracle_sample(case, n)
     val = units["metric_units"] * frac / dt
@@ -481,26 +545,31 @@ def run_reference(args):
         return None
     case = _as_dtype(W.WORKLOADS[args.workload](seed=args.seed), args.dtype)
     units = workload_units(case, args.workload)
-    per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    n, _ = _pick_heads(case, per_step_budget)
+    if args.pass_ == "bwd":
+        units = dict(units, flops=units["flops"] * 2.5, metric_units=units["metric_units"] * 2.5)
+        sample_fn = lambda: _oracle_bwd_sample(case)  # noqa: E731
+        what = "fp64 numpy backward oracle on one K/V head's q-head group of one sequence"
+    else:
+        per_step_budget = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+        n, _ = _pick_heads(case, per_step_budget)
+        sample_fn = lambda: _oracle_sample(case, n)  # noqa: E731
+        what = f"fp64 numpy oracle on {_n_pairs(case, n)} (sequence, q-head) pairs"
     for _ in range(args.warmup):
-        _oracle_sample(case, n)
+        sample_fn()
     times, frac = [], 0.0
     for _ in range(args.steps):
-        dt, frac = _oracle_sample(case, n)
+        dt, frac = sample_fn()
         times.append(dt)
     ms = sum(times) / len(times) * 1e3
     val = units["metric_units"] * frac / (ms / 1e3)
     cores = len(os.sched_getaffinity(0))
-    sample = (f"each step: fp64 numpy oracle on {_n_pairs(case, n)} (sequence, q-head) pairs = "
-              f"{frac * 100:.2f}% of "
-              f"the workload; value scaled to the workload's units")
+    sample = (f"each step: {what} = {frac * 100:.2f}% of the workload; value scaled to the workload's units")
     return {
-        "impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": units["unit"],
+        "impl": "reference", "metric": METRIC if args.pass_ == "fwd" else METRIC_BWD, "value": round(val, 6), "unit": units["unit"],
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": case["name"], "seed": args.seed},
+        "config": {"workload": case["name"], "seed": args.seed, "pass": args.pass_},
         "cpu_baseline": {"value": round(val, 6), "unit": units["unit"], "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(val, 6), "unit": units["unit"], "h2d_bytes_per_step": 0,
@@ -516,6 +585,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="causal_prefill_past_kv", choices=sorted(W.WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"],
+                    help="bwd: time fa_bwd (dq, dk, dv) after one untimed forward; prefill workloads")
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "f16"],
                     help="input type of q, k, v and out (fp16 peak = bf16 peak, as the nominal rates are equal)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

@@ -82,7 +82,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 4
+#define FA_ABI_VERSION 5
 
 typedef enum {
   FA_OK = 0,
@@ -273,6 +273,38 @@ int fa_fwd_kvcache_plan(const fa_tensor* q, const fa_tensor* k_cache, const fa_t
                         const fa_tensor* cache_seqlens, const fa_tensor* block_table,
                         int32_t window_left, int32_t window_right, float softcap, float scale,
                         int32_t causal, int32_t append, const fa_opts* opts, fa_plan* plan_out);
+
+/* Backward pass: dq, dk, dv of the forward for the same arguments
+ * (InfiniTrain pull request 193, "FlashAttention native backend": the
+ * FlashAttention-2 causal forward and backward kernels it builds; "Framework
+ * 与 autograd": the autograd function around them).  With P recomputed from
+ * the forward's LSE, Delta = rowsum(dout * out), dP = dout V^T and
+ * dS = P * (dP - Delta) * dx/ds (dx/ds = scale, or scale * (1 - tanh^2) under
+ * the soft-cap): dv = sum over a group's q-heads of P^T dout, dk = sum of
+ * dS^T q, dq = dS k.  ALiBi (opts->alibi_slopes) enters the logits as in the
+ * forward and gets no gradient.
+ *   q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, window, softcap, scale,
+ *                causal, opts: as given to fa_fwd (out and lse from it)
+ *   dout, dq     laid out like q (own strides), the input element type
+ *   dk, dv       laid out like k (own strides), the input element type
+ * No paged cache and no dense or top-k mask (the call takes neither).  The
+ * result does not depend on scheduling: no atomics, every gradient row is
+ * summed in a fixed order by one CTA.  dq/dk/dv rows of keys or queries
+ * that no pair reaches are written as 0.  Workspace: fa_bwd_plan's
+ * workspace_bytes (the forward's plus Delta, fp32 per query row and head). */
+int fa_bwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
+           const fa_tensor* lse, const fa_tensor* dout, const fa_tensor* dq, const fa_tensor* dk,
+           const fa_tensor* dv, const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+           int32_t window_left, int32_t window_right, float softcap, float scale, int32_t causal,
+           const fa_opts* opts);
+
+/* Host-only: validate the arguments of fa_bwd and describe its plan (as
+ * fa_fwd_plan; n_kernels counts the Delta, dk/dv and dq kernels). */
+int fa_bwd_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
+                const fa_tensor* lse, const fa_tensor* dout, const fa_tensor* dq, const fa_tensor* dk,
+                const fa_tensor* dv, const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+                int32_t window_left, int32_t window_right, float softcap, float scale, int32_t causal,
+                const fa_opts* opts, fa_plan* plan_out);
 
 /* Size of the static device scratch used by fa_fwd_noalloc (32 MiB). */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)

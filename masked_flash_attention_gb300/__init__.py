@@ -12,6 +12,8 @@ from ._lib import (  # noqa: F401
     alloc_workspace,
     describe,
     fa_abi_version,
+    fa_bwd,
+    fa_bwd_plan,
     fa_check_device_error,
     fa_fwd,
     fa_fwd_kvcache,

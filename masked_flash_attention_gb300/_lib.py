@@ -79,8 +79,13 @@ _ARGS = [_P(fa_tensor), _P(fa_tensor), _P(fa_tensor), _P(fa_tensor), _P(fa_tenso
 _KV_ARGS = [_P(fa_tensor)] * 10 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
                                    ctypes.c_int32, ctypes.c_int32, _P(fa_opts)]
 
+# fa_bwd / fa_bwd_plan: q, k, v, out, lse, dout, dq, dk, dv, cu_seqlens_q,
+# cu_seqlens_k, window_left, window_right, softcap, scale, causal, opts
+_BWD_ARGS = [_P(fa_tensor)] * 11 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                                    ctypes.c_int32, _P(fa_opts)]
+
 EXPORTS = ("fa_fwd", "fa_fwd_plan", "fa_fwd_workspace_size", "fa_fwd_kvcache", "fa_fwd_kvcache_plan",
-           "fa_check_device_error", "fa_status_string", "fa_abi_version")
+           "fa_bwd", "fa_bwd_plan", "fa_check_device_error", "fa_status_string", "fa_abi_version")
 
 
 def _load():
@@ -99,6 +104,10 @@ def _load():
     lib.fa_fwd_kvcache.restype = ctypes.c_int
     lib.fa_fwd_kvcache_plan.argtypes = _KV_ARGS + [_P(fa_plan)]
     lib.fa_fwd_kvcache_plan.restype = ctypes.c_int
+    lib.fa_bwd.argtypes = _BWD_ARGS
+    lib.fa_bwd.restype = ctypes.c_int
+    lib.fa_bwd_plan.argtypes = _BWD_ARGS + [_P(fa_plan)]
+    lib.fa_bwd_plan.restype = ctypes.c_int
     lib.fa_check_device_error.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _P(ctypes.c_uint32)]
     lib.fa_check_device_error.restype = ctypes.c_int
     lib.fa_status_string.argtypes = [ctypes.c_int]
@@ -321,6 +330,63 @@ def fa_fwd_kvcache(q, k_cache, v_cache, k_new, v_new, cache_seqlens, *, out=None
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_kvcache")
     return out, lse, workspace
+
+
+def _bwd_args(q, k, v, out, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, window_left, window_right,
+              softcap, scale, causal, opts):
+    descs = [describe(x) for x in (q, k, v, out, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k)]
+    args = [_ref(x) for x in descs] + [int(window_left), int(window_right), float(softcap),
+                                       float(scale or 0.0), int(bool(causal)), ctypes.byref(opts)]
+    return args, (descs, opts)
+
+
+def fa_bwd_plan(q, k, v, out, lse, dout, *, dq=None, dk=None, dv=None, cu_seqlens_q=None,
+                cu_seqlens_k=None, window_left=-1, window_right=-1, softcap=0.0, scale=None,
+                causal=False, max_seqlen_q=None, max_seqlen_k=None, debug_flags=0, stream=0, **_):
+    """Host-only plan query of fa_bwd; returns (status, plan dict)."""
+    dq = q if dq is None else dq
+    dk = k if dk is None else dk
+    dv = v if dv is None else dv
+    opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                     debug_flags=debug_flags)
+    args, keep = _bwd_args(q, k, v, out, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, window_left,
+                           window_right, softcap, scale, causal, opts)
+    plan = fa_plan()
+    rc = lib.fa_bwd_plan(*args, ctypes.byref(plan))
+    return rc, plan.as_dict()
+
+
+def fa_bwd(q, k, v, out, lse, dout, *, dq=None, dk=None, dv=None, cu_seqlens_q=None, cu_seqlens_k=None,
+           window_left=-1, window_right=-1, softcap=0.0, scale=None, causal=False, max_seqlen_q=None,
+           max_seqlen_k=None, workspace=None, stream=None, debug_flags=0, event_begin=None, event_end=None,
+           alibi_slopes=None, **_):
+    """Backward pass (fa_bwd of the C ABI): gradients of the forward for the
+    same arguments, ``out`` and ``lse`` from fa_fwd and ``dout`` = dL/dout.
+    Returns ``(dq, dk, dv, workspace)``; dq/dk/dv are allocated with torch when
+    not given.  Raises FaError on a non-zero status."""
+    if not q.is_cuda:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_bwd (tensors must be CUDA tensors)")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    alibi_slopes = _alibi(alibi_slopes, q)
+    opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                     debug_flags=debug_flags, event_begin=event_begin, event_end=event_end,
+                     alibi_slopes=alibi_slopes)
+    args, keep = _bwd_args(q, k, v, out, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, window_left,
+                           window_right, softcap, scale, causal, opts)
+    if workspace is None:
+        plan = fa_plan()
+        rc = lib.fa_bwd_plan(*args, ctypes.byref(plan))
+        if rc != FA_OK:
+            raise FaError(rc, "fa_bwd_plan")
+        workspace = alloc_workspace(plan.workspace_bytes, q.device)
+    opts.workspace = workspace.data_ptr()
+    opts.workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib.fa_bwd(*args)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv, workspace
 
 
 def fa_check_device_error(workspace, stream=None):

@@ -390,6 +390,48 @@ int check_device() {
 
 
 int run_plan(Plan& pl, const fa_opts* opts);  // enqueue a validated plan (below)
+
+// fa_bwd: the forward's arguments (validated by make_plan, without mask or
+// page table) plus dO, dq, dk, dv; Delta is appended to the workspace.
+int make_plan_bwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
+                  const fa_tensor* lse, const fa_tensor* dout, const fa_tensor* dq, const fa_tensor* dk,
+                  const fa_tensor* dv, const fa_tensor* cu_q, const fa_tensor* cu_k, int32_t wl, int32_t wr,
+                  float softcap, float scale, int32_t causal, const fa_opts* opts, Plan* pl, size_t* off_delta) {
+  int rc = make_plan(q, k, v, out, lse, cu_q, cu_k, nullptr, nullptr, wl, wr, softcap, scale, causal, opts, pl);
+  if (rc != FA_OK) return rc;
+  Params& P = pl->prm;
+  const fa_tensor* qs[2] = {dout, dq};
+  for (const fa_tensor* t : qs) {
+    if ((rc = check_bf16(t, (int)q->ndim))) return rc;
+    if (t->dtype != q->dtype) return FA_ERR_INVALID_ARG;
+    for (int i = 0; i < q->ndim; ++i)
+      if (t->shape[i] != q->shape[i]) return FA_ERR_INVALID_ARG;
+  }
+  const fa_tensor* ks[2] = {dk, dv};
+  for (const fa_tensor* t : ks) {
+    if ((rc = check_bf16(t, (int)k->ndim))) return rc;
+    if (t->dtype != q->dtype) return FA_ERR_INVALID_ARG;
+    for (int i = 0; i < k->ndim; ++i)
+      if (t->shape[i] != k->shape[i]) return FA_ERR_INVALID_ARG;
+  }
+  auto strides = [](const fa_tensor* t, int64_t& sb, int64_t& ss, int64_t& sh) {
+    if (t->ndim == 3) { sb = 0; ss = t->stride[0]; sh = t->stride[1]; }
+    else { sb = t->stride[0]; ss = t->stride[1]; sh = t->stride[2]; }
+  };
+  strides(dout, P.do_sb, P.do_ss, P.do_sh);
+  strides(dq, P.dq_sb, P.dq_ss, P.dq_sh);
+  strides(dk, P.dk_sb, P.dk_ss, P.dk_sh);
+  strides(dv, P.dv_sb, P.dv_ss, P.dv_sh);
+  P.dout = static_cast<const uint16_t*>(dout->data);
+  P.dq = static_cast<uint16_t*>(dq->data);
+  P.dk = static_cast<uint16_t*>(dk->data);
+  P.dv = static_cast<uint16_t*>(dv->data);
+  const int64_t rows = cu_q ? q->shape[0] : (int64_t)P.n_seq * P.Sq;
+  *off_delta = pl->pub.workspace_bytes;
+  pl->pub.workspace_bytes = align_up(*off_delta + (size_t)rows * P.Hq * 4);
+  pl->pub.n_kernels = (rows > 0 && P.Hq > 0) ? 3 : 0;
+  return FA_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -510,6 +552,46 @@ int run_plan(Plan& pl, const fa_opts* opts) {
 }  // namespace
 
 extern "C" {
+
+int fa_bwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
+           const fa_tensor* lse, const fa_tensor* dout, const fa_tensor* dq, const fa_tensor* dk,
+           const fa_tensor* dv, const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+           int32_t window_left, int32_t window_right, float softcap, float scale, int32_t causal,
+           const fa_opts* opts) {
+  Plan pl;
+  size_t off_delta = 0;
+  int rc = make_plan_bwd(q, k, v, out, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, window_left,
+                         window_right, softcap, scale, causal, opts, &pl, &off_delta);
+  if (rc != FA_OK) return rc;
+  if (!opts->workspace || (reinterpret_cast<uintptr_t>(opts->workspace) % kAlign) != 0 ||
+      opts->workspace_bytes < pl.pub.workspace_bytes)
+    return FA_ERR_WORKSPACE;
+  if ((rc = check_device()) != FA_OK) return rc;
+  bind_workspace(&pl, opts->workspace);
+  Params& P = pl.prm;
+  P.delta = reinterpret_cast<float*>(static_cast<unsigned char*>(opts->workspace) + off_delta);
+  cudaStream_t st = static_cast<cudaStream_t>(opts->stream);
+  cudaError_t e = launch_backward(P, st, static_cast<cudaEvent_t>(opts->event_begin));
+  if (e == cudaSuccess && opts->event_end) e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_end), st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_bwd_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
+                const fa_tensor* lse, const fa_tensor* dout, const fa_tensor* dq, const fa_tensor* dk,
+                const fa_tensor* dv, const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+                int32_t window_left, int32_t window_right, float softcap, float scale, int32_t causal,
+                const fa_opts* opts, fa_plan* plan_out) {
+  Plan pl;
+  size_t off_delta = 0;
+  int rc = make_plan_bwd(q, k, v, out, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, window_left,
+                         window_right, softcap, scale, causal, opts, &pl, &off_delta);
+  if (rc == FA_OK && plan_out) *plan_out = pl.pub;
+  return rc;
+}
 
 int fa_check_device_error(void* stream, void* workspace, uint32_t* info) {
   if (!workspace) return FA_ERR_INVALID_ARG;

@@ -26,6 +26,7 @@
 
 #include "fa_device.cuh"
 #include "host_util.h"
+#include "mma_sync.cuh"
 #include "tc_sm103.cuh"
 
 namespace mfa {
@@ -49,61 +50,6 @@ struct DecodeSmem {
   static_assert(kWarps * kDecodeRows * D * 4 <= kWarps * kWarpBytes, "merge buffer must fit");
   static_assert(2 * kWarps * kDecodeRows * 4 <= kQBytes, "warp statistics must fit over Q");
 };
-
-// swizzled 16-byte chunk offset (bytes) of (row, chunk) in a [rows][D] bf16 tile
-template <int D>
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return (uint32_t)((row * (D / 8) + (chunk ^ (row & 7))) * 16);
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-// m16n8k16, fp32 accumulate; A and B both bf16, or both fp16 when F16.
-template <bool F16>
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  if constexpr (F16)
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  else
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
-  return d;
-}
-// Two fp32 values rounded to nearest-even into a packed pair of the input
-// type (bf16, or fp16 when F16).
-template <bool F16>
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  if constexpr (F16) {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  } else {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-}
 
 // Address of key/value row j (head g) of sequence b.
 __device__ __forceinline__ const uint16_t* kv_row(const Params& p, const uint16_t* base, int64_t sb,

@@ -62,6 +62,16 @@ struct Params {
   int32_t cache_cap;  // cache rows a sequence may hold (block table width x page, or padded length)
   int32_t append;     // write the active rows into the cache
 
+  // backward (fa_bwd): dO and Delta = rowsum(dO * O) (workspace, LSE layout);
+  // dq like q, dk / dv like k / v
+  const uint16_t* dout;
+  int64_t do_sb, do_ss, do_sh;
+  uint16_t* dq;
+  uint16_t* dk;
+  uint16_t* dv;
+  int64_t dq_sb, dq_ss, dq_sh, dk_sb, dk_ss, dk_sh, dv_sb, dv_ss, dv_sh;
+  float* delta;
+
   // additive mask
   int32_t mask_kind;
   const float* mask; int64_t m_sb, m_sh, m_sq, m_sk; int32_t m_nb, m_nh;
@@ -97,5 +107,6 @@ cudaError_t launch_classify(const Params& p, cudaStream_t st);
 cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
 cudaError_t launch_prefill(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
 cudaError_t launch_prefill_f16(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);  // p.f16 inputs
+cudaError_t launch_backward(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
 
 }  // namespace mfa

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(fa.lib, n), n
         assert ctypes.cast(getattr(fa.lib, n), ctypes.c_void_p).value
-    assert fa.fa_abi_version() == 4
+    assert fa.fa_abi_version() == 5
     assert fa.fa_status_string(0) == "ok"
 
 
@@ -156,3 +156,19 @@ def test_kvcache_plan_rules():
     assert rc == 0 and p["path"] == _lib.FA_PATH_DECODE
     assert fa.fa_fwd_kvcache_plan(T(2, 3, 4, 64), T(3, 40, 2, 64), T(3, 40, 2, 64), T(2, 3, 2, 64),
                                   T(2, 3, 2, 64), cl, max_seqlen_k=13)[0] == E            # batch
+
+
+def test_bwd_plan_rules():
+    """fa_bwd_plan: the forward's arguments plus dout / dq like q and dk / dv
+    like k, one element type; three kernels; Delta in the workspace."""
+    E = _lib.FA_ERR_INVALID_ARG
+    q, k = T(2, 5, 4, 64), T(2, 7, 2, 64)
+    lse = T(2, 4, 5, dtype=torch.float32)
+    rc, p = fa.fa_bwd_plan(q, k, k, q, lse, q, causal=True)
+    assert rc == 0 and p["n_kernels"] == 3
+    rc2, p2 = fa.fa_fwd_plan(q, k, k, out=q, lse=lse, causal=True)
+    assert p["workspace_bytes"] >= p2["workspace_bytes"] + 2 * 4 * 5 * 4
+    assert fa.fa_bwd_plan(q, k, k, q, lse, T(2, 5, 4, 32), causal=True)[0] == E       # dout shape
+    assert fa.fa_bwd_plan(q, k, k, q, lse, q.half(), causal=True)[0] == E             # dout dtype
+    assert fa.fa_bwd_plan(q, k, k, q, lse, q, dk=T(2, 7, 4, 64))[0] == E             # dk heads
+    assert fa.fa_bwd_plan(q, k, k, q, lse, q, dq=T(2, 5, 4, 64)[..., ::2])[0] == E   # dq head-dim stride

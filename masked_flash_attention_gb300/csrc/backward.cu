@@ -233,9 +233,10 @@ __global__ void __launch_bounds__(kBwdThreads) dkdv_kernel(const Params p) {
     for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
       for (int e = 0; e < 4; ++e) st[nb][e] = dpt[nb][e] = 0.f;
+    // (the four accumulators take turns, so no MMA waits on the one before it)
 #pragma unroll
     for (int ks = 0; ks < D / 16; ks += 2) {
-      uint32_t ka[2][4], va[2][4];
+      uint32_t ka[2][4], va[2][4], qf[2][4], of[2][4];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int kr = 16 * warp + (lane & 7) + 8 * (mi & 1), kc = 2 * (ks + u) + (mi >> 1);
@@ -244,14 +245,16 @@ __global__ void __launch_bounds__(kBwdThreads) dkdv_kernel(const Params p) {
       }
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb) {
-        uint32_t qf[4], of[4];
-        ldsm_x4(sQ + swz<D>(8 * nb + (lane & 7), 2 * ks + mi), qf[0], qf[1], qf[2], qf[3]);
-        ldsm_x4(sO + swz<D>(8 * nb + (lane & 7), 2 * ks + mi), of[0], of[1], of[2], of[3]);
-        mma_bf16<F16>(st[nb], ka[0], qf[0], qf[1]);
-        mma_bf16<F16>(st[nb], ka[1], qf[2], qf[3]);
-        mma_bf16<F16>(dpt[nb], va[0], of[0], of[1]);
-        mma_bf16<F16>(dpt[nb], va[1], of[2], of[3]);
+        ldsm_x4(sQ + swz<D>(8 * nb + (lane & 7), 2 * ks + mi), qf[nb][0], qf[nb][1], qf[nb][2], qf[nb][3]);
+        ldsm_x4(sO + swz<D>(8 * nb + (lane & 7), 2 * ks + mi), of[nb][0], of[nb][1], of[nb][2], of[nb][3]);
       }
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+          mma_bf16<F16>(st[nb], ka[u], qf[nb][2 * u], qf[nb][2 * u + 1]);
+          mma_bf16<F16>(dpt[nb], va[u], of[nb][2 * u], of[nb][2 * u + 1]);
+        }
     }
     // P^T and dS^T; element e of n-block nb: key 16 warp + g8 + 8 (e >> 1), row 8 nb + 2 c4 + (e & 1)
     uint32_t pa[4], da[4];
@@ -277,16 +280,23 @@ __global__ void __launch_bounds__(kBwdThreads) dkdv_kernel(const Params p) {
     const uint32_t pA[4] = {pa[0], pa[1], pa[2], pa[3]};
     const uint32_t dA[4] = {da[0], da[1], da[2], da[3]};
     // dV += P^T dO, dK += dS^T Q: B = [16 rows x 8 d] per n-block, by transposed loads
+    // (the next n-pair's B fragments are loaded before this pair's MMAs)
+    const int rrt = (lane & 7) + 8 * ((lane >> 3) & 1);
+    uint32_t ob[2][4], qb[2][4];
+    ldsm_x4_t(sO + swz<D>(rrt, lane >> 4), ob[0][0], ob[0][1], ob[0][2], ob[0][3]);
+    ldsm_x4_t(sQ + swz<D>(rrt, lane >> 4), qb[0][0], qb[0][1], qb[0][2], qb[0][3]);
 #pragma unroll
     for (int np = 0; np < D / 16; ++np) {
-      const int rr = (lane & 7) + 8 * ((lane >> 3) & 1), cc = 2 * np + (lane >> 4);
-      uint32_t ob[4], qb[4];
-      ldsm_x4_t(sO + swz<D>(rr, cc), ob[0], ob[1], ob[2], ob[3]);
-      ldsm_x4_t(sQ + swz<D>(rr, cc), qb[0], qb[1], qb[2], qb[3]);
-      mma_bf16<F16>(dv[2 * np], pA, ob[0], ob[1]);
-      mma_bf16<F16>(dv[2 * np + 1], pA, ob[2], ob[3]);
-      mma_bf16<F16>(dk[2 * np], dA, qb[0], qb[1]);
-      mma_bf16<F16>(dk[2 * np + 1], dA, qb[2], qb[3]);
+      const int cur = np & 1;
+      if (np + 1 < D / 16) {
+        const int cc = 2 * (np + 1) + (lane >> 4);
+        ldsm_x4_t(sO + swz<D>(rrt, cc), ob[cur ^ 1][0], ob[cur ^ 1][1], ob[cur ^ 1][2], ob[cur ^ 1][3]);
+        ldsm_x4_t(sQ + swz<D>(rrt, cc), qb[cur ^ 1][0], qb[cur ^ 1][1], qb[cur ^ 1][2], qb[cur ^ 1][3]);
+      }
+      mma_bf16<F16>(dv[2 * np], pA, ob[cur][0], ob[cur][1]);
+      mma_bf16<F16>(dk[2 * np], dA, qb[cur][0], qb[cur][1]);
+      mma_bf16<F16>(dv[2 * np + 1], pA, ob[cur][2], ob[cur][3]);
+      mma_bf16<F16>(dk[2 * np + 1], dA, qb[cur][2], qb[cur][3]);
     }
   }
   cp_async_wait<0>();
@@ -396,19 +406,24 @@ __global__ void __launch_bounds__(kBwdThreads) dq_kernel(const Params p) {
       for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sa[nb][e] = dp[nb][e] = 0.f;
+      // (the four accumulators take turns, so no MMA waits on the one before it)
 #pragma unroll
-      for (int nb = 0; nb < 2; ++nb)
+      for (int ks = 0; ks < D / 16; ks += 2) {
+        uint32_t kf[2][4], vf[2][4];
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ks += 2) {
-          uint32_t kf[4], vf[4];
+        for (int nb = 0; nb < 2; ++nb) {
           const int kr = 16 * sk + 8 * nb + (lane & 7);
-          ldsm_x4(sK + swz<D>(kr, 2 * ks + mi), kf[0], kf[1], kf[2], kf[3]);
-          ldsm_x4(sV + swz<D>(kr, 2 * ks + mi), vf[0], vf[1], vf[2], vf[3]);
-          mma_bf16<F16>(sa[nb], qa[ks], kf[0], kf[1]);
-          mma_bf16<F16>(sa[nb], qa[ks + 1], kf[2], kf[3]);
-          mma_bf16<F16>(dp[nb], oa[ks], vf[0], vf[1]);
-          mma_bf16<F16>(dp[nb], oa[ks + 1], vf[2], vf[3]);
+          ldsm_x4(sK + swz<D>(kr, 2 * ks + mi), kf[nb][0], kf[nb][1], kf[nb][2], kf[nb][3]);
+          ldsm_x4(sV + swz<D>(kr, 2 * ks + mi), vf[nb][0], vf[nb][1], vf[nb][2], vf[nb][3]);
         }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+            mma_bf16<F16>(sa[nb], qa[ks + u], kf[nb][2 * u], kf[nb][2 * u + 1]);
+            mma_bf16<F16>(dp[nb], oa[ks + u], vf[nb][2 * u], vf[nb][2 * u + 1]);
+          }
+      }
       // dS; element e of n-block nb: row g8 + 8 (e >> 1), key 8 nb + 2 c4 + (e & 1)
       uint32_t da[4];
 #pragma unroll
@@ -428,13 +443,17 @@ __global__ void __launch_bounds__(kBwdThreads) dq_kernel(const Params p) {
       }
       const uint32_t dA[4] = {da[0], da[1], da[2], da[3]};
       // dQ += dS K: B = [16 keys x 8 d] per n-block, by transposed loads of K rows
+      const int rrt = 16 * sk + (lane & 7) + 8 * ((lane >> 3) & 1);
+      uint32_t kb[2][4];
+      ldsm_x4_t(sK + swz<D>(rrt, lane >> 4), kb[0][0], kb[0][1], kb[0][2], kb[0][3]);
 #pragma unroll
       for (int np = 0; np < D / 16; ++np) {
-        const int rr = 16 * sk + (lane & 7) + 8 * ((lane >> 3) & 1), cc = 2 * np + (lane >> 4);
-        uint32_t kb[4];
-        ldsm_x4_t(sK + swz<D>(rr, cc), kb[0], kb[1], kb[2], kb[3]);
-        mma_bf16<F16>(dq[2 * np], dA, kb[0], kb[1]);
-        mma_bf16<F16>(dq[2 * np + 1], dA, kb[2], kb[3]);
+        const int cur = np & 1;
+        if (np + 1 < D / 16)
+          ldsm_x4_t(sK + swz<D>(rrt, 2 * (np + 1) + (lane >> 4)), kb[cur ^ 1][0], kb[cur ^ 1][1], kb[cur ^ 1][2],
+                    kb[cur ^ 1][3]);
+        mma_bf16<F16>(dq[2 * np], dA, kb[cur][0], kb[cur][1]);
+        mma_bf16<F16>(dq[2 * np + 1], dA, kb[cur][2], kb[cur][3]);
       }
     }
   }

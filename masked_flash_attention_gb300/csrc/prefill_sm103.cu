@@ -636,12 +636,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (!tc::mbar_wait(refb + (gl & 1), (gl >> 1) & 1, abort_flag)) { ok = false; break; }
         m_ref = refv[(gl & 1) * 128 + row];
       }
+      // this warpgroup's O columns are read out of TMEM before its row sum is
+      // posted: the next unit's first PV overwrites O, and its P comes from a
+      // warpgroup that has passed the row-sum barrier, so every O read is
+      // ordered before that PV
+      if (!tc::mbar_wait(o_full, kk & 1, abort_flag)) { ok = false; break; }
+      tc::fence_after_sync();
+      uint32_t ro[kHalfD / 32][32];
+#pragma unroll
+      for (int c = 0; c < kHalfD / 32; ++c) tc::tmem_ld32(lane_base + kOCol + w * kHalfD + c * 32, ro[c]);
       rsum[w * 128 + row] = (r_own == m_ref || r_own == -INFINITY) ? l : l * fast_exp2(r_own - m_ref);
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
       tc::mbar_arrive(sumx);
-      if (!tc::mbar_wait(sumx, kk & 1, abort_flag) || !tc::mbar_wait(o_full, kk & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
+      if (!tc::mbar_wait(sumx, kk & 1, abort_flag)) { ok = false; break; }
       tc::fence_after_sync();
       const float lt = rsum[row] + rsum[128 + row];
       const bool empty = !(lt > 0.f);
@@ -656,12 +664,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const bool tma_rows = o_tma && row0 + 32 <= q_len;
 #pragma unroll
       for (int c = 0; c < kHalfD / 32; ++c) {
-        uint32_t r[32];
-        tc::tmem_ld32(lane_base + kOCol + w * kHalfD + c * 32, r);
+        const uint32_t* r = ro[c];
         // the staging tile is free once the previous TMA store has read it
         if (lane == 0) tc::bulk_wait_read_all();
         __syncwarp();
-        tc::tmem_wait_ld();
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
           uint4 o4;

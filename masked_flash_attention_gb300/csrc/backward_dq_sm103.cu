@@ -1,0 +1,352 @@
+// backward_dq_sm103.cu -- dQ of the backward pass on the 5th-generation tensor
+// cores: one CTA per (sequence, q-head, 128-row query tile), for every key tile
+// its rows can see
+//   S  = Q K^T,   dP = dO V^T                 (tcgen05, TMEM accumulators)
+//   dS = P * (dP - Delta) * dx/ds,  P = exp(x - LSE)   (one thread per row)
+//   dQ += dS K                                (tcgen05, dS read from TMEM)
+// the same products as the warp-level dq kernel (backward.cu), with the
+// operand layouts of the forward kernel: Q, dO, K and V tiles arrive by TMA
+// (128-byte swizzle, K-major for S and dP); K is also the MN-major B operand
+// of dQ += dS K, as V is for the forward's PV; dS is packed in place of the S
+// it came from, as the forward packs P.
+//
+// Thread 0 issues the TMA copies and the MMAs; all 512 threads turn S and dP
+// into dS: warpgroup k takes key columns [32 k, 32 k + 32) of every row (a
+// warp reaches TMEM lanes 32 (warp % 4) ...), so thread (k, r) owns row r,
+// 32 keys.  TMEM: S [0, 128), dS [128, 192), dP [256, 384), dQ [384, 384 + D).
+// K/V tiles in two buffers.  Order per key tile t: S(t), dP(t) -> rows ->
+// dQ(t) += dS(t) K(t); the next tile's S and dP are issued once every row has
+// read S(t) and dP(t) (right after dQ(t)), and the copy of tile t + 2 into
+// tile t's buffer waits for the commit that follows dQ(t).  Every wait is
+// bounded (FA_ERR_DEVICE_TIMEOUT on expiry).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "fa_device.cuh"
+#include "host_util.h"
+#include "tc_sm103.cuh"
+
+namespace mfa {
+
+namespace {
+
+constexpr int kTcRows = 128;   // query rows per CTA (TMEM lanes)
+constexpr int kTcKeys = 128;   // keys per tile
+constexpr uint32_t kTcCols = 512;
+
+template <int D>
+struct DqTcCfg {
+  static constexpr int kTile = 128 * D * 2;  // one 128-row tile
+  static constexpr int kQ = 0, kDO = kTile;
+  static constexpr int kKV = 2 * kTile;      // [2 buffers][K, V]
+  static constexpr int kBar = kKV + 4 * kTile;
+  static constexpr int kUsed = kBar + 256;
+  // at least 116 KB, so that one CTA (and its 512 TMEM columns) sits on an SM
+  static constexpr int kSmem = (kUsed > 116 * 1024 ? kUsed : 116 * 1024) + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ float tc_softcap_tanh(float x, float inv_cap) {
+  const float y = x * inv_cap;
+  const float t = fast_exp2(-2.f * kLog2e * fabsf(y));
+  return copysignf(__fdividef(1.f - t, 1.f + t), y);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t tc_pack2(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(512, 1)
+    dq_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                 const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+  using C = DqTcCfg<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int n_qt = (p.Sq + kTcRows - 1) / kTcRows;
+  const int qt = (int)(blockIdx.x % n_qt);
+  const int64_t r0 = blockIdx.x / n_qt;
+  const int h = (int)(r0 % p.Hq), b = (int)(r0 / p.Hq);
+  const int g = h / p.G;
+  // lengths from device memory, checked against the planned sizes
+  const int q_len = seq_qlen(p, b), kv_len = seq_klen(p, b);
+  {
+    bool bad = q_len < 0 || kv_len < 0 || q_len > p.Sq || kv_len > p.Sk;
+    if (p.cu_q) bad |= p.cu_q[b] < 0 || (int64_t)p.cu_q[b + 1] > p.tot_q;
+    if (p.cu_k) bad |= p.cu_k[b] < 0 || (int64_t)p.cu_k[b + 1] > p.tot_k;
+    if (bad) return;  // the dK/dV kernel reports it
+  }
+  const int i0 = qt * kTcRows;
+  if (i0 >= q_len) return;
+  const int off = kv_len - q_len;
+  int jlo, jhi;
+  key_range(p, i0, min(i0 + kTcRows, q_len) - 1, off, kv_len, jlo, jhi);
+  const int kb0 = jlo > 0 ? jlo / kTcKeys : 0;
+  const int nkb = jhi >= jlo ? jhi / kTcKeys - kb0 + 1 : 0;
+  const int wg = warp >> 2;                      // key columns [32 wg, 32 wg + 32)
+  const int row = 32 * (warp & 3) + (tid & 31), i = i0 + row;  // this thread's query row
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
+  uint64_t* q_full = bars;         // Q and dO landed
+  uint64_t* kv_full = bars + 1;    // [2] K/V buffer landed
+  uint64_t* s_done = bars + 3;     // S and dP of a tile written
+  uint64_t* ds_ready = bars + 4;   // dS of a tile written (512 threads)
+  uint64_t* q_done = bars + 5;     // dQ MMA of a tile (and all before it) done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  if (tid == 0) {
+    tc::mbar_init(q_full, 1);
+    tc::mbar_init(kv_full, 1);
+    tc::mbar_init(kv_full + 1, 1);
+    tc::mbar_init(s_done, 1);
+    tc::mbar_init(ds_ready, 512);
+    tc::mbar_init(q_done, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, kTcCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
+  constexpr uint32_t kDSCol = 128, kDPCol = 256, kDQCol = 384;
+
+  const int q_row0 = p.cu_q ? p.cu_q[b] : 0, q_b = p.cu_q ? 0 : b;
+  const int k_row0 = p.cu_k ? p.cu_k[b] : 0, k_b = p.cu_k ? 0 : b;
+  constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false, F16);
+  constexpr uint32_t idQ = tc::idesc_bf16_f32(128, D, false, true, F16);
+  const uint32_t sQ = tc::smem_u32(smem + C::kQ), sDO = tc::smem_u32(smem + C::kDO);
+  auto kv_base = [&](int buf) { return smem + C::kKV + buf * 2 * C::kTile; };
+  auto load_kv = [&](int t) {
+    unsigned char* dst = kv_base(t & 1);
+    tc::mbar_arrive_expect_tx(kv_full + (t & 1), 2 * C::kTile);
+    const int row_k = k_row0 + (kb0 + t) * kTcKeys;
+    for (int c = 0; c < D / 64; ++c) {
+      tc::tma_load_4d(dst + c * 16384, &tk, kv_full + (t & 1), c * 64, g, row_k, k_b);
+      tc::tma_load_4d(dst + C::kTile + c * 16384, &tv, kv_full + (t & 1), c * 64, g, row_k, k_b);
+    }
+  };
+  auto issue_s = [&](int t) {  // S(t) -> S, dP(t) -> dP
+    const uint32_t ka = tc::smem_u32(kv_base(t & 1)), va = ka + C::kTile;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+      tc::mma_ss(tbase, tc::sdesc_sw128(sQ + o, 16, 1024), tc::sdesc_sw128(ka + o, 16, 1024), idS,
+                 ks > 0 ? 1u : 0u);
+      tc::mma_ss(tbase + kDPCol, tc::sdesc_sw128(sDO + o, 16, 1024), tc::sdesc_sw128(va + o, 16, 1024), idS,
+                 ks > 0 ? 1u : 0u);
+    }
+    tc::mma_commit(s_done);
+  };
+
+  bool ok = true;
+  if (tid == 0 && nkb > 0) {
+    tc::tma_prefetch_desc(&tq);
+    tc::tma_prefetch_desc(&tdo);
+    tc::tma_prefetch_desc(&tk);
+    tc::tma_prefetch_desc(&tv);
+    tc::mbar_arrive_expect_tx(q_full, 2 * C::kTile);
+    for (int c = 0; c < D / 64; ++c) {
+      tc::tma_load_4d(smem + C::kQ + c * 16384, &tq, q_full, c * 64, h, q_row0 + i0, q_b);
+      tc::tma_load_4d(smem + C::kDO + c * 16384, &tdo, q_full, c * 64, h, q_row0 + i0, q_b);
+    }
+    load_kv(0);
+    if (nkb > 1) load_kv(1);
+    ok = tc::mbar_wait(q_full, 0, abort_flag) && tc::mbar_wait(kv_full, 0, abort_flag);
+    if (ok) {
+      tc::fence_after_sync();
+      issue_s(0);
+    } else {
+      *abort_flag = 1;
+    }
+  }
+  // this row's LSE (log2 units) and Delta
+  float lse2 = 0.f, dlt = 0.f;
+  if (i < q_len) {
+    const int64_t qrow = (int64_t)q_row0 + i;
+    lse2 = __ldg(p.lse + (p.cu_q ? 0 : (int64_t)b * p.lse_sb) + (int64_t)h * p.lse_sh + qrow * p.lse_ss) * kLog2e;
+    dlt = p.delta[p.cu_q ? (int64_t)h * p.tot_q + qrow : ((int64_t)b * p.Hq + h) * p.Sq + i];
+  }
+  const float slope2 = p.alibi ? __ldg(p.alibi + h) * kLog2e : 0.f;
+
+  for (int t = 0; t < nkb; ++t) {
+    // ---- the rows: S(t), dP(t) -> dS(t), this thread's 32 keys
+    if (!ok || !tc::mbar_wait(s_done, t & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    tc::fence_after_sync();
+    const int j0 = (kb0 + t) * kTcKeys;
+    {
+      const int c = wg;
+      uint32_t sv[32], dv[32];
+      tc::tmem_ld32(lane_base + 32 * c, sv);
+      tc::tmem_ld32(lane_base + kDPCol + 32 * c, dv);
+      tc::tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float ds[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = j0 + 32 * c + e + u;
+          const float s = __uint_as_float(sv[e + u]);
+          float x = -INFINITY, dxds = 0.f;
+          if (i < q_len && pair_allowed(p, i, j, off, kv_len)) {
+            if (p.softcap > 0.f) {
+              const float th = tc_softcap_tanh(s * p.scale, p.inv_softcap);
+              x = th * (p.softcap * kLog2e);
+              dxds = p.scale * (1.f - th * th);
+            } else {
+              x = s * p.scale_log2;
+              dxds = p.scale;
+            }
+            x -= slope2 * (float)abs(i + off - j);
+          }
+          const float pe = (x == -INFINITY) ? 0.f : fast_exp2(x - lse2);
+          ds[u] = pe * (__uint_as_float(dv[e + u]) - dlt) * dxds;
+        }
+        pk[e >> 1] = tc_pack2<F16>(ds[0], ds[1]);
+      }
+      tc::tmem_st16(lane_base + kDSCol + 16 * c, pk);  // dS keys [32 c, 32 c + 32), packed pairs
+    }
+    tc::tmem_wait_st();
+    tc::fence_before_sync();
+    tc::mbar_arrive(ds_ready);
+
+    // ---- thread 0: dQ(t) += dS(t) K(t); then S(t+1), dP(t+1); then the copy of tile t + 2
+    if (tid == 0) {
+      if (!tc::mbar_wait(ds_ready, t & 1, abort_flag)) {
+        ok = false;
+      } else {
+        tc::fence_after_sync();
+        const uint32_t ka = tc::smem_u32(kv_base(t & 1));
+#pragma unroll
+        for (int ks = 0; ks < kTcKeys / 16; ++ks)
+          tc::mma_ts(tbase + kDQCol, tbase + kDSCol + ks * 8, tc::sdesc_sw128(ka + ks * 2048, 16384, 1024), idQ,
+                     (t > 0 || ks > 0) ? 1u : 0u);
+        tc::mma_commit(q_done);
+        if (t + 1 < nkb) {
+          if (!tc::mbar_wait(kv_full + ((t + 1) & 1), ((t + 1) >> 1) & 1, abort_flag)) {
+            ok = false;
+          } else {
+            tc::fence_after_sync();
+            issue_s(t + 1);
+          }
+        }
+        if (ok && t + 2 < nkb) {
+          // tile t's buffer is free once dQ(t) (and everything before it) is done
+          if (!tc::mbar_wait(q_done, t & 1, abort_flag)) ok = false;
+          else load_kv(t + 2);
+        }
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  }
+  if (!ok && !*abort_flag) *abort_flag = 1;
+
+  // ---- epilogue: dQ rows out of TMEM (zero when no key tile was seen)
+  bool have = nkb > 0;
+  if (have && !*abort_flag) {
+    if (!tc::mbar_wait(q_done, (nkb - 1) & 1, abort_flag)) have = false;
+  }
+  if (*abort_flag) {
+    if (tid == 0) record_error(p, FA_ERR_DEVICE_TIMEOUT, 40);
+  } else {
+    // warpgroup k stores columns [32 k, 32 k + 32); the TMEM loads are
+    // warp-wide (every lane, rows past the sequence too), only rows inside it
+    // are stored
+    uint16_t* qp = p.dq + (p.cu_q ? 0 : (int64_t)b * p.dq_sb) + ((int64_t)q_row0 + min(i, q_len - 1)) * p.dq_ss +
+                   (int64_t)h * p.dq_sh;
+    tc::fence_after_sync();
+    for (int c = wg; c < D / 32; c += 4) {
+      uint32_t v[32];
+      if (have) {
+        tc::tmem_ld32(lane_base + kDQCol + 32 * c, v);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
+      }
+      if (i < q_len) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 w;
+          w.x = tc_pack2<F16>(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+          w.y = tc_pack2<F16>(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+          w.z = tc_pack2<F16>(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+          w.w = tc_pack2<F16>(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+          *reinterpret_cast<uint4*>(qp + 32 * c + e) = w;
+        }
+      }
+    }
+  }
+  if (*abort_flag && tid == 0) {
+    // let the copies and MMAs already issued finish before the CTA leaves
+    tc::mma_commit(q_done);
+    tc::mbar_wait_drain(q_done, nkb & 1, 100000000ull);
+    tc::mbar_wait_drain(kv_full, 0, 100000000ull);
+    tc::mbar_wait_drain(kv_full + 1, 0, 100000000ull);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tbase, kTcCols);
+}
+
+bool encode_tile(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int batch, int64_t s_h,
+                 int64_t s_row, int64_t s_b, bool f16) {
+  return encode_4d_bf16(m, base, d, heads, rows, batch, s_h, s_row, s_b, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, f16);
+}
+
+template <int D, bool F16>
+cudaError_t launch_dq_tc_d(const Params& p, cudaStream_t st, bool* launched) {
+  *launched = false;
+  const bool vq = p.cu_q != nullptr, vk = p.cu_k != nullptr;
+  const int64_t q_rows = vq ? p.tot_q : p.Sq, k_rows = vk ? p.tot_k : p.Sk;
+  const int qb = vq ? 1 : p.n_seq, kb = vk ? 1 : p.n_seq;
+  auto sb = [](int nb, int64_t s_b, int64_t s_row) { return (nb == 1 || s_b == 0) ? s_row : s_b; };
+  CUtensorMap mq, mdo, mk, mv;
+  if (q_rows <= 0 || k_rows <= 0) return cudaSuccess;
+  if (!encode_tile(&mq, p.q, D, p.Hq, q_rows, qb, p.q_sh, p.q_ss, sb(qb, p.q_sb, p.q_ss), F16) ||
+      !encode_tile(&mdo, p.dout, D, p.Hq, q_rows, qb, p.do_sh, p.do_ss, sb(qb, p.do_sb, p.do_ss), F16) ||
+      !encode_tile(&mk, p.k, D, p.Hkv, k_rows, kb, p.k_sh, p.k_ss, sb(kb, p.k_sb, p.k_ss), F16) ||
+      !encode_tile(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, sb(kb, p.v_sb, p.v_ss), F16))
+    return cudaSuccess;  // layout without tensor maps: the caller takes the warp-level kernel
+  cudaError_t e = ensure_smem_attr<dq_tc_kernel<D, F16>>(DqTcCfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t n_qt = (p.Sq + kTcRows - 1) / kTcRows;
+  const int64_t grid = (int64_t)p.n_seq * p.Hq * n_qt;
+  if (grid > 0) dq_tc_kernel<D, F16><<<(unsigned)grid, 512, DqTcCfg<D>::kSmem, st>>>(p, mq, mdo, mk, mv);
+  *launched = true;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// dQ on tcgen05; *launched = false (nothing enqueued) when a tensor map
+// cannot describe the layout.
+cudaError_t launch_dq_tc(const Params& p, cudaStream_t st, bool* launched) {
+  if (p.f16) return p.d == 64 ? launch_dq_tc_d<64, true>(p, st, launched) : launch_dq_tc_d<128, true>(p, st, launched);
+  return p.d == 64 ? launch_dq_tc_d<64, false>(p, st, launched) : launch_dq_tc_d<128, false>(p, st, launched);
+}
+
+}  // namespace mfa

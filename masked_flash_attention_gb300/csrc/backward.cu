@@ -478,15 +478,15 @@ cudaError_t launch_bwd_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin)
   const int64_t rows = p.cu_q ? p.tot_q : (int64_t)p.n_seq * p.Sq;
   const int64_t warps = rows * p.Hq;
   if (warps > 0) delta_kernel<D, F16><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // dK/dV and dQ on the tensor cores when tensor maps describe the layout,
+  // else the warp-level kernels below
+  bool tc = false;
+  if ((e = launch_bwd_tc(p, st, &tc)) != cudaSuccess || tc) return e;
   const int64_t n_kt = (p.Sk + kKeyTile - 1) / kKeyTile, n_qt = (p.Sq + kRowTile - 1) / kRowTile;
   const int64_t g1 = (int64_t)p.n_seq * p.Hkv * n_kt, g2 = (int64_t)p.n_seq * p.Hq * n_qt;
   if (g1 > 0) dkdv_kernel<D, F16><<<(unsigned)g1, kBwdThreads, DkdvSmem<D>::kTotal, st>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // dQ on the tensor cores when tensor maps describe the layout, else the
-  // warp-level kernel
-  bool tc_dq = false;
-  if ((e = launch_dq_tc(p, st, &tc_dq)) != cudaSuccess) return e;
-  if (!tc_dq && g2 > 0) dq_kernel<D, F16><<<(unsigned)g2, kBwdThreads, DqSmem<D>::kTotal, st>>>(p);
+  if (g2 > 0) dq_kernel<D, F16><<<(unsigned)g2, kBwdThreads, DqSmem<D>::kTotal, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,6 @@
-// backward_dq_sm103.cu -- dQ of the backward pass on the 5th-generation tensor
-// cores: one CTA per (sequence, q-head, 128-row query tile), for every key tile
-// its rows can see
+// backward_sm103.cu -- the backward pass on the 5th-generation tensor cores
+// (dK/dV kernel further down).  dQ: one CTA per (sequence, q-head, 128-row
+// query tile), for every key tile its rows can see
 //   S  = Q K^T,   dP = dO V^T                 (tcgen05, TMEM accumulators)
 //   dS = P * (dP - Delta) * dx/ds,  P = exp(x - LSE)   (one thread per row)
 //   dQ += dS K                                (tcgen05, dS read from TMEM)
@@ -311,6 +311,307 @@ __global__ void __launch_bounds__(512, 1)
   if (warp == 0) tc::tmem_dealloc(tbase, kTcCols);
 }
 
+// ---------------------------------------------------------------------------
+// dK, dV: one CTA per (sequence, K/V head, 128-key tile), over every 128-row
+// query block of the group's q-heads that can see the tile
+//   S^T = K Q^T, dP^T = V dO^T -> P^T, dS^T (thread (k, r): key r, query
+//   columns [32 k, 32 k + 32)) -> dV += P^T dO, dK += dS^T Q
+// TMEM: S^T [0, 128) then P^T in its first 64 columns, dP^T [128, 256) then
+// dS^T in its first 64, dV [256, 256 + D), dK [384, 384 + D).  A CTA barrier
+// separates the reads of S^T and dP^T from the writes over them; the next
+// block's S^T and dP^T are issued once dV and dK of this one are done.
+// Q/dO blocks in two buffers; LSE and Delta of a block's 128 query rows in two
+// shared buffers, filled a block ahead.
+// ---------------------------------------------------------------------------
+template <int D>
+struct DkdvTcCfg {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kK = 0, kV = kTile;
+  static constexpr int kQO = 2 * kTile;       // [2 buffers][Q, dO]
+  static constexpr int kStat = kQO + 4 * kTile;  // [2 buffers][lse2 128, delta 128] floats
+  static constexpr int kBar = kStat + 2 * 2 * 128 * 4;
+  static constexpr int kUsed = kBar + 256;
+  static constexpr int kSmem = (kUsed > 116 * 1024 ? kUsed : 116 * 1024) + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+template <int D, bool F16>
+__global__ void __launch_bounds__(512, 1)
+    dkdv_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+  using C = DkdvTcCfg<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int n_kt = (p.Sk + kTcKeys - 1) / kTcKeys;
+  const int kt = (int)(blockIdx.x % n_kt);
+  const int64_t r0 = blockIdx.x / n_kt;
+  const int g = (int)(r0 % p.Hkv), b = (int)(r0 / p.Hkv);
+  const int q_len = seq_qlen(p, b), kv_len = seq_klen(p, b);
+  {
+    bool bad = q_len < 0 || kv_len < 0 || q_len > p.Sq || kv_len > p.Sk;
+    if (p.cu_q) bad |= p.cu_q[b] < 0 || (int64_t)p.cu_q[b + 1] > p.tot_q;
+    if (p.cu_k) bad |= p.cu_k[b] < 0 || (int64_t)p.cu_k[b + 1] > p.tot_k;
+    if (bad) {
+      if (kt == 0 && g == 0 && tid == 0) record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)b);
+      return;
+    }
+  }
+  const int k0 = kt * kTcKeys;
+  if (k0 >= kv_len) return;
+  const int off = kv_len - q_len;
+  const int k1 = min(k0 + kTcKeys, kv_len) - 1;
+  int ilo = 0, ihi = q_len - 1;
+  if (p.causal) ilo = max(ilo, k0 - off);
+  if (p.wr >= 0) ilo = max(ilo, k0 - off - p.wr);
+  if (p.wl >= 0) ihi = min(ihi, k1 - off + p.wl);
+  const int qb0 = ilo > 0 ? ilo / kTcRows : 0;
+  const int nqb = ihi >= ilo ? ihi / kTcRows - qb0 + 1 : 0;
+  const int n_steps = nqb * p.G;
+  const int wg = warp >> 2;                                    // query columns [32 wg, 32 wg + 32)
+  const int row = 32 * (warp & 3) + (tid & 31), j = k0 + row;  // this thread's key
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
+  uint64_t* kv_full = bars;        // K and V landed
+  uint64_t* qo_full = bars + 1;    // [2] Q/dO buffer landed
+  uint64_t* s_done = bars + 3;     // S^T and dP^T of a block written
+  uint64_t* p_ready = bars + 4;    // P^T and dS^T written (512 threads)
+  uint64_t* m_done = bars + 5;     // dV and dK MMAs of a block (and all before them) done
+  uint64_t* rd_done = bars + 6;    // every thread has read S^T and dP^T of a block (512 threads)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* stat = reinterpret_cast<float*>(smem + C::kStat);
+  if (tid == 0) {
+    tc::mbar_init(kv_full, 1);
+    tc::mbar_init(qo_full, 1);
+    tc::mbar_init(qo_full + 1, 1);
+    tc::mbar_init(s_done, 1);
+    tc::mbar_init(p_ready, 512);
+    tc::mbar_init(m_done, 1);
+    tc::mbar_init(rd_done, 512);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, kTcCols);
+    tc::tmem_relinquish();
+  }
+  const int q_row0 = p.cu_q ? p.cu_q[b] : 0, q_b = p.cu_q ? 0 : b;
+  const int k_row0 = p.cu_k ? p.cu_k[b] : 0, k_b = p.cu_k ? 0 : b;
+  // LSE (log2 units) and Delta of step s's 128 query rows into buffer s & 1
+  auto load_stat = [&](int s) {
+    if (tid < 128) {
+      const int h = g * p.G + s / nqb;
+      const int i = (qb0 + s % nqb) * kTcRows + tid;
+      float l2 = 0.f, dl = 0.f;
+      if (i < q_len) {
+        const int64_t qrow = (int64_t)q_row0 + i;
+        l2 = __ldg(p.lse + (p.cu_q ? 0 : (int64_t)b * p.lse_sb) + (int64_t)h * p.lse_sh + qrow * p.lse_ss) * kLog2e;
+        dl = p.delta[p.cu_q ? (int64_t)h * p.tot_q + qrow : ((int64_t)b * p.Hq + h) * p.Sq + i];
+      }
+      stat[(s & 1) * 256 + tid] = l2;
+      stat[(s & 1) * 256 + 128 + tid] = dl;
+    }
+  };
+  if (n_steps > 0) load_stat(0);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
+  constexpr uint32_t kDPCol = 128, kDVCol = 256, kDKCol = 384;
+  constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false, F16);
+  constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true, F16);
+  const uint32_t sK = tc::smem_u32(smem + C::kK), sV = tc::smem_u32(smem + C::kV);
+  auto qo_base = [&](int buf) { return smem + C::kQO + buf * 2 * C::kTile; };
+  auto load_qo = [&](int s) {
+    unsigned char* dst = qo_base(s & 1);
+    const int h = g * p.G + s / nqb;
+    const int row_q = q_row0 + (qb0 + s % nqb) * kTcRows;
+    tc::mbar_arrive_expect_tx(qo_full + (s & 1), 2 * C::kTile);
+    for (int c = 0; c < D / 64; ++c) {
+      tc::tma_load_4d(dst + c * 16384, &tq, qo_full + (s & 1), c * 64, h, row_q, q_b);
+      tc::tma_load_4d(dst + C::kTile + c * 16384, &tdo, qo_full + (s & 1), c * 64, h, row_q, q_b);
+    }
+  };
+  auto issue_s = [&](int s) {  // S^T(s) -> [0, 128), dP^T(s) -> [128, 256)
+    const uint32_t qa = tc::smem_u32(qo_base(s & 1)), oa = qa + C::kTile;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+      tc::mma_ss(tbase, tc::sdesc_sw128(sK + o, 16, 1024), tc::sdesc_sw128(qa + o, 16, 1024), idS, ks > 0 ? 1u : 0u);
+      tc::mma_ss(tbase + kDPCol, tc::sdesc_sw128(sV + o, 16, 1024), tc::sdesc_sw128(oa + o, 16, 1024), idS,
+                 ks > 0 ? 1u : 0u);
+    }
+    tc::mma_commit(s_done);
+  };
+
+  bool ok = true;
+  if (tid == 0 && n_steps > 0) {
+    tc::tma_prefetch_desc(&tq);
+    tc::tma_prefetch_desc(&tdo);
+    tc::tma_prefetch_desc(&tk);
+    tc::tma_prefetch_desc(&tv);
+    tc::mbar_arrive_expect_tx(kv_full, 2 * C::kTile);
+    for (int c = 0; c < D / 64; ++c) {
+      tc::tma_load_4d(smem + C::kK + c * 16384, &tk, kv_full, c * 64, g, k_row0 + k0, k_b);
+      tc::tma_load_4d(smem + C::kV + c * 16384, &tv, kv_full, c * 64, g, k_row0 + k0, k_b);
+    }
+    load_qo(0);
+    if (n_steps > 1) load_qo(1);
+    ok = tc::mbar_wait(kv_full, 0, abort_flag) && tc::mbar_wait(qo_full, 0, abort_flag);
+    if (ok) {
+      tc::fence_after_sync();
+      issue_s(0);
+    } else {
+      *abort_flag = 1;
+    }
+  }
+
+  for (int s = 0; s < n_steps; ++s) {
+    const int h = g * p.G + s / nqb;
+    const int i0 = (qb0 + s % nqb) * kTcRows;
+    // ---- rows: S^T(s), dP^T(s) -> P^T(s), dS^T(s) for this thread's 32 query columns
+    if (!ok || !tc::mbar_wait(s_done, s & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    tc::fence_after_sync();
+    uint32_t sv[32], dv[32];
+    tc::tmem_ld32(lane_base + 32 * wg, sv);
+    tc::tmem_ld32(lane_base + kDPCol + 32 * wg, dv);
+    tc::tmem_wait_ld();
+    // every thread has read S^T and dP^T before any writes over them (a
+    // bounded wait, so that an abort cannot leave threads stuck)
+    tc::fence_before_sync();
+    tc::mbar_arrive(rd_done);
+    if (!tc::mbar_wait(rd_done, s & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    tc::fence_after_sync();
+    // every thread is past step s - 1: its LSE / Delta buffer takes step s + 1's
+    if (s + 1 < n_steps) load_stat(s + 1);
+    const float* l2s = stat + (s & 1) * 256;
+    const float* dls = l2s + 128;
+    const float a_slope = p.alibi ? __ldg(p.alibi + h) * kLog2e : 0.f;
+    uint32_t pk[16], dk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float pv[2], ds[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int q = 32 * wg + e + u, i = i0 + q;
+        const float sc = __uint_as_float(sv[e + u]);
+        float x = -INFINITY, dxds = 0.f;
+        if (i < q_len && pair_allowed(p, i, j, off, kv_len)) {
+          if (p.softcap > 0.f) {
+            const float th = tc_softcap_tanh(sc * p.scale, p.inv_softcap);
+            x = th * (p.softcap * kLog2e);
+            dxds = p.scale * (1.f - th * th);
+          } else {
+            x = sc * p.scale_log2;
+            dxds = p.scale;
+          }
+          x -= a_slope * (float)abs(i + off - j);
+        }
+        const float pe = (x == -INFINITY) ? 0.f : fast_exp2(x - l2s[q]);
+        pv[u] = pe;
+        ds[u] = pe * (__uint_as_float(dv[e + u]) - dls[q]) * dxds;
+      }
+      pk[e >> 1] = tc_pack2<F16>(pv[0], pv[1]);
+      dk[e >> 1] = tc_pack2<F16>(ds[0], ds[1]);
+    }
+    tc::tmem_st16(lane_base + 16 * wg, pk);           // P^T query columns [32 wg, +32), packed pairs
+    tc::tmem_st16(lane_base + kDPCol + 16 * wg, dk);  // dS^T
+    tc::tmem_wait_st();
+    tc::fence_before_sync();
+    tc::mbar_arrive(p_ready);
+
+    // ---- thread 0: dV += P^T dO, dK += dS^T Q; then S^T(s + 1), dP^T(s + 1); then the copy of step s + 2
+    if (tid == 0) {
+      if (!tc::mbar_wait(p_ready, s & 1, abort_flag)) {
+        ok = false;
+      } else {
+        tc::fence_after_sync();
+        const uint32_t qa = tc::smem_u32(qo_base(s & 1)), oa = qa + C::kTile;
+#pragma unroll
+        for (int ks = 0; ks < kTcRows / 16; ++ks) {
+          tc::mma_ts(tbase + kDVCol, tbase + ks * 8, tc::sdesc_sw128(oa + ks * 2048, 16384, 1024), idO,
+                     (s > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_ts(tbase + kDKCol, tbase + kDPCol + ks * 8, tc::sdesc_sw128(qa + ks * 2048, 16384, 1024), idO,
+                     (s > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(m_done);
+        if (s + 1 < n_steps) {
+          // S^T and dP^T of the next block overwrite P^T and dS^T: after dV, dK
+          if (!tc::mbar_wait(m_done, s & 1, abort_flag) ||
+              !tc::mbar_wait(qo_full + ((s + 1) & 1), ((s + 1) >> 1) & 1, abort_flag)) {
+            ok = false;
+          } else {
+            tc::fence_after_sync();
+            issue_s(s + 1);
+            if (s + 2 < n_steps) load_qo(s + 2);  // into this block's buffer, free after m_done
+          }
+        }
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  }
+  if (!ok && !*abort_flag) *abort_flag = 1;
+
+  // ---- epilogue: dK, dV rows out of TMEM (zero when no query block was seen)
+  bool have = n_steps > 0;
+  if (have && !*abort_flag) {
+    if (!tc::mbar_wait(m_done, (n_steps - 1) & 1, abort_flag)) have = false;
+  }
+  if (*abort_flag) {
+    if (tid == 0) record_error(p, FA_ERR_DEVICE_TIMEOUT, 41);
+  } else {
+    const int jc = min(j, kv_len - 1);
+    uint16_t* kp = p.dk + (p.cu_k ? 0 : (int64_t)b * p.dk_sb) + ((int64_t)k_row0 + jc) * p.dk_ss + (int64_t)g * p.dk_sh;
+    uint16_t* vp = p.dv + (p.cu_k ? 0 : (int64_t)b * p.dv_sb) + ((int64_t)k_row0 + jc) * p.dv_ss + (int64_t)g * p.dv_sh;
+    tc::fence_after_sync();
+    // warpgroup k: chunks k, k + 4, ... of [dV chunks | dK chunks]
+    for (int c = wg; c < 2 * (D / 32); c += 4) {
+      const bool is_k = c >= D / 32;
+      const int cc = is_k ? c - D / 32 : c;
+      uint32_t v[32];
+      if (have) {
+        tc::tmem_ld32(lane_base + (is_k ? kDKCol : kDVCol) + 32 * cc, v);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
+      }
+      if (j < kv_len) {
+        uint16_t* dst = (is_k ? kp : vp) + 32 * cc;
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          uint4 w;
+          w.x = tc_pack2<F16>(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+          w.y = tc_pack2<F16>(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+          w.z = tc_pack2<F16>(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+          w.w = tc_pack2<F16>(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+          *reinterpret_cast<uint4*>(dst + e) = w;
+        }
+      }
+    }
+  }
+  if (*abort_flag && tid == 0) {
+    tc::mma_commit(m_done);
+    tc::mbar_wait_drain(m_done, n_steps & 1, 100000000ull);
+    tc::mbar_wait_drain(kv_full, 0, 100000000ull);
+    tc::mbar_wait_drain(qo_full, 0, 100000000ull);
+    tc::mbar_wait_drain(qo_full + 1, 0, 100000000ull);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tbase, kTcCols);
+}
+
 bool encode_tile(CUtensorMap* m, const void* base, int d, int heads, int64_t rows, int batch, int64_t s_h,
                  int64_t s_row, int64_t s_b, bool f16) {
   return encode_4d_bf16(m, base, d, heads, rows, batch, s_h, s_row, s_b, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -318,7 +619,7 @@ bool encode_tile(CUtensorMap* m, const void* base, int d, int heads, int64_t row
 }
 
 template <int D, bool F16>
-cudaError_t launch_dq_tc_d(const Params& p, cudaStream_t st, bool* launched) {
+cudaError_t launch_bwd_tc_d(const Params& p, cudaStream_t st, bool* launched) {
   *launched = false;
   const bool vq = p.cu_q != nullptr, vk = p.cu_k != nullptr;
   const int64_t q_rows = vq ? p.tot_q : p.Sq, k_rows = vk ? p.tot_k : p.Sk;
@@ -333,6 +634,11 @@ cudaError_t launch_dq_tc_d(const Params& p, cudaStream_t st, bool* launched) {
     return cudaSuccess;  // layout without tensor maps: the caller takes the warp-level kernel
   cudaError_t e = ensure_smem_attr<dq_tc_kernel<D, F16>>(DqTcCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
+  if ((e = ensure_smem_attr<dkdv_tc_kernel<D, F16>>(DkdvTcCfg<D>::kSmem)) != cudaSuccess) return e;
+  const int64_t n_kt = (p.Sk + kTcKeys - 1) / kTcKeys;
+  const int64_t g1 = (int64_t)p.n_seq * p.Hkv * n_kt;
+  if (g1 > 0) dkdv_tc_kernel<D, F16><<<(unsigned)g1, 512, DkdvTcCfg<D>::kSmem, st>>>(p, mq, mdo, mk, mv);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t n_qt = (p.Sq + kTcRows - 1) / kTcRows;
   const int64_t grid = (int64_t)p.n_seq * p.Hq * n_qt;
   if (grid > 0) dq_tc_kernel<D, F16><<<(unsigned)grid, 512, DqTcCfg<D>::kSmem, st>>>(p, mq, mdo, mk, mv);
@@ -342,11 +648,11 @@ cudaError_t launch_dq_tc_d(const Params& p, cudaStream_t st, bool* launched) {
 
 }  // namespace
 
-// dQ on tcgen05; *launched = false (nothing enqueued) when a tensor map
-// cannot describe the layout.
-cudaError_t launch_dq_tc(const Params& p, cudaStream_t st, bool* launched) {
-  if (p.f16) return p.d == 64 ? launch_dq_tc_d<64, true>(p, st, launched) : launch_dq_tc_d<128, true>(p, st, launched);
-  return p.d == 64 ? launch_dq_tc_d<64, false>(p, st, launched) : launch_dq_tc_d<128, false>(p, st, launched);
+// dK/dV and dQ on tcgen05; *launched = false (nothing enqueued) when a tensor
+// map cannot describe the layout.
+cudaError_t launch_bwd_tc(const Params& p, cudaStream_t st, bool* launched) {
+  if (p.f16) return p.d == 64 ? launch_bwd_tc_d<64, true>(p, st, launched) : launch_bwd_tc_d<128, true>(p, st, launched);
+  return p.d == 64 ? launch_bwd_tc_d<64, false>(p, st, launched) : launch_bwd_tc_d<128, false>(p, st, launched);
 }
 
 }  // namespace mfa

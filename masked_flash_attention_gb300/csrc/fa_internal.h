@@ -108,8 +108,8 @@ cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin
 cudaError_t launch_prefill(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
 cudaError_t launch_prefill_f16(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);  // p.f16 inputs
 cudaError_t launch_backward(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
-// dQ of the backward on tcgen05; *launched = false (nothing enqueued) when a
-// tensor map cannot describe the layout
-cudaError_t launch_dq_tc(const Params& p, cudaStream_t st, bool* launched);
+// dK/dV and dQ of the backward on tcgen05; *launched = false (nothing
+// enqueued) when a tensor map cannot describe the layout
+cudaError_t launch_bwd_tc(const Params& p, cudaStream_t st, bool* launched);
 
 }  // namespace mfa

@@ -185,6 +185,13 @@ __global__ void __launch_bounds__(512, 1)
     dlt = p.delta[p.cu_q ? (int64_t)h * p.tot_q + qrow : ((int64_t)b * p.Hq + h) * p.Sq + i];
   }
   const float slope2 = p.alibi ? __ldg(p.alibi + h) * kLog2e : 0.f;
+  // the pair rules for this row as one interval of keys [jlo_i, jhi_i]
+  int jlo_i = 0, jhi_i = kv_len - 1;
+  if (i >= q_len) jhi_i = -1;
+  if (p.causal) jhi_i = min(jhi_i, i + off);
+  if (p.wl >= 0) jlo_i = max(jlo_i, i + off - p.wl);
+  if (p.wr >= 0) jhi_i = min(jhi_i, i + off + p.wr);
+  const bool plain = !(p.softcap > 0.f) && !p.alibi;  // logit = scale * s
 
   for (int t = 0; t < nkb; ++t) {
     // ---- the rows: S(t), dP(t) -> dS(t), this thread's 32 keys
@@ -201,15 +208,31 @@ __global__ void __launch_bounds__(512, 1)
       tc::tmem_ld32(lane_base + kDPCol + 32 * c, dv);
       tc::tmem_wait_ld();
       uint32_t pk[16];
+      const int jb = j0 + 32 * c;  // key of column 0 of this thread's chunk
+      if (plain) {
+        const float nl = -lse2, ds_scale = p.scale;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float ds[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int j = jb + e + u;
+            const bool in = (j >= jlo_i) & (j <= jhi_i);
+            const float pe = in ? fast_exp2(fmaf(__uint_as_float(sv[e + u]), p.scale_log2, nl)) : 0.f;
+            ds[u] = pe * (__uint_as_float(dv[e + u]) - dlt) * ds_scale;
+          }
+          pk[e >> 1] = tc_pack2<F16>(ds[0], ds[1]);
+        }
+      } else
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
         float ds[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int j = j0 + 32 * c + e + u;
+          const int j = jb + e + u;
           const float s = __uint_as_float(sv[e + u]);
           float x = -INFINITY, dxds = 0.f;
-          if (i < q_len && pair_allowed(p, i, j, off, kv_len)) {
+          if ((j >= jlo_i) & (j <= jhi_i)) {
             if (p.softcap > 0.f) {
               const float th = tc_softcap_tanh(s * p.scale, p.inv_softcap);
               x = th * (p.softcap * kLog2e);
@@ -371,6 +394,13 @@ __global__ void __launch_bounds__(512, 1)
   const int n_steps = nqb * p.G;
   const int wg = warp >> 2;                                    // query columns [32 wg, 32 wg + 32)
   const int row = 32 * (warp & 3) + (tid & 31), j = k0 + row;  // this thread's key
+  // the pair rules for this key as one interval of query rows [ilo_j, ihi_j]
+  int ilo_j = 0, ihi_j = q_len - 1;
+  if (j >= kv_len) ihi_j = -1;
+  if (p.causal) ilo_j = max(ilo_j, j - off);
+  if (p.wr >= 0) ilo_j = max(ilo_j, j - off - p.wr);
+  if (p.wl >= 0) ihi_j = min(ihi_j, j - off + p.wl);
+  const bool plain = !(p.softcap > 0.f) && !p.alibi;  // logit = scale * s
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
   uint64_t* kv_full = bars;        // K and V landed
@@ -497,31 +527,54 @@ __global__ void __launch_bounds__(512, 1)
     const float* dls = l2s + 128;
     const float a_slope = p.alibi ? __ldg(p.alibi + h) * kLog2e : 0.f;
     uint32_t pk[16], dk[16];
+    const int ib = i0 + 32 * wg;  // query row of column 0 of this thread's chunk
+    if (plain) {
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      float pv[2], ds[2];
+      for (int e4 = 0; e4 < 32; e4 += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(l2s + 32 * wg + e4);
+        const float4 d4 = *reinterpret_cast<const float4*>(dls + 32 * wg + e4);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pv[4], ds[4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int q = 32 * wg + e + u, i = i0 + q;
-        const float sc = __uint_as_float(sv[e + u]);
-        float x = -INFINITY, dxds = 0.f;
-        if (i < q_len && pair_allowed(p, i, j, off, kv_len)) {
-          if (p.softcap > 0.f) {
-            const float th = tc_softcap_tanh(sc * p.scale, p.inv_softcap);
-            x = th * (p.softcap * kLog2e);
-            dxds = p.scale * (1.f - th * th);
-          } else {
-            x = sc * p.scale_log2;
-            dxds = p.scale;
-          }
-          x -= a_slope * (float)abs(i + off - j);
+        for (int u = 0; u < 4; ++u) {
+          const int i = ib + e4 + u;
+          const bool in = (i >= ilo_j) & (i <= ihi_j);
+          const float pe = in ? fast_exp2(fmaf(__uint_as_float(sv[e4 + u]), p.scale_log2, -lv[u])) : 0.f;
+          pv[u] = pe;
+          ds[u] = pe * (__uint_as_float(dv[e4 + u]) - dl[u]) * p.scale;
         }
-        const float pe = (x == -INFINITY) ? 0.f : fast_exp2(x - l2s[q]);
-        pv[u] = pe;
-        ds[u] = pe * (__uint_as_float(dv[e + u]) - dls[q]) * dxds;
+        pk[e4 >> 1] = tc_pack2<F16>(pv[0], pv[1]);
+        pk[(e4 >> 1) + 1] = tc_pack2<F16>(pv[2], pv[3]);
+        dk[e4 >> 1] = tc_pack2<F16>(ds[0], ds[1]);
+        dk[(e4 >> 1) + 1] = tc_pack2<F16>(ds[2], ds[3]);
       }
-      pk[e >> 1] = tc_pack2<F16>(pv[0], pv[1]);
-      dk[e >> 1] = tc_pack2<F16>(ds[0], ds[1]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float pv[2], ds[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int q = 32 * wg + e + u, i = ib + e + u;
+          const float sc = __uint_as_float(sv[e + u]);
+          float x = -INFINITY, dxds = 0.f;
+          if ((i >= ilo_j) & (i <= ihi_j)) {
+            if (p.softcap > 0.f) {
+              const float th = tc_softcap_tanh(sc * p.scale, p.inv_softcap);
+              x = th * (p.softcap * kLog2e);
+              dxds = p.scale * (1.f - th * th);
+            } else {
+              x = sc * p.scale_log2;
+              dxds = p.scale;
+            }
+            x -= a_slope * (float)abs(i + off - j);
+          }
+          const float pe = (x == -INFINITY) ? 0.f : fast_exp2(x - l2s[q]);
+          pv[u] = pe;
+          ds[u] = pe * (__uint_as_float(dv[e + u]) - dls[q]) * dxds;
+        }
+        pk[e >> 1] = tc_pack2<F16>(pv[0], pv[1]);
+        dk[e >> 1] = tc_pack2<F16>(ds[0], ds[1]);
+      }
     }
     tc::tmem_st16(lane_base + 16 * wg, pk);           // P^T query columns [32 wg, +32), packed pairs
     tc::tmem_st16(lane_base + kDPCol + 16 * wg, dk);  // dS^T

@@ -106,3 +106,11 @@ def test_backward_deterministic():
     b = _run(c)
     for x, y in zip(a[1:], b[1:]):
         assert np.array_equal(x, y)
+
+
+def test_backward_broadcast_kv_layout():
+    # K/V broadcast over their heads (head stride 0)
+    c = W.random_case(1415, B=2, Sq=150, Sk=300, Hq=4, Hkv=2, d=64, causal=True)
+    k1, v1 = c["k"][:, :, :1], c["v"][:, :, :1]
+    c = dict(c, k=k1.expand(-1, -1, 2, -1), v=v1.expand(-1, -1, 2, -1))
+    check(c)

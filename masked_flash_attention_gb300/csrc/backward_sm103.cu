@@ -336,30 +336,36 @@ __global__ void __launch_bounds__(512, 1)
 
 // ---------------------------------------------------------------------------
 // dK, dV: one CTA per (sequence, K/V head, 128-key tile), over every 128-row
-// query block of the group's q-heads that can see the tile
-//   S^T = K Q^T, dP^T = V dO^T -> P^T, dS^T (thread (k, r): key r, query
-//   columns [32 k, 32 k + 32)) -> dV += P^T dO, dK += dS^T Q
-// TMEM: S^T [0, 128) then P^T in its first 64 columns, dP^T [128, 256) then
-// dS^T in its first 64, dV [256, 256 + D), dK [384, 384 + D).  A CTA barrier
-// separates the reads of S^T and dP^T from the writes over them; the next
-// block's S^T and dP^T are issued once dV and dK of this one are done.
-// Q/dO blocks in two buffers; LSE and Delta of a block's 128 query rows in two
-// shared buffers, filled a block ahead.
+// query block of the group's q-heads that can see the tile.  Each block is
+// taken in two halves of 64 query rows, h = 0, 1, so that the MMAs of one half
+// run while the rows work on the other:
+//   S^T_h = K Q_h^T, dP^T_h = V dO_h^T (N = 64) -> P^T_h, dS^T_h (thread
+//   (k, r): key r, query columns [16 k, 16 k + 16) of the half) ->
+//   dV += P^T_h dO_h, dK += dS^T_h Q_h (K = 64)
+// TMEM: S^T_h [64 h, 64 h + 64) then P^T_h over its first 32 columns, dP^T_h
+// [128 + 64 h, ...) then dS^T_h over its first 32, dV [256, 256 + D), dK
+// [384, 384 + D).  Warps 0-15 are the rows; warp 16 (one thread) issues TMA
+// copies and MMAs: dV/dK of half h as soon as its P^T/dS^T are written, then
+// S^T/dP^T of half h of the next block once those MMAs are done.  A bounded
+// CTA-wide barrier per half separates the reads of S^T_h/dP^T_h from the
+// writes over them.  Q/dO blocks in two buffers; LSE and Delta of a block's
+// query rows in two shared buffers, filled a block ahead.
 // ---------------------------------------------------------------------------
 template <int D>
 struct DkdvTcCfg {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kK = 0, kV = kTile;
-  static constexpr int kQO = 2 * kTile;       // [2 buffers][Q, dO]
+  static constexpr int kQO = 2 * kTile;          // [2 buffers][Q, dO]
   static constexpr int kStat = kQO + 4 * kTile;  // [2 buffers][lse2 128, delta 128] floats
   static constexpr int kBar = kStat + 2 * 2 * 128 * 4;
   static constexpr int kUsed = kBar + 256;
   static constexpr int kSmem = (kUsed > 116 * 1024 ? kUsed : 116 * 1024) + 1024;
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
+constexpr int kDkdvThreads = 544;  // 16 row warps + the issuer warp
 
 template <int D, bool F16>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(kDkdvThreads, 1)
     dkdv_tc_kernel(const Params p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
   using C = DkdvTcCfg<D>;
@@ -367,6 +373,7 @@ __global__ void __launch_bounds__(512, 1)
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5;
+  const bool issuer_warp = warp == 16;
   const int n_kt = (p.Sk + kTcKeys - 1) / kTcKeys;
   const int kt = (int)(blockIdx.x % n_kt);
   const int64_t r0 = blockIdx.x / n_kt;
@@ -392,8 +399,8 @@ __global__ void __launch_bounds__(512, 1)
   const int qb0 = ilo > 0 ? ilo / kTcRows : 0;
   const int nqb = ihi >= ilo ? ihi / kTcRows - qb0 + 1 : 0;
   const int n_steps = nqb * p.G;
-  const int wg = warp >> 2;                                    // query columns [32 wg, 32 wg + 32)
-  const int row = 32 * (warp & 3) + (tid & 31), j = k0 + row;  // this thread's key
+  const int wg = (warp >> 2) & 3;                              // row threads: query columns [16 wg, +16) of a half
+  const int row = 32 * (warp & 3) + (tid & 31), j = k0 + row;  // row threads: this thread's key
   // the pair rules for this key as one interval of query rows [ilo_j, ihi_j]
   int ilo_j = 0, ihi_j = q_len - 1;
   if (j >= kv_len) ihi_j = -1;
@@ -405,21 +412,22 @@ __global__ void __launch_bounds__(512, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
   uint64_t* kv_full = bars;        // K and V landed
   uint64_t* qo_full = bars + 1;    // [2] Q/dO buffer landed
-  uint64_t* s_done = bars + 3;     // S^T and dP^T of a block written
-  uint64_t* p_ready = bars + 4;    // P^T and dS^T written (512 threads)
-  uint64_t* m_done = bars + 5;     // dV and dK MMAs of a block (and all before them) done
-  uint64_t* rd_done = bars + 6;    // every thread has read S^T and dP^T of a block (512 threads)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7);
+  uint64_t* s_done = bars + 3;     // [2 halves] S^T_h and dP^T_h of a block written
+  uint64_t* rd_done = bars + 5;    // [2 halves] every row thread has read them (512)
+  uint64_t* p_ready = bars + 7;    // [2 halves] P^T_h and dS^T_h written (512)
+  uint64_t* m_done = bars + 9;     // [2 halves] dV/dK MMAs of a half (and all before them) done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* stat = reinterpret_cast<float*>(smem + C::kStat);
   if (tid == 0) {
     tc::mbar_init(kv_full, 1);
-    tc::mbar_init(qo_full, 1);
-    tc::mbar_init(qo_full + 1, 1);
-    tc::mbar_init(s_done, 1);
-    tc::mbar_init(p_ready, 512);
-    tc::mbar_init(m_done, 1);
-    tc::mbar_init(rd_done, 512);
+    for (int k = 0; k < 2; ++k) {
+      tc::mbar_init(qo_full + k, 1);
+      tc::mbar_init(s_done + k, 1);
+      tc::mbar_init(rd_done + k, 512);
+      tc::mbar_init(p_ready + k, 512);
+      tc::mbar_init(m_done + k, 1);
+    }
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -451,208 +459,221 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t tbase = *tmem_slot;
   const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp & 3)) << 16);
   constexpr uint32_t kDPCol = 128, kDVCol = 256, kDKCol = 384;
-  constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false, F16);
+  constexpr uint32_t idS = tc::idesc_bf16_f32(128, 64, false, false, F16);
   constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true, F16);
   const uint32_t sK = tc::smem_u32(smem + C::kK), sV = tc::smem_u32(smem + C::kV);
   auto qo_base = [&](int buf) { return smem + C::kQO + buf * 2 * C::kTile; };
-  auto load_qo = [&](int s) {
-    unsigned char* dst = qo_base(s & 1);
-    const int h = g * p.G + s / nqb;
-    const int row_q = q_row0 + (qb0 + s % nqb) * kTcRows;
-    tc::mbar_arrive_expect_tx(qo_full + (s & 1), 2 * C::kTile);
-    for (int c = 0; c < D / 64; ++c) {
-      tc::tma_load_4d(dst + c * 16384, &tq, qo_full + (s & 1), c * 64, h, row_q, q_b);
-      tc::tma_load_4d(dst + C::kTile + c * 16384, &tdo, qo_full + (s & 1), c * 64, h, row_q, q_b);
-    }
-  };
-  auto issue_s = [&](int s) {  // S^T(s) -> [0, 128), dP^T(s) -> [128, 256)
-    const uint32_t qa = tc::smem_u32(qo_base(s & 1)), oa = qa + C::kTile;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-      tc::mma_ss(tbase, tc::sdesc_sw128(sK + o, 16, 1024), tc::sdesc_sw128(qa + o, 16, 1024), idS, ks > 0 ? 1u : 0u);
-      tc::mma_ss(tbase + kDPCol, tc::sdesc_sw128(sV + o, 16, 1024), tc::sdesc_sw128(oa + o, 16, 1024), idS,
-                 ks > 0 ? 1u : 0u);
-    }
-    tc::mma_commit(s_done);
-  };
 
   bool ok = true;
-  if (tid == 0 && n_steps > 0) {
-    tc::tma_prefetch_desc(&tq);
-    tc::tma_prefetch_desc(&tdo);
-    tc::tma_prefetch_desc(&tk);
-    tc::tma_prefetch_desc(&tv);
-    tc::mbar_arrive_expect_tx(kv_full, 2 * C::kTile);
-    for (int c = 0; c < D / 64; ++c) {
-      tc::tma_load_4d(smem + C::kK + c * 16384, &tk, kv_full, c * 64, g, k_row0 + k0, k_b);
-      tc::tma_load_4d(smem + C::kV + c * 16384, &tv, kv_full, c * 64, g, k_row0 + k0, k_b);
-    }
-    load_qo(0);
-    if (n_steps > 1) load_qo(1);
-    ok = tc::mbar_wait(kv_full, 0, abort_flag) && tc::mbar_wait(qo_full, 0, abort_flag);
-    if (ok) {
-      tc::fence_after_sync();
-      issue_s(0);
-    } else {
-      *abort_flag = 1;
-    }
-  }
-
-  for (int s = 0; s < n_steps; ++s) {
-    const int h = g * p.G + s / nqb;
-    const int i0 = (qb0 + s % nqb) * kTcRows;
-    // ---- rows: S^T(s), dP^T(s) -> P^T(s), dS^T(s) for this thread's 32 query columns
-    if (!ok || !tc::mbar_wait(s_done, s & 1, abort_flag)) {
-      ok = false;
-      break;
-    }
-    tc::fence_after_sync();
-    uint32_t sv[32], dv[32];
-    tc::tmem_ld32(lane_base + 32 * wg, sv);
-    tc::tmem_ld32(lane_base + kDPCol + 32 * wg, dv);
-    tc::tmem_wait_ld();
-    // every thread has read S^T and dP^T before any writes over them (a
-    // bounded wait, so that an abort cannot leave threads stuck)
-    tc::fence_before_sync();
-    tc::mbar_arrive(rd_done);
-    if (!tc::mbar_wait(rd_done, s & 1, abort_flag)) {
-      ok = false;
-      break;
-    }
-    tc::fence_after_sync();
-    // every thread is past step s - 1: its LSE / Delta buffer takes step s + 1's
-    if (s + 1 < n_steps) load_stat(s + 1);
-    const float* l2s = stat + (s & 1) * 256;
-    const float* dls = l2s + 128;
-    const float a_slope = p.alibi ? __ldg(p.alibi + h) * kLog2e : 0.f;
-    uint32_t pk[16], dk[16];
-    const int ib = i0 + 32 * wg;  // query row of column 0 of this thread's chunk
-    if (plain) {
-#pragma unroll
-      for (int e4 = 0; e4 < 32; e4 += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(l2s + 32 * wg + e4);
-        const float4 d4 = *reinterpret_cast<const float4*>(dls + 32 * wg + e4);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pv[4], ds[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = ib + e4 + u;
-          const bool in = (i >= ilo_j) & (i <= ihi_j);
-          const float pe = in ? fast_exp2(fmaf(__uint_as_float(sv[e4 + u]), p.scale_log2, -lv[u])) : 0.f;
-          pv[u] = pe;
-          ds[u] = pe * (__uint_as_float(dv[e4 + u]) - dl[u]) * p.scale;
+  if (issuer_warp) {
+    // ------------------------------------------------------------ issuer
+    if ((tid & 31) == 0 && n_steps > 0) {
+      auto load_qo = [&](int s) {
+        unsigned char* dst = qo_base(s & 1);
+        const int h = g * p.G + s / nqb;
+        const int row_q = q_row0 + (qb0 + s % nqb) * kTcRows;
+        tc::mbar_arrive_expect_tx(qo_full + (s & 1), 2 * C::kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tc::tma_load_4d(dst + c * 16384, &tq, qo_full + (s & 1), c * 64, h, row_q, q_b);
+          tc::tma_load_4d(dst + C::kTile + c * 16384, &tdo, qo_full + (s & 1), c * 64, h, row_q, q_b);
         }
-        pk[e4 >> 1] = tc_pack2<F16>(pv[0], pv[1]);
-        pk[(e4 >> 1) + 1] = tc_pack2<F16>(pv[2], pv[3]);
-        dk[e4 >> 1] = tc_pack2<F16>(ds[0], ds[1]);
-        dk[(e4 >> 1) + 1] = tc_pack2<F16>(ds[2], ds[3]);
-      }
-    } else {
+      };
+      // S^T_h = K Q_h^T -> [64 h, +64), dP^T_h = V dO_h^T -> [128 + 64 h, +64)
+      auto issue_s = [&](int s, int hf) {
+        const uint32_t qa = tc::smem_u32(qo_base(s & 1)) + hf * 8192, oa = qa + C::kTile;
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        float pv[2], ds[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int q = 32 * wg + e + u, i = ib + e + u;
-          const float sc = __uint_as_float(sv[e + u]);
-          float x = -INFINITY, dxds = 0.f;
-          if ((i >= ilo_j) & (i <= ihi_j)) {
-            if (p.softcap > 0.f) {
-              const float th = tc_softcap_tanh(sc * p.scale, p.inv_softcap);
-              x = th * (p.softcap * kLog2e);
-              dxds = p.scale * (1.f - th * th);
-            } else {
-              x = sc * p.scale_log2;
-              dxds = p.scale;
-            }
-            x -= a_slope * (float)abs(i + off - j);
-          }
-          const float pe = (x == -INFINITY) ? 0.f : fast_exp2(x - l2s[q]);
-          pv[u] = pe;
-          ds[u] = pe * (__uint_as_float(dv[e + u]) - dls[q]) * dxds;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
+          tc::mma_ss(tbase + 64 * hf, tc::sdesc_sw128(sK + o, 16, 1024), tc::sdesc_sw128(qa + o, 16, 1024), idS,
+                     ks > 0 ? 1u : 0u);
+          tc::mma_ss(tbase + kDPCol + 64 * hf, tc::sdesc_sw128(sV + o, 16, 1024), tc::sdesc_sw128(oa + o, 16, 1024),
+                     idS, ks > 0 ? 1u : 0u);
         }
-        pk[e >> 1] = tc_pack2<F16>(pv[0], pv[1]);
-        dk[e >> 1] = tc_pack2<F16>(ds[0], ds[1]);
+        tc::mma_commit(s_done + hf);
+      };
+      tc::tma_prefetch_desc(&tq);
+      tc::tma_prefetch_desc(&tdo);
+      tc::tma_prefetch_desc(&tk);
+      tc::tma_prefetch_desc(&tv);
+      tc::mbar_arrive_expect_tx(kv_full, 2 * C::kTile);
+      for (int c = 0; c < D / 64; ++c) {
+        tc::tma_load_4d(smem + C::kK + c * 16384, &tk, kv_full, c * 64, g, k_row0 + k0, k_b);
+        tc::tma_load_4d(smem + C::kV + c * 16384, &tv, kv_full, c * 64, g, k_row0 + k0, k_b);
       }
-    }
-    tc::tmem_st16(lane_base + 16 * wg, pk);           // P^T query columns [32 wg, +32), packed pairs
-    tc::tmem_st16(lane_base + kDPCol + 16 * wg, dk);  // dS^T
-    tc::tmem_wait_st();
-    tc::fence_before_sync();
-    tc::mbar_arrive(p_ready);
-
-    // ---- thread 0: dV += P^T dO, dK += dS^T Q; then S^T(s + 1), dP^T(s + 1); then the copy of step s + 2
-    if (tid == 0) {
-      if (!tc::mbar_wait(p_ready, s & 1, abort_flag)) {
-        ok = false;
-      } else {
+      load_qo(0);
+      if (n_steps > 1) load_qo(1);
+      ok = tc::mbar_wait(kv_full, 0, abort_flag) && tc::mbar_wait(qo_full, 0, abort_flag);
+      if (ok) {
         tc::fence_after_sync();
+        issue_s(0, 0);
+        issue_s(0, 1);
+      }
+      for (int s = 0; ok && s < n_steps; ++s) {
         const uint32_t qa = tc::smem_u32(qo_base(s & 1)), oa = qa + C::kTile;
-#pragma unroll
-        for (int ks = 0; ks < kTcRows / 16; ++ks) {
-          tc::mma_ts(tbase + kDVCol, tbase + ks * 8, tc::sdesc_sw128(oa + ks * 2048, 16384, 1024), idO,
-                     (s > 0 || ks > 0) ? 1u : 0u);
-          tc::mma_ts(tbase + kDKCol, tbase + kDPCol + ks * 8, tc::sdesc_sw128(qa + ks * 2048, 16384, 1024), idO,
-                     (s > 0 || ks > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(m_done);
-        if (s + 1 < n_steps) {
-          // S^T and dP^T of the next block overwrite P^T and dS^T: after dV, dK
-          if (!tc::mbar_wait(m_done, s & 1, abort_flag) ||
-              !tc::mbar_wait(qo_full + ((s + 1) & 1), ((s + 1) >> 1) & 1, abort_flag)) {
+        for (int hf = 0; ok && hf < 2; ++hf) {
+          if (!tc::mbar_wait(p_ready + hf, s & 1, abort_flag)) {
             ok = false;
-          } else {
+            break;
+          }
+          tc::fence_after_sync();
+          // dV += P^T_h dO_h, dK += dS^T_h Q_h: K = the half's 64 query rows
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t acc = (s > 0 || hf > 0 || ks > 0) ? 1u : 0u;
+            const uint32_t ro = (4 * hf + ks) * 2048;
+            tc::mma_ts(tbase + kDVCol, tbase + 64 * hf + ks * 8, tc::sdesc_sw128(oa + ro, 16384, 1024), idO, acc);
+            tc::mma_ts(tbase + kDKCol, tbase + kDPCol + 64 * hf + ks * 8, tc::sdesc_sw128(qa + ro, 16384, 1024), idO,
+                       acc);
+          }
+          tc::mma_commit(m_done + hf);
+          if (s + 1 < n_steps) {
+            // the next block's S^T_h/dP^T_h overwrite P^T_h/dS^T_h: after these MMAs
+            if (!tc::mbar_wait(m_done + hf, s & 1, abort_flag) ||
+                (hf == 0 && !tc::mbar_wait(qo_full + ((s + 1) & 1), ((s + 1) >> 1) & 1, abort_flag))) {
+              ok = false;
+              break;
+            }
             tc::fence_after_sync();
-            issue_s(s + 1);
-            if (s + 2 < n_steps) load_qo(s + 2);  // into this block's buffer, free after m_done
+            issue_s(s + 1, hf);
           }
         }
+        // both halves' dV/dK MMAs are done: this block's Q/dO buffer takes block s + 2
+        if (ok && s + 2 < n_steps) load_qo(s + 2);
       }
       if (!ok) *abort_flag = 1;
     }
-  }
-  if (!ok && !*abort_flag) *abort_flag = 1;
-
-  // ---- epilogue: dK, dV rows out of TMEM (zero when no query block was seen)
-  bool have = n_steps > 0;
-  if (have && !*abort_flag) {
-    if (!tc::mbar_wait(m_done, (n_steps - 1) & 1, abort_flag)) have = false;
-  }
-  if (*abort_flag) {
-    if (tid == 0) record_error(p, FA_ERR_DEVICE_TIMEOUT, 41);
   } else {
-    const int jc = min(j, kv_len - 1);
-    uint16_t* kp = p.dk + (p.cu_k ? 0 : (int64_t)b * p.dk_sb) + ((int64_t)k_row0 + jc) * p.dk_ss + (int64_t)g * p.dk_sh;
-    uint16_t* vp = p.dv + (p.cu_k ? 0 : (int64_t)b * p.dv_sb) + ((int64_t)k_row0 + jc) * p.dv_ss + (int64_t)g * p.dv_sh;
-    tc::fence_after_sync();
-    // warpgroup k: chunks k, k + 4, ... of [dV chunks | dK chunks]
-    for (int c = wg; c < 2 * (D / 32); c += 4) {
-      const bool is_k = c >= D / 32;
-      const int cc = is_k ? c - D / 32 : c;
-      uint32_t v[32];
-      if (have) {
-        tc::tmem_ld32(lane_base + (is_k ? kDKCol : kDVCol) + 32 * cc, v);
+    // ------------------------------------------------------------ rows
+    for (int s = 0; s < n_steps; ++s) {
+      const int h = g * p.G + s / nqb;
+      const int i0 = (qb0 + s % nqb) * kTcRows;
+      const float* l2s = stat + (s & 1) * 256;
+      const float* dls = l2s + 128;
+      const float a_slope = p.alibi ? __ldg(p.alibi + h) * kLog2e : 0.f;
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!tc::mbar_wait(s_done + hf, s & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        uint32_t sv[16], dv[16];
+        tc::tmem_ld16(lane_base + 64 * hf + 16 * wg, sv);
+        tc::tmem_ld16(lane_base + kDPCol + 64 * hf + 16 * wg, dv);
         tc::tmem_wait_ld();
-      } else {
+        // every row thread has read S^T_h and dP^T_h before any writes over them
+        tc::fence_before_sync();
+        tc::mbar_arrive(rd_done + hf);
+        if (!tc::mbar_wait(rd_done + hf, s & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        // every row thread is past block s - 1: its LSE / Delta buffer takes block s + 1's
+        if (hf == 0 && s + 1 < n_steps) load_stat(s + 1);
+        const int qc = 64 * hf + 16 * wg;  // column of sv[0] within the block
+        uint32_t pk[8], dk[8];
+        if (plain) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = 0u;
+          for (int e4 = 0; e4 < 16; e4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(l2s + qc + e4);
+            const float4 d4 = *reinterpret_cast<const float4*>(dls + qc + e4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dl[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], ds[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = i0 + qc + e4 + u;
+              const bool in = (i >= ilo_j) & (i <= ihi_j);
+              const float pe = in ? fast_exp2(fmaf(__uint_as_float(sv[e4 + u]), p.scale_log2, -lv[u])) : 0.f;
+              pv[u] = pe;
+              ds[u] = pe * (__uint_as_float(dv[e4 + u]) - dl[u]) * p.scale;
+            }
+            pk[e4 >> 1] = tc_pack2<F16>(pv[0], pv[1]);
+            pk[(e4 >> 1) + 1] = tc_pack2<F16>(pv[2], pv[3]);
+            dk[e4 >> 1] = tc_pack2<F16>(ds[0], ds[1]);
+            dk[(e4 >> 1) + 1] = tc_pack2<F16>(ds[2], ds[3]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            float pv[2], ds[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int q = qc + e + u, i = i0 + q;
+              const float sc = __uint_as_float(sv[e + u]);
+              float x = -INFINITY, dxds = 0.f;
+              if ((i >= ilo_j) & (i <= ihi_j)) {
+                if (p.softcap > 0.f) {
+                  const float th = tc_softcap_tanh(sc * p.scale, p.inv_softcap);
+                  x = th * (p.softcap * kLog2e);
+                  dxds = p.scale * (1.f - th * th);
+                } else {
+                  x = sc * p.scale_log2;
+                  dxds = p.scale;
+                }
+                x -= a_slope * (float)abs(i + off - j);
+              }
+              const float pe = (x == -INFINITY) ? 0.f : fast_exp2(x - l2s[q]);
+              pv[u] = pe;
+              ds[u] = pe * (__uint_as_float(dv[e + u]) - dls[q]) * dxds;
+            }
+            pk[e >> 1] = tc_pack2<F16>(pv[0], pv[1]);
+            dk[e >> 1] = tc_pack2<F16>(ds[0], ds[1]);
+          }
+        }
+        tc::tmem_st8(lane_base + 64 * hf + 8 * wg, pk);           // P^T_h, packed pairs
+        tc::tmem_st8(lane_base + kDPCol + 64 * hf + 8 * wg, dk);  // dS^T_h
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        tc::mbar_arrive(p_ready + hf);
       }
-      if (j < kv_len) {
-        uint16_t* dst = (is_k ? kp : vp) + 32 * cc;
+      if (!ok) break;
+    }
+    if (!ok && !*abort_flag) *abort_flag = 1;
+  }
+
+  // ---- epilogue (row threads): dK, dV rows out of TMEM (zero when no query block was seen)
+  if (!issuer_warp) {
+    bool have = n_steps > 0;
+    if (have && !*abort_flag) {
+      if (!tc::mbar_wait(m_done, (n_steps - 1) & 1, abort_flag) ||
+          !tc::mbar_wait(m_done + 1, (n_steps - 1) & 1, abort_flag))
+        have = false;
+    }
+    if (*abort_flag) {
+      if (tid == 0) record_error(p, FA_ERR_DEVICE_TIMEOUT, 41);
+    } else {
+      const int jc = min(j, kv_len - 1);
+      uint16_t* kp = p.dk + (p.cu_k ? 0 : (int64_t)b * p.dk_sb) + ((int64_t)k_row0 + jc) * p.dk_ss + (int64_t)g * p.dk_sh;
+      uint16_t* vp = p.dv + (p.cu_k ? 0 : (int64_t)b * p.dv_sb) + ((int64_t)k_row0 + jc) * p.dv_ss + (int64_t)g * p.dv_sh;
+      tc::fence_after_sync();
+      // warpgroup k: chunks k, k + 4, ... of [dV chunks | dK chunks]
+      for (int c = wg; c < 2 * (D / 32); c += 4) {
+        const bool is_k = c >= D / 32;
+        const int cc = is_k ? c - D / 32 : c;
+        uint32_t v[32];
+        if (have) {
+          tc::tmem_ld32(lane_base + (is_k ? kDKCol : kDVCol) + 32 * cc, v);
+          tc::tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint4 w;
-          w.x = tc_pack2<F16>(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-          w.y = tc_pack2<F16>(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-          w.z = tc_pack2<F16>(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-          w.w = tc_pack2<F16>(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
-          *reinterpret_cast<uint4*>(dst + e) = w;
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        if (j < kv_len) {
+          uint16_t* dst = (is_k ? kp : vp) + 32 * cc;
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w;
+            w.x = tc_pack2<F16>(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            w.y = tc_pack2<F16>(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            w.z = tc_pack2<F16>(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+            w.w = tc_pack2<F16>(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+            *reinterpret_cast<uint4*>(dst + e) = w;
+          }
         }
       }
     }
-  }
-  if (*abort_flag && tid == 0) {
+  } else if (*abort_flag && (tid & 31) == 0) {
+    // let the copies and MMAs already issued finish before the CTA leaves
     tc::mma_commit(m_done);
     tc::mbar_wait_drain(m_done, n_steps & 1, 100000000ull);
     tc::mbar_wait_drain(kv_full, 0, 100000000ull);
@@ -690,7 +711,7 @@ cudaError_t launch_bwd_tc_d(const Params& p, cudaStream_t st, bool* launched) {
   if ((e = ensure_smem_attr<dkdv_tc_kernel<D, F16>>(DkdvTcCfg<D>::kSmem)) != cudaSuccess) return e;
   const int64_t n_kt = (p.Sk + kTcKeys - 1) / kTcKeys;
   const int64_t g1 = (int64_t)p.n_seq * p.Hkv * n_kt;
-  if (g1 > 0) dkdv_tc_kernel<D, F16><<<(unsigned)g1, 512, DkdvTcCfg<D>::kSmem, st>>>(p, mq, mdo, mk, mv);
+  if (g1 > 0) dkdv_tc_kernel<D, F16><<<(unsigned)g1, kDkdvThreads, DkdvTcCfg<D>::kSmem, st>>>(p, mq, mdo, mk, mv);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t n_qt = (p.Sq + kTcRows - 1) / kTcRows;
   const int64_t grid = (int64_t)p.n_seq * p.Hq * n_qt;

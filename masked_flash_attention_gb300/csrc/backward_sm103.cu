@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(512, 1)
 
   for (int t = 0; t < nkb; ++t) {
     // ---- the rows: S(t), dP(t) -> dS(t), this thread's 32 keys
-    if (!ok || !tc::mbar_wait(s_done, t & 1, abort_flag)) {
+    if (!ok || !tc::mbar_wait_spin(s_done, t & 1, abort_flag)) {
       ok = false;
       break;
     }
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(512, 1)
 
     // ---- thread 0: dQ(t) += dS(t) K(t); then S(t+1), dP(t+1); then the copy of tile t + 2
     if (tid == 0) {
-      if (!tc::mbar_wait(ds_ready, t & 1, abort_flag)) {
+      if (!tc::mbar_wait_spin(ds_ready, t & 1, abort_flag)) {
         ok = false;
       } else {
         tc::fence_after_sync();
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(512, 1)
                      (t > 0 || ks > 0) ? 1u : 0u);
         tc::mma_commit(q_done);
         if (t + 1 < nkb) {
-          if (!tc::mbar_wait(kv_full + ((t + 1) & 1), ((t + 1) >> 1) & 1, abort_flag)) {
+          if (!tc::mbar_wait_spin(kv_full + ((t + 1) & 1), ((t + 1) >> 1) & 1, abort_flag)) {
             ok = false;
           } else {
             tc::fence_after_sync();
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         if (ok && t + 2 < nkb) {
           // tile t's buffer is free once dQ(t) (and everything before it) is done
-          if (!tc::mbar_wait(q_done, t & 1, abort_flag)) ok = false;
+          if (!tc::mbar_wait_spin(q_done, t & 1, abort_flag)) ok = false;
           else load_kv(t + 2);
         }
       }
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(512, 1)
   // ---- epilogue: dQ rows out of TMEM (zero when no key tile was seen)
   bool have = nkb > 0;
   if (have && !*abort_flag) {
-    if (!tc::mbar_wait(q_done, (nkb - 1) & 1, abort_flag)) have = false;
+    if (!tc::mbar_wait_spin(q_done, (nkb - 1) & 1, abort_flag)) have = false;
   }
   if (*abort_flag) {
     if (tid == 0) record_error(p, FA_ERR_DEVICE_TIMEOUT, 40);
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       for (int s = 0; ok && s < n_steps; ++s) {
         const uint32_t qa = tc::smem_u32(qo_base(s & 1)), oa = qa + C::kTile;
         for (int hf = 0; ok && hf < 2; ++hf) {
-          if (!tc::mbar_wait(p_ready + hf, s & 1, abort_flag)) {
+          if (!tc::mbar_wait_spin(p_ready + hf, s & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -528,8 +528,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
           tc::mma_commit(m_done + hf);
           if (s + 1 < n_steps) {
             // the next block's S^T_h/dP^T_h overwrite P^T_h/dS^T_h: after these MMAs
-            if (!tc::mbar_wait(m_done + hf, s & 1, abort_flag) ||
-                (hf == 0 && !tc::mbar_wait(qo_full + ((s + 1) & 1), ((s + 1) >> 1) & 1, abort_flag))) {
+            if (!tc::mbar_wait_spin(m_done + hf, s & 1, abort_flag) ||
+                (hf == 0 && !tc::mbar_wait_spin(qo_full + ((s + 1) & 1), ((s + 1) >> 1) & 1, abort_flag))) {
               ok = false;
               break;
             }
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
       const float* dls = l2s + 128;
       const float a_slope = p.alibi ? __ldg(p.alibi + h) * kLog2e : 0.f;
       for (int hf = 0; hf < 2; ++hf) {
-        if (!tc::mbar_wait(s_done + hf, s & 1, abort_flag)) {
+        if (!tc::mbar_wait_spin(s_done + hf, s & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
         // every row thread has read S^T_h and dP^T_h before any writes over them
         tc::fence_before_sync();
         tc::mbar_arrive(rd_done + hf);
-        if (!tc::mbar_wait(rd_done + hf, s & 1, abort_flag)) {
+        if (!tc::mbar_wait_spin(rd_done + hf, s & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -635,8 +635,8 @@ __global__ void __launch_bounds__(kDkdvThreads, 1)
   if (!issuer_warp) {
     bool have = n_steps > 0;
     if (have && !*abort_flag) {
-      if (!tc::mbar_wait(m_done, (n_steps - 1) & 1, abort_flag) ||
-          !tc::mbar_wait(m_done + 1, (n_steps - 1) & 1, abort_flag))
+      if (!tc::mbar_wait_spin(m_done, (n_steps - 1) & 1, abort_flag) ||
+          !tc::mbar_wait_spin(m_done + 1, (n_steps - 1) & 1, abort_flag))
         have = false;
     }
     if (*abort_flag) {

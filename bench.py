@@ -57,9 +57,9 @@ KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_dev
 # time: once the kernel changes the figure no longer applies and is reported
 # as null.
 MEASURED_TRAFFIC = {
-    ("causal_prefill_past_kv", "prefill_kernel"): ("730d1135f4de5d0e", 108879104),
-    ("paged_varlen_decode", "decode_kernel"): ("5297f26e60532d02", 761683712),
-    ("paged_decode_append", "decode_kernel"): ("5297f26e60532d02", 760071680),
+    ("causal_prefill_past_kv", "prefill_kernel"): ("db2516573b2872b7", 109785344),
+    ("paged_varlen_decode", "decode_kernel"): ("3c3a08fb3ca10ae0", 761721344),
+    ("paged_decode_append", "decode_kernel"): ("3c3a08fb3ca10ae0", 760100096),
 }
 
 

@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int pg;
     const int kj0 = chunk_key0(k, partial, live, pg);
     if (!live) return;
-    if (TMA && KV2 && kj0 + kChunkKeys > geo.lc) return;  // active rows: filled by the warp
+    if (TMA && KV2 && kj0 >= geo.lc) return;  // active rows only: filled by the warp
     if (TMA) {
       if (lane == 0) {
         const int st = k % kWarpStages;
@@ -422,12 +422,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   };
 
-  // TMA mode, two-source form: a chunk that holds active rows is copied by
-  // the warp itself when its turn comes: cached rows from the cache, active
-  // rows from k_new / v_new, rows past the keys as zeros.
-  auto fill_chunk = [&](int k, int kj0) {
+  // TMA mode, two-source form: rows [r0, 16) of a chunk that holds active
+  // rows are written by the warp itself when its turn comes: active rows from
+  // k_new / v_new, rows past the keys as zeros (r0 = 0 for a chunk of active
+  // rows only; for a chunk that starts in the cache the TMA copy brought the
+  // cached rows, and r0 is the first active row).
+  auto fill_chunk = [&](int k, int kj0, int r0) {
     const uint32_t sK = sW + (k % kWarpStages) * S::kStageBytes;
-    for (int idx = lane; idx < kChunkKeys * S::kChunks; idx += 32) {
+    for (int idx = lane + r0 * S::kChunks; idx < kChunkKeys * S::kChunks; idx += 32) {
       const int r = idx / S::kChunks, c = idx % S::kChunks;
       const int j = kj0 + r;
       uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
@@ -494,15 +496,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!live) continue;
     if (TMA) {
       const int st = k % kWarpStages;
-      if (KV2 && kj0 + kChunkKeys > geo.lc) {
-        fill_chunk(k, kj0);  // no copy was issued for this stage: its barrier phase is unchanged
+      if (KV2 && kj0 >= geo.lc) {
+        fill_chunk(k, kj0, 0);  // no copy was issued for this stage: its barrier phase is unchanged
       } else {
         if (!tc::mbar_wait(kv_full + st, (kv_phase >> st) & 1, abort_flag)) {
           ok = false;
           break;
         }
         kv_phase ^= 1u << st;
-        if (kj0 + kChunkKeys > geo.kv_len) {
+        if (KV2 && kj0 + kChunkKeys > geo.lc) {
+          fill_chunk(k, kj0, geo.lc - kj0);  // the active rows over the copied cache rows
+        } else if (kj0 + kChunkKeys > geo.kv_len) {
           // a sequence's last chunk: the box also brought the page's unused
           // rows, which may hold anything (and P = 0 times a NaN is a NaN):
           // zero those V rows

@@ -114,3 +114,20 @@ def test_backward_broadcast_kv_layout():
     k1, v1 = c["k"][:, :, :1], c["v"][:, :, :1]
     c = dict(c, k=k1.expand(-1, -1, 2, -1), v=v1.expand(-1, -1, 2, -1))
     check(c)
+
+
+def test_backward_varlen_with_empty_sequences():
+    # sequences without query rows, without keys, and ordinary ones
+    g = torch.Generator().manual_seed(1416)
+    lq = torch.tensor([0, 37, 130, 5, 0])
+    lk = torch.tensor([40, 0, 260, 5, 0])
+    cu_q = torch.zeros(6, dtype=torch.int32)
+    cu_k = torch.zeros(6, dtype=torch.int32)
+    cu_q[1:] = torch.cumsum(lq, 0)
+    cu_k[1:] = torch.cumsum(lk, 0)
+    q = torch.randn(int(cu_q[-1]), 4, 128, generator=g).to(torch.bfloat16)
+    k = torch.randn(int(cu_k[-1]), 2, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(int(cu_k[-1]), 2, 128, generator=g).to(torch.bfloat16)
+    params = W.base_params(scale=128 ** -0.5, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=130,
+                           max_seqlen_k=260, causal=True)
+    check(dict(name="bwd_varlen_empty", q=q, k=k, v=v, params=params))

@@ -200,3 +200,17 @@ def test_paged_decode_ignores_stale_page_rows():
     out, lse, _ = run_gpu(c2)
     ro, rl = run_oracle(c)
     compare(out, lse, ro, rl, "stale_rows")
+
+
+def test_kvcache_sequences_without_new_tokens():
+    # packed q with zero-length sequences: nothing is read from or appended for them
+    c = _case(125, 5, 300, 8, 2, 128, page=16, q_max=3)
+    lens = torch.tensor([2, 0, 3, 0, 1], dtype=torch.int32)
+    cu = torch.zeros(6, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0)
+    n = int(cu[-1])
+    c["q"], c["k_new"], c["v_new"] = c["q"][:n], c["k_new"][:n], c["v_new"][:n]
+    c["cu_q"] = cu
+    c["max_q"] = 3
+    c["max_k"] = int((c["cache_lens"].long() + lens.long()).max())
+    _check_append(c, *_check(c, "kvcache_no_new_tokens", append=True, causal=True))

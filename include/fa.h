@@ -92,7 +92,9 @@ typedef enum {
   FA_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, tensor-map encode) */
   FA_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait gave up (reported by fa_check_device_error) */
   FA_ERR_DEVICE_BOUNDS = 6,  /* a kernel met an out-of-range index, e.g. a page (ditto) */
-  FA_ERR_NO_DEVICE = 7       /* no usable sm_103 device is current */
+  FA_ERR_NO_DEVICE = 7,      /* no usable sm_103 device is current */
+  FA_ERR_DEVICE_VALUE = 8    /* FA_DEBUG_VALIDATE found a mask value the call does not take (reported
+                              * by fa_check_device_error; info = the mask tile or top-k bucket) */
 } fa_status;
 
 typedef enum { FA_DTYPE_BF16 = 1, FA_DTYPE_F32 = 2, FA_DTYPE_I32 = 3, FA_DTYPE_F16 = 4 } fa_dtype;
@@ -124,6 +126,8 @@ typedef struct {
 
 /* Debug flags (opts->debug_flags). */
 #define FA_DEBUG_NO_SKIP 0x1u /* schedule EMPTY tiles too (as PARTIAL): exercises the -inf guard */
+#define FA_DEBUG_VALIDATE 0x4u /* check mask values on the device: a dense mask must be finite or -inf,
+                                * top-k scores finite (FA_ERR_DEVICE_VALUE otherwise); off by default */
 
 typedef struct {
   void* stream;            /* cudaStream_t to enqueue on; NULL = legacy default stream */

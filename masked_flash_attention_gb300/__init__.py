@@ -7,6 +7,7 @@ package is its thin Python binding.  Build the library with
 from ._lib import (  # noqa: F401
     EXPORTS,
     FA_DEBUG_NO_SKIP,
+    FA_DEBUG_VALIDATE,
     FA_OK,
     FaError,
     alloc_workspace,

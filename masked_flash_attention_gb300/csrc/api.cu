@@ -447,6 +447,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "CUDA runtime error";
     case FA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case FA_ERR_DEVICE_BOUNDS: return "device index out of range";
+    case FA_ERR_DEVICE_VALUE: return "mask value not accepted (NaN, +inf, or a non-finite top-k score)";
     case FA_ERR_NO_DEVICE: return "no sm_103 device";
     default: return "unknown status";
   }

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) mask_summary_kernel(const Params p) {
   const int kj0 = kt * kKeysPerTile;
   const int kj1 = min(kj0 + kKeysPerTile, p.Sk) - 1;
   const int nr = i1 - i0 + 1, nk = kj1 - kj0 + 1;
-  bool any_nonneg = false, any_nonzero = false;
+  bool any_nonneg = false, any_nonzero = false, any_bad = false;
   if (nr > 0 && nk > 0) {
     const float* base = p.mask + (int64_t)mb * p.m_sb + (int64_t)mh * p.m_sh;
     for (int e = threadIdx.x; e < nr * nk; e += blockDim.x) {
@@ -35,10 +35,13 @@ __global__ void __launch_bounds__(256) mask_summary_kernel(const Params p) {
       float m = __ldg(base + (int64_t)r * p.m_sq + (int64_t)j * p.m_sk);
       any_nonneg |= (m != -INFINITY);
       any_nonzero |= (m != 0.f);
+      any_bad |= !(m < INFINITY);  // NaN or +inf
     }
   }
   int nonneg = __syncthreads_or(any_nonneg);
   int nonzero = __syncthreads_or(any_nonzero);
+  if ((p.debug_flags & FA_DEBUG_VALIDATE) && __syncthreads_or(any_bad) && threadIdx.x == 0)
+    record_error(p, FA_ERR_DEVICE_VALUE, (uint32_t)blk);
   if (threadIdx.x == 0) {
     uint8_t cls = !nonneg ? kMaskEmpty : (!nonzero ? kMaskZero : kMaskMixed);
     p.mask_summary[blk] = cls;
@@ -99,7 +102,9 @@ __global__ void __launch_bounds__(256) topk_bucket_sort_kernel(const Params p) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int j = c * kKeysPerTile + 4 * lane + k;
-    v[k] = j < n ? (((uint64_t)ordered_desc(__ldg(z + (int64_t)j * p.z_sk)) << 32) | (uint32_t)j) : ~0ull;
+    const float zj = j < n ? __ldg(z + (int64_t)j * p.z_sk) : 0.f;
+    if ((p.debug_flags & FA_DEBUG_VALIDATE) && !isfinite(zj)) record_error(p, FA_ERR_DEVICE_VALUE, (uint32_t)c);
+    v[k] = j < n ? (((uint64_t)ordered_desc(zj) << 32) | (uint32_t)j) : ~0ull;
   }
 #pragma unroll
   for (int size = 2; size <= 128; size <<= 1) {

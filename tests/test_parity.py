@@ -384,3 +384,38 @@ def test_alibi_slopes_checked():
     q = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(fa.FaError):
         fa._lib._alibi(torch.zeros(3), q)  # wrong length (and not on a device)
+
+
+# ---------------------------------------------------------------------------
+# FA_DEBUG_VALIDATE: mask values checked on the device
+# ---------------------------------------------------------------------------
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")])
+def test_validate_dense_mask_values(bad):
+    import masked_flash_attention_gb300 as fa
+    c = W.random_case(920, B=1, Sq=200, Sk=300, Hq=2, Hkv=2, d=64, causal=False)
+    m = W.random_dense_mask(920, 200, 300)
+    m[150, 77] = bad
+    p = to_dev(dict(c["params"], mask=m))
+    q, k, v = c["q"].to(DEV), c["k"].to(DEV), c["v"].to(DEV)
+    _, _, ws = fa.fa_fwd(q, k, v, debug_flags=fa.FA_DEBUG_VALIDATE, **p)
+    rc, info = fa.fa_check_device_error(ws)
+    assert rc == fa._lib.FA_ERR_DEVICE_VALUE
+    # -inf and finite values pass; without the flag nothing is checked
+    m2 = W.random_dense_mask(920, 200, 300)
+    _, _, ws = fa.fa_fwd(q, k, v, debug_flags=fa.FA_DEBUG_VALIDATE, **to_dev(dict(c["params"], mask=m2)))
+    assert fa.fa_check_device_error(ws)[0] == 0
+    _, _, ws = fa.fa_fwd(q, k, v, **p)
+    assert fa.fa_check_device_error(ws)[0] == 0
+
+
+@pytest.mark.gpu
+def test_validate_topk_scores():
+    import masked_flash_attention_gb300 as fa
+    c = W.random_case(921, B=1, Sq=256, Sk=256, Hq=2, Hkv=2, d=64, causal=True)
+    z = W.random_zero_hold_states(921, 1, 2, 256)
+    z[0, 1, 40] = float("nan")
+    p = to_dev(dict(c["params"], zero_hold_states=z, keep_window=32))
+    _, _, ws = fa.fa_fwd(c["q"].to(DEV), c["k"].to(DEV), c["v"].to(DEV), debug_flags=fa.FA_DEBUG_VALIDATE, **p)
+    assert fa.fa_check_device_error(ws)[0] == fa._lib.FA_ERR_DEVICE_VALUE

@@ -239,12 +239,34 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def _dist():
+    """torch.distributed when launched with WORLD_SIZE > 1: NCCL between GPUs,
+    gloo on a host without one (where the multi-rank host logic is tested)."""
     if int(os.environ.get("WORLD_SIZE", "1")) > 1:
         import torch.distributed as dist
         if not dist.is_initialized():
-            dist.init_process_group("nccl")
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         return dist
     return None
+
+
+def max_over_ranks(dist, x, device="cpu"):
+    """The slowest rank's figure: each rank times its own replica."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_case(args, rank):
+    """Rank ``rank``'s replica: the workload's shapes drawn from its own seed.
+    Ranks share no data, so the step needs no collective."""
+    return _as_dtype(W.WORKLOADS[args.workload](seed=args.seed + rank), args.dtype)
+
+
+def job_value(metric_units, world, ms_per_step):
+    """Whole-job throughput: each of ``world`` ranks runs one replica per step."""
+    return metric_units * world / (ms_per_step / 1e3)
 
 
 def run_gpu(args):
@@ -256,7 +278,7 @@ def run_gpu(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    case = _as_dtype(W.WORKLOADS[args.workload](seed=args.seed + rank), args.dtype)
+    case = replica_case(args, rank)
     units = workload_units(case, args.workload)
     bwd = args.pass_ == "bwd"
     if bwd:
@@ -338,13 +360,11 @@ def run_gpu(args):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     total_ms = sum(step_ms)
+    total_ms = max_over_ranks(dist, total_ms, dev)
     if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
         dist.barrier()
     ms_per_step = total_ms / args.steps
-    value = units["metric_units"] * world / (ms_per_step / 1e3)
+    value = job_value(units["metric_units"], world, ms_per_step)
 
     # ---- end to end: pinned host inputs in, outputs back, same public call ----
     hq, hk, hv = (case["q"].pin_memory(), case["k"].pin_memory(), case["v"].pin_memory())
@@ -393,11 +413,8 @@ def run_gpu(args):
         torch.cuda.synchronize()
         e2e_ms.append(a.elapsed_time(b))
     e2e_total = sum(e2e_ms)
-    if dist:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = units["metric_units"] * world / (e2e_total / args.steps / 1e3)
+    e2e_total = max_over_ranks(dist, e2e_total, dev)
+    e2e_value = job_value(units["metric_units"], world, e2e_total / args.steps)
     rc_, info = fa.fa_check_device_error(ws)
     assert rc_ == 0, (rc_, info)
 

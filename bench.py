@@ -57,7 +57,7 @@ KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_dev
 # time: once the kernel changes the figure no longer applies and is reported
 # as null.
 MEASURED_TRAFFIC = {
-    ("causal_prefill_past_kv", "prefill_kernel"): ("db2516573b2872b7", 109785344),
+    ("causal_prefill_past_kv", "prefill_kernel"): ("5368a2381db92a05", 109785344),
     ("paged_varlen_decode", "decode_kernel"): ("4dc990c24adb4906", 761226752),
     ("paged_decode_append", "decode_kernel"): ("4dc990c24adb4906", 761924096),
 }

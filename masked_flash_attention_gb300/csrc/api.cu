@@ -7,6 +7,7 @@
 // unsupported feature must report an error, and a wrong dtype must be caught
 // at the entry).  No path here falls back to anything: an argument the kernels
 // cannot take is an error code.
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -372,20 +373,22 @@ void bind_workspace(Plan* pl, void* ws) {
 
 // The device must be an sm_103 part (checked once per device).
 int check_device() {
-  static int cached[64];  // 0 unknown, 1 ok, 2 bad
+  static std::atomic<int> cached[64];  // 0 unknown, 1 ok, 2 bad
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_NO_DEVICE;
   if (dev < 0 || dev >= 64) return FA_ERR_NO_DEVICE;
-  if (cached[dev] == 0) {
+  int c = cached[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
       cudaGetLastError();
       return FA_ERR_NO_DEVICE;
     }
-    cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    c = (major == 10 && minor == 3) ? 1 : 2;
+    cached[dev].store(c, std::memory_order_relaxed);
   }
-  return cached[dev] == 1 ? FA_OK : FA_ERR_NO_DEVICE;
+  return c == 1 ? FA_OK : FA_ERR_NO_DEVICE;
 }
 
 

@@ -45,6 +45,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstring>
 #include <mutex>
@@ -732,17 +733,20 @@ bool encode_out(CUtensorMap* m, void* base, int d, int heads, int64_t rows, int 
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, f16);
 }
 
+// SM count of the current device (cached per device; safe to call from
+// several host threads).
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
-      n = 1;
+  static std::atomic<int> cached[64];
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  const int n = cached[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+    cudaGetLastError();
+    return 1;
   }
-  return n;
+  cached[dev].store(v, std::memory_order_relaxed);
+  return v;
 }
 
 template <int D, int MK, bool SC, bool AL, bool F16>
@@ -751,12 +755,14 @@ cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap
                              cudaEvent_t ev_begin) {
   // setmaxnreg.inc would wait forever if the block were launched with fewer
   // registers than the split assumes: launch only when the build matches.
-  static int regs = -1;
+  static std::atomic<int> launch_regs{-1};
+  int regs = launch_regs.load(std::memory_order_relaxed);
   if (regs < 0) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MK, SC, AL, F16>);
     if (e != cudaSuccess) return e;
     regs = fa.numRegs;
+    launch_regs.store(regs, std::memory_order_relaxed);
   }
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL, F16>>(PCfg<D>::kSmem);

@@ -17,6 +17,9 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmfa_gb300.so")
 
+# FA_ABI_VERSION of include/fa.h that the structures below describe
+ABI_VERSION = 5
+
 FA_OK = 0
 FA_ERR_INVALID_ARG = 1
 FA_ERR_UNSUPPORTED = 2
@@ -116,6 +119,10 @@ def _load():
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_abi_version.argtypes = []
     lib.fa_abi_version.restype = ctypes.c_int
+    # a library built from other headers would read these structures wrongly
+    if lib.fa_abi_version() != ABI_VERSION:
+        raise ImportError(f"{LIB_PATH} has ABI {lib.fa_abi_version()}, this binding describes ABI {ABI_VERSION}: "
+                          "rebuild it with `python -c 'import __graft_entry__ as g; g.build()'`")
     return lib
 
 

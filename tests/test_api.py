@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(fa.lib, n), n
         assert ctypes.cast(getattr(fa.lib, n), ctypes.c_void_p).value
-    assert fa.fa_abi_version() == 5
+    assert fa.fa_abi_version() == 5 == _lib.ABI_VERSION
     assert fa.fa_status_string(0) == "ok"
 
 
@@ -172,3 +172,8 @@ def test_bwd_plan_rules():
     assert fa.fa_bwd_plan(q, k, k, q, lse, q.half(), causal=True)[0] == E             # dout dtype
     assert fa.fa_bwd_plan(q, k, k, q, lse, q, dk=T(2, 7, 4, 64))[0] == E             # dk heads
     assert fa.fa_bwd_plan(q, k, k, q, lse, q, dq=T(2, 5, 4, 64)[..., ::2])[0] == E   # dq head-dim stride
+
+
+def test_binding_abi_matches_header():
+    txt = open(os.path.join(ROOT, "include", "fa.h")).read()
+    assert int(re.search(r"#define FA_ABI_VERSION (\d+)", txt).group(1)) == _lib.ABI_VERSION

@@ -122,10 +122,25 @@ def useful_pairs(case):
         if p["zero_hold_states"] is not None:
             cnt = np.minimum(cnt, p["keep_window"])
         total += int(cnt.sum()) * Hq
-    if p["mask"] is not None:  # dense mask: count finite entries over allowed pairs
-        m = p["mask"]
-        total = int(torch.isfinite(m).sum().item()) * (q.shape[0] if m.dim() == 2 else 1) * \
-            (Hq if m.dim() == 2 else 1)
+    if p["mask"] is not None:  # dense mask: its finite entries among the allowed pairs
+        fin = torch.isfinite(p["mask"]).numpy()
+        if fin.ndim == 2:
+            fin = fin[None, None]
+        total = 0
+        for b, (Sq, Sk) in enumerate(lens):
+            i = np.arange(Sq, dtype=np.int64)[:, None]
+            j = np.arange(Sk, dtype=np.int64)[None, :]
+            off = Sk - Sq
+            ok = np.ones((Sq, Sk), dtype=bool)
+            if p["causal"]:
+                ok &= j <= i + off
+            if p["window_left"] >= 0:
+                ok &= j >= i + off - p["window_left"]
+            if p["window_right"] >= 0:
+                ok &= j <= i + off + p["window_right"]
+            for h in range(Hq):
+                mb = fin[b if fin.shape[0] > 1 else 0, h if fin.shape[1] > 1 else 0, :Sq, :Sk]
+                total += int((mb & ok).sum())
     return total
 
 

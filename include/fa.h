@@ -87,7 +87,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,    /* bad dtype, shape, stride, alignment, Hq % Hkv, d, window, ... */
-  FA_ERR_UNSUPPORTED = 2,    /* a valid combination this build does not implement */
+  FA_ERR_UNSUPPORTED = 2,    /* a valid combination the library does not implement */
   FA_ERR_WORKSPACE = 3,      /* workspace missing, too small or not 256-byte aligned */
   FA_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, tensor-map encode) */
   FA_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait gave up (reported by fa_check_device_error) */

@@ -326,14 +326,20 @@ int fa_bwd_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, cons
  *   - A problem whose scratch need (fa_fwd_workspace_size) exceeds
  *     FA_NOALLOC_SCRATCH_BYTES is rejected with FA_ERR_WORKSPACE.
  *   - The first call on a device looks up the array's device address (a
- *     one-time set-up per device, done with that device current); make that
- *     first call before any stream capture.
+ *     one-time set-up per device, done with that device current, and done
+ *     again only if the device's context was destroyed and re-created, e.g.
+ *     after cudaDeviceReset); make that first call before any stream capture.
  *   - All calls share the array: calls that overlap on the GPU (other
  *     streams, other threads) race on it; serialise them.
  *   - Each call clears the array's device error word before its kernels run,
- *     so faults recorded by the kernels (a bad page index, inconsistent
- *     sequence lengths) are not reported to the caller; use fa_fwd with a
- *     workspace and fa_check_device_error when that matters. */
+ *     and the word cannot be read back, so nothing the kernels record there
+ *     reaches the caller: a bad page index or inconsistent sequence lengths
+ *     (FA_ERR_DEVICE_BOUNDS) and a bounded wait that gave up
+ *     (FA_ERR_DEVICE_TIMEOUT) still return FA_OK, with `out` not valid.  Use
+ *     fa_fwd with a workspace and fa_check_device_error when that matters.
+ *   - For the same reason opts->debug_flags with FA_DEBUG_VALIDATE (whose
+ *     only result is FA_ERR_DEVICE_VALUE in that word) is refused with
+ *     FA_ERR_UNSUPPORTED. */
 int fa_fwd_noalloc(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
                    const fa_tensor* out, const fa_tensor* lse,
                    const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,

@@ -90,7 +90,8 @@ _BWD_ARGS = [_P(fa_tensor)] * 11 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_flo
                                     ctypes.c_int32, _P(fa_opts)]
 
 EXPORTS = ("fa_fwd", "fa_fwd_plan", "fa_fwd_workspace_size", "fa_fwd_kvcache", "fa_fwd_kvcache_plan",
-           "fa_bwd", "fa_bwd_plan", "fa_check_device_error", "fa_status_string", "fa_abi_version")
+           "fa_bwd", "fa_bwd_plan", "fa_fwd_noalloc", "fa_check_device_error", "fa_status_string",
+           "fa_abi_version")
 
 
 def _load():
@@ -99,6 +100,10 @@ def _load():
             f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
             "(there is no CPU fallback)")
     lib = ctypes.CDLL(LIB_PATH)
+    missing = [name for name in EXPORTS if not hasattr(lib, name)]
+    if missing:
+        raise ImportError(f"{LIB_PATH} lacks {', '.join(missing)}: rebuild it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
     lib.fa_fwd.argtypes = _ARGS
     lib.fa_fwd.restype = ctypes.c_int
     lib.fa_fwd_plan.argtypes = _ARGS + [_P(fa_plan)]
@@ -113,6 +118,8 @@ def _load():
     lib.fa_bwd.restype = ctypes.c_int
     lib.fa_bwd_plan.argtypes = _BWD_ARGS + [_P(fa_plan)]
     lib.fa_bwd_plan.restype = ctypes.c_int
+    lib.fa_fwd_noalloc.argtypes = _ARGS
+    lib.fa_fwd_noalloc.restype = ctypes.c_int
     lib.fa_check_device_error.argtypes = [ctypes.c_void_p, ctypes.c_void_p, _P(ctypes.c_uint32)]
     lib.fa_check_device_error.restype = ctypes.c_int
     lib.fa_status_string.argtypes = [ctypes.c_int]
@@ -409,15 +416,17 @@ def fa_check_device_error(workspace, stream=None):
 def fa_fwd_noalloc(q, k, v, *, out, lse, cu_seqlens_q=None, cu_seqlens_k=None, block_table=None,
                    mask=None, zero_hold_states=None, keep_window=0, window_left=-1, window_right=-1,
                    softcap=0.0, scale=None, causal=False, max_seqlen_q=None, max_seqlen_k=None,
-                   stream=None, debug_flags=0, alibi_slopes=None, **_):
+                   stream=None, debug_flags=0, alibi_slopes=None, workspace=None, event_begin=None,
+                   event_end=None):
     """fa_fwd_noalloc of the C ABI: the forward pass for callers that may not
     allocate device memory.  ``out`` and ``lse`` are caller-provided; the
     library's static device scratch replaces the workspace, so nothing is
-    allocated by this call.  Raises FaError on a non-zero status (a problem
-    too large for the static scratch gives FA_ERR_WORKSPACE)."""
+    allocated by this call.  A workspace or timing events cannot be used here
+    and are refused rather than ignored.  Raises FaError on a non-zero status
+    (a problem too large for the static scratch gives FA_ERR_WORKSPACE)."""
+    if workspace is not None or event_begin is not None or event_end is not None:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_fwd_noalloc (takes no workspace and no timing events)")
     fn = lib.fa_fwd_noalloc
-    fn.argtypes = _ARGS
-    fn.restype = ctypes.c_int
     alibi_slopes = _alibi(alibi_slopes, q)
     opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                      debug_flags=debug_flags, alibi_slopes=alibi_slopes)

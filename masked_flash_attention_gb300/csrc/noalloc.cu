@@ -14,6 +14,7 @@
 // is larger are rejected with FA_ERR_WORKSPACE; all calls share the array, so
 // calls that overlap on the GPU (different streams, different threads) race
 // on it and must be serialised by the caller.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -29,24 +30,78 @@ constexpr size_t kNoAllocScratchBytes = FA_NOALLOC_SCRATCH_BYTES;
 // cudaGetSymbolAddress, per device, below.
 static __device__ __align__(256) unsigned char g_scratch[kNoAllocScratchBytes];
 
+// Driver calls reached through the runtime's entry-point query (no link
+// against libcuda): the current context and its process-unique ID.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct CtxFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const CtxFns& ctx_fns() {
+  static CtxFns f;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess) {
+      f.get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+      f.get_id = reinterpret_cast<CtxGetIdFn>(b);
+    }
+    cudaGetLastError();
+  });
+  return f;
+}
+
 constexpr int kMaxDevices = 64;
-void* g_scratch_dev[kMaxDevices];  // device address of g_scratch, per device
+// Device address of g_scratch per device, with the ID of the context it was
+// looked up in.  The module (and so the array) is loaded again, possibly at
+// another address, when a device's primary context is destroyed and created
+// anew (cudaDeviceReset, or releasing the primary context), so the address is
+// only reused while the current context is the same one.
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;  // 0: not looked up yet
+  void* addr = nullptr;
+};
+ScratchSlot g_slots[kMaxDevices];
 std::mutex g_setup_mutex;
 
-// One-time set-up per device (with that device current): look up the device
-// address of the static scratch.  Returns nullptr on failure.
+// Device address of the static scratch for the current context of device
+// `dev` (set-up once per device and context, with that device current).
+// Returns nullptr on failure.
 void* scratch_address(int dev) {
+  const CtxFns& f = ctx_fns();
+  if (!f.get_current || !f.get_id) return nullptr;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_dev[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    g_scratch_dev[dev] = p;
+  ScratchSlot& s = g_slots[dev];
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  const bool have_ctx = f.get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr;
+  if (have_ctx && f.get_id(ctx, &id) == CUDA_SUCCESS && id != 0 && id == s.ctx_id && s.addr) return s.addr;
+  // look the address up (this also makes the runtime bind the device's
+  // primary context when the thread has none yet), then record the context
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    s = ScratchSlot{};
+    return nullptr;
   }
-  return g_scratch_dev[dev];
+  ctx = nullptr;
+  id = 0;
+  if (f.get_current(&ctx) != CUDA_SUCCESS || !ctx || f.get_id(ctx, &id) != CUDA_SUCCESS || id == 0) {
+    s = ScratchSlot{};
+    return nullptr;
+  }
+  s.ctx_id = id;
+  s.addr = p;
+  return p;
 }
 
 }  // namespace
@@ -58,6 +113,9 @@ extern "C" int fa_fwd_noalloc(const fa_tensor* q, const fa_tensor* k, const fa_t
                               int32_t window_left, int32_t window_right, float softcap,
                               float scale, int32_t causal, const fa_opts* opts) {
   if (!opts) return FA_ERR_INVALID_ARG;
+  // the device error word is cleared by every call and cannot be read back,
+  // so a device-side value check could never be reported: refuse it
+  if (opts->debug_flags & FA_DEBUG_VALIDATE) return FA_ERR_UNSUPPORTED;
   fa_opts o = *opts;
   o.workspace = nullptr;
   o.workspace_bytes = 0;

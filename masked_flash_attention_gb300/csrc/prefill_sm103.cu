@@ -21,8 +21,8 @@
 //   warp 1      QK issuer (one thread), Q prefetch, TMEM owner
 //   warp 2      TMA producer: V tiles through an NS-stage ring
 //   warp 3      PV issuer (one thread)
-//   warps 4..7  softmax, key columns 0..63 of every tile
-//   warps 8..11 softmax, key columns 64..127
+//   warps 4..7  softmax warpgroup 0: the even key tiles of a unit's sequence
+//   warps 8..11 softmax warpgroup 1: the odd ones
 // TMEM (512 columns): S in two buffers [0,128) [128,256) (fp32), P in two
 // buffers [256,320) [320,384) (input type, two per column), O in [384, 384 + D).
 // With S and P double-buffered QK(j+1) runs while the softmax of tile j does,
@@ -30,11 +30,12 @@
 // softmax only when it is slower than QK + PV.  The MMA queue is shallow (an
 // issuing thread stalls on tcgen05.mma almost at once), so QK and PV come from
 // two threads: each one's waits overlap the other's MMAs.
-// Each softmax thread owns half a row (32x32b TMEM loads); the two halves
-// exchange their row maxima through shared memory once per tile and add their
-// row sums at the end.  The running max is the exponent reference and is only
-// raised when the row max exceeds it by more than 2^8 (in log2 units), so O in
-// TMEM is rarely rescaled.  A fully masked row keeps reference -inf,
+// The two softmax warpgroups take alternate key tiles of the same 128 rows;
+// each thread owns one whole 128-key row of its tile (32x32b TMEM loads).  The
+// exponent reference of a row is handed from tile to tile through shared
+// memory, and the two warpgroups' row sums are added at the end.  The
+// reference is only raised when the row max exceeds it by more than 2^8 (in
+// log2 units), so O in TMEM is rarely rescaled.  A fully masked row keeps reference -inf,
 // exponentiates against 0, and ends with l = 0: O = 0, LSE = -inf.
 //
 // Every mbarrier wait is bounded (1 s); on a time-out the kernel records

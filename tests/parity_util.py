@@ -7,9 +7,10 @@ import masked_flash_attention_gb300 as fa
 from oracle import attention as O
 
 # Tolerances for bf16 outputs against the fp64 oracle (max-abs, mean-abs on
-# O; absolute on fp32 LSE).  Beside them, internal gates: relative L1 error of
-# O and per-(row-block) cosine similarity, so that an all-zero or garbage O
-# cannot pass on long rows where |O| is itself below the max-abs bound.
+# O; absolute on fp32 LSE).  Beside them, internal gates taken per (sequence,
+# q-head) block of rows: relative L1 error of O and cosine similarity, so that
+# an all-zero or garbage O cannot pass on long rows where |O| is itself below
+# the max-abs bound, and one wrong head cannot hide among many good ones.
 MAX_ABS = 2e-2
 MEAN_ABS = 2e-3
 LSE_ABS = 1e-3
@@ -44,8 +45,10 @@ def lse_as_out_rows(lse, out_ndim):
     return np.moveaxis(lse, -1, 1) if out_ndim == 4 else lse.T
 
 
-def compare(out, lse, ref_o, ref_l, name=""):
-    """Assert the parity bar; returns a dict of the measured errors."""
+def compare(out, lse, ref_o, ref_l, name="", cu_seqlens=None):
+    """Assert the parity bar; returns a dict of the measured errors (the
+    block gates report their worst block).  ``cu_seqlens`` splits a packed
+    [T, H, d] output into its sequences."""
     assert out.shape == ref_o.shape, (out.shape, ref_o.shape)
     assert lse.shape == ref_l.shape, (lse.shape, ref_l.shape)
     assert np.isfinite(out).all(), f"{name}: non-finite O"
@@ -66,15 +69,33 @@ def compare(out, lse, ref_o, ref_l, name=""):
     if fin.any():
         res["lse_abs"] = float(np.abs(lse[fin] - ref_l[fin]).max())
         assert res["lse_abs"] <= LSE_ABS, f"{name}: max |dLSE| {res['lse_abs']}"
-    denom = np.abs(ref_o).sum()
-    if denom > 0:
-        res["rel_l1"] = float(err.sum() / denom)
-        assert res["rel_l1"] <= REL_L1, f"{name}: relative L1 {res['rel_l1']}"
-        a = out.reshape(-1).astype(np.float64)
-        b = ref_o.reshape(-1)
-        cos = float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b) + 1e-300))
-        res["cos"] = cos
-        assert cos >= COS_MIN, f"{name}: cosine {cos}"
+    res["rel_l1"], res["cos"] = 0.0, 1.0
+    for key, sl in head_blocks(out.shape, cu_seqlens):
+        g, r = out[sl].reshape(-1).astype(np.float64), ref_o[sl].reshape(-1)
+        denom = np.abs(r).sum()
+        if denom == 0:  # every row of the block is fully masked (checked above)
+            continue
+        rel = float(np.abs(g - r).sum() / denom)
+        cos = float(g @ r / (np.linalg.norm(g) * np.linalg.norm(r) + 1e-300))
+        res["rel_l1"] = max(res["rel_l1"], rel)
+        res["cos"] = min(res["cos"], cos)
+        assert rel <= REL_L1, f"{name}: relative L1 {rel} in block {key}"
+        assert cos >= COS_MIN, f"{name}: cosine {cos} in block {key}"
     return res
 
 
+def head_blocks(shape, cu_seqlens=None):
+    """(key, index) of every (sequence, q-head) block of rows of an output
+    shaped [B, S, H, d], or [T, H, d] packed by ``cu_seqlens`` (without it,
+    one block per head)."""
+    if len(shape) == 4:
+        for b in range(shape[0]):
+            for h in range(shape[2]):
+                yield (b, h), (b, slice(None), h)
+        return
+    cu = [0, shape[0]] if cu_seqlens is None else [int(x) for x in cu_seqlens]
+    for s in range(len(cu) - 1):
+        if cu[s + 1] == cu[s]:
+            continue
+        for h in range(shape[1]):
+            yield (s, h), (slice(cu[s], cu[s + 1]), h)

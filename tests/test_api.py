@@ -177,3 +177,19 @@ def test_bwd_plan_rules():
 def test_binding_abi_matches_header():
     txt = open(os.path.join(ROOT, "include", "fa.h")).read()
     assert int(re.search(r"#define FA_ABI_VERSION (\d+)", txt).group(1)) == _lib.ABI_VERSION
+
+
+def test_binding_requires_every_declared_function():
+    """The binding refuses a library that lacks an entry point the header
+    declares (an older build), instead of failing only when it is called."""
+    assert sorted(_lib.EXPORTS) == header_functions()
+
+
+def test_noalloc_refuses_workspace_and_events():
+    """fa_fwd_noalloc takes no workspace and no timing events: passing them
+    is an error, not silently ignored (checked before any device work)."""
+    q = T(1, 4, 2, 64)
+    for kw in (dict(workspace=T(256, dtype=torch.uint8)), dict(event_begin=object()), dict(event_end=object())):
+        with pytest.raises(fa.FaError) as e:
+            fa.fa_fwd_noalloc(q, q, q, out=q, lse=T(1, 2, 4, dtype=torch.float32), **kw)
+        assert e.value.status == _lib.FA_ERR_INVALID_ARG

@@ -294,6 +294,63 @@ def test_random_tiny_vs_brute(seed):
         np.testing.assert_allclose(lse[0, h], np.array(bl), rtol=0, atol=1e-13)
 
 
+def _per_head_masks(seed, B, H, Sq, Sk):
+    """[B, H, Sq, Sk] fp32 masks whose (b, h) slices all differ (each slice
+    drawn from its own seed, with some -inf and some finite biases)."""
+    return torch.stack([torch.stack([W.random_dense_mask(seed + 31 * b + h, Sq, Sk, p_neg_inf=0.25)
+                                     for h in range(H)]) for b in range(B)])
+
+
+@pytest.mark.parametrize("form", ["full", "broadcast_batch", "broadcast_head"])
+def test_per_batch_and_head_mask_against_brute(form):
+    """The [B|1, Hq|1, q_len, kv_len] mask form: each (sequence, q-head) takes
+    its own slice.  Checked against the scalar brute force run per (b, h)
+    with that slice as a plain 2-D mask, on a grouped-query case (Hq = 4,
+    Hkv = 2, B = 2) where every slice differs, so that swapping b and h, or
+    indexing the mask by the K/V head instead of the q-head, fails.  The
+    broadcast forms use stride-0 views (torch expand), as a caller would pass
+    them (ExecuTorch pull request 10466, "Summary": a [q_len, kv_len] mask
+    added to q@k; one per head is the same rule applied head by head)."""
+    B, Hq, Hkv, Sq, Sk, d = 2, 4, 2, 3, 6, 4
+    G = Hq // Hkv
+    c = W.random_case(61, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, d=d, causal=True)
+    if form == "full":
+        m = _per_head_masks(61, B, Hq, Sq, Sk)
+    elif form == "broadcast_batch":
+        m = _per_head_masks(62, 1, Hq, Sq, Sk).expand(B, -1, -1, -1)
+        assert m.stride(0) == 0
+    else:
+        m = _per_head_masks(63, B, 1, Sq, Sk).expand(-1, Hq, -1, -1)
+        assert m.stride(1) == 0
+    # no two (b, h) slices coincide where the form gives them their own
+    flat = m.reshape(B * Hq, Sq * Sk).numpy()
+    distinct = {tuple(np.nan_to_num(r, neginf=-1e300)) for r in flat}
+    assert len(distinct) == {"full": B * Hq, "broadcast_batch": Hq, "broadcast_head": B}[form]
+    out, lse = run(c, mask=m)
+    for b in range(B):
+        for h in range(Hq):
+            bo, bl = brute.attention(f64(c["q"][b, :, h]).tolist(), f64(c["k"][b, :, h // G]).tolist(),
+                                     f64(c["v"][b, :, h // G]).tolist(), scale=c["params"]["scale"],
+                                     causal=True, mask=m[b, h].double().numpy().tolist())
+            np.testing.assert_allclose(out[b, :, h], np.array(bo), rtol=0, atol=1e-13)
+            np.testing.assert_allclose(lse[b, h], np.array(bl), rtol=0, atol=1e-13)
+
+
+def test_per_head_mask_catches_wrong_head_index():
+    """The check above can fail: a mask read with the K/V head index
+    (h // G) instead of the q-head differs from the oracle on the same
+    inputs.  Planted on the CPU by handing the oracle the mis-indexed
+    mask."""
+    B, Hq, Hkv, Sq, Sk, d = 1, 4, 2, 3, 6, 4
+    G = Hq // Hkv
+    c = W.random_case(64, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, d=d)
+    m = _per_head_masks(64, B, Hq, Sq, Sk)
+    wrong = m[:, [h // G for h in range(Hq)]]
+    out, _ = run(c, mask=m)
+    out_wrong, _ = run(c, mask=wrong)
+    assert np.abs(out - out_wrong).max() > 1e-3
+
+
 def test_every_zero_neginf_mask_4x4():
     """Every 0/-inf pattern of a 4x4 tile: rows with no kept key are exactly
     zero with LSE -inf, nothing is NaN; a stride-sample also matches the

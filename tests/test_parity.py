@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 def check(case, **over):
     out, lse, _ = run_gpu(case, **over)
     ref_o, ref_l = run_oracle(case, **over)
-    return compare(out, lse, ref_o, ref_l, case["name"])
+    return compare(out, lse, ref_o, ref_l, case["name"], cu_seqlens=case["params"].get("cu_seqlens_q"))
 
 
 # ---------------------------------------------------------------------------
@@ -171,7 +171,7 @@ def test_paged(page):
     paged["params"] = dict(case["params"], block_table=bt)
     out, lse, _ = run_gpu(paged)
     ref_o, ref_l = run_oracle(case)   # same sequences, contiguous
-    compare(out, lse, ref_o, ref_l, "paged")
+    compare(out, lse, ref_o, ref_l, "paged", cu_seqlens=case["params"]["cu_seqlens_q"])
 
 
 def test_paged_decode_workload_small():
@@ -199,7 +199,8 @@ def test_bad_page_index_is_reported():
 
 def _sampled(case, n_rows=48, seed=0):
     """Run the GPU on the whole workload; compare sampled (b, h, i) rows with
-    the oracle evaluated row by row."""
+    the oracle evaluated row by row.  Each sampled row is its own block for
+    the relative-L1 and cosine gates."""
     out, lse, _ = run_gpu(case)
     p = dict(case["params"])
     q, k, v = case["q"], case["k"], case["v"]
@@ -218,8 +219,9 @@ def _sampled(case, n_rows=48, seed=0):
                                   v[b, :, h // G].double().numpy(), [i], Sq, Sk, scale=p["scale"],
                                   z=z, **kw)
         ro.append(o_[0]); rl.append(l_[0]); go.append(out[b, i, h]); gl.append(lse[b, h, i])
-    return compare(np.array(go)[None, :, None, :], np.array(gl)[None, None, :],
-                   np.array(ro)[None, :, None, :], np.array(rl)[None, None, :], case["name"])
+    n = len(rows)
+    return compare(np.array(go)[:, None, None, :], np.array(gl)[:, None, None],
+                   np.array(ro)[:, None, None, :], np.array(rl)[:, None, None], case["name"])
 
 
 def test_causal_prefill_past_kv_full():

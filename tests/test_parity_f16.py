@@ -20,7 +20,7 @@ def check(case, **over):
     assert case["q"].dtype == F16
     out, lse, _ = run_gpu(case, **over)
     ref_o, ref_l = run_oracle(case, **over)
-    return compare(out, lse, ref_o, ref_l, case["name"] + "_f16")
+    return compare(out, lse, ref_o, ref_l, case["name"] + "_f16", cu_seqlens=case["params"].get("cu_seqlens_q"))
 
 
 def _assert_path(case, path, **over):
@@ -126,7 +126,7 @@ def test_paged_decode_f16(page):
     paged = dict(case, k=kc, v=vc, params=dict(params, block_table=bt))
     out, lse, _ = run_gpu(paged)
     ref_o, ref_l = run_oracle(case)
-    compare(out, lse, ref_o, ref_l, f"paged{page}_f16")
+    compare(out, lse, ref_o, ref_l, f"paged{page}_f16", cu_seqlens=case["params"]["cu_seqlens_q"])
 
 
 def test_f16_results_differ_from_bf16_reading():

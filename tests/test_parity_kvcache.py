@@ -99,7 +99,7 @@ def _oracle(c, **kw):
 def _check(c, name, append=False, **kw):
     out, lse, kc, vc = _run(c, append=append, **kw)
     ro, rl = _oracle(c, **kw)
-    compare(out, lse, ro, rl, name)
+    compare(out, lse, ro, rl, name, cu_seqlens=c["cu_q"])
     return kc, vc
 
 
@@ -199,7 +199,7 @@ def test_paged_decode_ignores_stale_page_rows():
     c2 = dict(c, k=kc, v=vc)
     out, lse, _ = run_gpu(c2)
     ro, rl = run_oracle(c)
-    compare(out, lse, ro, rl, "stale_rows")
+    compare(out, lse, ro, rl, "stale_rows", cu_seqlens=c["params"].get("cu_seqlens_q"))
 
 
 def test_kvcache_sequences_without_new_tokens():

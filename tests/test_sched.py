@@ -49,16 +49,18 @@ def oracle_classes(case, plan, **over):
     for b in range(B):
         for hs in range(plan["n_heads_sched"]):
             heads = range(hs * G, hs * G + G) if decode else [hs]
-            X = []
+            X, M = [], []
             for h in heads:
+                mh = None if m is None else (m.numpy() if m.dim() == 2 else m[b, h].numpy())
                 x = O.logits_rows(q[b, :, h].double().numpy(), k[b, :, h // G].double().numpy(),
                                   np.arange(Sq), Sq, Sk, scale=p["scale"] or d ** -0.5,
                                   causal=p["causal"], window_left=p["window_left"],
                                   window_right=p["window_right"], softcap=p["softcap"],
-                                  mask_rows=None if m is None else (m.numpy() if m.dim() == 2 else m[b, h].numpy()),
-                                  z=None if z is None else z[b, h].numpy(), keep_window=p["keep_window"])
+                                  mask_rows=mh, z=None if z is None else z[b, h].numpy(),
+                                  keep_window=p["keep_window"])
                 X.append(x)
-            X = np.stack(X)
+                M.append(np.zeros((Sq, Sk)) if mh is None else mh)
+            X, M = np.stack(X), np.stack(M)
             for rt in range(n_rt):
                 if decode:
                     R = plan["rows_per_tile"]  # packed rows (query, head-in-group)
@@ -69,9 +71,11 @@ def oracle_classes(case, plan, **over):
                 item = (b * plan["n_heads_sched"] + hs) * n_rt + rt
                 for kt in range(nk):
                     blk = X[:, i0:i1 + 1, kt * KT:min(Sk, (kt + 1) * KT)]
+                    mblk = M[:, i0:i1 + 1, kt * KT:min(Sk, (kt + 1) * KT)]
                     if blk.size == 0 or np.all(blk == -np.inf):
                         cls[item, kt] = 0
-                    elif np.all(np.isfinite(blk)) and z is None and (m is None or True):
+                    elif np.all(np.isfinite(blk)) and z is None and np.all(mblk == 0):
+                        # nothing masked and no additive term: the tile needs no predicate
                         cls[item, kt] = 1
                     else:
                         cls[item, kt] = 2
@@ -133,6 +137,9 @@ def test_dense_mask_classes_exact():
     assert np.array_equal(got == 0, want == 0)
     # the all-zero tiles stay FULL, the mixed ones are PARTIAL
     assert got[0, 2] == 1 and got[0, 4] == 2 and got[0, 5] == 2
+    # a tile with finite non-zero mask values is never FULL (that would drop its bias)
+    assert want[0, 4] == 2 and want[0, 5] == 2
+    assert np.all(want[got == 1] == 1)
 
 
 def test_topk_kept_sets_exact(golden):
@@ -173,3 +180,34 @@ def test_inconsistent_lengths_are_reported():
     out, lse, ws = fa.fa_fwd(q.to(DEV), k.to(DEV), v.to(DEV), **to_dev(p))
     rc, info = fa.fa_check_device_error(ws)
     assert rc == fa._lib.FA_ERR_DEVICE_BOUNDS
+
+
+def test_topk_kept_sets_at_full_workload_shape():
+    """Kept sets of the dynamic top-k workload itself (B=2, H=16, T=8192,
+    keep_window=2048, causal), with ties quantised in: the expiry rows the
+    GPU writes, read back as per-row kept sets, equal the oracle's per-row
+    sort on sampled rows of every (b, h), including the rows where the
+    window first fills (2047, 2048) and the last row
+    (flash-sparse-attention issue 11, "Current Status": position match 1.0)."""
+    case = W.dynamic_topk(seed=0)
+    p = dict(case["params"])
+    B, Sq, H, _ = case["q"].shape
+    Sk = case["k"].shape[1]
+    keep = p["keep_window"]
+    z = torch.round(p["zero_hold_states"] * 4.0) / 4.0   # ties on
+    plan, counts, tiles, stats, ws = worklist(case, zero_hold_states=z)
+    e = ws.cpu()[plan["off_topk_e"]:plan["off_topk_e"] + 4 * B * H * Sk].view(torch.int32).numpy()
+    e = e.reshape(B, H, Sk).astype(np.int64)
+    off = Sk - Sq
+    rng = np.random.default_rng(5)
+    keys = np.arange(Sk)
+    for b in range(B):
+        for h in range(H):
+            zn = z[b, h].numpy()
+            rows = {0, keep - 2, keep - 1, keep, keep + 1, Sq - 1} | set(rng.integers(0, Sq, 6).tolist())
+            for i in sorted(rows):
+                cand = O.allowed_pairs([i], keys, Sq, Sk, causal=True)[0]
+                want = np.zeros(Sk, bool)
+                want[O.topk_kept_row(zn, cand, keep)] = True
+                got = (keys <= i + off) & (i < e[b, h])
+                assert np.array_equal(got, want), (b, h, i, int((got != want).sum()))

@@ -5,14 +5,15 @@ a static device array inside the library, so the caller passes only inputs
 and outputs.  These tests call it through the C ABI and check it against
 fa_fwd (which uses a caller-provided workspace) within the parity tolerances,
 on two calls in a row, since the static scratch keeps the previous call's
-contents.  The file is named to be collected last."""
+contents; one case also goes straight to the fp64 oracle.  The file is
+named to be collected last."""
 import numpy as np
 import pytest
 import torch
 
 import masked_flash_attention_gb300 as fa
 import workloads as W
-from parity_util import DEV, LSE_ABS, MAX_ABS, MEAN_ABS, to_dev
+from parity_util import DEV, LSE_ABS, MAX_ABS, MEAN_ABS, compare, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -65,3 +66,52 @@ def test_noalloc_rejects_problems_beyond_the_static_scratch():
     with pytest.raises(fa.FaError) as e:
         fa.fa_fwd_noalloc(q, k, k, out=out, lse=lse)
     assert e.value.status == fa._lib.FA_ERR_WORKSPACE
+
+
+def test_noalloc_against_the_oracle():
+    """Directly against the fp64 oracle (not only through fa_fwd), on a
+    prefill case with a ragged tail and on the worked example's decode."""
+    for case in (W.random_case(22, B=2, Sq=200, Sk=450, Hq=8, Hkv=2, d=128, causal=True),
+                 W.sliding_window_decode(seed=5)):
+        p = to_dev(case["params"])
+        q, k, v = case["q"].to(DEV), case["k"].to(DEV), case["v"].to(DEV)
+        ref_o, ref_l = run_oracle(case)
+        for _ in range(2):
+            out = torch.full_like(q, float("nan"))
+            lse = torch.full(ref_l.shape, float("nan"), dtype=torch.float32, device=DEV)
+            fa.fa_fwd_noalloc(q, k, v, out=out, lse=lse, **p)
+            torch.cuda.synchronize()
+            compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, case["name"] + "_noalloc")
+
+
+def test_noalloc_allocates_nothing():
+    """The entry point's reason to exist: after one warm-up call (which also
+    loads the kernels), further calls leave both torch's allocator and the
+    device's free memory unchanged."""
+    case = W.paged_varlen_decode(seed=3, n_seq=8, max_len=2500)
+    p = to_dev(case["params"])
+    q, k, v = case["q"].to(DEV), case["k"].to(DEV), case["v"].to(DEV)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=DEV)
+    fa.fa_fwd_noalloc(q, k, v, out=out, lse=lse, **p)
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated(DEV)
+    free0 = torch.cuda.mem_get_info(DEV)[0]
+    for _ in range(5):
+        fa.fa_fwd_noalloc(q, k, v, out=out, lse=lse, **p)
+        torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated(DEV) == alloc0
+    assert torch.cuda.mem_get_info(DEV)[0] == free0
+
+
+def test_noalloc_refuses_device_validation():
+    """FA_DEBUG_VALIDATE reports only through the device error word, which
+    this entry point clears and cannot return: the flag is refused."""
+    case = W.random_case(23, B=1, Sq=3, Sk=300, Hq=4, Hkv=2, d=64, causal=True)
+    p = to_dev(case["params"])
+    q, k, v = case["q"].to(DEV), case["k"].to(DEV), case["v"].to(DEV)
+    out = torch.empty_like(q)
+    lse = torch.empty(1, 4, 3, dtype=torch.float32, device=DEV)
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_fwd_noalloc(q, k, v, out=out, lse=lse, debug_flags=fa.FA_DEBUG_VALIDATE, **p)
+    assert e.value.status == fa._lib.FA_ERR_UNSUPPORTED

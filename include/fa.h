@@ -168,13 +168,18 @@ typedef enum { FA_TILE_EMPTY = 0, FA_TILE_FULL = 1, FA_TILE_PARTIAL = 2 } fa_til
  * tile is 8 consecutive packed rows p = i * (Hq/Hkv) + (h % (Hq/Hkv)) of that
  * K/V head's query heads.  Keys are cut into tiles of keys_per_tile.
  *
- * Work list in the workspace after fa_fwd (device memory, int32):
+ * Work list in the workspace after fa_fwd (device memory, int32), written by
+ * the scheduler kernel on the DECODE path and on the PREFILL path with a
+ * dense or top-k mask:
  *   counts[n_items]                   at workspace + off_counts
  *   tiles[n_items][n_k_tiles]         at workspace + off_tiles;
  *     entry = (k_tile << 1) | (class == FA_TILE_PARTIAL); only the first
  *     counts[item] entries are valid; EMPTY tiles never appear.
+ * On the PREFILL path without a mask the pair rules alone classify the tiles,
+ * so the attention kernel derives each item's list itself (the same tiles,
+ * in the same order) and these two arrays are not written.
  *   stats: int64 [3] = tiles scheduled FULL, PARTIAL, and key tiles left out
- *     as EMPTY, at workspace + off_stats.
+ *     as EMPTY, at workspace + off_stats (every path).
  *   top-k masks only: int32 e[n_seq][Hq][Sk] at workspace + off_topk_e, the
  *     first query row at which key j is no longer kept (key j is kept on rows
  *     i with j <= i + Sk - Sq and i < e; INT32_MAX = never dropped,

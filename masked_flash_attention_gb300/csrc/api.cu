@@ -299,6 +299,9 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   }
   // prefill carries ALiBi only without a dense or top-k mask (decode: any)
   if (P.path == FA_PATH_PREFILL && P.alibi && mask_kind != FA_MASK_NONE) return FA_ERR_UNSUPPORTED;
+  // without a dense or top-k mask the pair rules alone decide every tile: the
+  // prefill kernel classifies its units' tiles itself and no scheduler kernel runs
+  P.sched_inline = (P.path == FA_PATH_PREFILL && mask_kind == FA_MASK_NONE) ? 1 : 0;
   P.n_kt = ceil_div(Sk, kKeysPerTile);
   P.n_items = n_seq * (int64_t)P.n_heads_sched * P.n_row_tiles;
   if (Sq == 0 || n_seq == 0) P.n_items = 0;
@@ -350,6 +353,7 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   pub.n_items = P.n_items;
   pub.off_topk_e = (mask_kind == FA_MASK_TOPK) ? pl->off_topk_e : 0;
   pub.n_kernels = P.n_items == 0 ? 0
+                  : P.sched_inline ? 1
                   : 2 + (P.n_splits > 1) + (mask_kind == FA_MASK_DENSE) + 2 * (mask_kind == FA_MASK_TOPK);
   pub.workspace_bytes = off;
   P.n_kt = n_kt_alloc;
@@ -535,12 +539,17 @@ int run_plan(Plan& pl, const fa_opts* opts) {
   bind_workspace(&pl, opts->workspace);
   cudaStream_t st = static_cast<cudaStream_t>(opts->stream);
   const Params& P = pl.prm;
-  if (cudaMemsetAsync(P.stats, 0, 3 * sizeof(long long), st) != cudaSuccess) return FA_ERR_CUDA;
+  // the counters are accumulated by the scheduler kernels, or written whole by
+  // the prefill kernel when it schedules inline
+  if ((!P.sched_inline || P.n_items == 0) && cudaMemsetAsync(P.stats, 0, 3 * sizeof(long long), st) != cudaSuccess)
+    return FA_ERR_CUDA;
   if (P.n_items == 0) return FA_OK;
   cudaError_t e = cudaSuccess;
-  if (P.mask_kind == FA_MASK_DENSE) e = launch_mask_summary(P, st);
-  if (e == cudaSuccess && P.mask_kind == FA_MASK_TOPK) e = launch_topk_prep(P, st);
-  if (e == cudaSuccess) e = launch_classify(P, st);
+  if (!P.sched_inline) {
+    if (P.mask_kind == FA_MASK_DENSE) e = launch_mask_summary(P, st);
+    if (e == cudaSuccess && P.mask_kind == FA_MASK_TOPK) e = launch_topk_prep(P, st);
+    if (e == cudaSuccess) e = launch_classify(P, st);
+  }
   cudaEvent_t ev_begin = static_cast<cudaEvent_t>(opts->event_begin);
   if (e == cudaSuccess)
     e = (P.path == FA_PATH_PREFILL) ? launch_prefill(P, st, ev_begin) : launch_decode(P, st, ev_begin);

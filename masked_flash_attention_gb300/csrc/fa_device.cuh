@@ -27,6 +27,20 @@ __device__ __forceinline__ void record_error(const Params& p, uint32_t code, uin
   if (atomicCAS(&p.ws->error, 0u, code) == 0u) atomicExch(&p.ws->error_info, info);
 }
 
+// True when sequence b's lengths, read from device memory, do not fit the
+// sizes the host planned for (an item of such a sequence is skipped and the
+// fault recorded, so nothing indexes with them).
+__device__ __forceinline__ bool seq_lengths_bad(const Params& p, int b, int q_len, int kv_len) {
+  bool bad = q_len < 0 || kv_len < 0 || q_len > p.Sq || kv_len > p.Sk;
+  if (p.cu_q) bad |= p.cu_q[b] < 0 || (int64_t)p.cu_q[b + 1] > p.tot_q;
+  if (p.cu_k && !p.block_table) bad |= p.cu_k[b] < 0 || (int64_t)p.cu_k[b + 1] > p.tot_k;
+  if (p.cache_len) {  // two-source form: cached rows within the cache, appended rows too
+    const int64_t lc = __ldg(p.cache_len + b);
+    bad |= lc < 0 || lc > p.cache_cap || lc + q_len > p.Sk || (p.append && lc + q_len > p.cache_cap);
+  }
+  return bad;
+}
+
 // Query-row span [i0, i1] (inclusive, unclipped) of row tile `rt`.  For the
 // decode path rows are packed (query, head-in-group) with `pack` = Hq/Hkv.
 __device__ __forceinline__ void tile_rows(const Params& p, int rt, int& i0, int& i1) {

@@ -79,6 +79,10 @@ struct Params {
 
   // scheduler
   int32_t path;
+  // 1: the prefill kernel derives each unit's key tiles from the pair rules
+  // (no dense or top-k mask), so no scheduler kernel runs and its lists are
+  // not written; the kernel's first CTA writes the counters
+  int32_t sched_inline;
   int32_t rows_per_tile, n_row_tiles, n_heads_sched, n_kt;
   int64_t n_items;
   int32_t* item_count;   // [n_items]

@@ -96,15 +96,25 @@ struct PCfg {
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
 };
 
-// One work unit: 128 query rows of one q-head of one sequence.
+// One work unit: 128 query rows of one q-head of one sequence.  Its key tiles
+// come from the scheduler kernel's list, or -- when the pair rules alone decide
+// them (no dense or top-k mask: INL, the host's p.sched_inline) -- from the
+// unit's geometry: tiles kt0 .. kt0 + count - 1, those with relative index in
+// [fl, fh] FULL and the others PARTIAL, exactly what the scheduler kernel
+// would have listed.
 struct Unit {
   bool present;  // the tile holds rows of the sequence
-  bool valid;    // the scheduler accepted the sequence
+  bool valid;    // the sequence's lengths passed the checks
   int b, h, rt, count;
-  const int32_t* tiles;
+  int kt0, fl, fh;       // INL
+  const int32_t* tiles;  // scheduler list (not INL)
 };
 
+// Floor of a / 128 for any sign of a.
+__device__ __forceinline__ int floor_div128(int a) { return a >= 0 ? a / 128 : -((127 - a) / 128); }
+
 // Unit u, longest query tiles first (row tile descending), q-heads fastest.
+template <bool INL>
 __device__ __forceinline__ Unit unit_at(const Params& p, int u) {
   Unit w;
   const int per = p.n_seq * p.Hq;
@@ -112,22 +122,107 @@ __device__ __forceinline__ Unit unit_at(const Params& p, int u) {
   const int r = u % per;
   w.h = r % p.Hq;
   w.b = r / p.Hq;
-  w.present = w.rt * 128 < seq_qlen(p, w.b);
-  const int64_t item = ((int64_t)w.b * p.Hq + w.h) * p.n_row_tiles + w.rt;
-  const int c = w.present ? __ldg(p.item_count + item) : -1;
-  w.valid = c >= 0;
-  w.count = c > 0 ? c : 0;
-  w.tiles = p.item_tiles + item * p.n_kt;
+  const int q_len = seq_qlen(p, w.b);
+  w.present = w.rt * 128 < q_len;
+  if constexpr (INL) {
+    const int kv_len = seq_klen(p, w.b);
+    w.valid = !seq_lengths_bad(p, w.b, q_len, kv_len);
+    w.count = 0;
+    w.kt0 = 0;
+    w.fl = 1;
+    w.fh = 0;
+    if (w.valid && w.present && kv_len > 0) {
+      const int i0 = w.rt * 128, i1 = min(i0 + 127, q_len - 1), off = kv_len - q_len;
+      int jlo = 0, jhi = kv_len - 1;
+      const bool no_skip = (p.debug_flags & FA_DEBUG_NO_SKIP) != 0;
+      if (!no_skip) key_range(p, i0, i1, off, kv_len, jlo, jhi);
+      if (jlo <= jhi) {
+        w.kt0 = jlo / kKeysPerTile;
+        w.count = jhi / kKeysPerTile - w.kt0 + 1;
+        if (!no_skip) {
+          // tile_all_allowed as a range of tiles: the last key of the tile at
+          // most hi, its first key at least lo
+          int hi = kv_len - 1, lo = INT_MIN / 2;
+          if (p.causal) hi = min(hi, i0 + off);
+          if (p.wr >= 0) hi = min(hi, i0 + off + p.wr);
+          if (p.wl >= 0) lo = i1 + off - p.wl;
+          const int kt_hi = floor_div128(hi - (kKeysPerTile - 1));
+          const int kt_lo = lo <= 0 ? 0 : -floor_div128(-lo);
+          w.fl = max(kt_lo, w.kt0) - w.kt0;
+          w.fh = kt_hi - w.kt0;
+        }
+      }
+    }
+  } else {
+    const int64_t item = ((int64_t)w.b * p.Hq + w.h) * p.n_row_tiles + w.rt;
+    const int c = w.present ? __ldg(p.item_count + item) : -1;
+    w.valid = c >= 0;
+    w.count = c > 0 ? c : 0;
+    w.tiles = p.item_tiles + item * p.n_kt;
+  }
   return w;
+}
+
+// Entry i of a unit's key-tile list: (key tile << 1) | PARTIAL.
+template <bool INL>
+__device__ __forceinline__ int unit_entry(const Unit& w, int i) {
+  if constexpr (INL) return ((w.kt0 + i) << 1) | ((i < w.fl || i > w.fh) ? 1 : 0);
+  else return __ldg(w.tiles + i);
+}
+
+// Inline scheduling: the scheduler's counters (tiles scheduled FULL and
+// PARTIAL, key tiles left out as EMPTY) over every unit of the launch, and
+// the length checks of every sequence, by one warp.  Units of one (sequence,
+// row tile) differ only in the q-head, so each pair is counted once, times Hq.
+__device__ __noinline__ void inline_sched_stats(const Params& p) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long nf = 0, np = 0, ne = 0;
+  const int64_t n = (int64_t)p.n_seq * p.n_row_tiles;
+  for (int64_t t = lane; t < n; t += 32) {
+    const int b = (int)(t / p.n_row_tiles), rt = (int)(t % p.n_row_tiles);
+    const int q_len = seq_qlen(p, b), kv_len = seq_klen(p, b);
+    if (seq_lengths_bad(p, b, q_len, kv_len)) {
+      if (rt == 0) record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)b);
+      continue;
+    }
+    const int i0 = rt * 128;
+    if (i0 >= q_len || kv_len <= 0) continue;
+    const int i1 = min(i0 + 127, q_len - 1), off = kv_len - q_len;
+    const int n_kt_b = (kv_len + kKeysPerTile - 1) / kKeysPerTile;
+    const bool no_skip = (p.debug_flags & FA_DEBUG_NO_SKIP) != 0;
+    int jlo = 0, jhi = kv_len - 1;
+    if (!no_skip) key_range(p, i0, i1, off, kv_len, jlo, jhi);
+    int count = 0, full = 0;
+    if (jlo <= jhi) {
+      const int kt0 = jlo / kKeysPerTile, kt1 = jhi / kKeysPerTile;
+      count = kt1 - kt0 + 1;
+      for (int kt = kt0; kt <= kt1 && !no_skip; ++kt)
+        full += tile_all_allowed(p, i0, i1, kt * kKeysPerTile, kt * kKeysPerTile + kKeysPerTile - 1, off, kv_len);
+    }
+    nf += (unsigned long long)full * p.Hq;
+    np += (unsigned long long)(count - full) * p.Hq;
+    ne += (unsigned long long)(n_kt_b - count) * p.Hq;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    nf += __shfl_xor_sync(0xffffffffu, nf, o);
+    np += __shfl_xor_sync(0xffffffffu, np, o);
+    ne += __shfl_xor_sync(0xffffffffu, ne, o);
+  }
+  if (lane == 0) {
+    p.stats[0] = nf;
+    p.stats[1] = np;
+    p.stats[2] = ne;
+  }
 }
 
 __device__ __forceinline__ int n_units(const Params& p) { return p.n_row_tiles * p.n_seq * p.Hq; }
 
 // Next unit with key tiles at or after u (this CTA's stride), or -1.
+template <bool INL>
 __device__ __forceinline__ int next_busy(const Params& p, int u, Unit& w) {
   const int n = n_units(p);
   for (; u < n; u += gridDim.x) {
-    w = unit_at(p, u);
+    w = unit_at<INL>(p, u);
     if (w.present && w.valid && w.count > 0) return u;
   }
   return -1;
@@ -226,6 +321,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const int o_tma) {
   using C = PCfg<D>;
   constexpr int NS = C::NS;
+  constexpr bool INL = (MK == FA_MASK_NONE);  // the host sets p.sched_inline exactly then
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -298,12 +394,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int j = 0;
       bool ok = true;
       Unit w;
-      for (int u = next_busy(p, blockIdx.x, w); ok && u >= 0; u = next_busy(p, u + gridDim.x, w)) {
+      for (int u = next_busy<INL>(p, blockIdx.x, w); ok && u >= 0; u = next_busy<INL>(p, u + gridDim.x, w)) {
         const int kv_row0 = p.cu_k ? p.cu_k[w.b] : 0;
         const int kv_b = p.cu_k ? 0 : w.b;
         const int g = w.h / p.G;
         for (int i = 0; i < w.count; ++i, ++j) {
-          const int kt = __ldg(w.tiles + i) >> 1;
+          const int kt = unit_entry<INL>(w, i) >> 1;
           const int s = j % NS;
           if (j >= NS && !tc::mbar_wait(empty + s, ((j / NS) - 1) & 1, abort_flag)) {
             fail(p, abort_flag, is_k ? 1 : 7);
@@ -346,11 +442,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       bool ok = true;
       int g = 0, kk = 0;  // tiles and busy units so far
       Unit w, wn;
-      int u = next_busy(p, blockIdx.x, w);
+      int u = next_busy<INL>(p, blockIdx.x, w);
       if (u >= 0) load_q(w, 0);
       for (; ok && u >= 0; ++kk) {
         const int qb = kk & 1;
-        const int un = next_busy(p, u + gridDim.x, wn);
+        const int un = next_busy<INL>(p, u + gridDim.x, wn);
         if (!tc::mbar_wait(q_full + qb, (kk >> 1) & 1, abort_flag)) { ok = false; break; }
         for (int i = 0; i < w.count; ++i, ++g) {
           const int s = g % NS, sb = g & 1;
@@ -400,7 +496,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       bool ok = true;
       int g = 0;
       Unit w;
-      for (int u = next_busy(p, blockIdx.x, w); ok && u >= 0; u = next_busy(p, u + gridDim.x, w)) {
+      for (int u = next_busy<INL>(p, blockIdx.x, w); ok && u >= 0; u = next_busy<INL>(p, u + gridDim.x, w)) {
         for (int i = 0; i < w.count; ++i, ++g) {
           const int s = g % NS, pb = g & 1;
           if (!tc::mbar_wait(p_full + pb, (g >> 1) & 1, abort_flag) ||
@@ -449,15 +545,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     bool ok = true;
     int g = 0, kk = 0;  // tiles and busy units so far (all of them, both parities)
     const int nu = n_units(p);
-    // the next unit's descriptor and first list entry are read a unit ahead,
-    // so that no global-memory latency sits between two units
+    // Scheduler lists: the next unit's descriptor and first list entry are
+    // read a unit ahead, so that no global-memory latency sits between two
+    // units.  Inline scheduling: descriptors and entries are arithmetic,
+    // computed where they are needed (nothing held across the tile loop).
     Unit un_next;
-    if (blockIdx.x < nu) un_next = unit_at(p, blockIdx.x);
+    if (!INL && blockIdx.x < nu) un_next = unit_at<INL>(p, blockIdx.x);
     int ent_first = 0;
     bool ent_first_ok = false;
     for (int u = blockIdx.x; ok && u < nu; u += gridDim.x) {
-      const Unit un = un_next;
-      if (u + (int)gridDim.x < nu) un_next = unit_at(p, u + gridDim.x);
+      const Unit un = INL ? unit_at<INL>(p, u) : un_next;
+      if (!INL && u + (int)gridDim.x < nu) un_next = unit_at<INL>(p, u + gridDim.x);
       const bool pre_ok = ent_first_ok;
       ent_first_ok = false;
       if (!un.present || !un.valid) continue;
@@ -477,18 +575,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       float l = 0.f;
       // the first tile of the unit is this warpgroup's if g is of its parity
       const int it0 = (g & 1) == w ? 0 : 1;
-      int ent_cur = pre_ok ? ent_first : (it0 < un.count ? __ldg(un.tiles + it0) : 0);
+      int ent_cur = (INL || !pre_ok) ? (it0 < un.count ? unit_entry<INL>(un, it0) : 0) : ent_first;
       for (int it = it0; it < un.count; it += 2) {
         const int gt = g + it;  // global index of this tile
         const int par = w;      // == gt & 1
-        const int ent = ent_cur;
-        if (it + 2 < un.count) {
-          ent_cur = __ldg(un.tiles + it + 2);
+        const int ent = INL ? unit_entry<INL>(un, it) : ent_cur;
+        if (INL) {
+        } else if (it + 2 < un.count) {
+          ent_cur = unit_entry<INL>(un, it + 2);
         } else if (u + (int)gridDim.x < nu && un_next.present && un_next.valid && un_next.count > 0) {
           // this warpgroup's first entry of the next unit
           const int itn = ((g + un.count) & 1) == w ? 0 : 1;
           if (itn < un_next.count) {
-            ent_first = __ldg(un_next.tiles + itn);
+            ent_first = unit_entry<INL>(un_next, itn);
             ent_first_ok = true;
           }
         }
@@ -713,6 +812,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 1) tc::tmem_dealloc(tbase, kTmemCols);
+  if (INL && blockIdx.x == 0 && warp == 2) inline_sched_stats(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -798,6 +898,8 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
   if (units > INT_MAX) return cudaErrorInvalidValue;
   const int grid = (int)(units < sm_count() ? units : sm_count());
   const bool sc = p.softcap > 0.f;
+  // the kernels schedule inline exactly for the mask-free variants
+  if ((p.sched_inline != 0) != (p.mask_kind == FA_MASK_NONE)) return cudaErrorInvalidValue;
   if (p.alibi) {  // the planner allows ALiBi in prefill only without a mask
     if (p.mask_kind != FA_MASK_NONE) return cudaErrorInvalidValue;
     return sc ? launch_prefill_v<D, FA_MASK_NONE, true, true, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)

@@ -285,14 +285,7 @@ __global__ void __launch_bounds__(256) classify_kernel(const Params p) {
   const int q_len = seq_qlen(p, b), kv_len = seq_klen(p, b);
   // the lengths come from device memory: check them against the sizes the
   // host planned for before anything indexes with them
-  bool bad = q_len < 0 || kv_len < 0 || q_len > p.Sq || kv_len > p.Sk;
-  if (p.cu_q) bad |= p.cu_q[b] < 0 || (int64_t)p.cu_q[b + 1] > p.tot_q;
-  if (p.cu_k && !p.block_table) bad |= p.cu_k[b] < 0 || (int64_t)p.cu_k[b + 1] > p.tot_k;
-  if (p.cache_len) {  // two-source form: cached rows within the cache, appended rows too
-    const int64_t lc = __ldg(p.cache_len + b);
-    bad |= lc < 0 || lc > p.cache_cap || lc + q_len > p.Sk || (p.append && lc + q_len > p.cache_cap);
-  }
-  if (bad) {
+  if (seq_lengths_bad(p, b, q_len, kv_len)) {
     if (lane == 0) {
       p.item_count[item] = -1;  // the attention kernels leave this item alone
       record_error(p, FA_ERR_DEVICE_BOUNDS, (uint32_t)b);

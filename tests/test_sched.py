@@ -211,3 +211,33 @@ def test_topk_kept_sets_at_full_workload_shape():
                 want[O.topk_kept_row(zn, cand, keep)] = True
                 got = (keys <= i + off) & (i < e[b, h])
                 assert np.array_equal(got, want), (b, h, i, int((got != want).sum()))
+
+
+@pytest.mark.parametrize("seed,B,Sq,Sk,Hq,Hkv,d,extra", [
+    (0, 2, 300, 700, 4, 2, 128, dict(causal=True)),                                   # past KV, ragged
+    (1, 1, 260, 520, 2, 2, 64, dict(causal=True, window_left=150, window_right=20)),  # window
+    (2, 1, 400, 200, 2, 1, 128, dict(causal=True)),                                   # q_len > kv_len
+    (3, 1, 200, 333, 2, 2, 64, dict(causal=False)),
+])
+def test_prefill_inline_schedule_counts(seed, B, Sq, Sk, Hq, Hkv, d, extra):
+    """Without a mask the prefill kernel classifies its own tiles (no
+    scheduler kernel runs): the counters it writes equal the FULL / PARTIAL /
+    EMPTY classes recomputed from the oracle's logits, and EMPTY tiles are
+    never among the scheduled ones (their count is exact)."""
+    case = W.random_case(seed, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, d=d, **extra)
+    rc, plan = fa.fa_fwd_plan(case["q"], case["k"], case["v"], **case["params"])
+    assert rc == 0 and plan["path"] == fa._lib.FA_PATH_PREFILL and plan["n_kernels"] == 1
+    ws = fa.alloc_workspace(plan["workspace_bytes"], DEV)
+    ws[plan["off_stats"]:plan["off_stats"] + 24] = 7          # stale counters must be overwritten
+    run_gpu(case, workspace=ws)
+    stats = ws.cpu()[plan["off_stats"]:plan["off_stats"] + 24].view(torch.int64).numpy()
+    want = oracle_classes(case, plan)
+    n_kt_seq = -(-Sk // plan["keys_per_tile"])
+    if Sk % plan["keys_per_tile"]:
+        # a tile reaching past the last key is never FULL: the kernel masks the
+        # keys it lacks (the scheduler kernel applies the same rule)
+        last = want[:, n_kt_seq - 1]
+        last[last == 1] = 2
+    assert stats[0] == int((want == 1).sum())
+    assert stats[1] == int((want == 2).sum())
+    assert stats[2] == int((want[:, :n_kt_seq] == 0).sum())

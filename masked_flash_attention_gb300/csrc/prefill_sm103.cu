@@ -9,9 +9,10 @@
 // them out of each item's key-tile list.
 //
 // Persistent kernel: one CTA per SM walks the work units (sequence, q-head,
-// 128-row query tile) longest first, unit u going to CTA u mod grid, so the
-// pipelines run on from one unit into the next (Q of the next unit is fetched
-// while the current one runs; its first QK overlaps the current epilogue).
+// 128-row query tile) longest first, in rounds of one unit per CTA with every
+// other round in reverse CTA order (serpentine), so the pipelines run on from
+// one unit into the next (Q of the next unit is fetched while the current one
+// runs; its first QK overlaps the current epilogue).
 // Grouped-query heads read their K/V head directly (InfiniTrain pull request
 // 193 "Transformer 接入": no expansion); neighbouring units are the q-heads of
 // one group, so their K/V tiles are served from L2.
@@ -217,15 +218,27 @@ __device__ __noinline__ void inline_sched_stats(const Params& p) {
 
 __device__ __forceinline__ int n_units(const Params& p) { return p.n_row_tiles * p.n_seq * p.Hq; }
 
-// Next unit with key tiles at or after u (this CTA's stride), or -1.
+// The unit this CTA takes in round r: the grid takes the units (longest
+// first) in rounds of gridDim.x, every other round in reverse CTA order, so
+// that the CTA taking a round's longest unit takes the next round's shortest
+// (with units of falling length this balances the CTAs' loads far better
+// than unit u -> CTA u mod grid).  Past the last unit in some round, a CTA is
+// past it in every later round.
+__device__ __forceinline__ int round_unit(int r) {
+  const int c = (r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+  return r * (int)gridDim.x + c;
+}
+
+// Next round at or after r whose unit has key tiles, or -1.
 template <bool INL>
-__device__ __forceinline__ int next_busy(const Params& p, int u, Unit& w) {
+__device__ __forceinline__ int next_busy(const Params& p, int r, Unit& w) {
   const int n = n_units(p);
-  for (; u < n; u += gridDim.x) {
+  for (;; ++r) {
+    const int u = round_unit(r);
+    if (u >= n) return -1;
     w = unit_at<INL>(p, u);
-    if (w.present && w.valid && w.count > 0) return u;
+    if (w.present && w.valid && w.count > 0) return r;
   }
-  return -1;
 }
 
 // Two fp32 values rounded to nearest-even into one packed pair of the input
@@ -394,7 +407,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int j = 0;
       bool ok = true;
       Unit w;
-      for (int u = next_busy<INL>(p, blockIdx.x, w); ok && u >= 0; u = next_busy<INL>(p, u + gridDim.x, w)) {
+      for (int r = next_busy<INL>(p, 0, w); ok && r >= 0; r = next_busy<INL>(p, r + 1, w)) {
         const int kv_row0 = p.cu_k ? p.cu_k[w.b] : 0;
         const int kv_b = p.cu_k ? 0 : w.b;
         const int g = w.h / p.G;
@@ -442,11 +455,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       bool ok = true;
       int g = 0, kk = 0;  // tiles and busy units so far
       Unit w, wn;
-      int u = next_busy<INL>(p, blockIdx.x, w);
+      int u = next_busy<INL>(p, 0, w);  // round
       if (u >= 0) load_q(w, 0);
       for (; ok && u >= 0; ++kk) {
         const int qb = kk & 1;
-        const int un = next_busy<INL>(p, u + gridDim.x, wn);
+        const int un = next_busy<INL>(p, u + 1, wn);
         if (!tc::mbar_wait(q_full + qb, (kk >> 1) & 1, abort_flag)) { ok = false; break; }
         for (int i = 0; i < w.count; ++i, ++g) {
           const int s = g % NS, sb = g & 1;
@@ -496,7 +509,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       bool ok = true;
       int g = 0;
       Unit w;
-      for (int u = next_busy<INL>(p, blockIdx.x, w); ok && u >= 0; u = next_busy<INL>(p, u + gridDim.x, w)) {
+      for (int r = next_busy<INL>(p, 0, w); ok && r >= 0; r = next_busy<INL>(p, r + 1, w)) {
         for (int i = 0; i < w.count; ++i, ++g) {
           const int s = g % NS, pb = g & 1;
           if (!tc::mbar_wait(p_full + pb, (g >> 1) & 1, abort_flag) ||
@@ -550,12 +563,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // units.  Inline scheduling: descriptors and entries are arithmetic,
     // computed where they are needed (nothing held across the tile loop).
     Unit un_next;
-    if (!INL && blockIdx.x < nu) un_next = unit_at<INL>(p, blockIdx.x);
+    if (!INL && round_unit(0) < nu) un_next = unit_at<INL>(p, round_unit(0));
     int ent_first = 0;
     bool ent_first_ok = false;
-    for (int u = blockIdx.x; ok && u < nu; u += gridDim.x) {
-      const Unit un = INL ? unit_at<INL>(p, u) : un_next;
-      if (!INL && u + (int)gridDim.x < nu) un_next = unit_at<INL>(p, u + gridDim.x);
+    for (int r = 0; ok && round_unit(r) < nu; ++r) {
+      const int u_next = round_unit(r + 1);  // >= nu: no next unit
+      const Unit un = INL ? unit_at<INL>(p, round_unit(r)) : un_next;
+      if (!INL && u_next < nu) un_next = unit_at<INL>(p, u_next);
       const bool pre_ok = ent_first_ok;
       ent_first_ok = false;
       if (!un.present || !un.valid) continue;
@@ -583,7 +597,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (INL) {
         } else if (it + 2 < un.count) {
           ent_cur = unit_entry<INL>(un, it + 2);
-        } else if (u + (int)gridDim.x < nu && un_next.present && un_next.valid && un_next.count > 0) {
+        } else if (u_next < nu && un_next.present && un_next.valid && un_next.count > 0) {
           // this warpgroup's first entry of the next unit
           const int itn = ((g + un.count) & 1) == w ? 0 : 1;
           if (itn < un_next.count) {

@@ -82,7 +82,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 5
+#define FA_ABI_VERSION 6
 
 typedef enum {
   FA_OK = 0,
@@ -183,7 +183,18 @@ typedef enum { FA_TILE_EMPTY = 0, FA_TILE_FULL = 1, FA_TILE_PARTIAL = 2 } fa_til
  *   top-k masks only: int32 e[n_seq][Hq][Sk] at workspace + off_topk_e, the
  *     first query row at which key j is no longer kept (key j is kept on rows
  *     i with j <= i + Sk - Sq and i < e; INT32_MAX = never dropped,
- *     INT32_MIN = never kept). */
+ *     INT32_MIN = never kept).
+ *   top-k masks on the PREFILL path: the keys some row of an item keeps,
+ *     gathered (the attention kernel computes exactly these keys, as dense
+ *     128-key tiles): counts[item] = number of gathered tiles and tiles[]
+ *     entry t = (t << 1) | PARTIAL for gathered tile t (FULL: every row of
+ *     the item keeps every key of the tile); at workspace + off_topk_list,
+ *     per item n_k_tiles * 128 entries of two uint32, the first
+ *     counts[item] * 128 set: first the keys every row of the item keeps,
+ *     then the others, each group in key order; x = key | lo << 16 |
+ *     hi << 24 where the item's rows row0 + lo .. row0 + hi - 1 keep the key
+ *     (row0 = first row of the item; lo = 128, hi = 0 pads the last tile),
+ *     y = the key's bias z * log2(e) as fp32 bits. */
 typedef struct {
   int32_t path;            /* fa_path */
   int32_t n_seq;
@@ -200,6 +211,7 @@ typedef struct {
   size_t off_tiles;
   size_t off_stats;
   size_t off_topk_e;       /* 0 unless the mask is FA_MASK_TOPK */
+  size_t off_topk_list;    /* 0 unless FA_MASK_TOPK on the PREFILL path */
   int64_t n_kernels;       /* kernel launches one fa_fwd call enqueues */
   size_t workspace_bytes;  /* minimum workspace size */
 } fa_plan;

@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmfa_gb300.so")
 
 # FA_ABI_VERSION of include/fa.h that the structures below describe
-ABI_VERSION = 5
+ABI_VERSION = 6
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = 1
@@ -66,7 +66,8 @@ class fa_plan(ctypes.Structure):
                 ("tiles_per_split", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("n_items", ctypes.c_int64), ("off_counts", ctypes.c_size_t),
                 ("off_tiles", ctypes.c_size_t), ("off_stats", ctypes.c_size_t),
-                ("off_topk_e", ctypes.c_size_t), ("n_kernels", ctypes.c_int64),
+                ("off_topk_e", ctypes.c_size_t), ("off_topk_list", ctypes.c_size_t),
+                ("n_kernels", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):

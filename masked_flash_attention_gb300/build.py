@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmfa_gb300.so")
-SOURCES = ["api.cu", "sched.cu", "decode.cu", "prefill_sm103.cu", "prefill_f16.cu", "backward.cu", "backward_sm103.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "sched.cu", "topk.cu", "decode.cu", "prefill_sm103.cu", "prefill_f16.cu", "backward.cu", "backward_sm103.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
          "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

@@ -59,7 +59,8 @@ struct KvNew {
 struct Plan {
   fa_plan pub;
   Params prm;
-  size_t off_summary, off_topk_e, off_topk_maxe, off_topk_sorted, off_part_o, off_part_lse;
+  size_t off_summary, off_topk_e, off_topk_maxe, off_topk_runs, off_topk_rank, off_topk_rho, off_topk_list,
+      off_topk_full, off_part_o, off_part_lse;
 };
 
 int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
@@ -297,6 +298,14 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
     P.n_heads_sched = (int32_t)Hkv;
     P.n_row_tiles = ceil_div(Sq * G, kDecodeRows);
   }
+  // the top-k prefill gathers K/V rows through a 2-D view [B * Sk rows, one
+  // row of all K/V heads]: each batch's rows must follow the previous batch's
+  // rows and a row's heads must fit inside the row stride
+  if (P.path == FA_PATH_PREFILL && mask_kind == FA_MASK_TOPK) {
+    const bool kv_rows = (n_seq == 1 || (P.k_sb == Sk * P.k_ss && P.v_sb == Sk * P.v_ss)) &&
+                         (Hkv - 1) * P.k_sh + d <= P.k_ss && (Hkv - 1) * P.v_sh + d <= P.v_ss;
+    if (!kv_rows) return FA_ERR_UNSUPPORTED;
+  }
   // prefill carries ALiBi only without a dense or top-k mask (decode: any)
   if (P.path == FA_PATH_PREFILL && P.alibi && mask_kind != FA_MASK_NONE) return FA_ERR_UNSUPPORTED;
   // without a dense or top-k mask the pair rules alone decide every tile: the
@@ -334,8 +343,17 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   if (mask_kind == FA_MASK_TOPK) off = align_up(off + (size_t)n_seq * Hq * Sk * 4);
   pl->off_topk_maxe = off;
   if (mask_kind == FA_MASK_TOPK) off = align_up(off + (size_t)n_seq * Hq * n_kt_alloc * 4);
-  pl->off_topk_sorted = off;
-  if (mask_kind == FA_MASK_TOPK) off = align_up(off + (size_t)n_seq * Hq * n_kt_alloc * kKeysPerTile * 8);
+  pl->off_topk_runs = off;
+  if (mask_kind == FA_MASK_TOPK) off = align_up(off + (size_t)n_seq * Hq * topk_n_runs((int)Sk) * 2048 * 8);
+  pl->off_topk_rank = off;
+  if (mask_kind == FA_MASK_TOPK) off = align_up(off + (size_t)n_seq * Hq * Sk * 4);
+  pl->off_topk_rho = off;
+  if (mask_kind == FA_MASK_TOPK) off = align_up(off + (size_t)n_seq * Hq * Sk * 4);
+  pl->off_topk_list = off;
+  if (mask_kind == FA_MASK_TOPK && P.path == FA_PATH_PREFILL)
+    off = align_up(off + (size_t)P.n_items * n_kt_alloc * kKeysPerTile * 8);
+  pl->off_topk_full = off;
+  if (mask_kind == FA_MASK_TOPK && P.path == FA_PATH_PREFILL) off = align_up(off + (size_t)P.n_items * 4);
   pl->off_part_o = off;
   if (P.n_splits > 1) off = align_up(off + (size_t)P.n_items * P.n_splits * kDecodeRows * d * 4);
   pl->off_part_lse = off;
@@ -352,9 +370,13 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   pub.tiles_per_split = P.tiles_per_split;
   pub.n_items = P.n_items;
   pub.off_topk_e = (mask_kind == FA_MASK_TOPK) ? pl->off_topk_e : 0;
+  pub.off_topk_list = (mask_kind == FA_MASK_TOPK && P.path == FA_PATH_PREFILL) ? pl->off_topk_list : 0;
+  // top-k: sort runs, ranks, expiry rows, then the gathered lists (prefill,
+  // which replace the scheduler kernel) or the tile maxima (decode)
   pub.n_kernels = P.n_items == 0 ? 0
                   : P.sched_inline ? 1
-                  : 2 + (P.n_splits > 1) + (mask_kind == FA_MASK_DENSE) + 2 * (mask_kind == FA_MASK_TOPK);
+                  : (mask_kind == FA_MASK_TOPK && P.path == FA_PATH_PREFILL) ? 5
+                  : 2 + (P.n_splits > 1) + (mask_kind == FA_MASK_DENSE) + 4 * (mask_kind == FA_MASK_TOPK);
   pub.workspace_bytes = off;
   P.n_kt = n_kt_alloc;
   return FA_OK;
@@ -370,7 +392,11 @@ void bind_workspace(Plan* pl, void* ws) {
   P.mask_summary = base + pl->off_summary;
   P.topk_e = reinterpret_cast<int32_t*>(base + pl->off_topk_e);
   P.topk_tile_maxe = reinterpret_cast<int32_t*>(base + pl->off_topk_maxe);
-  P.topk_sorted = reinterpret_cast<uint64_t*>(base + pl->off_topk_sorted);
+  P.topk_runs = reinterpret_cast<uint64_t*>(base + pl->off_topk_runs);
+  P.topk_rank = reinterpret_cast<int32_t*>(base + pl->off_topk_rank);
+  P.topk_rho = reinterpret_cast<int32_t*>(base + pl->off_topk_rho);
+  P.topk_list = reinterpret_cast<uint2*>(base + pl->off_topk_list);
+  P.topk_full = reinterpret_cast<int32_t*>(base + pl->off_topk_full);
   P.part_o = reinterpret_cast<float*>(base + pl->off_part_o);
   P.part_lse = reinterpret_cast<float*>(base + pl->off_part_lse);
 }
@@ -548,7 +574,9 @@ int run_plan(Plan& pl, const fa_opts* opts) {
   if (!P.sched_inline) {
     if (P.mask_kind == FA_MASK_DENSE) e = launch_mask_summary(P, st);
     if (e == cudaSuccess && P.mask_kind == FA_MASK_TOPK) e = launch_topk_prep(P, st);
-    if (e == cudaSuccess) e = launch_classify(P, st);
+    // on the many-row path the top-k preparation has listed each unit's keys
+    const bool listed = P.mask_kind == FA_MASK_TOPK && P.path == FA_PATH_PREFILL;
+    if (e == cudaSuccess && !listed) e = launch_classify(P, st);
   }
   cudaEvent_t ev_begin = static_cast<cudaEvent_t>(opts->event_begin);
   if (e == cudaSuccess)

@@ -90,8 +90,12 @@ struct Params {
   unsigned long long* stats;  // [3]
   uint8_t* mask_summary; // [m_nb][m_nh][n_row_tiles][n_kt]
   int32_t* topk_e;       // [n_seq][Hq][Sk]: first query row at which key j is dropped
-  int32_t* topk_tile_maxe;  // [n_seq][Hq][n_kt]
-  uint64_t* topk_sorted; // [n_seq][Hq][n_kt * 128]: per 128-key bucket, its keys' words sorted
+  int32_t* topk_tile_maxe;  // [n_seq][Hq][n_kt] (few-row path)
+  uint64_t* topk_runs;   // [n_seq][Hq][runs][2048]: sorted runs of (z order << 32 | index) words
+  int32_t* topk_rank;    // [n_seq][Hq][Sk]: key of rank t (0 = best)
+  int32_t* topk_rho;     // [n_seq][Hq][Sk]: rank of key j
+  uint2* topk_list;      // [n_items][n_kt * 128]: gathered keys of each unit (many-row path)
+  int32_t* topk_full;    // [n_items]: leading gathered tiles whose keys every row of the unit keeps
 
   // decode split-KV
   int32_t n_splits, tiles_per_split;
@@ -104,7 +108,10 @@ struct Params {
 
 // ---- launchers (defined in the .cu files; all enqueue on `st`) ----
 cudaError_t launch_mask_summary(const Params& p, cudaStream_t st);
+// Top-k preparation (topk.cu): expiry rows, then the gathered key lists and
+// counts (many-row path) or the per-tile maxima (few-row path).
 cudaError_t launch_topk_prep(const Params& p, cudaStream_t st);
+int topk_n_runs(int Sk);
 cudaError_t launch_classify(const Params& p, cudaStream_t st);
 // The attention launchers record `ev_begin` (if not null) on the stream right
 // before the kernel itself is enqueued, after all host-side preparation.

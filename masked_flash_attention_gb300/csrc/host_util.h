@@ -67,4 +67,21 @@ inline bool encode_4d_bf16(CUtensorMap* m, const void* base, int d, int heads, i
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map of 2-byte elements {cols, rows} (row stride s_row elements) with
+// box {box_cols, 1} and 128-byte swizzle, for tile::gather4 loads of single
+// rows.  False when the driver rejects the layout or has no encoder.
+inline bool encode_rows_bf16(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t s_row,
+                             int box_cols, bool f16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)s_row * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, 1};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace mfa

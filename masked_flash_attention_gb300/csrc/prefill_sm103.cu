@@ -85,12 +85,15 @@ struct PCfg {
   static constexpr int kVOff = kKOff + NS * kTileBytes;
   static constexpr int kAuxOff = kVOff + NS * kTileBytes;
   // aux: barriers and flags (512 B), row references [2][128] floats, row
-  // sums [2][128] floats, top-k staging [2 warpgroups][2][128] int2
+  // sums [2][128] floats, top-k staging [2 warpgroups][2 buffers]
   static constexpr int kRedOff = kAuxOff + 512;
   static constexpr int kSumOff = kRedOff + 2 * 128 * 4;
   static constexpr int kTopkOff = kSumOff + 2 * 128 * 4;
   // output staging: per softmax warp 32 rows x 32 output columns
-  static constexpr int kStageOff = (kTopkOff + 2 * 2 * 128 * 8 + 1023) / 1024 * 1024;  // swizzle-aligned
+  // top-k staging, per warpgroup and buffer: first keeping row, number of
+  // keeping rows (int) and bias (fp32) of each of the tile's 128 columns
+  static constexpr int kTopkBuf = 3 * 128 * 4;
+  static constexpr int kStageOff = (kTopkOff + 2 * 2 * kTopkBuf + 1023) / 1024 * 1024;  // swizzle-aligned
   static constexpr int kSmem = kStageOff + 8 * 2048 + 1024;  // + alignment slack
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
   static_assert(kStageOff % 1024 == 0, "TMA store source alignment");
@@ -115,7 +118,7 @@ struct Unit {
 __device__ __forceinline__ int floor_div128(int a) { return a >= 0 ? a / 128 : -((127 - a) / 128); }
 
 // Unit u, longest query tiles first (row tile descending), q-heads fastest.
-template <bool INL>
+template <bool INL, bool GTH = false>
 __device__ __forceinline__ Unit unit_at(const Params& p, int u) {
   Unit w;
   const int per = p.n_seq * p.Hq;
@@ -160,15 +163,26 @@ __device__ __forceinline__ Unit unit_at(const Params& p, int u) {
     w.valid = c >= 0;
     w.count = c > 0 ? c : 0;
     w.tiles = p.item_tiles + item * p.n_kt;
+    if constexpr (GTH) w.fl = w.present ? __ldg(p.topk_full + item) : 0;  // leading FULL gathered tiles
   }
   return w;
 }
 
-// Entry i of a unit's key-tile list: (key tile << 1) | PARTIAL.
-template <bool INL>
+// Entry i of a unit's key-tile list: (key tile << 1) | PARTIAL.  A top-k
+// unit's tiles are gathered keys (GTH): always PARTIAL, no key tile.
+template <bool INL, bool GTH = false>
 __device__ __forceinline__ int unit_entry(const Unit& w, int i) {
-  if constexpr (INL) return ((w.kt0 + i) << 1) | ((i < w.fl || i > w.fh) ? 1 : 0);
+  if constexpr (GTH) return i < w.fl ? 0 : 1;
+  else if constexpr (INL) return ((w.kt0 + i) << 1) | ((i < w.fl || i > w.fh) ? 1 : 0);
   else return __ldg(w.tiles + i);
+}
+
+// The gathered keys of a top-k unit: n_kt * 128 entries (x = key index |
+// first keeping row << 16 | first row past the keeping ones << 24, rows
+// relative to the unit's tile; y = bias in log2 units); count * 128 are set.
+__device__ __forceinline__ const uint2* unit_glist(const Params& p, const Unit& w) {
+  const int64_t item = ((int64_t)w.b * p.Hq + w.h) * p.n_row_tiles + w.rt;
+  return p.topk_list + item * ((int64_t)p.n_kt * kKeysPerTile);
 }
 
 // Inline scheduling: the scheduler's counters (tiles scheduled FULL and
@@ -230,13 +244,13 @@ __device__ __forceinline__ int round_unit(int r) {
 }
 
 // Next round at or after r whose unit has key tiles, or -1.
-template <bool INL>
+template <bool INL, bool GTH = false>
 __device__ __forceinline__ int next_busy(const Params& p, int r, Unit& w) {
   const int n = n_units(p);
   for (;; ++r) {
     const int u = round_unit(r);
     if (u >= n) return -1;
-    w = unit_at<INL>(p, u);
+    w = unit_at<INL, GTH>(p, u);
     if (w.present && w.valid && w.count > 0) return r;
   }
 }
@@ -335,6 +349,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   using C = PCfg<D>;
   constexpr int NS = C::NS;
   constexpr bool INL = (MK == FA_MASK_NONE);  // the host sets p.sched_inline exactly then
+  constexpr bool GTH = (MK == FA_MASK_TOPK);   // tiles of gathered keys (2-D K/V maps)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -393,7 +408,52 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-  if (warp == 0 || warp == 2) {
+  if (GTH && (warp == 0 || warp == 2)) {
+    // ------------------------------------------------------------ producers (gathered keys)
+    // The whole warp: each lane gathers 4 of the tile's 128 key rows (one
+    // tile::gather4 per 64-column half) from the 2-D K/V view whose row
+    // b * Sk + j holds key j of sequence b, every head side by side.
+    const bool is_k = (warp == 0);
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    unsigned char* ring = smem + (is_k ? C::kKOff : C::kVOff);
+    if (lane == 0) tc::tma_prefetch_desc(map);
+    int j = 0;
+    bool ok = true;
+    Unit w;
+    for (int r = next_busy<INL, GTH>(p, 0, w); ok && r >= 0; r = next_busy<INL, GTH>(p, r + 1, w)) {
+      const int row0 = w.b * p.Sk;
+      const int x0 = (w.h / p.G) * (int)(is_k ? p.k_sh : p.v_sh);
+      const uint4* lst = reinterpret_cast<const uint4*>(unit_glist(p, w));
+      for (int i = 0; i < w.count; ++i, ++j) {
+        const int s = j % NS;
+        // this lane's four keys (two entries per 16 bytes), read before the wait
+        const uint4 ea = __ldg(lst + (i * kKeysPerTile + 4 * lane) / 2);
+        const uint4 eb = __ldg(lst + (i * kKeysPerTile + 4 * lane) / 2 + 1);
+        bool go = true;
+        if (lane == 0 && j >= NS) go = tc::mbar_wait(empty + s, ((j / NS) - 1) & 1, abort_flag);
+        go = __shfl_sync(0xffffffffu, go, 0);
+        if (!go) {
+          if (lane == 0) fail(p, abort_flag, is_k ? 1 : 7);
+          ok = false;
+          break;
+        }
+        if (lane == 0) tc::mbar_arrive_expect_tx(full + s, C::kTileBytes);
+        __syncwarp();
+        for (int c = 0; c < D / 64; ++c)
+          tc::tma_gather4_2d(ring + s * C::kTileBytes + c * 16384 + lane * 512, map, full + s, x0 + c * 64,
+                             row0 + (int)(ea.x & 0xffffu), row0 + (int)(ea.z & 0xffffu),
+                             row0 + (int)(eb.x & 0xffffu), row0 + (int)(eb.z & 0xffffu));
+      }
+    }
+    if (lane == 0 && *abort_flag) {
+      // let the copies already issued land before the CTA can exit
+      const int first = j > NS ? j - NS : 0;
+      for (int jj = first; jj < j; ++jj) tc::mbar_wait_drain(full + jj % NS, (jj / NS) & 1, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------ producers
     // K (warp 0) and V (warp 2) tiles of every busy unit, in order, through
     // their rings; a stage is refilled once the MMAs that read it are done.
@@ -407,7 +467,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int j = 0;
       bool ok = true;
       Unit w;
-      for (int r = next_busy<INL>(p, 0, w); ok && r >= 0; r = next_busy<INL>(p, r + 1, w)) {
+      for (int r = next_busy<INL, GTH>(p, 0, w); ok && r >= 0; r = next_busy<INL, GTH>(p, r + 1, w)) {
         const int kv_row0 = p.cu_k ? p.cu_k[w.b] : 0;
         const int kv_b = p.cu_k ? 0 : w.b;
         const int g = w.h / p.G;
@@ -455,11 +515,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       bool ok = true;
       int g = 0, kk = 0;  // tiles and busy units so far
       Unit w, wn;
-      int u = next_busy<INL>(p, 0, w);  // round
+      int u = next_busy<INL, GTH>(p, 0, w);  // round
       if (u >= 0) load_q(w, 0);
       for (; ok && u >= 0; ++kk) {
         const int qb = kk & 1;
-        const int un = next_busy<INL>(p, u + 1, wn);
+        const int un = next_busy<INL, GTH>(p, u + 1, wn);
         if (!tc::mbar_wait(q_full + qb, (kk >> 1) & 1, abort_flag)) { ok = false; break; }
         for (int i = 0; i < w.count; ++i, ++g) {
           const int s = g % NS, sb = g & 1;
@@ -509,7 +569,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       bool ok = true;
       int g = 0;
       Unit w;
-      for (int r = next_busy<INL>(p, 0, w); ok && r >= 0; r = next_busy<INL>(p, r + 1, w)) {
+      for (int r = next_busy<INL, GTH>(p, 0, w); ok && r >= 0; r = next_busy<INL, GTH>(p, r + 1, w)) {
         for (int i = 0; i < w.count; ++i, ++g) {
           const int s = g % NS, pb = g & 1;
           if (!tc::mbar_wait(p_full + pb, (g >> 1) & 1, abort_flag) ||
@@ -553,7 +613,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const uint32_t lane_base = tbase + ((uint32_t)(32 * wq) << 16);
     float* refv = reinterpret_cast<float*>(smem + C::kRedOff);  // [2 tile parity][128]
     float* rsum = reinterpret_cast<float*>(smem + C::kSumOff);  // [2 warpgroups][128]
-    int2* kbuf = reinterpret_cast<int2*>(smem + C::kTopkOff) + w * 256;  // [2][128]
+    unsigned char* kbuf = smem + C::kTopkOff + w * 2 * C::kTopkBuf;  // [2 buffers][lo, len, bias][128]
     constexpr int kHalfD = D / 2;  // O columns each warpgroup rescales and stores
     bool ok = true;
     int g = 0, kk = 0;  // tiles and busy units so far (all of them, both parities)
@@ -562,14 +622,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // read a unit ahead, so that no global-memory latency sits between two
     // units.  Inline scheduling: descriptors and entries are arithmetic,
     // computed where they are needed (nothing held across the tile loop).
+    // (gathered top-k units: the same, their entries being arithmetic too)
+    constexpr bool kArith = INL || GTH;
     Unit un_next;
-    if (!INL && round_unit(0) < nu) un_next = unit_at<INL>(p, round_unit(0));
+    if (!kArith && round_unit(0) < nu) un_next = unit_at<INL, GTH>(p, round_unit(0));
     int ent_first = 0;
     bool ent_first_ok = false;
     for (int r = 0; ok && round_unit(r) < nu; ++r) {
       const int u_next = round_unit(r + 1);  // >= nu: no next unit
-      const Unit un = INL ? unit_at<INL>(p, round_unit(r)) : un_next;
-      if (!INL && u_next < nu) un_next = unit_at<INL>(p, u_next);
+      const Unit un = kArith ? unit_at<INL, GTH>(p, round_unit(r)) : un_next;
+      if (!kArith && u_next < nu) un_next = unit_at<INL, GTH>(p, u_next);
       const bool pre_ok = ent_first_ok;
       ent_first_ok = false;
       if (!un.present || !un.valid) continue;
@@ -583,18 +645,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       int jlo_r, jhi_r;
       row_key_range(p, i, q_len, kv_len, off, jlo_r, jhi_r);
+      const uint2* glist = GTH ? unit_glist(p, un) : nullptr;
+
       const float alibi_l2 = AL ? __ldg(p.alibi + h) * kLog2e : 0.f;  // ALiBi slope, log2 units
       float m_ref = -INFINITY;  // reference after the last tile seen
       float r_own = -INFINITY;  // reference this warpgroup's row sum is against
       float l = 0.f;
       // the first tile of the unit is this warpgroup's if g is of its parity
       const int it0 = (g & 1) == w ? 0 : 1;
-      int ent_cur = (INL || !pre_ok) ? (it0 < un.count ? unit_entry<INL>(un, it0) : 0) : ent_first;
+      // gathered keys: this thread's column entry of the warpgroup's next tile,
+      // read a tile ahead so that its latency hides behind the current one
+      uint2 gnext = make_uint2(0, 0);
+      if (GTH && it0 < un.count) gnext = __ldg(glist + it0 * kKeysPerTile + wtid);
+      int ent_cur = (kArith || !pre_ok) ? (it0 < un.count ? unit_entry<INL, GTH>(un, it0) : 0) : ent_first;
       for (int it = it0; it < un.count; it += 2) {
         const int gt = g + it;  // global index of this tile
         const int par = w;      // == gt & 1
-        const int ent = INL ? unit_entry<INL>(un, it) : ent_cur;
-        if (INL) {
+        const int ent = kArith ? unit_entry<INL, GTH>(un, it) : ent_cur;
+        if (kArith) {
         } else if (it + 2 < un.count) {
           ent_cur = unit_entry<INL>(un, it + 2);
         } else if (u_next < nu && un_next.present && un_next.valid && un_next.count > 0) {
@@ -609,15 +677,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const bool part = ent & 1;
         const int kb = (gt >> 1) & 1;  // top-k staging buffer
         if (MK == FA_MASK_TOPK) {
-          const int jj = j0 + wtid;
-          int2 v = make_int2(kRowNever, 0);
-          if (jj < kv_len) {
-            const int64_t bh = (int64_t)b * p.Hq + h;
-            v.x = __ldg(p.topk_e + bh * p.Sk + jj);
-            v.y = __float_as_int(
-                __ldg(p.z + (int64_t)b * p.z_sb + (int64_t)h * p.z_sh + (int64_t)jj * p.z_sk) * kLog2e);
-          }
-          kbuf[kb * 128 + wtid] = v;
+          // column wtid of the gathered tile: the rows of this tile that keep
+          // its key ([lo, hi), 8 bits each) and its bias
+          const uint2 en = gnext;
+          if (it + 2 < un.count) gnext = __ldg(glist + (it + 2) * kKeysPerTile + wtid);
+          int* kb_lo = reinterpret_cast<int*>(kbuf + kb * C::kTopkBuf);
+          const int lo = (int)((en.x >> 16) & 0xffu), hi = (int)(en.x >> 24);
+          kb_lo[wtid] = lo;
+          kb_lo[128 + wtid] = hi - lo;  // hi <= lo (padding) reads as no row
+          reinterpret_cast<uint32_t*>(kb_lo + 256)[wtid] = en.y;
           tc::mbar_arrive(kready + 2 * w + kb);
           if (!tc::mbar_wait(kready + 2 * w + kb, (gt >> 2) & 1, abort_flag)) { ok = false; break; }
         }
@@ -640,10 +708,41 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         tc::mbar_arrive_relaxed(s_free + par);  // the QK two tiles on may overwrite this S buffer
         // logits in log2 units; a FULL tile without soft-cap keeps raw scores
         // and folds the scale into the exponent below
-        const bool plain = !SC && !part && !AL;
+        const bool plain = !SC && !part && !AL && MK != FA_MASK_TOPK;
         float mx;
         if (plain) {
           mx = row_max128(x) * p.scale_log2;
+        } else if constexpr (MK == FA_MASK_TOPK) {
+          // gathered keys: logit + bias; a PARTIAL tile also drops the keys
+          // this row does not keep ((unsigned)(row - lo) >= number of rows)
+          const int* kb_lo = reinterpret_cast<const int*>(kbuf + kb * C::kTopkBuf);
+          const float4* kb_z = reinterpret_cast<const float4*>(kb_lo + 256);
+          const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float4 z4 = kb_z[c];
+            float2 a = x[2 * c], bq = x[2 * c + 1];
+            if (SC) {
+              a = make_float2(softcap_log2(a.x * p.scale, p.softcap, p.inv_softcap) + z4.x,
+                              softcap_log2(a.y * p.scale, p.softcap, p.inv_softcap) + z4.y);
+              bq = make_float2(softcap_log2(bq.x * p.scale, p.softcap, p.inv_softcap) + z4.z,
+                               softcap_log2(bq.y * p.scale, p.softcap, p.inv_softcap) + z4.w);
+            } else {
+              a = fma2(a, sl2, make_float2(z4.x, z4.y));
+              bq = fma2(bq, sl2, make_float2(z4.z, z4.w));
+            }
+            if (part) {
+              const int4 lo4 = reinterpret_cast<const int4*>(kb_lo)[c];
+              const int4 n4 = reinterpret_cast<const int4*>(kb_lo + 128)[c];
+              a.x = (unsigned)(row - lo4.x) < (unsigned)n4.x ? a.x : -INFINITY;
+              a.y = (unsigned)(row - lo4.y) < (unsigned)n4.y ? a.y : -INFINITY;
+              bq.x = (unsigned)(row - lo4.z) < (unsigned)n4.z ? bq.x : -INFINITY;
+              bq.y = (unsigned)(row - lo4.w) < (unsigned)n4.w ? bq.y : -INFINITY;
+            }
+            x[2 * c] = a;
+            x[2 * c + 1] = bq;
+          }
+          mx = row_max128(x);
         } else {
           const int clo = jlo_r - j0, chi = jhi_r - j0;
           const float* mrow = nullptr;
@@ -662,11 +761,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             bool keep = !part || (e >= clo && e <= chi);
             if (MK == FA_MASK_DENSE && part) {
               if (keep) v += __ldg(mrow + (int64_t)e * p.m_sk) * kLog2e;
-            }
-            if (MK == FA_MASK_TOPK) {
-              const int2 kv = kbuf[kb * 128 + e];
-              keep = keep && (i < kv.x);
-              v += __int_as_float(kv.y);
             }
             v = keep ? v : -INFINITY;
             if (e & 1) x[e >> 1].y = v; else x[e >> 1].x = v;
@@ -902,10 +996,19 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
   // without a valid map (unusual strides) the epilogue uses plain stores
   const int o_tma = encode_out(&mo, p.o, D, p.Hq, q_rows, qb, p.o_sh, p.o_ss, o_sb, F16) ? 1 : 0;
   if (!o_tma) memset(&mo, 0, sizeof(mo));
-  if (!encode_bshd(&mq, p.q, D, p.Hq, q_rows, qb, p.q_sh, p.q_ss, q_sb, F16) ||
-      !encode_bshd(&mk, p.k, D, p.Hkv, k_rows, kb, p.k_sh, p.k_ss, k_sb, F16) ||
-      !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb, F16))
+  if (!encode_bshd(&mq, p.q, D, p.Hq, q_rows, qb, p.q_sh, p.q_ss, q_sb, F16)) return cudaErrorInvalidValue;
+  if (p.mask_kind == FA_MASK_TOPK) {
+    // gathered keys: 2-D views with row b * Sk + j = key j of sequence b (all
+    // heads of a key side by side; the planner checked that the layout is one)
+    if (vk) return cudaErrorInvalidValue;
+    const int64_t rows = (int64_t)p.n_seq * p.Sk;
+    if (!encode_rows_bf16(&mk, p.k, (int64_t)(p.Hkv - 1) * p.k_sh + D, rows, p.k_ss, 64, F16) ||
+        !encode_rows_bf16(&mv, p.v, (int64_t)(p.Hkv - 1) * p.v_sh + D, rows, p.v_ss, 64, F16))
+      return cudaErrorInvalidValue;
+  } else if (!encode_bshd(&mk, p.k, D, p.Hkv, k_rows, kb, p.k_sh, p.k_ss, k_sb, F16) ||
+             !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb, F16)) {
     return cudaErrorInvalidValue;
+  }
   // one CTA per SM (persistent), never more CTAs than work units
   const int64_t units = (int64_t)p.n_row_tiles * p.n_seq * p.Hq;
   if (units <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(fa.lib, n), n
         assert ctypes.cast(getattr(fa.lib, n), ctypes.c_void_p).value
-    assert fa.fa_abi_version() == 5 == _lib.ABI_VERSION
+    assert fa.fa_abi_version() == 6 == _lib.ABI_VERSION
     assert fa.fa_status_string(0) == "ok"
 
 
@@ -193,3 +193,19 @@ def test_noalloc_refuses_workspace_and_events():
         with pytest.raises(fa.FaError) as e:
             fa.fa_fwd_noalloc(q, q, q, out=q, lse=T(1, 2, 4, dtype=torch.float32), **kw)
         assert e.value.status == _lib.FA_ERR_INVALID_ARG
+
+
+def test_topk_prefill_layout_rule():
+    """The many-row top-k path gathers key rows from a view where row
+    b * Sk + j holds key j of sequence b with its heads side by side: a
+    batch-contiguous bshd layout is taken, a [B, H, S, d] layout passed as a
+    transposed view is refused (FA_ERR_UNSUPPORTED; the few-row path takes
+    any layout)."""
+    q = T(1, 300, 2, 64)
+    z = torch.zeros(1, 2, 300)
+    k = T(1, 300, 2, 64)
+    assert plan(q, k, k, causal=True, zero_hold_states=z, keep_window=50)[0] == 0
+    kt = T(1, 2, 300, 64).transpose(1, 2)
+    assert plan(q, kt, kt, causal=True, zero_hold_states=z, keep_window=50)[0] == _lib.FA_ERR_UNSUPPORTED
+    qd = T(1, 2, 2, 64)   # few rows: decode path, any layout
+    assert plan(qd, kt, kt, causal=True, zero_hold_states=z[:, :, :300], keep_window=50)[0] == 0

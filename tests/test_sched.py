@@ -142,11 +142,69 @@ def test_dense_mask_classes_exact():
     assert np.all(want[got == 1] == 1)
 
 
+LOG2E32 = np.float32(1.4426950408889634)
+
+
+def check_gathered_lists(case, plan, ws, z, keep, units=None):
+    """Top-k on the many-row path: each unit's gathered key list holds the
+    keys some row of the unit keeps by the oracle's per-row sort -- first those
+    every row of the unit keeps, then the others, each group in key order;
+    each entry's rows [lo, hi) are exactly the unit's rows keeping that key;
+    its bias is z_j * log2(e) (fp32); the last tile is padded with entries no
+    row keeps; counts[item] is the number of 128-key tiles, and exactly the
+    tiles made only of keys every row keeps are FULL in the work list."""
+    p = case["params"]
+    B, Sq, H, _ = case["q"].shape
+    Sk = case["k"].shape[1]
+    n_rt, nk, KT = plan["n_row_tiles"], plan["n_k_tiles"], plan["keys_per_tile"]
+    n_items = plan["n_items"]
+    w = ws.cpu()
+    counts = w[plan["off_counts"]:plan["off_counts"] + 4 * n_items].view(torch.int32).numpy()
+    tiles = w[plan["off_tiles"]:plan["off_tiles"] + 4 * n_items * nk].view(torch.int32).numpy().reshape(n_items, nk)
+    lists = w[plan["off_topk_list"]:plan["off_topk_list"] + 8 * n_items * nk * KT].view(torch.int32).numpy()
+    lists = lists.reshape(n_items, nk * KT, 2).view(np.uint32)
+    keys = np.arange(Sk)
+    for b in range(B):
+        for h in range(H):
+            zn = z[b, h].numpy()
+            ok = O.allowed_pairs(np.arange(Sq), keys, Sq, Sk, causal=p["causal"])
+            kept = np.zeros((Sq, Sk), bool)
+            for rt in range(n_rt):
+                if units is not None and (b, h, rt) not in units:
+                    continue
+                r0, r1 = rt * 128, min(rt * 128 + 127, Sq - 1)
+                for i in range(r0, r1 + 1):
+                    kept[i, O.topk_kept_row(zn, ok[i], keep)] = True
+                item = (b * H + h) * n_rt + rt
+                every = kept[r0:r1 + 1].all(axis=0)
+                union = np.nonzero(kept[r0:r1 + 1].any(axis=0))[0]
+                union = np.concatenate([union[every[union]], union[~every[union]]])
+                n_every = int(every.sum())
+                ent = lists[item, :counts[item] * KT]
+                assert counts[item] == -(-len(union) // KT), (b, h, rt)
+                want_tiles = [(t << 1) | int(t >= n_every // KT) for t in range(counts[item])]
+                assert list(tiles[item, :counts[item]]) == want_tiles, (b, h, rt)
+                real, pad = ent[:len(union)], ent[len(union):]
+                assert np.array_equal(real[:, 0] & 0xffff, union), (b, h, rt)
+                lo, hi = (real[:, 0] >> 16) & 0xff, real[:, 0] >> 24
+                rows = kept[r0:r1 + 1, union]                  # [rows, keys]
+                first = rows.argmax(axis=0)
+                last = rows.shape[0] - 1 - rows[::-1].argmax(axis=0)
+                assert np.array_equal(lo, first) and np.array_equal(hi, last + 1), (b, h, rt)
+                assert all(rows[first[c]:last[c] + 1, c].all() for c in range(len(union))), "kept rows not an interval"
+                bias = (zn[union].astype(np.float32) * LOG2E32).view(np.uint32)
+                assert np.array_equal(real[:, 1], bias), (b, h, rt)
+                assert np.all(((pad[:, 0] >> 16) & 0xff) == 128) and np.all((pad[:, 0] >> 24) == 0)
+
+
 def test_topk_kept_sets_exact(golden):
     g = golden("fsa_mask_agreement.json")
     for seed, Sq, Sk, keep, causal, ties in [(0, 300, 300, 40, True, True), (1, 64, 500, 100, True, False),
                                              (2, 7, 260, 30, False, True), (3, 4, 4, 2, True, False),
-                                             (4, 40, 9000, 3000, True, True)]:  # > 64 key buckets
+                                             (4, 40, 9000, 3000, True, True),   # > 64 key buckets
+                                             (5, 260, 700, 200, True, True),    # many rows over past keys
+                                             (6, 200, 333, 50, False, True),    # many rows, not causal
+                                             (7, 130, 2500, 3000, True, False)]:  # keep_window above every row
         case = W.random_case(seed, B=1, Sq=Sq, Sk=Sk, Hq=2, Hkv=2, d=64, causal=causal)
         z = W.random_zero_hold_states(seed, 1, 2, Sk, ties=ties)
         plan, counts, tiles, stats, ws = worklist(case, zero_hold_states=z, keep_window=keep)
@@ -163,10 +221,13 @@ def test_topk_kept_sets_exact(golden):
                 n_match += int((got == want).sum())
                 n_total += Sk
         assert n_match / n_total == g["position_match"]
-        # EMPTY tiles are a subset of the truly empty ones, and no kept pair is lost
-        got = gpu_classes(plan, counts, tiles)
-        want = oracle_classes(case, plan, zero_hold_states=z, keep_window=keep)
-        assert np.all(want[got == 0] == 0)
+        if plan["path"] == fa._lib.FA_PATH_PREFILL:
+            check_gathered_lists(case, dict(plan), ws, z, keep)
+        else:
+            # EMPTY tiles are a subset of the truly empty ones, and no kept pair is lost
+            got = gpu_classes(plan, counts, tiles)
+            want = oracle_classes(case, plan, zero_hold_states=z, keep_window=keep)
+            assert np.all(want[got == 0] == 0)
 
 
 def test_inconsistent_lengths_are_reported():
@@ -211,6 +272,9 @@ def test_topk_kept_sets_at_full_workload_shape():
                 want[O.topk_kept_row(zn, cand, keep)] = True
                 got = (keys <= i + off) & (i < e[b, h])
                 assert np.array_equal(got, want), (b, h, i, int((got != want).sum()))
+    # the gathered lists of units where the window is filling, just full, and at the end
+    units = {(0, 0, 0), (0, 3, 15), (0, 5, 16), (1, 7, 17), (1, 15, 63), (0, 9, 40)}
+    check_gathered_lists(case, dict(plan), ws, z, keep, units=units)
 
 
 @pytest.mark.parametrize("seed,B,Sq,Sk,Hq,Hkv,d,extra", [

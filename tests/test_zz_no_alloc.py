@@ -7,6 +7,8 @@ fa_fwd (which uses a caller-provided workspace) within the parity tolerances,
 on two calls in a row, since the static scratch keeps the previous call's
 contents; one case also goes straight to the fp64 oracle.  The file is
 named to be collected last."""
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -95,13 +97,22 @@ def test_noalloc_allocates_nothing():
     lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=DEV)
     fa.fa_fwd_noalloc(q, k, v, out=out, lse=lse, **p)
     torch.cuda.synchronize()
-    alloc0 = torch.cuda.memory_allocated(DEV)
-    free0 = torch.cuda.mem_get_info(DEV)[0]
-    for _ in range(5):
-        fa.fa_fwd_noalloc(q, k, v, out=out, lse=lse, **p)
-        torch.cuda.synchronize()
-    assert torch.cuda.memory_allocated(DEV) == alloc0
-    assert torch.cuda.mem_get_info(DEV)[0] == free0
+    # tensors left by earlier tests must not be freed in the middle of the
+    # measurement (that would lower the counts): collect first, then hold
+    gc.collect()
+    gc.disable()
+    try:
+        alloc0 = torch.cuda.memory_allocated(DEV)
+        free0 = torch.cuda.mem_get_info(DEV)[0]
+        for _ in range(5):
+            fa.fa_fwd_noalloc(q, k, v, out=out, lse=lse, **p)
+            torch.cuda.synchronize()
+        alloc1 = torch.cuda.memory_allocated(DEV)
+        free1 = torch.cuda.mem_get_info(DEV)[0]
+    finally:
+        gc.enable()
+    assert alloc1 == alloc0
+    assert free1 == free0
 
 
 def test_noalloc_refuses_device_validation():

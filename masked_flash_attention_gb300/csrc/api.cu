@@ -313,6 +313,8 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   P.sched_inline = (P.path == FA_PATH_PREFILL && mask_kind == FA_MASK_NONE) ? 1 : 0;
   P.n_kt = ceil_div(Sk, kKeysPerTile);
   P.n_items = n_seq * (int64_t)P.n_heads_sched * P.n_row_tiles;
+  P.div_units = make_fastdiv((uint32_t)(n_seq * Hq > 0 ? n_seq * Hq : 1));
+  P.div_hq = make_fastdiv((uint32_t)(Hq > 0 ? Hq : 1));
   if (Sq == 0 || n_seq == 0) P.n_items = 0;
 
   // split-KV factor: enough CTAs to cover the GPU a few times over

@@ -22,6 +22,11 @@ __device__ __forceinline__ int seq_klen(const Params& p, int b) {
   return p.cu_k ? (p.cu_k[b + 1] - p.cu_k[b]) : p.Sk;
 }
 
+// n / f.d for 0 <= n < 2^31 (see FastDiv).
+__device__ __forceinline__ int fast_div(int n, const FastDiv& f) {
+  return f.d == 1 ? n : (int)(__umulhi((uint32_t)n, f.mul) >> f.shr);
+}
+
 // Record the first device fault; later ones are dropped.
 __device__ __forceinline__ void record_error(const Params& p, uint32_t code, uint32_t info) {
   if (atomicCAS(&p.ws->error, 0u, code) == 0u) atomicExch(&p.ws->error_info, info);

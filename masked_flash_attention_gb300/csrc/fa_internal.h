@@ -15,6 +15,26 @@ constexpr int kPrefillRows = 128;     // query rows per prefill item (tcgen05 M)
 constexpr int kDecodeRows = 8;        // packed rows per decode item (mma N)
 constexpr int kMaxTopkKeys = 16384;   // top-k preparation keeps all keys of a row in smem
 
+// Division by a divisor fixed for a launch, as a multiply-high and a shift
+// (T. Granlund and P. Montgomery, "Division by Invariant Integers using
+// Multiplication", PLDI 1994, with a rounded-up multiplier): exact for
+// 0 <= n < 2^31.  Built on the host, applied on the device.
+struct FastDiv {
+  uint32_t d, mul, shr;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f{d, 0u, 0u};
+  if (d > 1) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;  // ceil(log2 d)
+    const uint64_t p = 31 + l;
+    f.mul = (uint32_t)(((1ull << p) + d - 1) / d);
+    f.shr = (uint32_t)(p - 32);
+  }
+  return f;
+}
+
 // Workspace header (first 256 bytes of the workspace).
 struct WsHeader {
   uint32_t error;       // fa_status of the first device fault, 0 = none
@@ -83,6 +103,8 @@ struct Params {
   // (no dense or top-k mask), so no scheduler kernel runs and its lists are
   // not written; the kernel's first CTA writes the counters
   int32_t sched_inline;
+  FastDiv div_units;  // prefill unit index -> row tile: n_seq * Hq
+  FastDiv div_hq;     // -> sequence: Hq
   int32_t rows_per_tile, n_row_tiles, n_heads_sched, n_kt;
   int64_t n_items;
   int32_t* item_count;   // [n_items]

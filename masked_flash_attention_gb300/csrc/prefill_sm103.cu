@@ -121,11 +121,11 @@ __device__ __forceinline__ int floor_div128(int a) { return a >= 0 ? a / 128 : -
 template <bool INL, bool GTH = false>
 __device__ __forceinline__ Unit unit_at(const Params& p, int u) {
   Unit w;
-  const int per = p.n_seq * p.Hq;
-  w.rt = p.n_row_tiles - 1 - u / per;
-  const int r = u % per;
-  w.h = r % p.Hq;
-  w.b = r / p.Hq;
+  const int q = fast_div(u, p.div_units);
+  w.rt = p.n_row_tiles - 1 - q;
+  const int r = u - q * (p.n_seq * p.Hq);
+  w.b = fast_div(r, p.div_hq);
+  w.h = r - w.b * p.Hq;
   const int q_len = seq_qlen(p, w.b);
   w.present = w.rt * 128 < q_len;
   if constexpr (INL) {
@@ -620,9 +620,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int nu = n_units(p);
     // Scheduler lists: the next unit's descriptor and first list entry are
     // read a unit ahead, so that no global-memory latency sits between two
-    // units.  Inline scheduling: descriptors and entries are arithmetic,
-    // computed where they are needed (nothing held across the tile loop).
-    // (gathered top-k units: the same, their entries being arithmetic too)
+    // units.  Inline scheduling and gathered top-k units: descriptors and
+    // entries are arithmetic (divisions by multiply-shift), computed where
+    // they are needed, so nothing is held across the tile loop.
     constexpr bool kArith = INL || GTH;
     Unit un_next;
     if (!kArith && round_unit(0) < nu) un_next = unit_at<INL, GTH>(p, round_unit(0));

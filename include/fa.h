@@ -126,6 +126,10 @@ typedef struct {
 
 /* Debug flags (opts->debug_flags). */
 #define FA_DEBUG_NO_SKIP 0x1u /* schedule EMPTY tiles too (as PARTIAL): exercises the -inf guard */
+#define FA_DEBUG_WITHHOLD 0x2u /* test only: the prefill kernel's key producer withholds each CTA's first
+                                * key tile (unmasked or dense-mask variants), so that the waits behind it
+                                * give up after their bound (FA_ERR_DEVICE_TIMEOUT); the output is then
+                                * undefined */
 #define FA_DEBUG_VALIDATE 0x4u /* check mask values on the device: a dense mask must be finite or -inf,
                                 * top-k scores finite (FA_ERR_DEVICE_VALUE otherwise); off by default */
 

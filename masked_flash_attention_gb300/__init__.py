@@ -8,6 +8,7 @@ from ._lib import (  # noqa: F401
     EXPORTS,
     FA_DEBUG_NO_SKIP,
     FA_DEBUG_VALIDATE,
+    FA_DEBUG_WITHHOLD,
     FA_OK,
     FaError,
     alloc_workspace,

@@ -33,6 +33,7 @@ FA_ERR_DEVICE_VALUE = 8
 FA_DTYPE_BF16, FA_DTYPE_F32, FA_DTYPE_I32, FA_DTYPE_F16 = 1, 2, 3, 4
 FA_MASK_NONE, FA_MASK_DENSE, FA_MASK_TOPK = 0, 1, 2
 FA_DEBUG_NO_SKIP = 0x1
+FA_DEBUG_WITHHOLD = 0x2
 FA_DEBUG_VALIDATE = 0x4
 FA_PATH_DECODE, FA_PATH_PREFILL = 1, 2
 FA_TILE_EMPTY, FA_TILE_FULL, FA_TILE_PARTIAL = 0, 1, 2

@@ -464,6 +464,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       uint64_t* empty = is_k ? k_empty : v_empty;
       unsigned char* ring = smem + (is_k ? C::kKOff : C::kVOff);
       tc::tma_prefetch_desc(map);
+      // test only: the first key tile is never sent, so every wait behind it
+      // runs out (FA_DEBUG_WITHHOLD)
+      const bool withhold = is_k && (p.debug_flags & FA_DEBUG_WITHHOLD);
       int j = 0;
       bool ok = true;
       Unit w;
@@ -472,6 +475,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int kv_b = p.cu_k ? 0 : w.b;
         const int g = w.h / p.G;
         for (int i = 0; i < w.count; ++i, ++j) {
+          if (withhold && j == 0) continue;
           const int kt = unit_entry<INL>(w, i) >> 1;
           const int s = j % NS;
           if (j >= NS && !tc::mbar_wait(empty + s, ((j / NS) - 1) & 1, abort_flag)) {
@@ -486,9 +490,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
       }
       if (*abort_flag) {
-        // let the copies already issued land before the CTA can exit
+        // let the copies already issued land before the CTA can exit (the
+        // withheld tile was never issued)
         const int first = j > NS ? j - NS : 0;
-        for (int jj = first; jj < j; ++jj) tc::mbar_wait_drain(full + jj % NS, (jj / NS) & 1, 100000000ull);
+        for (int jj = first; jj < j; ++jj)
+          if (!(withhold && jj == 0)) tc::mbar_wait_drain(full + jj % NS, (jj / NS) & 1, 100000000ull);
       }
     }
     __syncwarp();

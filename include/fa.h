@@ -231,6 +231,32 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v,
            int32_t window_left, int32_t window_right, float softcap, float scale,
            int32_t causal, const fa_opts* opts);
 
+/* Debug dump: fa_fwd (no page table, no mask, bf16, prefill path, no ALiBi;
+ * FA_ERR_UNSUPPORTED otherwise) through a debug build of the prefill kernel
+ * that also copies, for the 128 query rows of tile `row_tile` of sequence
+ * `seq` and q-head `head`, the intermediate values of every key tile that
+ * unit visits, into the caller's device buffer `dump` (fp32):
+ *   S[it][row][key]          raw Q K^T, before scale and masks, at dump;
+ *   P[it][row][key]          the probabilities as rounded for P V (0 where a
+ *                            key is dropped), at dump + n_k_tiles * 128 * 128;
+ *   ref[it][row]             the row's exponent reference in log2 units
+ *                            (P = exp2(logit * log2 e - ref)), at
+ *                            dump + 2 * n_k_tiles * 128 * 128.
+ * Entry it is the it-th key tile of the unit's list; the debug build writes
+ * that unit's count and list into the workspace work list (counts[item],
+ * tiles[item][...], as documented for fa_fwd_plan) whichever path scheduled
+ * it.  dump_bytes must be at least fa_debug_dump_bytes(n_k_tiles of the
+ * plan); entries past the list's end are left unwritten.  The output and LSE
+ * are as fa_fwd's.  A dump of one block's intermediate values for
+ * step-by-step comparison, as flash-sparse-attention issue 11 "Next Steps"
+ * proposes for its minimal example. */
+int fa_fwd_debug_dump(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
+                      const fa_tensor* lse, const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+                      int32_t window_left, int32_t window_right, float softcap, float scale, int32_t causal,
+                      const fa_opts* opts, int32_t seq, int32_t head, int32_t row_tile, float* dump,
+                      size_t dump_bytes);
+size_t fa_debug_dump_bytes(int64_t n_k_tiles);
+
 /* Host-only: validate the arguments of fa_fwd and describe its plan
  * (pointers are checked for alignment but never dereferenced; opts->workspace
  * may be NULL).  Same status codes as fa_fwd, except FA_ERR_WORKSPACE. */

@@ -17,7 +17,9 @@ from ._lib import (  # noqa: F401
     fa_bwd,
     fa_bwd_plan,
     fa_check_device_error,
+    fa_debug_dump_bytes_of,
     fa_fwd,
+    fa_fwd_debug_dump,
     fa_fwd_kvcache,
     fa_fwd_kvcache_plan,
     fa_fwd_noalloc,

@@ -93,7 +93,7 @@ _BWD_ARGS = [_P(fa_tensor)] * 11 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_flo
 
 EXPORTS = ("fa_fwd", "fa_fwd_plan", "fa_fwd_workspace_size", "fa_fwd_kvcache", "fa_fwd_kvcache_plan",
            "fa_bwd", "fa_bwd_plan", "fa_fwd_noalloc", "fa_check_device_error", "fa_status_string",
-           "fa_abi_version")
+           "fa_abi_version", "fa_fwd_debug_dump", "fa_debug_dump_bytes")
 
 
 def _load():
@@ -128,6 +128,13 @@ def _load():
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_abi_version.argtypes = []
     lib.fa_abi_version.restype = ctypes.c_int
+    lib.fa_fwd_debug_dump.argtypes = [_P(fa_tensor)] * 7 + [ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                                            ctypes.c_float, ctypes.c_int32, _P(fa_opts),
+                                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                            ctypes.c_void_p, ctypes.c_size_t]
+    lib.fa_fwd_debug_dump.restype = ctypes.c_int
+    lib.fa_debug_dump_bytes.argtypes = [ctypes.c_int64]
+    lib.fa_debug_dump_bytes.restype = ctypes.c_size_t
     # a library built from other headers would read these structures wrongly
     if lib.fa_abi_version() != ABI_VERSION:
         raise ImportError(f"{LIB_PATH} has ABI {lib.fa_abi_version()}, this binding describes ABI {ABI_VERSION}: "
@@ -281,6 +288,49 @@ def fa_fwd(q, k, v, *, out=None, lse=None, cu_seqlens_q=None, cu_seqlens_k=None,
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
     return out, lse, workspace
+
+
+def fa_fwd_debug_dump(q, k, v, seq, head, row_tile, *, cu_seqlens_q=None, cu_seqlens_k=None, window_left=-1,
+                      window_right=-1, softcap=0.0, scale=None, causal=False, max_seqlen_q=None,
+                      max_seqlen_k=None, stream=None, **_):
+    """fa_fwd through the prefill kernel's debug build, which also copies the
+    intermediate values of the 128 query rows of tile ``row_tile`` of sequence
+    ``seq``, q-head ``head``.  Returns ``(out, lse, workspace, dump)`` with
+    ``dump = {"S": [n, 128, 128], "P": [n, 128, 128], "ref": [n, 128]}`` (fp32,
+    entry it = the it-th key tile in the unit's list; n = the plan's n_k_tiles;
+    entries past the list's end are unwritten)."""
+    if not q.is_cuda:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_fwd_debug_dump (tensors must be CUDA tensors)")
+    kw = dict(cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k, window_left=window_left,
+              window_right=window_right, softcap=softcap, scale=scale, causal=causal, max_seqlen_q=max_seqlen_q,
+              max_seqlen_k=max_seqlen_k)
+    rc, plan = fa_fwd_plan(q, k, v, **kw)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_debug_dump (plan)")
+    n_kt = plan["n_k_tiles"]
+    dump = torch.empty(lib.fa_debug_dump_bytes(n_kt) // 4, dtype=torch.float32, device=q.device)
+    oshape, lshape = _out_shapes(q, cu_seqlens_q, max_seqlen_q)
+    out = torch.empty(oshape, dtype=q.dtype, device=q.device)
+    lse = torch.empty(lshape, dtype=torch.float32, device=q.device)
+    workspace = alloc_workspace(plan["workspace_bytes"], q.device)
+    opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k)
+    opts.workspace = workspace.data_ptr()
+    opts.workspace_bytes = workspace.numel() * workspace.element_size()
+    descs = [describe(x) for x in (q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k)]
+    rc = lib.fa_fwd_debug_dump(*[_ref(x) for x in descs], int(window_left), int(window_right), float(softcap),
+                               float(scale or 0.0), int(bool(causal)), ctypes.byref(opts), int(seq), int(head),
+                               int(row_tile), dump.data_ptr(), dump.numel() * 4)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_debug_dump")
+    s_len = n_kt * 128 * 128
+    parts = {"S": dump[:s_len].view(n_kt, 128, 128), "P": dump[s_len:2 * s_len].view(n_kt, 128, 128),
+             "ref": dump[2 * s_len:2 * s_len + n_kt * 128].view(n_kt, 128)}
+    return out, lse, workspace, parts
+
+
+def fa_debug_dump_bytes_of(n_k_tiles: int) -> int:
+    """Bytes fa_fwd_debug_dump needs for a plan with ``n_k_tiles`` key tiles."""
+    return int(lib.fa_debug_dump_bytes(int(n_k_tiles)))
 
 
 def _kv_args(q, k_cache, v_cache, k_new, v_new, out, lse, cu_seqlens_q, cache_seqlens, block_table,

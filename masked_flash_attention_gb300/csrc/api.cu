@@ -525,6 +525,32 @@ int fa_fwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_
   return run_plan(pl, opts);
 }
 
+int fa_fwd_debug_dump(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
+                      const fa_tensor* lse, const fa_tensor* cu_seqlens_q, const fa_tensor* cu_seqlens_k,
+                      int32_t window_left, int32_t window_right, float softcap, float scale, int32_t causal,
+                      const fa_opts* opts, int32_t seq, int32_t head, int32_t row_tile, float* dump,
+                      size_t dump_bytes) {
+  Plan pl;
+  int rc = make_plan(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, nullptr, nullptr, window_left, window_right,
+                     softcap, scale, causal, opts, &pl);
+  if (rc != FA_OK) return rc;
+  Params& P = pl.prm;
+  // the debug instantiations: prefill path, bf16, no ALiBi
+  if (P.path != FA_PATH_PREFILL || P.f16 || P.alibi) return FA_ERR_UNSUPPORTED;
+  if (!dump || seq < 0 || seq >= P.n_seq || head < 0 || head >= P.Hq || row_tile < 0 || row_tile >= P.n_row_tiles)
+    return FA_ERR_INVALID_ARG;
+  if (dump_bytes < fa_debug_dump_bytes(pl.pub.n_k_tiles)) return FA_ERR_INVALID_ARG;
+  P.dump = dump;
+  P.dump_b = seq;
+  P.dump_h = head;
+  P.dump_rt = row_tile;
+  return run_plan(pl, opts);
+}
+
+size_t fa_debug_dump_bytes(int64_t n_k_tiles) {
+  return n_k_tiles <= 0 ? 0 : (size_t)n_k_tiles * (2 * 128 * 128 + 128) * sizeof(float);
+}
+
 int fa_fwd_kvcache(const fa_tensor* q, const fa_tensor* k_cache, const fa_tensor* v_cache,
                    const fa_tensor* k_new, const fa_tensor* v_new, const fa_tensor* out,
                    const fa_tensor* lse, const fa_tensor* cu_seqlens_q,

@@ -126,6 +126,15 @@ struct Params {
 
   WsHeader* ws;
   uint32_t debug_flags;
+
+  // debug dump (fa_fwd_debug_dump): for the unit (dump_b, dump_h, dump_rt)
+  // the prefill kernel's debug instantiation writes, per entry it of the
+  // unit's key-tile list, raw S [it][row][key] and P [n_kt + it][row][key]
+  // (fp32; P as rounded for PV) and the exponent reference of each row
+  // [2 n_kt x 128 x 128 + it x 128 + row], and the unit's list into the
+  // work list; null = off
+  float* dump;
+  int32_t dump_b, dump_h, dump_rt;
 };
 
 // ---- launchers (defined in the .cu files; all enqueue on `st`) ----

@@ -341,8 +341,9 @@ __device__ __forceinline__ void row_key_range(const Params& p, int i, int q_len,
 
 // MK: additive term kind (FA_MASK_NONE / DENSE / TOPK); SC: logit soft-cap on;
 // AL: ALiBi slopes on (only with MK == FA_MASK_NONE); F16: inputs, P and the
-// output are fp16 (else bf16).
-template <int D, int MK, bool SC, bool AL, bool F16>
+// output are fp16 (else bf16); DBG: the debug instantiation, which also
+// writes S, P and the exponent references of one unit to Params::dump.
+template <int D, int MK, bool SC, bool AL, bool F16, bool DBG = false>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     prefill_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const int o_tma) {
@@ -651,6 +652,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
       int jlo_r, jhi_r;
       row_key_range(p, i, q_len, kv_len, off, jlo_r, jhi_r);
+      const bool dumped = DBG && b == p.dump_b && h == p.dump_h && un.rt == p.dump_rt;
+      if (DBG && dumped && w == 0 && wtid == 0) {  // the unit's list, so that entries map to key tiles
+        const int64_t item = ((int64_t)b * p.Hq + h) * p.n_row_tiles + un.rt;
+        p.item_count[item] = un.count;
+        for (int e = 0; e < un.count; ++e) p.item_tiles[item * p.n_kt + e] = unit_entry<INL, GTH>(un, e);
+      }
       const uint2* glist = GTH ? unit_glist(p, un) : nullptr;
 
       const float alibi_l2 = AL ? __ldg(p.alibi + h) * kLog2e : 0.f;  // ALiBi slope, log2 units
@@ -709,6 +716,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               x[c * 16 + e] = make_float2(__uint_as_float(r[c][2 * e]), __uint_as_float(r[c][2 * e + 1]));
+        }
+        if constexpr (DBG) {
+          if (dumped) {  // raw S of this row over the tile's 128 keys
+            float4* dst = reinterpret_cast<float4*>(p.dump + ((int64_t)it * 128 + row) * 128);
+#pragma unroll
+            for (int e4 = 0; e4 < 32; ++e4)
+              dst[e4] = make_float4(x[2 * e4].x, x[2 * e4].y, x[2 * e4 + 1].x, x[2 * e4 + 1].y);
+          }
         }
         tc::fence_before_sync();
         tc::mbar_arrive_relaxed(s_free + par);  // the QK two tiles on may overwrite this S buffer
@@ -831,6 +846,28 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
               acc[e & 3] = add2(acc[e & 3], pe);
               pk[c][e] = pack2<F16>(pe.x, pe.y);
             }
+        }
+        if constexpr (DBG) {
+          if (dumped) {  // P as rounded for PV, and the reference
+            float* dp = p.dump + ((int64_t)(p.n_kt + it) * 128 + row) * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                float lo, hi;
+                if constexpr (F16) {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk[c][e]));
+                  lo = f.x;
+                  hi = f.y;
+                } else {
+                  lo = __uint_as_float(pk[c][e] << 16);
+                  hi = __uint_as_float(pk[c][e] & 0xffff0000u);
+                }
+                dp[2 * (c * 16 + e)] = lo;
+                dp[2 * (c * 16 + e) + 1] = hi;
+              }
+            p.dump[(int64_t)2 * p.n_kt * 128 * 128 + (int64_t)it * 128 + row] = eref;
+          }
         }
         // this P buffer is free once the PV two tiles back is done
         if (gt >= 2 && !tc::mbar_wait(p_free + par, ((gt - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -964,7 +1001,7 @@ int sm_count() {
   return v;
 }
 
-template <int D, int MK, bool SC, bool AL, bool F16>
+template <int D, int MK, bool SC, bool AL, bool F16, bool DBG = false>
 cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& mv, const CUtensorMap& mo, int o_tma, int grid,
                              cudaEvent_t ev_begin) {
@@ -974,16 +1011,16 @@ cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap
   int regs = launch_regs.load(std::memory_order_relaxed);
   if (regs < 0) {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MK, SC, AL, F16>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, MK, SC, AL, F16, DBG>);
     if (e != cudaSuccess) return e;
     regs = fa.numRegs;
     launch_regs.store(regs, std::memory_order_relaxed);
   }
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL, F16>>(PCfg<D>::kSmem);
+  cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL, F16, DBG>>(PCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-  prefill_kernel<D, MK, SC, AL, F16><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
+  prefill_kernel<D, MK, SC, AL, F16, DBG><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
   return cudaGetLastError();
 }
 
@@ -1023,6 +1060,16 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
   const bool sc = p.softcap > 0.f;
   // the kernels schedule inline exactly for the mask-free variants
   if ((p.sched_inline != 0) != (p.mask_kind == FA_MASK_NONE)) return cudaErrorInvalidValue;
+  if (p.dump) {  // the debug instantiations: bf16, no additive term (the planner checks)
+    if constexpr (F16) {
+      return cudaErrorInvalidValue;
+    } else {
+      if (p.alibi || p.mask_kind != FA_MASK_NONE) return cudaErrorInvalidValue;
+      return sc ? launch_prefill_v<D, FA_MASK_NONE, true, false, F16, true>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_NONE, false, false, F16, true>(p, st, mq, mk, mv, mo, o_tma, grid,
+                                                                              ev_begin);
+    }
+  }
   if (p.alibi) {  // the planner allows ALiBi in prefill only without a mask
     if (p.mask_kind != FA_MASK_NONE) return cudaErrorInvalidValue;
     return sc ? launch_prefill_v<D, FA_MASK_NONE, true, true, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)

@@ -209,3 +209,9 @@ def test_topk_prefill_layout_rule():
     assert plan(q, kt, kt, causal=True, zero_hold_states=z, keep_window=50)[0] == _lib.FA_ERR_UNSUPPORTED
     qd = T(1, 2, 2, 64)   # few rows: decode path, any layout
     assert plan(qd, kt, kt, causal=True, zero_hold_states=z[:, :, :300], keep_window=50)[0] == 0
+
+
+def test_debug_dump_size():
+    # S and P (128 x 128 fp32 each) and one reference per row, per key tile
+    assert fa.fa_debug_dump_bytes_of(0) == 0
+    assert fa.fa_debug_dump_bytes_of(3) == 3 * (2 * 128 * 128 + 128) * 4

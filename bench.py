@@ -432,6 +432,9 @@ def run_gpu(args):
     e2e_value = job_value(units["metric_units"], world, e2e_total / args.steps)
     rc_, info = fa.fa_check_device_error(ws)
     assert rc_ == 0, (rc_, info)
+    # the scheduler's counters of the last call: key tiles computed FULL or
+    # PARTIAL, and left out as EMPTY (never computed)
+    st = ws[plan["off_stats"]:plan["off_stats"] + 24].cpu().view(torch.int64).tolist() if not bwd else None
 
     if rank != 0:
         return None
@@ -474,8 +477,11 @@ def run_gpu(args):
         "e2e": {"value": round(e2e_value, 3), "unit": units["unit"], "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_total / args.steps, 5)},
         "gpu_launches": int(plan["n_kernels"]) * args.steps,
+        "latency_us": round(ms_per_step * 1e3, 2),
         "clocks": clk.summary(),
     }
+    if st is not None:
+        line["sched"] = {"full": st[0], "partial": st[1], "empty": st[2]}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, units, args)
     return line

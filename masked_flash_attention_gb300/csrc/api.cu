@@ -321,7 +321,9 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   int n_kt_alloc = P.n_kt > 0 ? P.n_kt : 1;
   P.n_splits = 1;
   P.tiles_per_split = n_kt_alloc;
-  if (P.path == FA_PATH_DECODE && P.n_items > 0) {
+  if (P.path == FA_PATH_DECODE && P.n_items > 0 && n_kt_alloc > 8) {
+    // (at most 8 key tiles: one CTA per item, no combine pass -- splitting
+    // such short rows costs more in launches than it saves)
     const int64_t target_ctas = 152 * 16;
     if (P.n_items < target_ctas / 2) {
       int64_t tps = (P.n_items * (int64_t)n_kt_alloc + target_ctas - 1) / target_ctas;

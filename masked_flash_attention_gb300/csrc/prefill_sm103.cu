@@ -729,7 +729,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         tc::mbar_arrive_relaxed(s_free + par);  // the QK two tiles on may overwrite this S buffer
         // logits in log2 units; a FULL tile without soft-cap keeps raw scores
         // and folds the scale into the exponent below
-        const bool plain = !SC && !part && !AL && MK != FA_MASK_TOPK;
+        // Without an additive term, soft-cap or ALiBi every tile takes the
+        // plain path: a PARTIAL tile first sets the raw scores of the keys
+        // outside this row's range to -inf (the scale is positive, so a raw
+        // -inf stays -inf through the folded scale), which keeps a single copy
+        // of the exponent code in these variants.
+        constexpr bool kRawMask = MK == FA_MASK_NONE && !SC && !AL;
+        if (kRawMask && part) {
+          // the row keeps e with clo <= e <= clo + span; a row keeping no key
+          // (jhi_r < jlo_r) gets a start no e reaches
+          const bool none = jhi_r < jlo_r;
+          const int clo = none ? (1 << 20) : jlo_r - j0;
+          const unsigned span = none ? 0u : (unsigned)(jhi_r - jlo_r);
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            x[e].x = (unsigned)(2 * e - clo) <= span ? x[e].x : -INFINITY;
+            x[e].y = (unsigned)(2 * e + 1 - clo) <= span ? x[e].y : -INFINITY;
+          }
+        }
+        const bool plain = kRawMask || (!SC && !part && !AL && MK != FA_MASK_TOPK);
         float mx;
         if (plain) {
           mx = row_max128(x) * p.scale_log2;

@@ -361,10 +361,14 @@ def run_gpu(args):
           for _ in range(args.steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # one more untimed step: the sampler's start-up pause leaves the GPU
+        # idle, and the first step after an idle GPU runs slow
+        flush.zero_()
+        step()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
         for i in range(args.steps):
             flush.zero_()
             kev[i][0].record(); kev[i][1].record()  # materialise the handles

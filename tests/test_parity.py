@@ -421,3 +421,48 @@ def test_validate_topk_scores():
     p = to_dev(dict(c["params"], zero_hold_states=z, keep_window=32))
     _, _, ws = fa.fa_fwd(c["q"].to(DEV), c["k"].to(DEV), c["v"].to(DEV), debug_flags=fa.FA_DEBUG_VALIDATE, **p)
     assert fa.fa_check_device_error(ws)[0] == fa._lib.FA_ERR_DEVICE_VALUE
+
+
+# ---------------------------------------------------------------------------
+# Mask-free prefill at shapes whose unit counts do not divide the SM count:
+# ragged rows over past keys, square causal at d = 64, a sliding window, the
+# soft-cap variant, and full rows of 8 key tiles each
+# ---------------------------------------------------------------------------
+
+UNEVEN = [
+    (2, 1000, 1500, 16, 4, 128, dict(causal=True)),
+    (4, 1024, 1024, 12, 12, 64, dict(causal=True)),
+    (4, 700, 2000, 16, 4, 128, dict(causal=True, window_left=300)),
+    (1, 1500, 1500, 32, 8, 128, dict(causal=True, softcap=20.0)),
+    (1, 1024, 1024, 24, 24, 128, dict(causal=False)),
+]
+
+
+@pytest.mark.parametrize("i", range(len(UNEVEN)))
+def test_prefill_uneven_units(i):
+    import masked_flash_attention_gb300 as fa
+    B, Sq, Sk, Hq, Hkv, d, extra = UNEVEN[i]
+    c = W.random_case(1800 + i, B=B, Sq=Sq, Sk=Sk, Hq=Hq, Hkv=Hkv, d=d, **extra)
+    rc, plan = fa.fa_fwd_plan(c["q"], c["k"], c["v"], **c["params"])
+    assert rc == 0 and plan["path"] == fa._lib.FA_PATH_PREFILL, plan
+    check(c)
+
+
+def test_prefill_alibi_repeat_on_one_workspace():
+    """The ALiBi variant, called twice in a row on one workspace with the
+    outputs poisoned in between: nothing left in the workspace by the first
+    call may leak into the second."""
+    import masked_flash_attention_gb300 as fa
+    c = W.random_case(1810, B=1, Sq=1200, Sk=1600, Hq=32, Hkv=8, d=64, causal=True)
+    slopes = _alibi_slopes(32)
+    p = dict(c["params"], alibi_slopes=slopes)
+    ref_o, ref_l = run_oracle(c, alibi_slopes=slopes)
+    q, k, v = c["q"].to(DEV), c["k"].to(DEV), c["v"].to(DEV)
+    out, lse, ws = fa.fa_fwd(q, k, v, **to_dev(p))
+    for _ in range(2):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        fa.fa_fwd(q, k, v, out=out, lse=lse, workspace=ws, **to_dev(p))
+        torch.cuda.synchronize()
+        assert fa.fa_check_device_error(ws)[0] == 0
+        compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, "alibi repeat")

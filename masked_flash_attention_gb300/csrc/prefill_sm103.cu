@@ -61,15 +61,27 @@ namespace mfa {
 namespace {
 
 constexpr int kPrefillThreads = 384;
+// The top-k variants gather their key rows with TMA tile::gather4, which one
+// warp issues at only about one copy per 65-90 cycles; they launch a fourth
+// warpgroup (warps 12..15) whose warps share the K and V gathers with the two
+// producer warps, three warps per operand.
+constexpr int kGatherThreads = 512;
 // Register split (setmaxnreg): the kernel is built to launch with exactly
-// kLaunchRegs per thread; warpgroup 0 (producers, issuers) gives registers
+// kLaunchRegs per thread (kGatherLaunchRegs for the top-k variants);
+// warpgroup 0 (producers, issuers) and the gather warpgroup give registers
 // back and the two softmax warpgroups take them, so that a 128-key row of S
 // fits in registers.
 constexpr int kLaunchRegs = 168;
+constexpr int kGatherLaunchRegs = 128;
 constexpr int kProducerRegs = 72;
+constexpr int kGatherProducerRegs = 40;
 constexpr int kSoftmaxRegs = 216;
 static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs <= kPrefillThreads * kLaunchRegs,
               "the register split must fit the block's launch allocation");
+static_assert(256 * kGatherProducerRegs + 256 * kSoftmaxRegs <= kGatherThreads * kGatherLaunchRegs,
+              "the register split must fit the block's launch allocation");
+__host__ __device__ constexpr int prefill_threads(int mk) { return mk == FA_MASK_TOPK ? kGatherThreads : kPrefillThreads; }
+__host__ __device__ constexpr int prefill_launch_regs(int mk) { return mk == FA_MASK_TOPK ? kGatherLaunchRegs : kLaunchRegs; }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // S buffers: kSCol + 128 * buf
 constexpr uint32_t kPCol = 256;  // P buffers: kPCol + 64 * buf
@@ -344,7 +356,7 @@ __device__ __forceinline__ void row_key_range(const Params& p, int i, int q_len,
 // output are fp16 (else bf16); DBG: the debug instantiation, which also
 // writes S, P and the exponent references of one unit to Params::dump.
 template <int D, int MK, bool SC, bool AL, bool F16, bool DBG = false>
-__global__ void __launch_bounds__(kPrefillThreads, 1)
+__global__ void __launch_bounds__(prefill_threads(MK), 1)
     prefill_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const int o_tma) {
   using C = PCfg<D>;
@@ -390,9 +402,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
     tc::mbar_init(sumx, 256);
     for (int s = 0; s < NS; ++s) {
-      tc::mbar_init(k_full + s, 1);
+      // gathered tiles: each of the operand's three gather warps arrives
+      tc::mbar_init(k_full + s, GTH ? 3 : 1);
       tc::mbar_init(k_empty + s, 1);
-      tc::mbar_init(v_full + s, 1);
+      tc::mbar_init(v_full + s, GTH ? 3 : 1);
       tc::mbar_init(v_empty + s, 1);
     }
     tc::mbar_init(o_full, 1);
@@ -408,13 +421,23 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc::fence_after_sync();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-  if (GTH && (warp == 0 || warp == 2)) {
+  if (GTH && (warp < 4 || warp >= 12)) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGatherProducerRegs));
+  } else if (!GTH && warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+  }
+  if (GTH && (warp == 0 || warp == 2 || warp >= 12)) {
     // ------------------------------------------------------------ producers (gathered keys)
-    // The whole warp: each lane gathers 4 of the tile's 128 key rows (one
-    // tile::gather4 per 64-column half) from the 2-D K/V view whose row
-    // b * Sk + j holds key j of sequence b, every head side by side.
-    const bool is_k = (warp == 0);
+    // Three warps per operand (K: warps 0, 12, 13; V: 2, 14, 15).  A tile's
+    // 128 key rows come in 32 groups of 4, each one tile::gather4 per
+    // 64-column half, from the 2-D K/V view whose row b * Sk + j holds key j
+    // of sequence b, every head side by side; lane l of the operand's warp
+    // `part` takes row group 3 l + part.  Each warp waits for the stage to be
+    // free itself and arrives on its full barrier with the bytes it sends.
+    const bool is_k = warp == 0 || warp == 12 || warp == 13;
+    const int part = warp < 12 ? 0 : 1 + (warp & 1);
+    const int rg = 3 * lane + part;  // this lane's row group (none when >= 32)
+    const uint32_t my_bytes = (uint32_t)((32 - part + 2) / 3) * (4u * D * 2u);
     const CUtensorMap* map = is_k ? &tmk : &tmv;
     uint64_t* full = is_k ? k_full : v_full;
     uint64_t* empty = is_k ? k_empty : v_empty;
@@ -430,8 +453,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       for (int i = 0; i < w.count; ++i, ++j) {
         const int s = j % NS;
         // this lane's four keys (two entries per 16 bytes), read before the wait
-        const uint4 ea = __ldg(lst + (i * kKeysPerTile + 4 * lane) / 2);
-        const uint4 eb = __ldg(lst + (i * kKeysPerTile + 4 * lane) / 2 + 1);
+        uint4 ea = make_uint4(0, 0, 0, 0), eb = ea;
+        if (rg < 32) {
+          ea = __ldg(lst + (i * kKeysPerTile + 4 * rg) / 2);
+          eb = __ldg(lst + (i * kKeysPerTile + 4 * rg) / 2 + 1);
+        }
         bool go = true;
         if (lane == 0 && j >= NS) go = tc::mbar_wait(empty + s, ((j / NS) - 1) & 1, abort_flag);
         go = __shfl_sync(0xffffffffu, go, 0);
@@ -440,12 +466,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           ok = false;
           break;
         }
-        if (lane == 0) tc::mbar_arrive_expect_tx(full + s, C::kTileBytes);
+        if (lane == 0) tc::mbar_arrive_expect_tx(full + s, my_bytes);
         __syncwarp();
-        for (int c = 0; c < D / 64; ++c)
-          tc::tma_gather4_2d(ring + s * C::kTileBytes + c * 16384 + lane * 512, map, full + s, x0 + c * 64,
-                             row0 + (int)(ea.x & 0xffffu), row0 + (int)(ea.z & 0xffffu),
-                             row0 + (int)(eb.x & 0xffffu), row0 + (int)(eb.z & 0xffffu));
+        if (rg < 32)
+          for (int c = 0; c < D / 64; ++c)
+            tc::tma_gather4_2d(ring + s * C::kTileBytes + c * 16384 + rg * 512, map, full + s, x0 + c * 64,
+                               row0 + (int)(ea.x & 0xffffu), row0 + (int)(ea.z & 0xffffu),
+                               row0 + (int)(eb.x & 0xffffu), row0 + (int)(eb.z & 0xffffu));
       }
     }
     if (lane == 0 && *abort_flag) {
@@ -1034,11 +1061,11 @@ cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap
     regs = fa.numRegs;
     launch_regs.store(regs, std::memory_order_relaxed);
   }
-  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  if (regs != prefill_launch_regs(MK)) return cudaErrorInvalidConfiguration;
   cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL, F16, DBG>>(PCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-  prefill_kernel<D, MK, SC, AL, F16, DBG><<<(unsigned)grid, kPrefillThreads, PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
+  prefill_kernel<D, MK, SC, AL, F16, DBG><<<(unsigned)grid, prefill_threads(MK), PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
   return cudaGetLastError();
 }
 

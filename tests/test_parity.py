@@ -309,10 +309,11 @@ def test_prefill_dense_mask_per_head():
     check(c, mask=m)
 
 
-@pytest.mark.parametrize("causal,ties", [(True, True), (True, False), (False, True)])
-def test_prefill_topk(causal, ties):
-    c = W.random_case(323, B=1, Sq=400, Sk=400, Hq=2, Hkv=2, d=128, causal=causal)
-    z = W.random_zero_hold_states(323, 1, 2, 400, ties=ties)
+@pytest.mark.parametrize("causal,ties,Sq,Sk", [(True, True, 400, 400), (True, False, 400, 400), (False, True, 400, 400),
+                                              (True, True, 300, 457)])
+def test_prefill_topk(causal, ties, Sq, Sk):
+    c = W.random_case(323, B=1, Sq=Sq, Sk=Sk, Hq=2, Hkv=2, d=128, causal=causal)
+    z = W.random_zero_hold_states(323, 1, 2, Sk, ties=ties)
     _assert_prefill(c, zero_hold_states=z, keep_window=100)
     check(c, zero_hold_states=z, keep_window=100)
 

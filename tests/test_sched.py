@@ -204,7 +204,8 @@ def test_topk_kept_sets_exact(golden):
                                              (4, 40, 9000, 3000, True, True),   # > 64 key buckets
                                              (5, 260, 700, 200, True, True),    # many rows over past keys
                                              (6, 200, 333, 50, False, True),    # many rows, not causal
-                                             (7, 130, 2500, 3000, True, False)]:  # keep_window above every row
+                                             (7, 130, 2500, 3000, True, False),  # keep_window above every row
+                                             (8, 300, 457, 120, True, True)]:    # key count not a multiple of 4
         case = W.random_case(seed, B=1, Sq=Sq, Sk=Sk, Hq=2, Hkv=2, d=64, causal=causal)
         z = W.random_zero_hold_states(seed, 1, 2, Sk, ties=ties)
         plan, counts, tiles, stats, ws = worklist(case, zero_hold_states=z, keep_window=keep)

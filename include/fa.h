@@ -153,7 +153,7 @@ typedef struct {
    * flash_attn_varlen_func call (the pages give no formula; this linear
    * distance penalty, aligned bottom-right like the causal rule, is the plain
    * reading).  Read by the kernels, so it must stay valid until they finish.
- * On the prefill path ALiBi cannot be combined with a dense or top-k mask
+ * On the prefill path ALiBi cannot be combined with a top-k mask
  * (FA_ERR_UNSUPPORTED); the decode path takes any combination. */
   const void* alibi_slopes;
 } fa_opts;

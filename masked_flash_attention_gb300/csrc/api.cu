@@ -13,6 +13,7 @@
 #include <cstring>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "fa_internal.h"
 
@@ -306,8 +307,9 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
                          (Hkv - 1) * P.k_sh + d <= P.k_ss && (Hkv - 1) * P.v_sh + d <= P.v_ss;
     if (!kv_rows) return FA_ERR_UNSUPPORTED;
   }
-  // prefill carries ALiBi only without a dense or top-k mask (decode: any)
-  if (P.path == FA_PATH_PREFILL && P.alibi && mask_kind != FA_MASK_NONE) return FA_ERR_UNSUPPORTED;
+  // prefill carries ALiBi without a mask or with a dense one, not with top-k
+  // (decode: any)
+  if (P.path == FA_PATH_PREFILL && P.alibi && mask_kind == FA_MASK_TOPK) return FA_ERR_UNSUPPORTED;
   // without a dense or top-k mask the pair rules alone decide every tile: the
   // prefill kernel classifies its units' tiles itself and no scheduler kernel runs
   P.sched_inline = (P.path == FA_PATH_PREFILL && mask_kind == FA_MASK_NONE) ? 1 : 0;
@@ -583,10 +585,27 @@ int fa_fwd_kvcache_plan(const fa_tensor* q, const fa_tensor* k_cache, const fa_t
 
 }  // extern "C"
 
+thread_local bool mfa::g_trace_ranges = true;
+
 namespace {
+
+// NVTX range around the host-side enqueue of one stage (a profiler's trace
+// shows it beside the stage's kernels); none while g_trace_ranges is off.
+struct TraceRange {
+  bool on;
+  explicit TraceRange(const char* name) : on(mfa::g_trace_ranges) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~TraceRange() {
+    if (on) nvtxRangePop();
+  }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
 
 // Bind the workspace and enqueue a validated plan's kernels on opts->stream.
 int run_plan(Plan& pl, const fa_opts* opts) {
+  TraceRange tr_call("mfa.fwd");
   int rc;
   if (!opts->workspace || (reinterpret_cast<uintptr_t>(opts->workspace) % kAlign) != 0 ||
       opts->workspace_bytes < pl.pub.workspace_bytes)
@@ -602,15 +621,26 @@ int run_plan(Plan& pl, const fa_opts* opts) {
   if (P.n_items == 0) return FA_OK;
   cudaError_t e = cudaSuccess;
   if (!P.sched_inline) {
-    if (P.mask_kind == FA_MASK_DENSE) e = launch_mask_summary(P, st);
-    if (e == cudaSuccess && P.mask_kind == FA_MASK_TOPK) e = launch_topk_prep(P, st);
+    if (P.mask_kind == FA_MASK_DENSE) {
+      TraceRange tr("mfa.mask_summary");
+      e = launch_mask_summary(P, st);
+    }
+    if (e == cudaSuccess && P.mask_kind == FA_MASK_TOPK) {
+      TraceRange tr("mfa.topk_prep");
+      e = launch_topk_prep(P, st);
+    }
     // on the many-row path the top-k preparation has listed each unit's keys
     const bool listed = P.mask_kind == FA_MASK_TOPK && P.path == FA_PATH_PREFILL;
-    if (e == cudaSuccess && !listed) e = launch_classify(P, st);
+    if (e == cudaSuccess && !listed) {
+      TraceRange tr("mfa.classify");
+      e = launch_classify(P, st);
+    }
   }
   cudaEvent_t ev_begin = static_cast<cudaEvent_t>(opts->event_begin);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    TraceRange tr(P.path == FA_PATH_PREFILL ? "mfa.prefill" : "mfa.decode");
     e = (P.path == FA_PATH_PREFILL) ? launch_prefill(P, st, ev_begin) : launch_decode(P, st, ev_begin);
+  }
   if (e == cudaSuccess && opts->event_end)
     e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_end), st);
   if (e != cudaSuccess) {
@@ -642,6 +672,7 @@ int fa_bwd(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_
   Params& P = pl.prm;
   P.delta = reinterpret_cast<float*>(static_cast<unsigned char*>(opts->workspace) + off_delta);
   cudaStream_t st = static_cast<cudaStream_t>(opts->stream);
+  TraceRange tr("mfa.bwd");
   cudaError_t e = launch_backward(P, st, static_cast<cudaEvent_t>(opts->event_begin));
   if (e == cudaSuccess && opts->event_end) e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_end), st);
   if (e != cudaSuccess) {

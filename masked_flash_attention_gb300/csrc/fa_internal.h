@@ -143,6 +143,9 @@ cudaError_t launch_mask_summary(const Params& p, cudaStream_t st);
 // counts (many-row path) or the per-tile maxima (few-row path).
 cudaError_t launch_topk_prep(const Params& p, cudaStream_t st);
 int topk_n_runs(int Sk);
+// NVTX ranges around the forward and backward stages (on unless a caller on
+// this thread turns them off; fa_fwd_noalloc does, around its call).
+extern thread_local bool g_trace_ranges;
 cudaError_t launch_classify(const Params& p, cudaStream_t st);
 // The attention launchers record `ev_begin` (if not null) on the stream right
 // before the kernel itself is enqueued, after all host-side preparation.

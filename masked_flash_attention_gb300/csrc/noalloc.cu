@@ -140,6 +140,11 @@ extern "C" int fa_fwd_noalloc(const fa_tensor* q, const fa_tensor* k, const fa_t
   }
   o.workspace = scratch;
   o.workspace_bytes = kNoAllocScratchBytes;
-  return fa_fwd(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask, window_left,
-                window_right, softcap, scale, causal, &o);
+  // no profiler ranges on this path: it calls nothing beyond the CUDA runtime
+  const bool trace = mfa::g_trace_ranges;
+  mfa::g_trace_ranges = false;
+  const int r = fa_fwd(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask, window_left,
+                       window_right, softcap, scale, causal, &o);
+  mfa::g_trace_ranges = trace;
+  return r;
 }

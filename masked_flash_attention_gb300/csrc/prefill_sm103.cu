@@ -1115,8 +1115,11 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
                                                                               ev_begin);
     }
   }
-  if (p.alibi) {  // the planner allows ALiBi in prefill only without a mask
-    if (p.mask_kind != FA_MASK_NONE) return cudaErrorInvalidValue;
+  if (p.alibi) {  // the planner allows ALiBi in prefill without a mask or with a dense one
+    if (p.mask_kind == FA_MASK_TOPK) return cudaErrorInvalidValue;
+    if (p.mask_kind == FA_MASK_DENSE)
+      return sc ? launch_prefill_v<D, FA_MASK_DENSE, true, true, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
+                : launch_prefill_v<D, FA_MASK_DENSE, false, true, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
     return sc ? launch_prefill_v<D, FA_MASK_NONE, true, true, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin)
               : launch_prefill_v<D, FA_MASK_NONE, false, true, F16>(p, st, mq, mk, mv, mo, o_tma, grid, ev_begin);
   }

@@ -367,12 +367,29 @@ def test_alibi_with_dense_mask():
 
 
 @pytest.mark.gpu
-def test_alibi_with_mask_on_prefill_is_unsupported():
+@pytest.mark.parametrize("seed,Sq,Sk,d,per_head,extra", [
+    (911, 260, 400, 128, False, dict(causal=True)),
+    (912, 300, 300, 64, True, dict(causal=True, softcap=20.0)),
+    (913, 200, 333, 128, True, dict(causal=False, window_left=150, window_right=40)),
+])
+def test_alibi_with_dense_mask_prefill(seed, Sq, Sk, d, per_head, extra):
+    # prefill path: the ALiBi penalty and a dense mask on the same logits
+    c = W.random_case(seed, B=1, Sq=Sq, Sk=Sk, Hq=4, Hkv=2, d=d, **extra)
+    if per_head:
+        m = torch.stack([W.random_dense_mask(seed + h, Sq, Sk, p_neg_inf=0.3) for h in range(4)])[None]
+    else:
+        m = W.random_dense_mask(seed, Sq, Sk)
+    _assert_prefill(c, mask=m, alibi_slopes=_alibi_slopes(4))
+    check(c, mask=m, alibi_slopes=_alibi_slopes(4))
+
+
+@pytest.mark.gpu
+def test_alibi_with_topk_on_prefill_is_unsupported():
     import masked_flash_attention_gb300 as fa
-    c = W.random_case(911, B=1, Sq=260, Sk=400, Hq=4, Hkv=2, d=128, causal=True)
-    m = W.random_dense_mask(911, 260, 400)
+    c = W.random_case(914, B=1, Sq=260, Sk=400, Hq=4, Hkv=4, d=128, causal=True)
+    z = W.random_zero_hold_states(914, 1, 4, 400, ties=False)
     with pytest.raises(fa.FaError) as e:
-        run_gpu(c, mask=m, alibi_slopes=_alibi_slopes(4))
+        run_gpu(c, zero_hold_states=z, keep_window=50, alibi_slopes=_alibi_slopes(4))
     assert e.value.status == fa._lib.FA_ERR_UNSUPPORTED
 
 

@@ -18,9 +18,9 @@
 // one group, so their K/V tiles are served from L2.
 //
 // Warp roles (12 warps):
-//   warp 0      TMA producer: K tiles through an NS-stage ring
+//   warp 0      TMA producer: K tiles through an NSK-stage ring
 //   warp 1      QK issuer (one thread), Q prefetch, TMEM owner
-//   warp 2      TMA producer: V tiles through an NS-stage ring
+//   warp 2      TMA producer: V tiles through an NSV-stage ring
 //   warp 3      PV issuer (one thread)
 //   warps 4..7  softmax warpgroup 0: the even key tiles of a unit's sequence
 //   warps 8..11 softmax warpgroup 1: the odd ones
@@ -88,14 +88,23 @@ constexpr uint32_t kPCol = 256;  // P buffers: kPCol + 64 * buf
 constexpr uint32_t kOCol = 384;  // O
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int D>
+template <int D, bool GTH = false>
 struct PCfg {
-  static constexpr int NS = (D == 128) ? 2 : 4;    // K/V ring stages
+  // Ring stages and Q buffers.  At d = 128 a third K stage (so that a K
+  // tile's copy has a tile period more to land before its QK) is paid for
+  // with the second Q buffer: the next unit's Q is then fetched once the
+  // current unit's QKs are done, which the epilogue hides (the causal-prefill
+  // workload 124.3 -> 114.7 us, the Llama-3 layer 408 -> 376 us).  The
+  // gathered top-k tiles keep two Q buffers and two K stages (with three K
+  // stages and one Q buffer they measured 371 us against 351 us).
+  static constexpr int NQ = (D == 128 && !GTH) ? 1 : 2;             // Q buffers
+  static constexpr int NSK = (D == 128) ? (GTH ? 2 : 3) : 4;        // K ring stages
+  static constexpr int NSV = (D == 128) ? 2 : 4;    // V ring stages
   static constexpr int kTileBytes = 128 * D * 2;    // one 128-row tile of 2-byte elements
-  static constexpr int kQOff = 0;                   // two Q buffers
-  static constexpr int kKOff = 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + NS * kTileBytes;
-  static constexpr int kAuxOff = kVOff + NS * kTileBytes;
+  static constexpr int kQOff = 0;                   // NQ Q buffers
+  static constexpr int kKOff = NQ * kTileBytes;
+  static constexpr int kVOff = kKOff + NSK * kTileBytes;
+  static constexpr int kAuxOff = kVOff + NSV * kTileBytes;
   // aux: barriers and flags (512 B), row references [2][128] floats, row
   // sums [2][128] floats, top-k staging [2 warpgroups][2 buffers]
   static constexpr int kRedOff = kAuxOff + 512;
@@ -359,8 +368,8 @@ template <int D, int MK, bool SC, bool AL, bool F16, bool DBG = false>
 __global__ void __launch_bounds__(prefill_threads(MK), 1)
     prefill_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const int o_tma) {
-  using C = PCfg<D>;
-  constexpr int NS = C::NS;
+  using C = PCfg<D, MK == FA_MASK_TOPK>;
+  constexpr int NSK = C::NSK, NSV = C::NSV, NQ = C::NQ;
   constexpr bool INL = (MK == FA_MASK_NONE);  // the host sets p.sched_inline exactly then
   constexpr bool GTH = (MK == FA_MASK_TOPK);   // tiles of gathered keys (2-D K/V maps)
   extern __shared__ unsigned char smem_raw[];
@@ -371,11 +380,11 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kAuxOff);
   uint64_t* q_full = bars;            // [2] Q buffer loaded
   uint64_t* q_empty = q_full + 2;     // [2] QKs reading a Q buffer done
-  uint64_t* k_full = q_empty + 2;     // [NS]
-  uint64_t* k_empty = k_full + NS;    // [NS]
-  uint64_t* v_full = k_empty + NS;    // [NS]
-  uint64_t* v_empty = v_full + NS;    // [NS]
-  uint64_t* s_full = v_empty + NS;    // [2] S buffer written by QK
+  uint64_t* k_full = q_empty + 2;     // [NSK]
+  uint64_t* k_empty = k_full + NSK;   // [NSK]
+  uint64_t* v_full = k_empty + NSK;   // [NSV]
+  uint64_t* v_empty = v_full + NSV;   // [NSV]
+  uint64_t* s_full = v_empty + NSV;   // [2] S buffer written by QK
   uint64_t* s_free = s_full + 2;      // [2] S buffer read by the softmax (128 arrivals)
   uint64_t* p_full = s_free + 2;      // [2] P buffer written, O rescaled (128 arrivals)
   uint64_t* p_free = p_full + 2;      // [2] PV reading a P buffer done
@@ -401,10 +410,12 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
       tc::mbar_init(kready + 2 + k, 128);
     }
     tc::mbar_init(sumx, 256);
-    for (int s = 0; s < NS; ++s) {
-      // gathered tiles: each of the operand's three gather warps arrives
+    // gathered tiles: each of the operand's three gather warps arrives
+    for (int s = 0; s < NSK; ++s) {
       tc::mbar_init(k_full + s, GTH ? 3 : 1);
       tc::mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       tc::mbar_init(v_full + s, GTH ? 3 : 1);
       tc::mbar_init(v_empty + s, 1);
     }
@@ -442,6 +453,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
     uint64_t* full = is_k ? k_full : v_full;
     uint64_t* empty = is_k ? k_empty : v_empty;
     unsigned char* ring = smem + (is_k ? C::kKOff : C::kVOff);
+    const int NS = is_k ? NSK : NSV;
     if (lane == 0) tc::tma_prefetch_desc(map);
     int j = 0;
     bool ok = true;
@@ -491,6 +503,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
       unsigned char* ring = smem + (is_k ? C::kKOff : C::kVOff);
+      const int NS = is_k ? NSK : NSV;
       tc::tma_prefetch_desc(map);
       // test only: the first key tile is never sent, so every wait behind it
       // runs out (FA_DEBUG_WITHHOLD)
@@ -529,14 +542,15 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
     // S[g % 2] = Q K_g^T for the g-th tile this CTA processes, as soon as the
-    // softmax has read that S buffer two tiles back.  Also fetches Q: the next
-    // unit's Q while the current unit runs (two buffers).
+    // softmax has read that S buffer two tiles back.  Also fetches Q: with two
+    // buffers the next unit's Q while the current unit runs, with one the next
+    // unit's Q once the current unit's QKs are done.
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(128, 128, false, false, F16);
       const uint32_t sQ = tc::smem_u32(smem + C::kQOff);
       const uint32_t sK = tc::smem_u32(smem + C::kKOff);
       tc::tma_prefetch_desc(&tmq);
-      int nq = 0;  // Q copies issued; copy l goes to buffer l & 1
+      int nq = 0;  // Q copies issued; copy l goes to buffer l % NQ
       auto load_q = [&](const Unit& w, int qb) {
         ++nq;
         const int q_row0 = p.cu_q ? p.cu_q[w.b] : 0;
@@ -552,12 +566,12 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
       int u = next_busy<INL, GTH>(p, 0, w);  // round
       if (u >= 0) load_q(w, 0);
       for (; ok && u >= 0; ++kk) {
-        const int qb = kk & 1;
+        const int qb = kk % NQ;
         const int un = next_busy<INL, GTH>(p, u + 1, wn);
-        if (!tc::mbar_wait(q_full + qb, (kk >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(q_full + qb, (kk / NQ) & 1, abort_flag)) { ok = false; break; }
         for (int i = 0; i < w.count; ++i, ++g) {
-          const int s = g % NS, sb = g & 1;
-          if (!tc::mbar_wait(k_full + s, (g / NS) & 1, abort_flag)) { ok = false; break; }
+          const int s = g % NSK, sb = g & 1;
+          if (!tc::mbar_wait(k_full + s, (g / NSK) & 1, abort_flag)) { ok = false; break; }
           if (g >= 2 && !tc::mbar_wait(s_free + sb, ((g - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t qa = sQ + qb * C::kTileBytes, ka = sK + s * C::kTileBytes;
@@ -569,7 +583,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
           }
           tc::mma_commit(s_full + sb);
           tc::mma_commit(k_empty + s);
-          if (i == 0 && un >= 0) {
+          if (NQ == 2 && i == 0 && un >= 0) {
             // next unit's Q into the other buffer, last read by unit kk - 1
             if (kk >= 1 && !tc::mbar_wait(q_empty + (qb ^ 1), ((kk - 1) >> 1) & 1, abort_flag)) {
               ok = false;
@@ -580,6 +594,14 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
         }
         if (!ok) break;
         tc::mma_commit(q_empty + qb);
+        if (NQ == 1 && un >= 0) {
+          // one buffer: the next unit's Q once this unit's QKs have read it
+          if (!tc::mbar_wait(q_empty, kk & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          load_q(wn, 0);
+        }
         u = un;
         w = wn;
       }
@@ -588,8 +610,8 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
       tc::mbar_wait_drain(drained, 0, 200000000ull);
       if (*abort_flag) {
         // let the last Q copies land before the CTA can exit
-        for (int l = nq > 2 ? nq - 2 : 0; l < nq; ++l)
-          tc::mbar_wait_drain(q_full + (l & 1), (l >> 1) & 1, 100000000ull);
+        for (int l = nq > NQ ? nq - NQ : 0; l < nq; ++l)
+          tc::mbar_wait_drain(q_full + (l % NQ), (l / NQ) & 1, 100000000ull);
       }
     }
     __syncwarp();
@@ -605,9 +627,9 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
       Unit w;
       for (int r = next_busy<INL, GTH>(p, 0, w); ok && r >= 0; r = next_busy<INL, GTH>(p, r + 1, w)) {
         for (int i = 0; i < w.count; ++i, ++g) {
-          const int s = g % NS, pb = g & 1;
+          const int s = g % NSV, pb = g & 1;
           if (!tc::mbar_wait(p_full + pb, (g >> 1) & 1, abort_flag) ||
-              !tc::mbar_wait(v_full + s, (g / NS) & 1, abort_flag)) {
+              !tc::mbar_wait(v_full + s, (g / NSV) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -1062,10 +1084,11 @@ cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap
     launch_regs.store(regs, std::memory_order_relaxed);
   }
   if (regs != prefill_launch_regs(MK)) return cudaErrorInvalidConfiguration;
-  cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL, F16, DBG>>(PCfg<D>::kSmem);
+  using C = PCfg<D, MK == FA_MASK_TOPK>;
+  cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL, F16, DBG>>(C::kSmem);
   if (e != cudaSuccess) return e;
   if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-  prefill_kernel<D, MK, SC, AL, F16, DBG><<<(unsigned)grid, prefill_threads(MK), PCfg<D>::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
+  prefill_kernel<D, MK, SC, AL, F16, DBG><<<(unsigned)grid, prefill_threads(MK), C::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
   return cudaGetLastError();
 }
 

@@ -57,12 +57,12 @@ KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_dev
 # time: once the kernel changes the figure no longer applies and is reported
 # as null.
 MEASURED_TRAFFIC = {
-    ("causal_prefill_past_kv", "prefill_kernel"): ("faa30765b1defcf0", 103863296 + 9367040),
-    ("gpt2_small_layer", "prefill_kernel"): ("faa30765b1defcf0", 37830144 + 144896),
-    ("llama3_8b_layer", "prefill_kernel"): ("faa30765b1defcf0", 100763392 + 35154432),
-    ("dynamic_topk", "prefill_kernel"): ("faa30765b1defcf0", 201495296 + 52023040),
-    ("paged_varlen_decode", "decode_kernel"): ("4dc990c24adb4906", 761226752),
-    ("paged_decode_append", "decode_kernel"): ("4dc990c24adb4906", 761924096),
+    ("causal_prefill_past_kv", "prefill_kernel"): ("9df8eaf9a30e8b5c", 104366848 + 9394944),
+    ("gpt2_small_layer", "prefill_kernel"): ("9df8eaf9a30e8b5c", 37830144 + 122624),
+    ("llama3_8b_layer", "prefill_kernel"): ("9df8eaf9a30e8b5c", 100860160 + 37312512),
+    ("dynamic_topk", "prefill_kernel"): ("9df8eaf9a30e8b5c", 199035904 + 51283712),
+    ("paged_varlen_decode", "decode_kernel"): ("9018a256470fb146", 752910848 + 9687040),
+    ("paged_decode_append", "decode_kernel"): ("9018a256470fb146", 752864256 + 9860096),
 }
 
 

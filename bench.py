@@ -57,10 +57,10 @@ KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_dev
 # time: once the kernel changes the figure no longer applies and is reported
 # as null.
 MEASURED_TRAFFIC = {
-    ("causal_prefill_past_kv", "prefill_kernel"): ("9df8eaf9a30e8b5c", 104366848 + 9394944),
-    ("gpt2_small_layer", "prefill_kernel"): ("9df8eaf9a30e8b5c", 37830144 + 122624),
-    ("llama3_8b_layer", "prefill_kernel"): ("9df8eaf9a30e8b5c", 100860160 + 37312512),
-    ("dynamic_topk", "prefill_kernel"): ("9df8eaf9a30e8b5c", 199035904 + 51283712),
+    ("causal_prefill_past_kv", "prefill_kernel"): ("716c5b360ef63b81", 104366848 + 9394944),
+    ("gpt2_small_layer", "prefill_kernel"): ("716c5b360ef63b81", 37830144 + 122624),
+    ("llama3_8b_layer", "prefill_kernel"): ("716c5b360ef63b81", 100860160 + 37312512),
+    ("dynamic_topk", "prefill_kernel"): ("716c5b360ef63b81", 199035904 + 51283712),
     ("paged_varlen_decode", "decode_kernel"): ("9018a256470fb146", 752910848 + 9687040),
     ("paged_decode_append", "decode_kernel"): ("9018a256470fb146", 752864256 + 9860096),
 }

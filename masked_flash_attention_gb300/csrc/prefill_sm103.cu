@@ -5,25 +5,28 @@
 // request 10466 "Summary": q@k is cut into chunks along both the query and the
 // key dimension, the softmax is accumulated progressively and rescaled at the
 // end; an all -inf chunk must not poison the running values.  Chunks whose
-// every pair is masked are not computed at all: the scheduler (sched.cu) left
-// them out of each item's key-tile list.
+// every pair is masked are not computed at all: with a dense or top-k mask the
+// scheduler (sched.cu, topk.cu) left them out of each item's key-tile list;
+// without one the kernel derives each unit's tiles from its geometry.
 //
 // Persistent kernel: one CTA per SM walks the work units (sequence, q-head,
 // 128-row query tile) longest first, in rounds of one unit per CTA with every
 // other round in reverse CTA order (serpentine), so the pipelines run on from
 // one unit into the next (Q of the next unit is fetched while the current one
-// runs; its first QK overlaps the current epilogue).
+// runs, or at d = 128 once its QKs are done; its first QK overlaps the current
+// epilogue).
 // Grouped-query heads read their K/V head directly (InfiniTrain pull request
 // 193 "Transformer 接入": no expansion); neighbouring units are the q-heads of
 // one group, so their K/V tiles are served from L2.
 //
-// Warp roles (12 warps):
+// Warp roles (12 warps; 16 in the top-k variants):
 //   warp 0      TMA producer: K tiles through an NSK-stage ring
 //   warp 1      QK issuer (one thread), Q prefetch, TMEM owner
 //   warp 2      TMA producer: V tiles through an NSV-stage ring
 //   warp 3      PV issuer (one thread)
 //   warps 4..7  softmax warpgroup 0: the even key tiles of a unit's sequence
 //   warps 8..11 softmax warpgroup 1: the odd ones
+//   warps 12..15 (top-k) more K and V gather issuers
 // TMEM (512 columns): S in two buffers [0,128) [128,256) (fp32), P in two
 // buffers [256,320) [320,384) (input type, two per column), O in [384, 384 + D).
 // With S and P double-buffered QK(j+1) runs while the softmax of tile j does,

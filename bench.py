@@ -333,9 +333,9 @@ def run_gpu(args):
     ev_ke = torch.cuda.Event(enable_timing=True)
     ev_kb.record(); ev_ke.record()
 
-    def step(timing=False, kb=None, ke=None):
+    def step(timing=False, kb=None, ke=None, ka=None):
         call(q, k, v, kvx, out=out, lse=lse, workspace=ws, stream=stream.cuda_stream, event_begin=kb,
-             event_end=ke)
+             event_end=ke, event_attn_end=ka)
 
     if bwd:
         # the forward once (untimed) for out and lse; each step is one fa_bwd
@@ -348,7 +348,7 @@ def run_gpu(args):
         assert rc == 0, rc
         ws = fa.alloc_workspace(plan["workspace_bytes"], dev)
 
-        def step(timing=False, kb=None, ke=None):  # noqa: F811
+        def step(timing=False, kb=None, ke=None, ka=None):  # noqa: F811
             fa.fa_bwd(q, k, v, out, lse, dout, dq=gq, dk=gk, dv=gv, workspace=ws, stream=stream.cuda_stream,
                       event_begin=kb, event_end=ke, **gp)
 
@@ -362,8 +362,10 @@ def run_gpu(args):
     # ---- device-resident timing ----
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    # per step: the attention kernel's begin, the end of the attention kernel
+    # itself, the end of the call's last pass (the decode path's split combine)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         # one more untimed step: the sampler's start-up pause leaves the GPU
         # idle, and the first step after an idle GPU runs slow
@@ -374,13 +376,16 @@ def run_gpu(args):
         torch.cuda.synchronize()
         for i in range(args.steps):
             flush.zero_()
-            kev[i][0].record(); kev[i][1].record()  # materialise the handles
+            kev[i][0].record(); kev[i][1].record(); kev[i][2].record()  # materialise the handles
             ev[i][0].record()
-            step(kb=kev[i][0], ke=kev[i][1])
+            step(kb=kev[i][0], ke=kev[i][2], ka=None if bwd else kev[i][1])
             ev[i][1].record()
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    # the dominant kernel alone (the backward: its three kernels); the passes
+    # after it (split combine) are reported beside it
+    kern_ms = [a.elapsed_time(c if bwd else b) for a, b, c in kev]
+    after_ms = [0.0 if bwd else b.elapsed_time(c) for a, b, c in kev]
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(dist, total_ms, dev)
     if dist:
@@ -460,6 +465,8 @@ def run_gpu(args):
     if bwd:
         roof["kernel"] = "backward (delta_kernel, dkdv_kernel, dq_kernel)"
     roof["kernel_ms"] = round(kern_avg, 5)
+    if not bwd:
+        roof["after_kernel_ms"] = round(sum(after_ms) / len(after_ms), 5)  # split combine (decode), else ~0
     roof["traffic"] = args.traffic if args.traffic is not None else measured_traffic(args.workload, roof["kernel"])
     if units["bytes"] is not None or roof["bound"] == "tensor":
         roof["algorithmic_bytes"] = units["bytes"] if units["bytes"] is not None else algorithmic_io_bytes(case)

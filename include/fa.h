@@ -82,7 +82,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 6
+#define FA_ABI_VERSION 7
 
 typedef enum {
   FA_OK = 0,
@@ -156,6 +156,12 @@ typedef struct {
  * On the prefill path ALiBi cannot be combined with a top-k mask
  * (FA_ERR_UNSUPPORTED); the decode path takes any combination. */
   const void* alibi_slopes;
+  /* Optional cudaEvent_t (NULL = none), recorded on `stream` right after the
+   * main attention kernel itself, before the split combine pass of the
+   * decode path (for the prefill path, at the same point as event_end):
+   * with event_begin it times the attention kernel alone.  fa_fwd and
+   * fa_fwd_kvcache only. */
+  void* event_attn_end;
 } fa_opts;
 
 /* Kernel path chosen by the planner. */

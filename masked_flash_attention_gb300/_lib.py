@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmfa_gb300.so")
 
 # FA_ABI_VERSION of include/fa.h that the structures below describe
-ABI_VERSION = 6
+ABI_VERSION = 7
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = 1
@@ -56,7 +56,8 @@ class fa_opts(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("max_seqlen_q", ctypes.c_int32),
                 ("max_seqlen_k", ctypes.c_int32), ("debug_flags", ctypes.c_uint32),
                 ("reserved", ctypes.c_int32), ("event_begin", ctypes.c_void_p),
-                ("event_end", ctypes.c_void_p), ("alibi_slopes", ctypes.c_void_p)]
+                ("event_end", ctypes.c_void_p), ("alibi_slopes", ctypes.c_void_p),
+                ("event_attn_end", ctypes.c_void_p)]
 
 
 class fa_plan(ctypes.Structure):
@@ -201,11 +202,12 @@ def _out_shapes(q, cu_seqlens_q, max_seqlen_q):
 
 
 def make_opts(stream=None, workspace=None, max_seqlen_q=0, max_seqlen_k=0, debug_flags=0,
-              event_begin=None, event_end=None, alibi_slopes=None):
+              event_begin=None, event_end=None, alibi_slopes=None, event_attn_end=None):
     o = fa_opts()
     o.alibi_slopes = alibi_slopes.data_ptr() if alibi_slopes is not None else None
     o.event_begin = event_begin.cuda_event if event_begin is not None else None
     o.event_end = event_end.cuda_event if event_end is not None else None
+    o.event_attn_end = event_attn_end.cuda_event if event_attn_end is not None else None
     o.stream = stream if stream is not None else torch.cuda.current_stream().cuda_stream
     o.workspace = workspace.data_ptr() if workspace is not None else None
     o.workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
@@ -257,7 +259,7 @@ def fa_fwd(q, k, v, *, out=None, lse=None, cu_seqlens_q=None, cu_seqlens_k=None,
            block_table=None, mask=None, zero_hold_states=None, keep_window=0, window_left=-1,
            window_right=-1, softcap=0.0, scale=None, causal=False, max_seqlen_q=None,
            max_seqlen_k=None, workspace=None, stream=None, debug_flags=0, event_begin=None,
-           event_end=None, alibi_slopes=None, **_):
+           event_end=None, alibi_slopes=None, event_attn_end=None, **_):
     """Masked attention forward on the GPU through the C ABI.  Returns
     ``(out, lse, workspace)``; ``out``/``lse``/``workspace`` are allocated with
     torch when not given.  ``alibi_slopes``: optional fp32 CUDA tensor [Hq].
@@ -272,7 +274,7 @@ def fa_fwd(q, k, v, *, out=None, lse=None, cu_seqlens_q=None, cu_seqlens_k=None,
     alibi_slopes = _alibi(alibi_slopes, q)
     opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                      debug_flags=debug_flags, event_begin=event_begin, event_end=event_end,
-                     alibi_slopes=alibi_slopes)
+                     alibi_slopes=alibi_slopes, event_attn_end=event_attn_end)
     args, keep = _args(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, block_table, mask,
                        zero_hold_states, keep_window, window_left, window_right, softcap,
                        scale or 0.0, causal, opts)
@@ -366,7 +368,7 @@ def fa_fwd_kvcache(q, k_cache, v_cache, k_new, v_new, cache_seqlens, *, out=None
                    cu_seqlens_q=None, block_table=None, window_left=-1, window_right=-1, softcap=0.0,
                    scale=None, causal=True, append=False, max_seqlen_q=None, max_seqlen_k=None,
                    workspace=None, stream=None, debug_flags=0, event_begin=None, event_end=None,
-                   alibi_slopes=None, **_):
+                   alibi_slopes=None, event_attn_end=None, **_):
     """Attention over a KV cache plus the step's active keys (fa_fwd_kvcache of
     the C ABI): sequence s sees cache rows [0, cache_seqlens[s]) and then its
     own active rows ``k_new``/``v_new`` (laid out like ``q``); with ``append``
@@ -383,7 +385,7 @@ def fa_fwd_kvcache(q, k_cache, v_cache, k_new, v_new, cache_seqlens, *, out=None
     alibi_slopes = _alibi(alibi_slopes, q)
     opts = make_opts(stream=stream, max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                      debug_flags=debug_flags, event_begin=event_begin, event_end=event_end,
-                     alibi_slopes=alibi_slopes)
+                     alibi_slopes=alibi_slopes, event_attn_end=event_attn_end)
     args, keep = _kv_args(q, k_cache, v_cache, k_new, v_new, out, lse, cu_seqlens_q, cache_seqlens,
                           block_table, window_left, window_right, softcap, scale, causal, append, opts)
     if workspace is None:
@@ -469,14 +471,14 @@ def fa_fwd_noalloc(q, k, v, *, out, lse, cu_seqlens_q=None, cu_seqlens_k=None, b
                    mask=None, zero_hold_states=None, keep_window=0, window_left=-1, window_right=-1,
                    softcap=0.0, scale=None, causal=False, max_seqlen_q=None, max_seqlen_k=None,
                    stream=None, debug_flags=0, alibi_slopes=None, workspace=None, event_begin=None,
-                   event_end=None):
+                   event_end=None, event_attn_end=None):
     """fa_fwd_noalloc of the C ABI: the forward pass for callers that may not
     allocate device memory.  ``out`` and ``lse`` are caller-provided; the
     library's static device scratch replaces the workspace, so nothing is
     allocated by this call.  A workspace or timing events cannot be used here
     and are refused rather than ignored.  Raises FaError on a non-zero status
     (a problem too large for the static scratch gives FA_ERR_WORKSPACE)."""
-    if workspace is not None or event_begin is not None or event_end is not None:
+    if workspace is not None or event_begin is not None or event_end is not None or event_attn_end is not None:
         raise FaError(FA_ERR_INVALID_ARG, "fa_fwd_noalloc (takes no workspace and no timing events)")
     fn = lib.fa_fwd_noalloc
     alibi_slopes = _alibi(alibi_slopes, q)

@@ -637,9 +637,15 @@ int run_plan(Plan& pl, const fa_opts* opts) {
     }
   }
   cudaEvent_t ev_begin = static_cast<cudaEvent_t>(opts->event_begin);
+  cudaEvent_t ev_attn_end = static_cast<cudaEvent_t>(opts->event_attn_end);
   if (e == cudaSuccess) {
     TraceRange tr(P.path == FA_PATH_PREFILL ? "mfa.prefill" : "mfa.decode");
-    e = (P.path == FA_PATH_PREFILL) ? launch_prefill(P, st, ev_begin) : launch_decode(P, st, ev_begin);
+    if (P.path == FA_PATH_PREFILL) {
+      e = launch_prefill(P, st, ev_begin);
+      if (e == cudaSuccess && ev_attn_end) e = cudaEventRecord(ev_attn_end, st);
+    } else {
+      e = launch_decode(P, st, ev_begin, ev_attn_end);
+    }
   }
   if (e == cudaSuccess && opts->event_end)
     e = cudaEventRecord(static_cast<cudaEvent_t>(opts->event_end), st);

@@ -662,7 +662,7 @@ bool decode_maps(const Params& p, CUtensorMap* mk, CUtensorMap* mv) {
 }
 
 template <int D, bool F16, bool KV2>
-cudaError_t launch_decode_v(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
+cudaError_t launch_decode_v(const Params& p, cudaStream_t st, cudaEvent_t ev_begin, cudaEvent_t ev_attn_end) {
   cudaError_t e;
   const int64_t grid = p.n_items * p.n_splits;
   using S = DecodeSmem<D>;
@@ -681,6 +681,7 @@ cudaError_t launch_decode_v(const Params& p, cudaStream_t st, cudaEvent_t ev_beg
     decode_kernel<D, false, F16, KV2><<<(unsigned)grid, kThreads, S::kTotal, st>>>(p, mk, mv);
   }
   e = cudaGetLastError();
+  if (e == cudaSuccess && ev_attn_end) e = cudaEventRecord(ev_attn_end, st);
   if (e != cudaSuccess || p.n_splits <= 1) return e;
   combine_kernel<D, F16><<<(unsigned)p.n_items, 32 * kDecodeRows, 0, st>>>(p);
   return cudaGetLastError();
@@ -689,16 +690,23 @@ cudaError_t launch_decode_v(const Params& p, cudaStream_t st, cudaEvent_t ev_beg
 // KV2: keys from two sources (fa_fwd_kvcache), a separate instantiation so
 // that the one-source kernels carry none of its code
 template <int D, bool F16>
-cudaError_t launch_decode_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
-  return p.cache_len ? launch_decode_v<D, F16, true>(p, st, ev_begin) : launch_decode_v<D, F16, false>(p, st, ev_begin);
+cudaError_t launch_decode_d(const Params& p, cudaStream_t st, cudaEvent_t ev_begin, cudaEvent_t ev_attn_end) {
+  return p.cache_len ? launch_decode_v<D, F16, true>(p, st, ev_begin, ev_attn_end)
+                     : launch_decode_v<D, F16, false>(p, st, ev_begin, ev_attn_end);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
-  if (p.n_items <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
-  if (p.f16) return p.d == 64 ? launch_decode_d<64, true>(p, st, ev_begin) : launch_decode_d<128, true>(p, st, ev_begin);
-  return p.d == 64 ? launch_decode_d<64, false>(p, st, ev_begin) : launch_decode_d<128, false>(p, st, ev_begin);
+cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin, cudaEvent_t ev_attn_end) {
+  if (p.n_items <= 0) {
+    cudaError_t e = ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
+    return (e == cudaSuccess && ev_attn_end) ? cudaEventRecord(ev_attn_end, st) : e;
+  }
+  if (p.f16)
+    return p.d == 64 ? launch_decode_d<64, true>(p, st, ev_begin, ev_attn_end)
+                     : launch_decode_d<128, true>(p, st, ev_begin, ev_attn_end);
+  return p.d == 64 ? launch_decode_d<64, false>(p, st, ev_begin, ev_attn_end)
+                   : launch_decode_d<128, false>(p, st, ev_begin, ev_attn_end);
 }
 
 }  // namespace mfa

@@ -149,7 +149,7 @@ extern thread_local bool g_trace_ranges;
 cudaError_t launch_classify(const Params& p, cudaStream_t st);
 // The attention launchers record `ev_begin` (if not null) on the stream right
 // before the kernel itself is enqueued, after all host-side preparation.
-cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
+cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin, cudaEvent_t ev_attn_end);
 cudaError_t launch_prefill(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
 cudaError_t launch_prefill_f16(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);  // p.f16 inputs
 cudaError_t launch_backward(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);

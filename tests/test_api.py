@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(fa.lib, n), n
         assert ctypes.cast(getattr(fa.lib, n), ctypes.c_void_p).value
-    assert fa.fa_abi_version() == 6 == _lib.ABI_VERSION
+    assert fa.fa_abi_version() == 7 == _lib.ABI_VERSION
     assert fa.fa_status_string(0) == "ok"
 
 
@@ -215,3 +215,26 @@ def test_debug_dump_size():
     # S and P (128 x 128 fp32 each) and one reference per row, per key tile
     assert fa.fa_debug_dump_bytes_of(0) == 0
     assert fa.fa_debug_dump_bytes_of(3) == 3 * (2 * 128 * 128 + 128) * 4
+
+
+@pytest.mark.gpu
+def test_attention_end_event():
+    """event_attn_end is recorded after the attention kernel itself and before
+    the decode path's split combine: begin <= attention end <= end, and the
+    results do not depend on the events."""
+    import workloads as W
+    dev = torch.device("cuda:0")
+    case = W.paged_varlen_decode(seed=3, n_seq=8)
+    p = {k_: (v_.to(dev) if isinstance(v_, torch.Tensor) else v_) for k_, v_ in case["params"].items()}
+    q, k, v = case["q"].to(dev), case["k"].to(dev), case["v"].to(dev)
+    rc, plan = fa.fa_fwd_plan(q, k, v, **p)
+    assert rc == 0 and plan["n_splits"] > 1, plan
+    out0, lse0, ws = fa.fa_fwd(q, k, v, **p)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for e in ev:
+        e.record()  # torch creates the event handles on their first record
+    out1, lse1, _ = fa.fa_fwd(q, k, v, workspace=ws, event_begin=ev[0], event_attn_end=ev[1], event_end=ev[2], **p)
+    torch.cuda.synchronize()
+    t_attn, t_all = ev[0].elapsed_time(ev[1]), ev[0].elapsed_time(ev[2])
+    assert 0.0 < t_attn <= t_all
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)

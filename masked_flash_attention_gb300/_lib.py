@@ -11,6 +11,7 @@ from __future__ import annotations
 import ctypes
 import math
 import os
+import struct
 
 import torch
 
@@ -160,20 +161,24 @@ def fa_abi_version() -> int:
     return lib.fa_abi_version()
 
 
+# fa_tensor's bytes: data pointer, dtype, ndim, shape[4], stride[4] (native
+# byte order, no padding), packed in one call: the struct is built on every
+# fa_fwd, so this keeps the host side of a call short
+_TENSOR_BYTES = struct.Struct("=Qii4q4q")
+assert _TENSOR_BYTES.size == ctypes.sizeof(fa_tensor)
+
+
 def describe(t: torch.Tensor | None):
     """fa_tensor for a torch tensor (None -> None)."""
     if t is None:
         return None
-    if t.dim() > 4:
+    nd = t.dim()
+    if nd > 4:
         raise ValueError("at most 4 dimensions")
-    d = fa_tensor()
-    d.data = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or 16)
-    d.dtype = _DTYPES.get(t.dtype, 0)
-    d.ndim = t.dim()
-    for i in range(t.dim()):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
-    return d
+    pad = (0,) * (4 - nd)
+    # an empty tensor may have no storage: a dummy non-null pointer (never read)
+    return fa_tensor.from_buffer_copy(_TENSOR_BYTES.pack(t.data_ptr() or 16, _DTYPES.get(t.dtype, 0), nd,
+                                                         *t.shape, *pad, *t.stride(), *pad))
 
 
 def _ref(x):

@@ -19,7 +19,7 @@
 // 193 "Transformer 接入": no expansion); neighbouring units are the q-heads of
 // one group, so their K/V tiles are served from L2.
 //
-// Warp roles (12 warps; 16 in the top-k variants):
+// Warp roles (12 warps; 16 in the top-k variants; 8 at d = 64 otherwise):
 //   warp 0      TMA producer: K tiles through an NSK-stage ring
 //   warp 1      QK issuer (one thread), Q prefetch, TMEM owner
 //   warp 2      TMA producer: V tiles through an NSV-stage ring
@@ -41,6 +41,10 @@
 // reference is only raised when the row max exceeds it by more than 2^8 (in
 // log2 units), so O in TMEM is rarely rescaled.  A fully masked row keeps reference -inf,
 // exponentiates against 0, and ends with l = 0: O = 0, LSE = -inf.
+// At d = 64 (no top-k) the tiles are short and a unit's fixed costs weigh
+// most, so a CTA has a single softmax warpgroup (warps 4..7, every tile of
+// its units) and 256 TMEM columns (S [0,128), P [128,192), O [192,256)), and
+// two CTAs share each SM: one CTA's unit epilogue overlaps the other's tiles.
 //
 // Every mbarrier wait is bounded (1 s); on a time-out the kernel records
 // FA_ERR_DEVICE_TIMEOUT in the workspace error word, every role stops, in-flight
@@ -83,26 +87,48 @@ static_assert(128 * kProducerRegs + 256 * kSoftmaxRegs <= kPrefillThreads * kLau
               "the register split must fit the block's launch allocation");
 static_assert(256 * kGatherProducerRegs + 256 * kSoftmaxRegs <= kGatherThreads * kGatherLaunchRegs,
               "the register split must fit the block's launch allocation");
-__host__ __device__ constexpr int prefill_threads(int mk) { return mk == FA_MASK_TOPK ? kGatherThreads : kPrefillThreads; }
-__host__ __device__ constexpr int prefill_launch_regs(int mk) { return mk == FA_MASK_TOPK ? kGatherLaunchRegs : kLaunchRegs; }
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 0;    // S buffers: kSCol + 128 * buf
-constexpr uint32_t kPCol = 256;  // P buffers: kPCol + 64 * buf
-constexpr uint32_t kOCol = 384;  // O
+// At d = 64 (no top-k) a CTA has one softmax warpgroup (8 warps) and two
+// CTAs share each SM: half the TMEM and shared memory each, and the same
+// 40 / 216 register split as the gather variants.
+constexpr int kPairThreads = 256;
+__host__ __device__ constexpr int prefill_threads(int d, int mk) {
+  return mk == FA_MASK_TOPK ? kGatherThreads : (d == 64 ? kPairThreads : kPrefillThreads);
+}
+__host__ __device__ constexpr int prefill_launch_regs(int d, int mk) {
+  return (mk == FA_MASK_TOPK || d == 64) ? kGatherLaunchRegs : kLaunchRegs;
+}
+__host__ __device__ constexpr int prefill_ctas_per_sm(int d, int mk) { return (d == 64 && mk != FA_MASK_TOPK) ? 2 : 1; }
+static_assert(128 * kGatherProducerRegs + 128 * kSoftmaxRegs <= kPairThreads * kGatherLaunchRegs,
+              "the register split must fit the block's launch allocation");
+static_assert(2 * kPairThreads * kGatherLaunchRegs <= 65536, "two CTAs per SM must fit the register file");
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D, bool GTH = false>
 struct PCfg {
+  // Softmax warpgroups per CTA.  Two take alternate key tiles of one unit
+  // (S and P double-buffered in TMEM).  At d = 64 without top-k a CTA has
+  // one, which takes every tile of its units, and two CTAs run on each SM:
+  // a unit's epilogue in one CTA (waiting for its last PV, normalising,
+  // storing) then overlaps the other CTA's tiles instead of stalling the
+  // SM's tensor pipe, as a shared O buffer would.
+  static constexpr int NW = (D == 64 && !GTH) ? 1 : 2;
+  // TMEM: S buffers (128 fp32 columns each), P buffers (128 keys of the
+  // input type, two per column) and O; 512 columns, 256 with NW == 1.
+  static constexpr uint32_t kCols = NW == 2 ? 512 : 256;
+  static constexpr uint32_t kSCol = 0;              // S buffer b: kSCol + 128 * b
+  static constexpr uint32_t kPCol = 128 * NW;       // P buffer b: kPCol + 64 * b
+  static constexpr uint32_t kOCol = kPCol + 64 * NW;
   // Ring stages and Q buffers.  At d = 128 a third K stage (so that a K
   // tile's copy has a tile period more to land before its QK) is paid for
   // with the second Q buffer: the next unit's Q is then fetched once the
   // current unit's QKs are done, which the epilogue hides (the causal-prefill
   // workload 124.3 -> 114.7 us, the Llama-3 layer 408 -> 376 us).  The
   // gathered top-k tiles keep two Q buffers and two K stages (with three K
-  // stages and one Q buffer they measured 371 us against 351 us).
-  static constexpr int NQ = (D == 128 && !GTH) ? 1 : 2;             // Q buffers
-  static constexpr int NSK = (D == 128) ? (GTH ? 2 : 3) : 4;        // K ring stages
-  static constexpr int NSV = (D == 128) ? 2 : 4;    // V ring stages
+  // stages and one Q buffer they measured 371 us against 351 us).  With two
+  // CTAs per SM each has two of everything.
+  static constexpr int NQ = (D == 128 && !GTH) ? 1 : 2;                          // Q buffers
+  static constexpr int NSK = (D == 128) ? (GTH ? 2 : 3) : (NW == 1 ? 2 : 4);     // K ring stages
+  static constexpr int NSV = (D == 128 || NW == 1) ? 2 : 4;                      // V ring stages
   static constexpr int kTileBytes = 128 * D * 2;    // one 128-row tile of 2-byte elements
   static constexpr int kQOff = 0;                   // NQ Q buffers
   static constexpr int kKOff = NQ * kTileBytes;
@@ -113,15 +139,15 @@ struct PCfg {
   static constexpr int kRedOff = kAuxOff + 512;
   static constexpr int kSumOff = kRedOff + 2 * 128 * 4;
   static constexpr int kTopkOff = kSumOff + 2 * 128 * 4;
-  // output staging: per softmax warp 32 rows x 32 output columns
   // top-k staging, per warpgroup and buffer: first keeping row, number of
   // keeping rows (int) and bias (fp32) of each of the tile's 128 columns
   static constexpr int kTopkBuf = 3 * 128 * 4;
-  static constexpr int kStageOff = (kTopkOff + 2 * 2 * kTopkBuf + 1023) / 1024 * 1024;  // swizzle-aligned
-  static constexpr int kSmem = kStageOff + 8 * 2048 + 1024;  // + alignment slack
-  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+  // output staging: per softmax warp 32 rows x 32 output columns
+  static constexpr int kStageOff = (kTopkOff + (GTH ? 2 * 2 * kTopkBuf : 0) + 1023) / 1024 * 1024;  // swizzle-aligned
+  static constexpr int kSmem = kStageOff + 4 * NW * 2048 + 1024;  // + alignment slack
+  static_assert(kSmem <= (NW == 2 ? 227 * 1024 : 113 * 1024), "shared memory budget");
   static_assert(kStageOff % 1024 == 0, "TMA store source alignment");
-  static_assert(kOCol + D <= kTmemCols, "TMEM budget");
+  static_assert(kOCol + D <= kCols, "TMEM budget");
 };
 
 // One work unit: 128 query rows of one q-head of one sequence.  Its key tiles
@@ -368,11 +394,12 @@ __device__ __forceinline__ void row_key_range(const Params& p, int i, int q_len,
 // output are fp16 (else bf16); DBG: the debug instantiation, which also
 // writes S, P and the exponent references of one unit to Params::dump.
 template <int D, int MK, bool SC, bool AL, bool F16, bool DBG = false>
-__global__ void __launch_bounds__(prefill_threads(MK), 1)
+__global__ void __launch_bounds__(prefill_threads(D, MK), prefill_ctas_per_sm(D, MK))
     prefill_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const int o_tma) {
   using C = PCfg<D, MK == FA_MASK_TOPK>;
-  constexpr int NSK = C::NSK, NSV = C::NSV, NQ = C::NQ;
+  constexpr int NSK = C::NSK, NSV = C::NSV, NQ = C::NQ, NW = C::NW;
+  constexpr uint32_t kSCol = C::kSCol, kPCol = C::kPCol, kOCol = C::kOCol;
   constexpr bool INL = (MK == FA_MASK_NONE);  // the host sets p.sched_inline exactly then
   constexpr bool GTH = (MK == FA_MASK_TOPK);   // tiles of gathered keys (2-D K/V maps)
   extern __shared__ unsigned char smem_raw[];
@@ -427,7 +454,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_alloc(tmem_slot, C::kCols);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -435,9 +462,9 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
   tc::fence_after_sync();
   const uint32_t tbase = *tmem_slot;
 
-  if (GTH && (warp < 4 || warp >= 12)) {
+  if ((GTH || NW == 1) && (warp < 4 || warp >= 12)) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kGatherProducerRegs));
-  } else if (!GTH && warp < 4) {
+  } else if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
   }
   if (GTH && (warp == 0 || warp == 2 || warp >= 12)) {
@@ -544,8 +571,8 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
-    // S[g % 2] = Q K_g^T for the g-th tile this CTA processes, as soon as the
-    // softmax has read that S buffer two tiles back.  Also fetches Q: with two
+    // S[g % NW] = Q K_g^T for the g-th tile this CTA processes, as soon as
+    // the softmax has read that S buffer NW tiles back.  Also fetches Q: with two
     // buffers the next unit's Q while the current unit runs, with one the next
     // unit's Q once the current unit's QKs are done.
     if (lane == 0) {
@@ -573,9 +600,9 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
         const int un = next_busy<INL, GTH>(p, u + 1, wn);
         if (!tc::mbar_wait(q_full + qb, (kk / NQ) & 1, abort_flag)) { ok = false; break; }
         for (int i = 0; i < w.count; ++i, ++g) {
-          const int s = g % NSK, sb = g & 1;
+          const int s = g % NSK, sb = g % NW;
           if (!tc::mbar_wait(k_full + s, (g / NSK) & 1, abort_flag)) { ok = false; break; }
-          if (g >= 2 && !tc::mbar_wait(s_free + sb, ((g - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (g >= NW && !tc::mbar_wait(s_free + sb, ((g - NW) / NW) & 1, abort_flag)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t qa = sQ + qb * C::kTileBytes, ka = sK + s * C::kTileBytes;
 #pragma unroll
@@ -620,7 +647,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
     __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------ PV issuer
-    // O (+)= P[g % 2] V_g once the softmax of tile g has written P (and
+    // O (+)= P[g % NW] V_g once the softmax of tile g has written P (and
     // rescaled O); the first tile of a unit overwrites O.
     if (lane == 0) {
       constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true, F16);
@@ -630,8 +657,8 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
       Unit w;
       for (int r = next_busy<INL, GTH>(p, 0, w); ok && r >= 0; r = next_busy<INL, GTH>(p, r + 1, w)) {
         for (int i = 0; i < w.count; ++i, ++g) {
-          const int s = g % NSV, pb = g & 1;
-          if (!tc::mbar_wait(p_full + pb, (g >> 1) & 1, abort_flag) ||
+          const int s = g % NSV, pb = g % NW;
+          if (!tc::mbar_wait(p_full + pb, (g / NW) & 1, abort_flag) ||
               !tc::mbar_wait(v_full + s, (g / NSV) & 1, abort_flag)) {
             ok = false;
             break;
@@ -665,7 +692,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
     // final reference and added at the end.  The warpgroups meet through
     // mbarriers (bounded waits), never through a named barrier, so that one
     // that gives up on a timed-out wait cannot leave the other stuck.
-    const int w = (warp - 4) >> 2;
+    const int w = NW == 2 ? (warp - 4) >> 2 : 0;
     const int wtid = tid - 128 - 128 * w;  // 0..127 within the warpgroup
     const int wq = warp & 3;               // TMEM lane quarter this warp may access
     const int row = 32 * wq + lane;
@@ -673,7 +700,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
     float* refv = reinterpret_cast<float*>(smem + C::kRedOff);  // [2 tile parity][128]
     float* rsum = reinterpret_cast<float*>(smem + C::kSumOff);  // [2 warpgroups][128]
     unsigned char* kbuf = smem + C::kTopkOff + w * 2 * C::kTopkBuf;  // [2 buffers][lo, len, bias][128]
-    constexpr int kHalfD = D / 2;  // O columns each warpgroup rescales and stores
+    constexpr int kHalfD = D / NW;  // O columns each warpgroup stores
     bool ok = true;
     int g = 0, kk = 0;  // tiles and busy units so far (all of them, both parities)
     const int nu = n_units(p);
@@ -717,22 +744,22 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
       float r_own = -INFINITY;  // reference this warpgroup's row sum is against
       float l = 0.f;
       // the first tile of the unit is this warpgroup's if g is of its parity
-      const int it0 = (g & 1) == w ? 0 : 1;
+      const int it0 = (NW == 1 || (g & 1) == w) ? 0 : 1;
       // gathered keys: this thread's column entry of the warpgroup's next tile,
       // read a tile ahead so that its latency hides behind the current one
       uint2 gnext = make_uint2(0, 0);
       if (GTH && it0 < un.count) gnext = __ldg(glist + it0 * kKeysPerTile + wtid);
       int ent_cur = (kArith || !pre_ok) ? (it0 < un.count ? unit_entry<INL, GTH>(un, it0) : 0) : ent_first;
-      for (int it = it0; it < un.count; it += 2) {
+      for (int it = it0; it < un.count; it += NW) {
         const int gt = g + it;  // global index of this tile
-        const int par = w;      // == gt & 1
+        const int par = w;      // == gt % NW
         const int ent = kArith ? unit_entry<INL, GTH>(un, it) : ent_cur;
         if (kArith) {
-        } else if (it + 2 < un.count) {
-          ent_cur = unit_entry<INL>(un, it + 2);
+        } else if (it + NW < un.count) {
+          ent_cur = unit_entry<INL>(un, it + NW);
         } else if (u_next < nu && un_next.present && un_next.valid && un_next.count > 0) {
           // this warpgroup's first entry of the next unit
-          const int itn = ((g + un.count) & 1) == w ? 0 : 1;
+          const int itn = (NW == 1 || ((g + un.count) & 1) == w) ? 0 : 1;
           if (itn < un_next.count) {
             ent_first = unit_entry<INL>(un_next, itn);
             ent_first_ok = true;
@@ -754,7 +781,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
           tc::mbar_arrive(kready + 2 * w + kb);
           if (!tc::mbar_wait(kready + 2 * w + kb, (gt >> 2) & 1, abort_flag)) { ok = false; break; }
         }
-        if (!tc::mbar_wait(s_full + par, (gt >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!tc::mbar_wait(s_full + par, (gt / NW) & 1, abort_flag)) { ok = false; break; }
         tc::fence_after_sync();
         float2 x[64];
         {
@@ -778,7 +805,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
           }
         }
         tc::fence_before_sync();
-        tc::mbar_arrive_relaxed(s_free + par);  // the QK two tiles on may overwrite this S buffer
+        tc::mbar_arrive_relaxed(s_free + par);  // the QK NW tiles on may overwrite this S buffer
         // logits in log2 units; a FULL tile without soft-cap keeps raw scores
         // and folds the scale into the exponent below
         // Without an additive term, soft-cap or ALiBi every tile takes the
@@ -858,18 +885,23 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
           }
           mx = row_max128(x);
         }
-        // the reference after tile gt - 1 (every tile's reference is posted,
-        // also across units, so that the two warpgroups stay in step)
-        if (gt >= 1 && !tc::mbar_wait(refb + (par ^ 1), ((gt - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
-        const float m_prev = (it == 0) ? -INFINITY : refv[(par ^ 1) * 128 + row];
+        // the reference after tile gt - 1 (with two warpgroups every tile's
+        // reference is posted, also across units, so that they stay in step)
+        if (NW == 2 && gt >= 1 && !tc::mbar_wait(refb + (par ^ 1), ((gt - 1) >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const float m_prev = (it == 0) ? -INFINITY : (NW == 2 ? refv[(par ^ 1) * 128 + row] : m_ref);
         // raise the exponent reference only when the row max outgrew it by 2^8
         const bool upd = mx > m_prev + kRescaleLog2;
         m_ref = upd ? mx : m_prev;
-        refv[par * 128 + row] = m_ref;
-        tc::mbar_arrive(refb + par);
+        if (NW == 2) {
+          refv[par * 128 + row] = m_ref;
+          tc::mbar_arrive(refb + par);
+        }
         if (it != 0 && __any_sync(0xffffffffu, upd && m_prev != -INFINITY)) {
           // O holds the PV of tile gt - 1 (against m_prev) once that PV is done
-          if (!tc::mbar_wait(p_free + (par ^ 1), ((gt - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!tc::mbar_wait(p_free + (gt - 1) % NW, ((gt - 1) / NW) & 1, abort_flag)) { ok = false; break; }
           tc::fence_after_sync();
           const float f = (upd && m_prev != -INFINITY) ? fast_exp2(m_prev - m_ref) : 1.f;
 #pragma unroll
@@ -939,8 +971,8 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
             p.dump[(int64_t)2 * p.n_kt * 128 * 128 + (int64_t)it * 128 + row] = eref;
           }
         }
-        // this P buffer is free once the PV two tiles back is done
-        if (gt >= 2 && !tc::mbar_wait(p_free + par, ((gt - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+        // this P buffer is free once the PV NW tiles back is done
+        if (gt >= NW && !tc::mbar_wait(p_free + par, ((gt - NW) / NW) & 1, abort_flag)) { ok = false; break; }
         const uint32_t pa = lane_base + kPCol + par * 64;
 #pragma unroll
         for (int c = 0; c < 4; ++c) tc::tmem_st16(pa + c * 16, pk[c]);
@@ -954,26 +986,35 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
       // ---- epilogue: both warpgroups' row sums against the final reference
       const int gl = g + un.count - 1;  // the unit's last tile
       g += un.count;
-      if ((gl & 1) != w) {
+      if (NW == 2 && (gl & 1) != w) {
         if (!tc::mbar_wait(refb + (gl & 1), (gl >> 1) & 1, abort_flag)) { ok = false; break; }
         m_ref = refv[(gl & 1) * 128 + row];
       }
       // this warpgroup's O columns are read out of TMEM before its row sum is
       // posted: the next unit's first PV overwrites O, and its P comes from a
-      // warpgroup that has passed the row-sum barrier, so every O read is
-      // ordered before that PV
+      // warpgroup that has passed the row-sum barrier (with one warpgroup:
+      // from this one, after the read), so every O read is ordered before
+      // that PV
       if (!tc::mbar_wait(o_full, kk & 1, abort_flag)) { ok = false; break; }
       tc::fence_after_sync();
       uint32_t ro[kHalfD / 32][32];
 #pragma unroll
       for (int c = 0; c < kHalfD / 32; ++c) tc::tmem_ld32(lane_base + kOCol + w * kHalfD + c * 32, ro[c]);
-      rsum[w * 128 + row] = (r_own == m_ref || r_own == -INFINITY) ? l : l * fast_exp2(r_own - m_ref);
-      tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      tc::mbar_arrive(sumx);
-      if (!tc::mbar_wait(sumx, kk & 1, abort_flag)) { ok = false; break; }
-      tc::fence_after_sync();
-      const float lt = rsum[row] + rsum[128 + row];
+      float lt;
+      if constexpr (NW == 2) {
+        rsum[w * 128 + row] = (r_own == m_ref || r_own == -INFINITY) ? l : l * fast_exp2(r_own - m_ref);
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        tc::mbar_arrive(sumx);
+        if (!tc::mbar_wait(sumx, kk & 1, abort_flag)) { ok = false; break; }
+        tc::fence_after_sync();
+        lt = rsum[row] + rsum[128 + row];
+      } else {
+        // one warpgroup: its row sum is against the last reference already
+        tc::tmem_wait_ld();
+        tc::fence_before_sync();
+        lt = l;
+      }
       const bool empty = !(lt > 0.f);
       const float inv = empty ? 0.f : 1.f / lt;
       // O / l through a warp-private staging tile: a thread packs its own row,
@@ -1032,7 +1073,7 @@ __global__ void __launch_bounds__(prefill_threads(MK), 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 1) tc::tmem_dealloc(tbase, kTmemCols);
+  if (warp == 1) tc::tmem_dealloc(tbase, C::kCols);
   if (INL && blockIdx.x == 0 && warp == 2) inline_sched_stats(p);
 }
 
@@ -1086,12 +1127,12 @@ cudaError_t launch_prefill_v(const Params& p, cudaStream_t st, const CUtensorMap
     regs = fa.numRegs;
     launch_regs.store(regs, std::memory_order_relaxed);
   }
-  if (regs != prefill_launch_regs(MK)) return cudaErrorInvalidConfiguration;
+  if (regs != prefill_launch_regs(D, MK)) return cudaErrorInvalidConfiguration;
   using C = PCfg<D, MK == FA_MASK_TOPK>;
   cudaError_t e = ensure_smem_attr<prefill_kernel<D, MK, SC, AL, F16, DBG>>(C::kSmem);
   if (e != cudaSuccess) return e;
   if (ev_begin && (e = cudaEventRecord(ev_begin, st)) != cudaSuccess) return e;
-  prefill_kernel<D, MK, SC, AL, F16, DBG><<<(unsigned)grid, prefill_threads(MK), C::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
+  prefill_kernel<D, MK, SC, AL, F16, DBG><<<(unsigned)grid, prefill_threads(D, MK), C::kSmem, st>>>(p, mq, mk, mv, mo, o_tma);
   return cudaGetLastError();
 }
 
@@ -1123,11 +1164,13 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
              !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb, F16)) {
     return cudaErrorInvalidValue;
   }
-  // one CTA per SM (persistent), never more CTAs than work units
+  // one CTA per SM (two at d = 64 without top-k; persistent), never more
+  // CTAs than work units
   const int64_t units = (int64_t)p.n_row_tiles * p.n_seq * p.Hq;
   if (units <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
   if (units > INT_MAX) return cudaErrorInvalidValue;
-  const int grid = (int)(units < sm_count() ? units : sm_count());
+  const int64_t slots = (int64_t)sm_count() * prefill_ctas_per_sm(D, p.mask_kind);
+  const int grid = (int)(units < slots ? units : slots);
   const bool sc = p.softcap > 0.f;
   // the kernels schedule inline exactly for the mask-free variants
   if ((p.sched_inline != 0) != (p.mask_kind == FA_MASK_NONE)) return cudaErrorInvalidValue;

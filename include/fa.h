@@ -70,7 +70,10 @@
  * error word in the first bytes of the workspace; fa_check_device_error()
  * reads and clears it.  The caller zero-fills the workspace's first 256 bytes
  * once, before its first use; fa_fwd never clears the word itself, so a fault
- * stays visible until it is checked.
+ * stays visible until it is checked.  The rest of those 256 bytes holds the
+ * arrival counts of the prefill tail split (fa_plan.tail_units), which every
+ * completed launch leaves at zero; fa_check_device_error clears all 256 bytes
+ * when it finds a fault.  One workspace serves one call at a time.
  */
 #ifndef MFA_GB300_FA_H
 #define MFA_GB300_FA_H
@@ -82,7 +85,7 @@
 extern "C" {
 #endif
 
-#define FA_ABI_VERSION 7
+#define FA_ABI_VERSION 8
 
 typedef enum {
   FA_OK = 0,
@@ -215,7 +218,9 @@ typedef struct {
   int32_t n_k_tiles;       /* key tiles of the longest key sequence */
   int32_t n_splits;        /* DECODE: key splits per item (1 = no combine pass) */
   int32_t tiles_per_split; /* DECODE: key tiles per split */
-  int32_t reserved;
+  int32_t tail_units;      /* PREFILL: units of the persistent grid's last round
+                              that two CTAs run as halves of their key tiles and
+                              merge by LSE (0 = none) */
   int64_t n_items;
   size_t off_counts;
   size_t off_tiles;

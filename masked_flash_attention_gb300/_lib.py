@@ -19,7 +19,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmfa_gb300.so")
 
 # FA_ABI_VERSION of include/fa.h that the structures below describe
-ABI_VERSION = 7
+ABI_VERSION = 8
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = 1
@@ -66,7 +66,7 @@ class fa_plan(ctypes.Structure):
                 ("n_heads_sched", ctypes.c_int32), ("n_row_tiles", ctypes.c_int32),
                 ("rows_per_tile", ctypes.c_int32), ("keys_per_tile", ctypes.c_int32),
                 ("n_k_tiles", ctypes.c_int32), ("n_splits", ctypes.c_int32),
-                ("tiles_per_split", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("tiles_per_split", ctypes.c_int32), ("tail_units", ctypes.c_int32),
                 ("n_items", ctypes.c_int64), ("off_counts", ctypes.c_size_t),
                 ("off_tiles", ctypes.c_size_t), ("off_stats", ctypes.c_size_t),
                 ("off_topk_e", ctypes.c_size_t), ("off_topk_list", ctypes.c_size_t),

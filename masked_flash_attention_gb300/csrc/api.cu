@@ -61,7 +61,7 @@ struct Plan {
   fa_plan pub;
   Params prm;
   size_t off_summary, off_topk_e, off_topk_maxe, off_topk_runs, off_topk_rank, off_topk_rho, off_topk_list,
-      off_topk_full, off_part_o, off_part_lse;
+      off_topk_full, off_part_o, off_part_lse, off_tail;
 };
 
 int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const fa_tensor* out,
@@ -364,6 +364,11 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   if (P.n_splits > 1) off = align_up(off + (size_t)P.n_items * P.n_splits * kDecodeRows * d * 4);
   pl->off_part_lse = off;
   if (P.n_splits > 1) off = align_up(off + (size_t)P.n_items * P.n_splits * kDecodeRows * 4);
+  // prefill: persistent grid and the split of its last round (mask-free units)
+  P.prefill_grid = P.tail_round = P.tail_units = 0;
+  if (P.path == FA_PATH_PREFILL && P.n_items > 0) plan_prefill_grid(P);
+  pl->off_tail = off;
+  if (P.tail_units > 0) off = align_up(off + (size_t)P.tail_units * 2 * (kPrefillRows * d + 256) * 4);
 
   pub.path = P.path;
   pub.n_seq = P.n_seq;
@@ -374,6 +379,7 @@ int make_plan(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v, const 
   pub.n_k_tiles = n_kt_alloc;
   pub.n_splits = P.n_splits;
   pub.tiles_per_split = P.tiles_per_split;
+  pub.tail_units = P.tail_units;
   pub.n_items = P.n_items;
   pub.off_topk_e = (mask_kind == FA_MASK_TOPK) ? pl->off_topk_e : 0;
   pub.off_topk_list = (mask_kind == FA_MASK_TOPK && P.path == FA_PATH_PREFILL) ? pl->off_topk_list : 0;
@@ -405,6 +411,8 @@ void bind_workspace(Plan* pl, void* ws) {
   P.topk_full = reinterpret_cast<int32_t*>(base + pl->off_topk_full);
   P.part_o = reinterpret_cast<float*>(base + pl->off_part_o);
   P.part_lse = reinterpret_cast<float*>(base + pl->off_part_lse);
+  P.tail_part = reinterpret_cast<float*>(base + pl->off_tail);
+  P.tail_flags = reinterpret_cast<uint32_t*>(base + kTailFlagsOff);
 }
 
 // The device must be an sm_103 part (checked once per device).
@@ -545,6 +553,7 @@ int fa_fwd_debug_dump(const fa_tensor* q, const fa_tensor* k, const fa_tensor* v
     return FA_ERR_INVALID_ARG;
   if (dump_bytes < fa_debug_dump_bytes(pl.pub.n_k_tiles)) return FA_ERR_INVALID_ARG;
   P.dump = dump;
+  P.tail_units = 0;  // the debug instantiation runs every unit whole
   P.dump_b = seq;
   P.dump_h = head;
   P.dump_rt = row_tile;
@@ -708,9 +717,10 @@ int fa_check_device_error(void* stream, void* workspace, uint32_t* info) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
   if (h.error != 0) {
-    WsHeader z;
-    memset(&z, 0, sizeof(z));
-    if (cudaMemcpy(workspace, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    // the header and the tail-split counts, which an aborted launch may have left set
+    unsigned char z[kWsHeadBytes];
+    memset(z, 0, sizeof(z));
+    if (cudaMemcpy(workspace, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
   }
   if (info) *info = h.error_info;
   return (int)h.error;

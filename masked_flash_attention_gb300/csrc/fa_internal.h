@@ -41,6 +41,11 @@ struct WsHeader {
   uint32_t error_info;  // detail of that fault
   uint32_t pad[2];
 };
+// The workspace's first kWsHeadBytes bytes are zero-filled by the caller
+// before its first use: the header, then the prefill tail-split arrival
+// counts (Params::tail_flags), which every launch leaves at zero again.
+constexpr size_t kWsHeadBytes = 256;
+constexpr size_t kTailFlagsOff = sizeof(WsHeader);
 
 // mask summary byte values
 enum : uint8_t { kMaskEmpty = 0, kMaskZero = 1, kMaskMixed = 2 };
@@ -119,6 +124,19 @@ struct Params {
   uint2* topk_list;      // [n_items][n_kt * 128]: gathered keys of each unit (many-row path)
   int32_t* topk_full;    // [n_items]: leading gathered tiles whose keys every row of the unit keeps
 
+  // prefill grid and its tail split: the persistent grid takes the units in
+  // rounds of prefill_grid; when the last round holds tail_units units (and
+  // at most half the grid), each of them is cut into two pieces over the two
+  // halves of its key tiles, run by two CTAs of that round; each piece
+  // stores its normalised O and log2-sum-exp (tail_part: per piece, O as
+  // [d][128 rows] then [2 warpgroups][128 rows], fp32), and the piece that
+  // finishes second merges the two and writes the output.  tail_flags: one
+  // 2-bit arrival count per (tail unit, softmax warpgroup), in the
+  // workspace's zero-filled head, returned to zero by the merging piece.
+  int32_t prefill_grid, tail_round, tail_units;
+  float* tail_part;
+  uint32_t* tail_flags;
+
   // decode split-KV
   int32_t n_splits, tiles_per_split;
   float* part_o;    // [n_items][n_splits][16][d]
@@ -151,6 +169,9 @@ cudaError_t launch_classify(const Params& p, cudaStream_t st);
 // before the kernel itself is enqueued, after all host-side preparation.
 cudaError_t launch_decode(const Params& p, cudaStream_t st, cudaEvent_t ev_begin, cudaEvent_t ev_attn_end);
 cudaError_t launch_prefill(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
+// Host: the prefill kernel's persistent grid for this device and the split of
+// its last round (Params::prefill_grid, tail_round, tail_units).
+void plan_prefill_grid(Params& p);
 cudaError_t launch_prefill_f16(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);  // p.f16 inputs
 cudaError_t launch_backward(const Params& p, cudaStream_t st, cudaEvent_t ev_begin);
 // dK/dV and dQ of the backward on tcgen05; *launched = false (nothing

@@ -132,9 +132,10 @@ extern "C" int fa_fwd_noalloc(const fa_tensor* q, const fa_tensor* k, const fa_t
   void* scratch = scratch_address(dev);
   if (!scratch) return FA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(o.stream);
-  // the array keeps the previous call's contents: the error word must start
-  // at zero (the scheduler counters are cleared by every forward call)
-  if (cudaMemsetAsync(scratch, 0, sizeof(mfa::WsHeader), st) != cudaSuccess) {
+  // the array keeps the previous call's contents: the error word and the
+  // tail-split counts must start at zero (the scheduler counters are cleared
+  // by every forward call)
+  if (cudaMemsetAsync(scratch, 0, mfa::kWsHeadBytes, st) != cudaSuccess) {
     cudaGetLastError();
     return FA_ERR_CUDA;
   }

@@ -54,6 +54,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cstring>
@@ -156,6 +157,8 @@ struct PCfg {
 // unit's geometry: tiles kt0 .. kt0 + count - 1, those with relative index in
 // [fl, fh] FULL and the others PARTIAL, exactly what the scheduler kernel
 // would have listed.
+// A slot of a split last round (INL only, Params::tail_units) holds one of
+// the two pieces of a unit: a unit over half of its key tiles.
 struct Unit {
   bool present;  // the tile holds rows of the sequence
   bool valid;    // the sequence's lengths passed the checks
@@ -169,7 +172,7 @@ __device__ __forceinline__ int floor_div128(int a) { return a >= 0 ? a / 128 : -
 
 // Unit u, longest query tiles first (row tile descending), q-heads fastest.
 template <bool INL, bool GTH = false>
-__device__ __forceinline__ Unit unit_at(const Params& p, int u) {
+__device__ __forceinline__ Unit unit_of(const Params& p, int u) {
   Unit w;
   const int q = fast_div(u, p.div_units);
   w.rt = p.n_row_tiles - 1 - q;
@@ -214,6 +217,45 @@ __device__ __forceinline__ Unit unit_at(const Params& p, int u) {
     w.count = c > 0 ? c : 0;
     w.tiles = p.item_tiles + item * p.n_kt;
     if constexpr (GTH) w.fl = w.present ? __ldg(p.topk_full + item) : 0;  // leading FULL gathered tiles
+  }
+  return w;
+}
+
+// The piece slot `slot` holds: 0 for a whole unit; with a tail split, slot
+// t0 + k of the last round (t0 = tail_round * grid) holds piece 1 + (k & 1)
+// of tail unit tu = k >> 1, unit t0 + tu.
+template <bool INL>
+__device__ __forceinline__ int tail_piece(const Params& p, int slot, int& tu) {
+  tu = 0;
+  if (!INL || p.tail_units <= 0) return 0;  // the host splits d = 128 launches only
+  const int t0 = p.tail_round * (int)gridDim.x;
+  if (slot < t0) return 0;
+  tu = (slot - t0) >> 1;
+  return 1 + ((slot - t0) & 1);
+}
+
+// The unit (or piece) of slot `slot`.  The first piece of a split unit takes
+// its first ceil(count / 2) key tiles, the second the rest, as a unit whose
+// tiles start that many later; a unit of fewer than two tiles is not split
+// (its first piece takes it whole, its second is empty).
+template <bool INL, bool GTH = false>
+__device__ __forceinline__ Unit unit_at(const Params& p, int slot) {
+  int tu;
+  const int piece = tail_piece<INL>(p, slot, tu);
+  if (piece == 0) return unit_of<INL, GTH>(p, slot);
+  Unit w = unit_of<INL, GTH>(p, p.tail_round * (int)gridDim.x + tu);
+  if (w.present && w.valid && w.count >= 2) {
+    const int h1 = (w.count + 1) >> 1;
+    if (piece == 1) {
+      w.count = h1;
+    } else {
+      w.kt0 += h1;
+      w.fl -= h1;
+      w.fh -= h1;
+      w.count -= h1;
+    }
+  } else if (piece == 2) {
+    w.present = false;
   }
   return w;
 }
@@ -281,6 +323,10 @@ __device__ __noinline__ void inline_sched_stats(const Params& p) {
 }
 
 __device__ __forceinline__ int n_units(const Params& p) { return p.n_row_tiles * p.n_seq * p.Hq; }
+// Slots of the launch: one per unit, two per unit of a split last round.
+__device__ __forceinline__ int n_slots(const Params& p) {
+  return p.tail_units > 0 ? p.tail_round * (int)gridDim.x + 2 * p.tail_units : n_units(p);
+}
 
 // The unit this CTA takes in round r: the grid takes the units (longest
 // first) in rounds of gridDim.x, every other round in reverse CTA order, so
@@ -293,10 +339,10 @@ __device__ __forceinline__ int round_unit(int r) {
   return r * (int)gridDim.x + c;
 }
 
-// Next round at or after r whose unit has key tiles, or -1.
+// Next round at or after r whose slot has key tiles, or -1.
 template <bool INL, bool GTH = false>
 __device__ __forceinline__ int next_busy(const Params& p, int r, Unit& w) {
-  const int n = n_units(p);
+  const int n = n_slots(p);
   for (;; ++r) {
     const int u = round_unit(r);
     if (u >= n) return -1;
@@ -423,8 +469,11 @@ __global__ void __launch_bounds__(prefill_threads(D, MK), prefill_ctas_per_sm(D,
   uint64_t* sumx = drained + 2;       // [1] row sums of both warpgroups posted (256 arrivals)
   uint64_t* kready = sumx + 1;        // [2 warpgroups][2] top-k staging filled (128 arrivals)
   uint64_t* refb = kready + 4;        // [2 tile parity] row references posted (128 arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(refb + 2);
+  uint64_t* tdone = refb + 2;         // [2 warpgroups] tail piece stored (128 arrivals)
+  uint64_t* tflag = tdone + 2;        // [2 warpgroups] tail piece's merge decision posted (1 arrival)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tflag + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* tsec = abort_flag + 1;  // [2 warpgroups] 1: this piece merges, 2: gave up
 
   if (tid == 0) {
     for (int k = 0; k < 2; ++k) {
@@ -438,6 +487,8 @@ __global__ void __launch_bounds__(prefill_threads(D, MK), prefill_ctas_per_sm(D,
       tc::mbar_init(refb + k, 128);
       tc::mbar_init(kready + k, 128);
       tc::mbar_init(kready + 2 + k, 128);
+      tc::mbar_init(tdone + k, 128);
+      tc::mbar_init(tflag + k, 1);
     }
     tc::mbar_init(sumx, 256);
     // gathered tiles: each of the operand's three gather warps arrives
@@ -703,7 +754,7 @@ __global__ void __launch_bounds__(prefill_threads(D, MK), prefill_ctas_per_sm(D,
     constexpr int kHalfD = D / NW;  // O columns each warpgroup stores
     bool ok = true;
     int g = 0, kk = 0;  // tiles and busy units so far (all of them, both parities)
-    const int nu = n_units(p);
+    const int nu = n_slots(p);
     // Scheduler lists: the next unit's descriptor and first list entry are
     // read a unit ahead, so that no global-memory latency sits between two
     // units.  Inline scheduling and gathered top-k units: descriptors and
@@ -1017,51 +1068,128 @@ __global__ void __launch_bounds__(prefill_threads(D, MK), prefill_ctas_per_sm(D,
       }
       const bool empty = !(lt > 0.f);
       const float inv = empty ? 0.f : 1.f / lt;
-      // O / l through a warp-private staging tile: a thread packs its own row,
-      // then each store instruction writes 64 contiguous bytes of 8 rows
-      uint4* stg = reinterpret_cast<uint4*>(smem + C::kStageOff + (warp - 4) * 2048);  // [32 rows][4]
-      const int row0 = un.rt * 128 + 32 * wq;  // first row of this warp
+      const float lse2 = empty ? -INFINITY : m_ref + __log2f(lt);  // log2-sum-exp of the row
       const int64_t qbase = p.cu_q ? (int64_t)p.cu_q[b] : 0;
       uint16_t* obase = p.o + (p.cu_q ? 0 : (int64_t)b * p.o_sb) + (int64_t)h * p.o_sh;
-      // whole 32-row chunks inside the sequence leave by TMA store
-      const bool tma_rows = o_tma && row0 + 32 <= q_len;
+      // the piece this slot holds, worked out again here rather than kept
+      // live through the tile loop (a unit of fewer than two tiles is whole)
+      constexpr bool kTail = INL && NW == 2;  // compiled into the d = 128 variants only
+      int tu = 0;
+      int piece = kTail ? tail_piece<INL>(p, round_unit(r), tu) : 0;
+      if (piece == 1 && unit_of<INL, GTH>(p, p.tail_round * (int)gridDim.x + tu).count < 2) piece = 0;
+      if (kTail && piece != 0) {
+        // A piece of a split tail unit stores its normalised O and
+        // log2-sum-exp, per warpgroup half of the columns, [column][row] so
+        // that a warp's stores and loads are contiguous.  The piece whose
+        // warpgroup arrives second on the unit's 2-bit count (which it
+        // returns to zero) merges the two from memory and writes the rows:
+        // O = (O1 2^L1 + O2 2^L2) / (2^L1 + 2^L2), L = log2(2^L1 + 2^L2).
+        constexpr int kSlot = 128 * D + 256;
+        float* mine = p.tail_part + (int64_t)(2 * tu + piece - 1) * kSlot;
 #pragma unroll
-      for (int c = 0; c < kHalfD / 32; ++c) {
-        const uint32_t* r = ro[c];
-        // the staging tile is free once the previous TMA store has read it
-        if (lane == 0) tc::bulk_wait_read_all();
-        __syncwarp();
+        for (int c = 0; c < kHalfD / 32; ++c)
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          uint4 o4;
-          o4.x = pack2<F16>(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
-          o4.y = pack2<F16>(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
-          o4.z = pack2<F16>(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
-          o4.w = pack2<F16>(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
-          stg[lane * 4 + (v4 ^ ((lane >> 1) & 3))] = o4;  // swizzled: 4 wavefronts
-        }
-        if (tma_rows) {
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tc::tma_store_4d(&tmo, stg, w * kHalfD + c * 32, h, (int)(qbase + row0), p.cu_q ? 0 : b);
-            tc::bulk_commit();
+          for (int e = 0; e < 32; ++e) __stcg(mine + (w * kHalfD + c * 32 + e) * 128 + row, __uint_as_float(ro[c][e]) * inv);
+        __stcg(mine + 128 * D + w * 128 + row, lse2);
+        __threadfence();
+        tc::mbar_arrive(tdone + w);
+        if (wtid == 0) {
+          int dec = 2;
+          if (tc::mbar_wait(tdone + w, 0, abort_flag)) {
+            __threadfence();
+            const int f = 2 * (2 * tu + w);
+            uint32_t* word = p.tail_flags + (f >> 5);
+            const uint32_t old = atomicAdd(word, 1u << (f & 31));
+            dec = ((old >> (f & 31)) & 3u) == 1u ? 1 : 0;
+            if (dec == 1) atomicSub(word, 2u << (f & 31));
           }
-        } else {
+          tsec[w] = dec;
+          tc::mbar_arrive(tflag + w);
+        }
+        if (!tc::mbar_wait(tflag + w, 0, abort_flag) || tsec[w] == 2) { ok = false; break; }
+        if (tsec[w] == 1) {
+          __threadfence();
+          const float* oth = p.tail_part + (int64_t)(2 * tu + 2 - piece) * kSlot;
+          const float lo = __ldcg(oth + 128 * D + w * 128 + row);
+          const float mx = fmaxf(lse2, lo);
+          float fa = 0.f, fb = 0.f;  // weights of this piece's rows and the other's
+          float lm = -INFINITY;
+          if (mx != -INFINITY) {
+            const float ea = fast_exp2(lse2 - mx), eb = fast_exp2(lo - mx);
+            const float sum = ea + eb;
+            fa = ea / sum;
+            fb = eb / sum;
+            lm = mx + __log2f(sum);
+          }
+          if (i < q_len) {
+            uint16_t* orow = obase + (qbase + i) * p.o_ss + w * kHalfD;
+            // eight columns per step: a wider step (more loads in flight)
+            // measured slower, as the registers it takes cost the tile loop
+#pragma unroll 1
+            for (int c0 = 0; c0 < kHalfD; c0 += 8) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                v[e] = __ldcg(mine + (w * kHalfD + c0 + e) * 128 + row) * fa +
+                       __ldcg(oth + (w * kHalfD + c0 + e) * 128 + row) * fb;
+              uint4 o4;
+              o4.x = pack2<F16>(v[0], v[1]);
+              o4.y = pack2<F16>(v[2], v[3]);
+              o4.z = pack2<F16>(v[4], v[5]);
+              o4.w = pack2<F16>(v[6], v[7]);
+              *reinterpret_cast<uint4*>(orow + c0) = o4;
+            }
+            if (w == 0) {
+              float* lptr = p.lse + (p.cu_q ? 0 : (int64_t)b * p.lse_sb) + (int64_t)h * p.lse_sh + (qbase + i) * p.lse_ss;
+              *lptr = lm * kLn2;
+            }
+          }
+        }
+      } else {
+        // O / l through a warp-private staging tile: a thread packs its own row,
+        // then each store instruction writes 64 contiguous bytes of 8 rows
+        uint4* stg = reinterpret_cast<uint4*>(smem + C::kStageOff + (warp - 4) * 2048);  // [32 rows][4]
+        const int row0 = un.rt * 128 + 32 * wq;  // first row of this warp
+        // whole 32-row chunks inside the sequence leave by TMA store
+        const bool tma_rows = o_tma && row0 + 32 <= q_len;
+#pragma unroll
+        for (int c = 0; c < kHalfD / 32; ++c) {
+          const uint32_t* r = ro[c];
+          // the staging tile is free once the previous TMA store has read it
+          if (lane == 0) tc::bulk_wait_read_all();
           __syncwarp();
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int rr = 8 * k + (lane >> 2), q = lane & 3;
-            const uint4 o4 = stg[rr * 4 + (q ^ ((rr >> 1) & 3))];
-            if (row0 + rr < q_len)
-              *reinterpret_cast<uint4*>(obase + (qbase + row0 + rr) * p.o_ss + w * kHalfD + c * 32 + 8 * q) = o4;
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 o4;
+            o4.x = pack2<F16>(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
+            o4.y = pack2<F16>(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
+            o4.z = pack2<F16>(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
+            o4.w = pack2<F16>(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
+            stg[lane * 4 + (v4 ^ ((lane >> 1) & 3))] = o4;  // swizzled: 4 wavefronts
           }
-          __syncwarp();
+          if (tma_rows) {
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tc::tma_store_4d(&tmo, stg, w * kHalfD + c * 32, h, (int)(qbase + row0), p.cu_q ? 0 : b);
+              tc::bulk_commit();
+            }
+          } else {
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int rr = 8 * k + (lane >> 2), q = lane & 3;
+              const uint4 o4 = stg[rr * 4 + (q ^ ((rr >> 1) & 3))];
+              if (row0 + rr < q_len)
+                *reinterpret_cast<uint4*>(obase + (qbase + row0 + rr) * p.o_ss + w * kHalfD + c * 32 + 8 * q) = o4;
+            }
+            __syncwarp();
+          }
         }
-      }
-      if (w == 0 && i < q_len) {
-        float* lptr = p.lse + (p.cu_q ? 0 : (int64_t)b * p.lse_sb) + (int64_t)h * p.lse_sh + (qbase + i) * p.lse_ss;
-        *lptr = empty ? -INFINITY : (m_ref + __log2f(lt)) * kLn2;
+        if (w == 0 && i < q_len) {
+          float* lptr = p.lse + (p.cu_q ? 0 : (int64_t)b * p.lse_sb) + (int64_t)h * p.lse_sh + (qbase + i) * p.lse_ss;
+          *lptr = lse2 * kLn2;
+        }
       }
       ++kk;
     }
@@ -1164,13 +1292,12 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
              !encode_bshd(&mv, p.v, D, p.Hkv, k_rows, kb, p.v_sh, p.v_ss, v_sb, F16)) {
     return cudaErrorInvalidValue;
   }
-  // one CTA per SM (two at d = 64 without top-k; persistent), never more
-  // CTAs than work units
+  // the planner's grid (plan_prefill_grid)
   const int64_t units = (int64_t)p.n_row_tiles * p.n_seq * p.Hq;
   if (units <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
-  if (units > INT_MAX) return cudaErrorInvalidValue;
-  const int64_t slots = (int64_t)sm_count() * prefill_ctas_per_sm(D, p.mask_kind);
-  const int grid = (int)(units < slots ? units : slots);
+  if (units > INT_MAX || p.prefill_grid <= 0) return cudaErrorInvalidValue;
+  if (p.tail_units > 0 && (p.mask_kind != FA_MASK_NONE || p.dump)) return cudaErrorInvalidValue;
+  const int grid = p.prefill_grid;
   const bool sc = p.softcap > 0.f;
   // the kernels schedule inline exactly for the mask-free variants
   if ((p.sched_inline != 0) != (p.mask_kind == FA_MASK_NONE)) return cudaErrorInvalidValue;
@@ -1211,6 +1338,50 @@ cudaError_t launch_prefill_d(const Params& p, cudaStream_t st, cudaEvent_t ev_be
 // (prefill_f16.cu includes this file with MFA_PREFILL_F16_UNIT defined), so
 // that the two element types build in parallel.
 #ifndef MFA_PREFILL_F16_UNIT
+void plan_prefill_grid(Params& p) {
+  // one CTA per SM (two at d = 64 without top-k; persistent), never more
+  // CTAs than work units
+  const int64_t units = (int64_t)p.n_row_tiles * p.n_seq * p.Hq;
+  p.prefill_grid = p.tail_round = p.tail_units = 0;
+  if (units <= 0 || units > INT_MAX) return;
+  const int64_t slots = (int64_t)sm_count() * prefill_ctas_per_sm(p.d, p.mask_kind);
+  const int grid = (int)(units < slots ? units : slots);
+  p.prefill_grid = grid;
+  // Without a mask the units of a launch have nearly equal lengths (a causal
+  // launch over past keys) or fall in length from round to round; a last
+  // round that fills at most half the grid would leave most SMs idle while
+  // it runs, so its units are cut in two over their key tiles.  Each piece
+  // pays a unit's fixed costs and its rows a store, a load and a merge: the
+  // split is taken when every unit of that round has kTailMinTiles key tiles
+  // or more, which the host knows for sequences of one length (the last
+  // round holds the smallest row tiles: those of units rounds * grid ..
+  // units - 1).
+  constexpr int kTailMinTiles = 4;
+  const int64_t rounds = units / grid, left = units - rounds * grid;
+  constexpr int64_t kFlagBits = (int64_t)(kWsHeadBytes - kTailFlagsOff) * 8;
+  // (d = 64 launches run two CTAs per SM, whose units' epilogues already
+  // overlap: no split there)
+  if (p.mask_kind != FA_MASK_NONE || p.d != 128 || p.cu_q || p.cu_k || p.cache_len || rounds < 1 || left <= 0 ||
+      2 * left > grid || 4 * left > kFlagBits)
+    return;
+  const int64_t per_rt = (int64_t)p.n_seq * p.Hq;
+  const int rt_hi = p.n_row_tiles - 1 - (int)(rounds * grid / per_rt), rt_lo = p.n_row_tiles - 1 - (int)((units - 1) / per_rt);
+  const bool no_skip = (p.debug_flags & FA_DEBUG_NO_SKIP) != 0;
+  for (int rt = rt_lo; rt <= rt_hi; ++rt) {
+    // the unit's key range under the pair rules, as the kernel derives it
+    const int64_t i0 = (int64_t)rt * 128, i1 = std::min<int64_t>(i0 + 127, p.Sq - 1), off = (int64_t)p.Sk - p.Sq;
+    int64_t jlo = 0, jhi = p.Sk - 1;
+    if (!no_skip) {
+      if (p.causal) jhi = std::min(jhi, i1 + off);
+      if (p.wl >= 0) jlo = std::max(jlo, i0 + off - p.wl);
+      if (p.wr >= 0) jhi = std::min(jhi, i1 + off + p.wr);
+    }
+    if (jlo > jhi || jhi / kKeysPerTile - jlo / kKeysPerTile + 1 < kTailMinTiles) return;
+  }
+  p.tail_round = (int32_t)rounds;
+  p.tail_units = (int32_t)left;
+}
+
 cudaError_t launch_prefill(const Params& p, cudaStream_t st, cudaEvent_t ev_begin) {
   if (p.n_items <= 0) return ev_begin ? cudaEventRecord(ev_begin, st) : cudaSuccess;
   if (p.f16) return launch_prefill_f16(p, st, ev_begin);

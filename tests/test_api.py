@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
     for n in names:
         assert hasattr(fa.lib, n), n
         assert ctypes.cast(getattr(fa.lib, n), ctypes.c_void_p).value
-    assert fa.fa_abi_version() == 7 == _lib.ABI_VERSION
+    assert fa.fa_abi_version() == 8 == _lib.ABI_VERSION
     assert fa.fa_status_string(0) == "ok"
 
 

@@ -194,6 +194,53 @@ def test_bad_page_index_is_reported():
 
 
 # ---------------------------------------------------------------------------
+# Tail split: a persistent grid's last round that fills at most half the grid
+# runs each of its units as two pieces over the halves of its key tiles,
+# merged by LSE (ExecuTorch PR 10466 "Summary": chunks along the key
+# dimension, softmax accumulated progressively and rescaled at the end)
+# ---------------------------------------------------------------------------
+
+def _tail_hq(unit_rows, grid):
+    """Smallest even q-head count whose units overflow the grid by at most half of it."""
+    hq = grid // unit_rows + 1
+    hq += hq & 1
+    assert grid < unit_rows * hq <= grid + grid // 2
+    return hq
+
+
+TAIL = [
+    # B, Sq, Sk, d, group size, extra
+    (1, 500, 1000, 128, 2, dict()),                                    # ragged last key tile, 4 + 4 tiles
+    (2, 300, 1400, 128, 2, dict(causal=True, softcap=30.0)),           # causal over past keys, 5 + 5 tiles
+    (1, 1024, 2048, 128, 4, dict(causal=True, window_left=600)),       # sliding window, 3 + 3 tiles
+    (1, 640, 900, 128, 2, dict(causal=False, window_left=300, window_right=200)),  # 3 + 2 tiles
+]
+
+
+@pytest.mark.parametrize("i", range(len(TAIL)))
+def test_prefill_tail_split(i):
+    import masked_flash_attention_gb300 as fa
+    B, Sq, Sk, d, G, extra = TAIL[i]
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    rt = (Sq + 127) // 128
+    hq = _tail_hq(B * rt, grid)
+    case = W.random_case(1900 + i, B=B, Sq=Sq, Sk=Sk, Hq=hq, Hkv=hq // G, d=d, **extra)
+    p = to_dev(case["params"])
+    q, k, v = case["q"].to(DEV), case["k"].to(DEV), case["v"].to(DEV)
+    rc, plan = fa.fa_fwd_plan(q, k, v, **p)
+    assert rc == 0 and plan["tail_units"] == B * rt * hq - grid, plan
+    ref_o, ref_l = run_oracle(case)
+    ws = None
+    for rep in range(2):  # the second call reuses the workspace: the arrival counts are back at zero
+        out, lse, ws = fa.fa_fwd(q, k, v, workspace=ws, **p)
+        torch.cuda.synchronize()
+        rc, info = fa.fa_check_device_error(ws)
+        assert rc == 0, (rc, info)
+        assert int(ws[16:256].count_nonzero()) == 0
+        compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, f"{case['name']} call {rep}")
+
+
+# ---------------------------------------------------------------------------
 # Full-size workloads, sampled rows
 # ---------------------------------------------------------------------------
 

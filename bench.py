@@ -57,12 +57,12 @@ KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_dev
 # time: once the kernel changes the figure no longer applies and is reported
 # as null.
 MEASURED_TRAFFIC = {
-    ("causal_prefill_past_kv", "prefill_kernel"): ("716c5b360ef63b81", 104366848 + 9394944),
-    ("gpt2_small_layer", "prefill_kernel"): ("716c5b360ef63b81", 37830144 + 122624),
-    ("llama3_8b_layer", "prefill_kernel"): ("716c5b360ef63b81", 100860160 + 37312512),
-    ("dynamic_topk", "prefill_kernel"): ("716c5b360ef63b81", 199035904 + 51283712),
-    ("paged_varlen_decode", "decode_kernel"): ("9018a256470fb146", 752910848 + 9687040),
-    ("paged_decode_append", "decode_kernel"): ("9018a256470fb146", 752864256 + 9860096),
+    ("causal_prefill_past_kv", "prefill_kernel"): ("62e44ab1eb9999b2", 103775488 + 11407872),
+    ("gpt2_small_layer", "prefill_kernel"): ("62e44ab1eb9999b2", 37847040 + 120832),
+    ("llama3_8b_layer", "prefill_kernel"): ("62e44ab1eb9999b2", 100772096 + 37414656),
+    ("dynamic_topk", "prefill_kernel"): ("62e44ab1eb9999b2", 201289216 + 52963584),
+    ("paged_varlen_decode", "decode_kernel"): ("9d39f0003aa95bcf", 752926208 + 9257472),
+    ("paged_decode_append", "decode_kernel"): ("9d39f0003aa95bcf", 752866560 + 9434368),
 }
 
 

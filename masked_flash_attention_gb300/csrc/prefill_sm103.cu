@@ -15,6 +15,12 @@
 // one unit into the next (Q of the next unit is fetched while the current one
 // runs, or at d = 128 once its QKs are done; its first QK overlaps the current
 // epilogue).
+// When the last round would hold at most half the grid (a causal launch over
+// past keys: 512 units of almost equal length on 152 CTAs leave 56 for the
+// fourth round), each of its units is cut in two over its key tiles and run
+// by two CTAs; the two pieces' normalised rows are merged by their
+// log-sum-exp, the same rescaling the chunked softmax uses across chunks,
+// by whichever piece finishes second.
 // Grouped-query heads read their K/V head directly (InfiniTrain pull request
 // 193 "Transformer 接入": no expansion); neighbouring units are the q-heads of
 // one group, so their K/V tiles are served from L2.

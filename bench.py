@@ -363,7 +363,11 @@ def run_gpu(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     # per step: the attention kernel's begin, the end of the attention kernel
-    # itself, the end of the call's last pass (the decode path's split combine)
+    # itself, the end of the call's last pass (the decode path's split
+    # combine).  A prefill call has no pass after its kernel: its steps record
+    # no third event, as each timing event on the stream costs about 2 us of
+    # the step.
+    after_pass = bwd or plan["path"] == fa._lib.FA_PATH_DECODE
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
@@ -378,14 +382,14 @@ def run_gpu(args):
             flush.zero_()
             kev[i][0].record(); kev[i][1].record(); kev[i][2].record()  # materialise the handles
             ev[i][0].record()
-            step(kb=kev[i][0], ke=kev[i][2], ka=None if bwd else kev[i][1])
+            step(kb=kev[i][0], ke=kev[i][2] if after_pass else None, ka=None if bwd else kev[i][1])
             ev[i][1].record()
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     # the dominant kernel alone (the backward: its three kernels); the passes
     # after it (split combine) are reported beside it
     kern_ms = [a.elapsed_time(c if bwd else b) for a, b, c in kev]
-    after_ms = [0.0 if bwd else b.elapsed_time(c) for a, b, c in kev]
+    after_ms = [b.elapsed_time(c) if after_pass and not bwd else 0.0 for a, b, c in kev]
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(dist, total_ms, dev)
     if dist:

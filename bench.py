@@ -63,24 +63,34 @@ KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_dev
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; see profiles/), keyed
 # by workload and kernel, with the hash of the kernel's sources at capture
-# time: once the kernel changes the figure no longer applies and is reported
-# as null.
+# time (comments and white space left out): once the kernel's code changes the
+# figure no longer applies and is reported as null.
 MEASURED_TRAFFIC = {
-    ("causal_prefill_past_kv", "prefill_kernel"): ("62e44ab1eb9999b2", 103775488 + 11407872),
-    ("gpt2_small_layer", "prefill_kernel"): ("62e44ab1eb9999b2", 37847040 + 120832),
-    ("llama3_8b_layer", "prefill_kernel"): ("62e44ab1eb9999b2", 100772096 + 37414656),
-    ("dynamic_topk", "prefill_kernel"): ("62e44ab1eb9999b2", 201289216 + 52963584),
-    ("paged_varlen_decode", "decode_kernel"): ("9d39f0003aa95bcf", 752926208 + 9257472),
-    ("paged_decode_append", "decode_kernel"): ("9d39f0003aa95bcf", 752866560 + 9434368),
+    ("causal_prefill_past_kv", "prefill_kernel"): ("701a81111927638c", 103775488 + 11407872),
+    ("gpt2_small_layer", "prefill_kernel"): ("701a81111927638c", 37847040 + 120832),
+    ("llama3_8b_layer", "prefill_kernel"): ("701a81111927638c", 100772096 + 37414656),
+    ("dynamic_topk", "prefill_kernel"): ("701a81111927638c", 201289216 + 52963584),
+    ("paged_varlen_decode", "decode_kernel"): ("41c2ad86020fef38", 752926208 + 9257472),
+    ("paged_decode_append", "decode_kernel"): ("41c2ad86020fef38", 752866560 + 9434368),
 }
+
+
+def code_text(src):
+    """A C++/CUDA source without its comments and with runs of white space
+    collapsed: what the compiler sees, so that editing a comment does not
+    mark a measurement stale."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
 
 
 def kernel_hash(kernel):
     import hashlib
     m = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            m.update(fh.read())
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+            m.update(code_text(fh.read()).encode())
     return m.hexdigest()[:16]
 
 

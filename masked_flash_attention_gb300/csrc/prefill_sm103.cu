@@ -9,7 +9,7 @@
 // scheduler (sched.cu, topk.cu) left them out of each item's key-tile list;
 // without one the kernel derives each unit's tiles from its geometry.
 //
-// Persistent kernel: one CTA per SM walks the work units (sequence, q-head,
+// Persistent kernel: one CTA per SM (two at d = 64) walks the work units (sequence, q-head,
 // 128-row query tile) longest first, in rounds of one unit per CTA with every
 // other round in reverse CTA order (serpentine), so the pipelines run on from
 // one unit into the next (Q of the next unit is fetched while the current one

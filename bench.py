@@ -57,6 +57,13 @@ L2_BYTES = 129 << 20  # GB300 L2
 # a step that reads at least this much needs no flush: its own reads evict
 # whatever the previous step left in L2 before they could reuse it
 NO_FLUSH_READ_BYTES = 4 * L2_BYTES
+
+
+def flushes_l2(units, bwd=False):
+    """True when timed steps are separated by an L2 flush: unless a step reads
+    at least NO_FLUSH_READ_BYTES (known only for the byte-bound workloads;
+    the backward always flushes)."""
+    return bwd or units["bytes"] is None or units["bytes"] < NO_FLUSH_READ_BYTES
 CSRC = os.path.join(ROOT, "masked_flash_attention_gb300", "csrc")
 KERNEL_SOURCES = {"prefill_kernel": ["prefill_sm103.cu", "tc_sm103.cuh", "fa_device.cuh"],
                   "decode_kernel": ["decode.cu", "mma_sync.cuh", "fa_device.cuh"]}
@@ -349,7 +356,7 @@ def run_gpu(args):
     lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    big_reads = units["bytes"] is not None and units["bytes"] >= NO_FLUSH_READ_BYTES and not bwd
+    big_reads = not flushes_l2(units, bwd)
 
     def flush_l2():
         # the write evicts the inputs; the read of another buffer then evicts

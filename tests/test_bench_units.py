@@ -105,3 +105,26 @@ def test_kv_window_bytes(window_left):
         ok = O.allowed_pairs(np.arange(Sq), np.arange(Sk), Sq, Sk, True, window_left, -1)
         want += int(ok.any(axis=0).sum()) * Hkv * d * 2 * 2
     assert bench.kv_window_bytes(case) == want
+
+
+def test_l2_flush_rule():
+    """Timed steps are separated by an L2 flush unless a step's own reads are
+    several times L2 (the decode workloads); prefill and backward steps always
+    flush."""
+    tensor = dict(metric_units=1.0, unit="TFLOP/s", bound="tensor", flops=1.0, bytes=None)
+    small = dict(metric_units=0.1, unit="GB/s", bound="hbm", flops=1.0, bytes=bench.L2_BYTES * 2)
+    large = dict(small, bytes=749_203_456)  # K/V bytes of the paged-decode workload
+    assert bench.flushes_l2(tensor) and bench.flushes_l2(small)
+    assert not bench.flushes_l2(large)
+    assert bench.flushes_l2(large, bwd=True)
+    assert bench.NO_FLUSH_READ_BYTES >= 4 * bench.L2_BYTES
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The traffic table's key follows the kernels' code: a comment or white
+    space edit keeps it, any code edit changes it."""
+    src = 'int f(int a) {  // the sum\n  /* two\n lines */ return a + 1;\n}\n'
+    assert bench.code_text(src) == bench.code_text("int f(int a) {\n return a + 1; }  // other words")
+    assert bench.code_text(src) != bench.code_text("int f(int a) { return a + 2; }")
+    for kernel in bench.KERNEL_SOURCES:
+        assert len(bench.kernel_hash(kernel)) == 16

@@ -270,9 +270,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // splits slowest: every item's first split is dispatched before any second
+  // one, so the grid ends on the last splits of the longest sequences (partial
+  // or empty) rather than on the full-length splits of the last items
   const int64_t cta = blockIdx.x;
-  const int64_t item = cta / p.n_splits;
-  const int split = (int)(cta % p.n_splits);
+  const int split = (int)(cta / p.n_items);
+  const int64_t item = cta - (int64_t)split * p.n_items;
   const int count = p.item_count[item];
   if (count < 0) return;  // sequence rejected by the scheduler's length checks
   const int t_begin = split * p.tiles_per_split;

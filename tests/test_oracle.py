@@ -96,6 +96,52 @@ def test_fully_masked_row_is_zero_not_nan():
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse[0, :, 3:]))
 
 
+def _merge_by_lse(parts):
+    """Rows of attention over disjoint key chunks combined by their
+    log-sum-exp: L = log sum_c e^{L_c}, O = sum_c e^{L_c - L} O_c; a row that
+    no chunk lets see a key stays O = 0, L = -inf."""
+    lses = np.stack([l for _, l in parts])            # [chunks, B, H, S]
+    L = np.logaddexp.reduce(lses, axis=0)
+    out = np.zeros_like(parts[0][0])
+    for o, l in parts:
+        w = np.where(np.isfinite(L), np.exp(l - np.where(np.isfinite(L), L, 0.0)), 0.0)
+        out += o * np.moveaxis(w, 1, 2)[..., None]    # [B, H, S] -> [B, S, H, 1]
+    return out, L
+
+
+@pytest.mark.parametrize("split,all_neginf_chunk,empty_rows", [
+    (0.37, False, False),  # every row sees keys of both chunks
+    (0.5, True, True),     # the first chunk is all -inf for every row
+    (0.81, False, True),   # the first rows see no key of the second chunk
+])
+def test_key_chunks_merge_by_lse(split, all_neginf_chunk, empty_rows):
+    """ExecuTorch PR 10466 "Summary": attention may be computed chunk by
+    chunk along the keys, the softmax accumulated and rescaled at the end,
+    and an all -inf chunk must not poison the result.  Attention over all
+    keys equals the log-sum-exp merge of attention over two key chunks (each
+    chunk the other keys masked to -inf), rows that see no key in one chunk
+    included; the tail split of the prefill kernel and the decode combine
+    rely on exactly this."""
+    Sq, Sk = 9, 23
+    c = W.random_case(77, B=2, Sq=Sq, Sk=Sk, Hq=4, Hkv=2, d=8, causal=True)
+    m = int(round(split * Sk))
+    base = np.zeros((Sq, Sk))
+    if all_neginf_chunk:  # every key of the first chunk masked for every row
+        base[:, :m] = -np.inf
+    full_o, full_l = run(c, mask=torch.tensor(base))
+    chunk_a, chunk_b = base.copy(), base.copy()
+    chunk_a[:, m:] = -np.inf
+    chunk_b[:, :m] = -np.inf
+    parts = [run(c, mask=torch.tensor(chunk_a)), run(c, mask=torch.tensor(chunk_b))]
+    assert ((parts[0][1] == -np.inf).any() or (parts[1][1] == -np.inf).any()) == empty_rows
+    out, lse = _merge_by_lse(parts)
+    assert np.all(np.isfinite(out))
+    np.testing.assert_array_equal(lse == -np.inf, full_l == -np.inf)
+    np.testing.assert_allclose(out, full_o, rtol=0, atol=1e-13)
+    fin = np.isfinite(full_l)
+    np.testing.assert_allclose(lse[fin], full_l[fin], rtol=0, atol=1e-13)
+
+
 # ---------------------------------------------------------------------------
 # Causal: library routine, lower-triangular mask, bottom-right alignment
 # ---------------------------------------------------------------------------
